@@ -1,0 +1,176 @@
+/*
+ * moe_lora.h -- C ABI of libmoelora.so, the multi-LoRA fused MoE layer forward
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (AWS machine-learning blog "Efficiently serve dozens of
+ * fine-tuned models with vLLM on Amazon SageMaker AI and Amazon Bedrock",
+ * section "Implementing multi-LoRA inference for MoE models in vLLM",
+ * Figure 1): a router has sent every token t to k experts e = topk_ids[t][j]
+ * with weights w = topk_weights[t][j]; the token carries one adapter id
+ * l = token_lora_ids[t] (-1: base model only).  For every (token, slot) pair
+ *
+ *     g    = W1[e] x[t]   + B1[l][e] (A1[l][e] x[t])       (gate_up, 2I rows)
+ *     act  = SiLU(g[0:I]) * g[I:2I]                        (SiLU(u) = u/(1+e^-u))
+ *     d    = W2[e] act    + B2[l][e] (A2[l][e] act)        (down, H rows)
+ *
+ * and out[t] = bf16( sum_j w[t][j] * d[t*k+j] ).  Each LoRA term is the
+ * blog's shrink (z = x A, h_in -> r) followed by its expand (z B, r -> h_out),
+ * with no extra scale; it is left out when l = -1.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates or frees device memory; scratch lives in the caller's
+ *     workspace (size from moe_lora_workspace_bytes).
+ *   - bf16 tensors are raw IEEE bfloat16 bits.  All layouts are row-major
+ *     "[out][in]" (the reduction dimension is contiguous), i.e. the transposes
+ *     of the blog's h_in x h_out matrices:
+ *         x [T][H], W1 [E][2I][H] (gate rows 0..I-1, up rows I..2I-1),
+ *         W2 [E][H][I], A1 [L][E][r][H], B1 [L][E][2I][r],
+ *         A2 [L][E][r][I], B2 [L][E][H][r], out [T][H],
+ *         topk_ids [T][k] int32, topk_weights [T][k] float32,
+ *         token_lora_ids [T] int32.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Nothing synchronises the host except
+ *     moe_lora_get_status.  Inputs are never modified; `out` is fully
+ *     overwritten.
+ *   - Errors that the host can see (null pointers, bad sizes, misalignment,
+ *     a workspace that is too small) return a negative status before anything
+ *     is launched.  Errors only the device can see (an expert id outside
+ *     [0, E), an adapter id outside [-1, L)) leave the affected pairs out of
+ *     the result and set a status word in the workspace, read back by
+ *     moe_lora_get_status; no kernel traps.
+ *   - Alignment: every tensor pointer and the workspace must be 16-byte
+ *     aligned; H and I must be multiples of 8; r a multiple of 8 in [8, 64]
+ *     when L > 0.  Otherwise MOELORA_EUNSUPPORTED.
+ *   - The library keeps no state between calls beyond a per-device cache of
+ *     kernel attributes; calls on different workspaces may run concurrently.
+ */
+#ifndef MOE_LORA_H
+#define MOE_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOELORA_API __attribute__((visibility("default")))
+
+/* Problem sizes.  block_m is the bucket padding granularity (the tile height
+ * shared by every kernel of one forward, as the blog's section "Tuning kernel
+ * configurations" shares one BLOCK_SIZE_M across the four LoRA ops); 0 lets
+ * the library choose (16). */
+typedef struct moe_lora_dims {
+    int32_t T;       /* tokens, >= 0 */
+    int32_t H;       /* hidden size, > 0, multiple of 8 */
+    int32_t I;       /* intermediate size per expert, > 0, multiple of 8 */
+    int32_t E;       /* experts, > 0 */
+    int32_t k;       /* experts per token, > 0 */
+    int32_t L;       /* adapters, >= 0 (0: no LoRA; A and B pointers may be NULL) */
+    int32_t r;       /* LoRA rank: multiple of 8 in [8, 64] if L > 0, ignored if L == 0 */
+    int32_t block_m; /* 0 = default 16; otherwise a power of two in [1, 256] */
+} moe_lora_dims;
+
+/* Status codes (return values; moe_lora_strerror gives a message). */
+#define MOELORA_OK 0
+#define MOELORA_EINVAL (-1)        /* null pointer or impossible size */
+#define MOELORA_ENOSPC (-2)        /* workspace smaller than moe_lora_workspace_bytes */
+#define MOELORA_EUNSUPPORTED (-3)  /* valid but outside what the kernels handle (alignment, r > 64, ...) */
+#define MOELORA_ECUDA (-4)         /* a CUDA runtime call failed (e.g. no device) */
+#define MOELORA_EDEVICE_ID (-5)    /* the device met an out-of-range expert or adapter id */
+
+/* Human-readable message for a status code; never NULL. Host only. */
+MOELORA_API const char *moe_lora_strerror(int code);
+
+/* ABI version (major * 10000 + minor * 100 + patch). Host only. */
+MOELORA_API int moe_lora_version(void);
+
+/* Entries that moe_lora_align may write into sorted_ids:
+ * P + min(E*(L+1), P) * (block_m - 1) with P = T*k; tile_expert and tile_lora
+ * need capacity / block_m entries.  Returns < 0 (a status) on bad dims.
+ * Host only, pure. */
+MOELORA_API int64_t moe_lora_align_capacity(const moe_lora_dims *d);
+
+/* Bytes of device workspace that moe_lora_forward and moe_lora_align need
+ * for these dims (0 if the dims are invalid).  Host only, pure. */
+MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims *d);
+
+/*
+ * Expert x adapter bucketing of the T*k (token, slot) pairs: the extra
+ * adapter grid dimension the blog adds to fused_moe, and the compound
+ * sparsity (expert routing times adapter choice) it describes, both in the
+ * section "Implementing multi-LoRA inference for MoE models in vLLM".
+ *
+ * Pair p = t*k + j goes to bucket b = e*(L+1) + (l+1) with e = topk_ids[p],
+ * l = token_lora_ids[t]; buckets are laid out in ascending b, pairs keep
+ * ascending p inside a bucket, and each non-empty bucket is padded up to a
+ * multiple of block_m with the sentinel value P = T*k (empty buckets take no
+ * room).  Outputs (device pointers, int32):
+ *   sorted_ids      [moe_lora_align_capacity] -- entries past num_post_padded untouched
+ *   tile_expert     [capacity / block_m]      -- expert of each block_m-row tile
+ *   tile_lora       [capacity / block_m]      -- adapter of each tile (-1: base)
+ *   num_post_padded [1]                       -- total padded length
+ *   bucket_count    [E*(L+1)]                 -- valid pairs per bucket
+ *   bucket_offset   [E*(L+1) + 1]             -- padded start of each bucket
+ * Pairs with an out-of-range id are left out and flagged in the workspace
+ * status word (see moe_lora_get_status).  The result is unique and
+ * deterministic.  Returns a status; asynchronous on `stream`.
+ */
+MOELORA_API int moe_lora_align(const moe_lora_dims *d, const int32_t *topk_ids,
+                               const int32_t *token_lora_ids, int32_t *sorted_ids,
+                               int32_t *tile_expert, int32_t *tile_lora,
+                               int32_t *num_post_padded, int32_t *bucket_count,
+                               int32_t *bucket_offset, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
+/*
+ * The layer forward described at the top of this header, computed by the
+ * library's kernels in bf16 inputs / fp32 accumulation with one rounding of
+ * the result to bf16 (round to nearest even).  Intermediates (the LoRA
+ * shrink outputs and the activation) are kept in fp32 and bf16 respectively.
+ * A1, B1, A2, B2 may be NULL only when L == 0.  `out` [T][H] bf16 is fully
+ * overwritten.  The workspace must hold moe_lora_workspace_bytes(d) bytes;
+ * its contents on entry do not matter.  Results are deterministic (no
+ * floating-point atomics): the same inputs give the same bits.
+ * Returns a status; asynchronous on `stream`; capturable in a CUDA graph.
+ */
+MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
+                                 const int32_t *topk_ids, const float *topk_weights,
+                                 const int32_t *token_lora_ids, const void *W1,
+                                 const void *W2, const void *A1, const void *B1,
+                                 const void *A2, const void *B2, void *out,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then returns MOELORA_OK if the last align/forward that
+ * used this workspace met no out-of-range id, MOELORA_EDEVICE_ID if it did,
+ * or MOELORA_ECUDA if a CUDA call failed.  The only synchronising entry point.
+ */
+MOELORA_API int moe_lora_get_status(const void *workspace, void *stream);
+
+/*
+ * Where the forward keeps its intermediates inside the workspace, for
+ * diagnostics and per-kernel tests (byte offsets from the workspace start;
+ * 0 bytes means absent).  Rows are the valid pairs in bucket order (the
+ * unpadded order of moe_lora_align).
+ */
+typedef struct moe_lora_ws_layout {
+    size_t compact_ids;      /* int32 [P]: pair id of each row */
+    size_t compact_offset;   /* int32 [E*(L+1)+1]: first row of each bucket */
+    size_t z1;               /* float [S1][P][r]: gate_up shrink partials over S1 K-splits */
+    size_t act;              /* bf16 [P][I]: SiLU(gate)*up per row */
+    size_t z2;               /* float [S2][P][r]: down shrink partials over S2 K-splits */
+    size_t pair_out;         /* float [P][H]: w * d per pair id p */
+    int32_t s1, s2;          /* K-split counts of the two shrinks */
+    size_t total;            /* == moe_lora_workspace_bytes */
+} moe_lora_ws_layout;
+
+/* Fills *out for dims d; returns a status. Host only, pure. */
+MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims *d, moe_lora_ws_layout *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H */

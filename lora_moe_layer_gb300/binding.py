@@ -1,0 +1,166 @@
+"""Thin ctypes binding of libmoelora.so (include/moe_lora.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, turns tensors into device pointers and the stream into a
+cudaStream_t, and returns the C status code.  All compute runs in the CUDA
+library; if the library is missing this module raises instead of falling
+back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libmoelora.so")
+
+MOELORA_OK = 0
+MOELORA_EINVAL = -1
+MOELORA_ENOSPC = -2
+MOELORA_EUNSUPPORTED = -3
+MOELORA_ECUDA = -4
+MOELORA_EDEVICE_ID = -5
+
+# every symbol the header declares
+EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
+            "moe_lora_workspace_bytes", "moe_lora_align", "moe_lora_forward",
+            "moe_lora_get_status", "moe_lora_workspace_layout")
+
+
+class MoeLoraError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = code
+        super().__init__(f"{where}: status {code} ({moe_lora_strerror(code)})")
+
+
+class moe_lora_dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "L", "r", "block_m")]
+
+
+class moe_lora_ws_layout(ctypes.Structure):
+    _fields_ = [("compact_ids", ctypes.c_size_t), ("compact_offset", ctypes.c_size_t),
+                ("z1", ctypes.c_size_t), ("act", ctypes.c_size_t), ("z2", ctypes.c_size_t),
+                ("pair_out", ctypes.c_size_t), ("s1", ctypes.c_int32), ("s2", ctypes.c_int32),
+                ("total", ctypes.c_size_t)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Open libmoelora.so (built in-tree by lora_moe_layer_gb300.build)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with lora_moe_layer_gb300.build.build() "
+                           "(the layer has no non-CUDA implementation)")
+    lib = ctypes.CDLL(p)
+    V, SZ, I32, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int64
+    D = ctypes.POINTER(moe_lora_dims)
+    lib.moe_lora_strerror.restype = ctypes.c_char_p
+    lib.moe_lora_strerror.argtypes = [I32]
+    lib.moe_lora_version.restype = I32
+    lib.moe_lora_version.argtypes = []
+    lib.moe_lora_align_capacity.restype = I64
+    lib.moe_lora_align_capacity.argtypes = [D]
+    lib.moe_lora_workspace_bytes.restype = SZ
+    lib.moe_lora_workspace_bytes.argtypes = [D]
+    lib.moe_lora_align.restype = I32
+    lib.moe_lora_align.argtypes = [D, V, V, V, V, V, V, V, V, V, SZ, V]
+    lib.moe_lora_forward.restype = I32
+    lib.moe_lora_forward.argtypes = [D] + [V] * 12 + [SZ, V]
+    lib.moe_lora_get_status.restype = I32
+    lib.moe_lora_get_status.argtypes = [V, V]
+    lib.moe_lora_workspace_layout.restype = I32
+    lib.moe_lora_workspace_layout.argtypes = [D, ctypes.POINTER(moe_lora_ws_layout)]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- marshalling
+
+def dims(T: int, H: int, I: int, E: int, k: int, L: int, r: int, block_m: int = 0) -> moe_lora_dims:
+    return moe_lora_dims(T, H, I, E, k, L, r if L > 0 else 0, block_m)
+
+
+def _ptr(t) -> Optional[int]:
+    """Device pointer of a tensor (or pass an int address / None through)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ----------------------------------------------------------------- entry points
+
+def moe_lora_strerror(code: int) -> str:
+    return load().moe_lora_strerror(code).decode()
+
+
+def moe_lora_version() -> int:
+    return load().moe_lora_version()
+
+
+def moe_lora_align_capacity(d: moe_lora_dims) -> int:
+    return load().moe_lora_align_capacity(ctypes.byref(d))
+
+
+def moe_lora_workspace_bytes(d: moe_lora_dims) -> int:
+    return load().moe_lora_workspace_bytes(ctypes.byref(d))
+
+
+def moe_lora_workspace_layout(d: moe_lora_dims) -> dict:
+    out = moe_lora_ws_layout()
+    st = load().moe_lora_workspace_layout(ctypes.byref(d), ctypes.byref(out))
+    if st != MOELORA_OK:
+        raise MoeLoraError(st, "moe_lora_workspace_layout")
+    return {name: getattr(out, name) for name, _ in moe_lora_ws_layout._fields_}
+
+
+def moe_lora_align(d: moe_lora_dims, topk_ids, token_lora_ids, sorted_ids, tile_expert, tile_lora,
+                   num_post_padded, bucket_count, bucket_offset, workspace, stream=None,
+                   workspace_bytes: Optional[int] = None) -> int:
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    return load().moe_lora_align(ctypes.byref(d), _ptr(topk_ids), _ptr(token_lora_ids), _ptr(sorted_ids),
+                                 _ptr(tile_expert), _ptr(tile_lora), _ptr(num_post_padded),
+                                 _ptr(bucket_count), _ptr(bucket_offset), _ptr(workspace), wb,
+                                 _stream(stream))
+
+
+def moe_lora_forward(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2, B2,
+                     out, workspace, stream=None, workspace_bytes: Optional[int] = None) -> int:
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    return load().moe_lora_forward(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                   _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
+                                   _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb, _stream(stream))
+
+
+def moe_lora_get_status(workspace, stream=None) -> int:
+    return load().moe_lora_get_status(_ptr(workspace), _stream(stream))
+
+
+def check(status: int, where: str = "moe_lora") -> None:
+    if status != MOELORA_OK:
+        raise MoeLoraError(status, where)

@@ -1,0 +1,248 @@
+// align.cu -- expert x adapter bucketing of the (token, slot) pairs.
+//
+// The blog ("Efficiently serve dozens of fine-tuned models with vLLM on
+// Amazon SageMaker AI and Amazon Bedrock", section "Implementing multi-LoRA
+// inference for MoE models in vLLM") describes its fused_moe_lora kernel as
+// fused_moe plus one more grid dimension over the active adapters, because
+// MoE LoRA mixes two sparsities: expert routing and per-request adapter
+// choice.  Here that becomes one stable sort of the pairs by the key
+// b = e*(L+1) + (l+1): buckets in ascending b, pairs in ascending p inside a
+// bucket, each non-empty bucket padded to a multiple of block_m.
+//
+// One CTA of 16 warps.  Each warp owns a contiguous segment of pairs and keeps
+// a per-bucket histogram row (shared memory when it fits, else the workspace).
+// Pass 1 counts with warp match-any + popc (one leader per distinct key per
+// 32 pairs); the histogram rows are then turned into per-warp exclusive
+// prefixes, bucket sizes are scanned (warp shuffles) into padded and compact
+// offsets, and pass 2 places every pair at
+//     offset[b] + (pairs of b in earlier warps) + (earlier lanes of b in this step).
+// Walking each segment in order and the warps in order keeps ascending p.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moelora {
+
+namespace {
+
+constexpr int kAlignThreads = 512;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+__device__ __forceinline__ int2 warp_incl_scan2(int2 v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(kFull, v.x, o);
+        const int y = __shfl_up_sync(kFull, v.y, o);
+        if (lane >= o) {
+            v.x += x;
+            v.y += y;
+        }
+    }
+    return v;
+}
+
+// Block-wide exclusive scan of an int2 per thread; *total gets the sums.
+// sw needs kAlignWarps + 1 entries.  Contains __syncthreads.
+__device__ int2 block_excl_scan2(int2 v, int2* total, int2* sw) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int2 inc = warp_incl_scan2(v, lane);
+    if (lane == 31) sw[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int2 w = lane < kAlignWarps ? sw[lane] : make_int2(0, 0);
+        const int2 wi = warp_incl_scan2(w, lane);
+        if (lane < kAlignWarps) sw[lane] = make_int2(wi.x - w.x, wi.y - w.y);
+        if (lane == 31) sw[kAlignWarps] = wi;
+    }
+    __syncthreads();
+    const int2 base = sw[warp];
+    *total = sw[kAlignWarps];
+    const int2 r = make_int2(base.x + inc.x - v.x, base.y + inc.y - v.y);
+    __syncthreads();
+    return r;
+}
+
+// Exclusive scan over n items of (f(i), g(i)) written to out_a / out_b
+// (n + 1 entries each, the last being the total).  Items are split into
+// contiguous per-thread runs.
+template <typename F>
+__device__ void block_scan_items(int n, F item, int* out_a, int* out_b, int2* sw) {
+    const int per = (n + kAlignThreads - 1) / kAlignThreads;
+    const int beg = min(n, (int)threadIdx.x * per);
+    const int end = min(n, beg + per);
+    int2 local = make_int2(0, 0);
+    for (int i = beg; i < end; i++) {
+        const int2 v = item(i);
+        local.x += v.x;
+        local.y += v.y;
+    }
+    int2 total;
+    int2 run = block_excl_scan2(local, &total, sw);
+    for (int i = beg; i < end; i++) {
+        const int2 v = item(i);
+        if (out_a) out_a[i] = run.x;
+        if (out_b) out_b[i] = run.y;
+        run.x += v.x;
+        run.y += v.y;
+    }
+    if (threadIdx.x == 0) {
+        if (out_a) out_a[n] = total.x;
+        if (out_b) out_b[n] = total.y;
+    }
+}
+
+__global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
+    extern __shared__ __align__(16) int smem_hist[];
+    __shared__ int2 sw[kAlignWarps + 1];
+    // The first kernel of a forward is launched without a programmatic
+    // dependency, so this wait is a no-op; it stays for standalone use.
+    pdl_wait();
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int P = a.T * a.k;
+    const int L1 = a.L + 1;
+    const int NB = a.E * L1;
+    int* hist = a.hist_global ? a.hist_global : smem_hist;  // [kAlignWarps][NB]
+    WsHeader* hdr = a.hdr;
+
+    if (threadIdx.x == 0) hdr->status = 0;
+    for (int i = threadIdx.x; i < kAlignWarps * NB; i += kAlignThreads) hist[i] = 0;
+    __syncthreads();
+
+    // each warp owns pairs [seg_beg, seg_end), walked 32 at a time
+    const int seg = ((P + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
+    const int seg_beg = min(P, warp * seg);
+    const int seg_end = min(P, seg_beg + seg);
+    int* my_hist = hist + warp * NB;
+    int bad_bits = 0;
+
+    // pass 1: per-warp bucket counts
+    for (int base = seg_beg; base < seg_end; base += 32) {
+        const int p = base + lane;
+        int b = -1;
+        if (p < seg_end) {
+            const int e = a.topk_ids[p];
+            const int l = a.lora_ids[p / a.k];
+            const bool e_ok = e >= 0 && e < a.E;
+            const bool l_ok = l >= -1 && l < a.L;
+            if (e_ok && l_ok) b = e * L1 + (l + 1);
+            else bad_bits |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
+        }
+        const unsigned peers = __match_any_sync(kFull, b);
+        if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad_bits) atomicOr(&hdr->status, bad_bits);
+    __syncthreads();
+
+    // per bucket: exclusive prefix over warps, and the bucket size
+    for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
+        int run = 0;
+        for (int w = 0; w < kAlignWarps; w++) {
+            const int c = hist[w * NB + b];
+            hist[w * NB + b] = run;
+            run += c;
+        }
+        a.bucket_count[b] = run;
+    }
+    __syncthreads();
+
+    // padded offsets (bucket_offset) and compact offsets, both exclusive scans
+    const int bm = a.bm;
+    const int* cnt = a.bucket_count;
+    block_scan_items(
+        NB, [&](int b) { const int c = cnt[b]; return make_int2((c + bm - 1) / bm * bm, c); },
+        a.bucket_offset, a.compact_offset, sw);
+    __syncthreads();
+
+    // pass 2: stable placement
+    for (int base = seg_beg; base < seg_end; base += 32) {
+        const int p = base + lane;
+        int b = -1;
+        if (p < seg_end) {
+            const int e = a.topk_ids[p];
+            const int l = a.lora_ids[p / a.k];
+            if (e >= 0 && e < a.E && l >= -1 && l < a.L) b = e * L1 + (l + 1);
+        }
+        const unsigned peers = __match_any_sync(kFull, b);
+        if (b >= 0) {
+            const int rank = my_hist[b] + __popc(peers & lanemask_lt());
+            const int pos = a.bucket_offset[b] + rank;
+            const int cpos = a.compact_offset[b] + rank;
+            a.sorted_ids[pos] = p;
+            a.compact_ids[cpos] = p;
+        }
+        __syncwarp();
+        if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // padding sentinels
+    for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
+        const int end = a.bucket_offset[b + 1];
+        for (int q = a.bucket_offset[b] + cnt[b]; q < end; q++) a.sorted_ids[q] = P;
+    }
+    // per-tile (expert, adapter): the bucket holding row q*bm
+    const int total_padded = a.bucket_offset[NB];
+    const int n_tiles = total_padded / bm;
+    for (int q = threadIdx.x; q < n_tiles; q += kAlignThreads) {
+        const int row = q * bm;
+        int lo = 0, hi = NB;  // find the last b with bucket_offset[b] <= row < bucket_offset[b+1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.bucket_offset[mid] <= row) lo = mid;
+            else hi = mid;
+        }
+        a.tile_expert[q] = lo / L1;
+        a.tile_lora[q] = lo % L1 - 1;
+    }
+    if (threadIdx.x == 0) {
+        hdr->num_post_padded = total_padded;
+        hdr->n_valid = a.compact_offset[NB];
+        if (a.num_post_padded) *a.num_post_padded = total_padded;
+    }
+    if (a.active_experts) {
+        // compact list of experts with pairs, and of (e, l >= 0) buckets with pairs
+        const int* coff = a.compact_offset;
+        const int E = a.E;
+        block_scan_items(
+            E, [&](int e) { return make_int2(coff[(e + 1) * L1] > coff[e * L1] ? 1 : 0, 0); },
+            a.scan_tmp, nullptr, sw);
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += kAlignThreads)
+            if (coff[(e + 1) * L1] > coff[e * L1]) a.active_experts[a.scan_tmp[e]] = e;
+        if (threadIdx.x == 0) hdr->n_active = a.scan_tmp[E];
+        __syncthreads();
+        block_scan_items(
+            NB, [&](int b) { return make_int2((b % L1) != 0 && cnt[b] > 0 ? 1 : 0, 0); },
+            a.scan_tmp, nullptr, sw);
+        __syncthreads();
+        for (int b = threadIdx.x; b < NB; b += kAlignThreads)
+            if ((b % L1) != 0 && cnt[b] > 0) a.lora_buckets[a.scan_tmp[b]] = b;
+        if (threadIdx.x == 0) hdr->n_lora_buckets = a.scan_tmp[NB];
+    }
+    pdl_trigger();
+}
+
+}  // namespace
+
+int align_hist_smem_bytes(int E, int L) {
+    const long nb = (long)E * (L + 1);
+    const long bytes = nb * kAlignWarps * (long)sizeof(int);
+    return bytes <= kAlignMaxSmemHist ? (int)bytes : 0;
+}
+
+long align_hist_global_ints(int E, int L) {
+    return align_hist_smem_bytes(E, L) ? 0 : (long)E * (L + 1) * kAlignWarps;
+}
+
+cudaError_t init_align_attributes() {
+    return cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmemHist);
+}
+
+cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream) {
+    // first kernel of a forward: ordinary stream order behind whatever ran before
+    return launch_k(k_align, dim3(1), dim3(kAlignThreads), smem_bytes, stream, false, args);
+}
+
+}  // namespace moelora

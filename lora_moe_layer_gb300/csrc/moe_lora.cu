@@ -1,0 +1,362 @@
+// moe_lora.cu -- host side of the C ABI declared in include/moe_lora.h:
+// argument validation, workspace layout, per-device kernel set-up and the
+// launch sequence of one forward.
+//
+// One forward is six kernels on the caller's stream, chained with
+// programmatic dependent launch so each can be resident before its
+// predecessor drains (the blog's PDL step, "Efficiently serve dozens of
+// fine-tuned models with vLLM ...", section "Execution optimizations"):
+//   align -> [gate_up shrink] -> gate_up GEMV (+expand, SiLU*up)
+//         -> [down shrink] -> down GEMV (+expand, x weight) -> top-k reduce.
+// The shrinks are skipped when the layer has no adapters, and exit at once
+// when no token of the batch uses one (the blog's early exit, same section).
+// Nothing here allocates device memory or synchronises the host.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kernels.cuh"
+#include "moe_lora.h"
+
+namespace moelora {
+namespace {
+
+constexpr int kDefaultBlockM = 16;
+constexpr int kMaxDevices = 64;
+
+struct Layout {
+    int bm;
+    long P, NB, cap, tiles;
+    int s1, s2, kc_gu, kc_dn;
+    size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
+        compact_ids, active_experts, lora_buckets, scan_tmp, hist, z1, act, z2, pair_out, total;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+
+// host-checkable validation; returns a status
+int check_dims(const moe_lora_dims* d) {
+    if (!d) return MOELORA_EINVAL;
+    if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->L < 0) return MOELORA_EINVAL;
+    if (d->block_m != 0 && (!is_pow2(d->block_m) || d->block_m > 256)) return MOELORA_EINVAL;
+    if (d->L > 0) {
+        if (d->r <= 0) return MOELORA_EINVAL;
+        if (d->r % 8 != 0 || d->r > 64) return MOELORA_EUNSUPPORTED;
+    }
+    if (d->H % 8 != 0 || d->I % 8 != 0) return MOELORA_EUNSUPPORTED;
+    // index arithmetic of the kernels stays in int for these
+    const long long P = (long long)d->T * d->k;
+    const long long NB = (long long)d->E * (d->L + 1);
+    if (P > (1LL << 28) || NB > (1LL << 22)) return MOELORA_EUNSUPPORTED;
+    if ((long long)d->L * d->E * 64 > (1LL << 30)) return MOELORA_EUNSUPPORTED;
+    const int bm = d->block_m ? d->block_m : kDefaultBlockM;
+    const long long nonempty = std::min(NB, P);
+    if (P + nonempty * (bm - 1) > (1LL << 30)) return MOELORA_EUNSUPPORTED;
+    return MOELORA_OK;
+}
+
+int make_layout(const moe_lora_dims* d, Layout* L) {
+    const int st = check_dims(d);
+    if (st != MOELORA_OK) return st;
+    L->bm = d->block_m ? d->block_m : kDefaultBlockM;
+    L->P = (long)d->T * d->k;
+    L->NB = (long)d->E * (d->L + 1);
+    L->cap = L->P + std::min(L->NB, L->P) * (L->bm - 1);
+    L->tiles = L->cap / L->bm;
+    const int r = d->L > 0 ? d->r : 0;
+    L->s1 = d->L > 0 ? (d->H + kShrinkKC - 1) / kShrinkKC : 0;
+    L->s2 = d->L > 0 ? (d->I + kShrinkKC - 1) / kShrinkKC : 0;
+    L->kc_gu = std::min(d->H, 4096);
+    L->kc_dn = std::min(d->I, 4096);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
+    L->hdr = take(sizeof(WsHeader));
+    L->sorted_ids = take(sizeof(int32_t) * std::max<long>(L->cap, 1));
+    L->tile_expert = take(sizeof(int32_t) * std::max<long>(L->tiles, 1));
+    L->tile_lora = take(sizeof(int32_t) * std::max<long>(L->tiles, 1));
+    L->bucket_count = take(sizeof(int32_t) * L->NB);
+    L->bucket_offset = take(sizeof(int32_t) * (L->NB + 1));
+    L->compact_offset = take(sizeof(int32_t) * (L->NB + 1));
+    L->compact_ids = take(sizeof(int32_t) * std::max<long>(L->P, 1));
+    L->active_experts = take(sizeof(int32_t) * d->E);
+    L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
+    L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
+    L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
+    L->z1 = take(sizeof(float) * (size_t)L->s1 * L->P * r);
+    L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
+    L->z2 = take(sizeof(float) * (size_t)L->s2 * L->P * r);
+    L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
+    L->total = o;
+    return MOELORA_OK;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int gemv_bps_cache_smem = -1;
+    int gemv_bps = 1;
+    cudaError_t init_err = cudaSuccess;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+int device_setup(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOELORA_ECUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return MOELORA_EUNSUPPORTED;
+    DeviceInfo* info = &g_dev[dev];
+    std::call_once(g_once[dev], [info, dev]() {
+        cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = init_align_attributes();
+        if (e == cudaSuccess) e = init_shrink_attributes();
+        if (e == cudaSuccess) e = init_gemv_attributes();
+        if (e == cudaSuccess) info->gemv_bps = gemv_blocks_per_sm(gemv_smem_bytes(4096));
+        info->init_err = e;
+    });
+    if (info->init_err != cudaSuccess) return MOELORA_ECUDA;
+    *out = info;
+    return MOELORA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
+
+AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t* topk_ids,
+                          const int32_t* lora_ids, void* ws) {
+    AlignArgs a = {};
+    a.T = d->T; a.k = d->k; a.E = d->E; a.L = d->L; a.bm = L.bm;
+    a.topk_ids = topk_ids;
+    a.lora_ids = lora_ids;
+    a.sorted_ids = at<int32_t>(ws, L.sorted_ids);
+    a.tile_expert = at<int32_t>(ws, L.tile_expert);
+    a.tile_lora = at<int32_t>(ws, L.tile_lora);
+    a.num_post_padded = nullptr;
+    a.bucket_count = at<int32_t>(ws, L.bucket_count);
+    a.bucket_offset = at<int32_t>(ws, L.bucket_offset);
+    a.compact_offset = at<int32_t>(ws, L.compact_offset);
+    a.compact_ids = at<int32_t>(ws, L.compact_ids);
+    a.active_experts = at<int32_t>(ws, L.active_experts);
+    a.lora_buckets = at<int32_t>(ws, L.lora_buckets);
+    a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
+    a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
+    a.hdr = at<WsHeader>(ws, L.hdr);
+    return a;
+}
+
+}  // namespace
+}  // namespace moelora
+
+using namespace moelora;
+
+extern "C" {
+
+MOELORA_API const char* moe_lora_strerror(int code) {
+    switch (code) {
+        case MOELORA_OK: return "ok";
+        case MOELORA_EINVAL: return "invalid argument (null pointer or impossible size)";
+        case MOELORA_ENOSPC: return "workspace smaller than moe_lora_workspace_bytes()";
+        case MOELORA_EUNSUPPORTED: return "unsupported size or alignment (H, I multiples of 8; r multiple of 8 <= 64; 16-byte aligned pointers)";
+        case MOELORA_ECUDA: return "a CUDA runtime call failed";
+        case MOELORA_EDEVICE_ID: return "the device met an expert or adapter id out of range; those pairs were left out";
+        default: return "unknown status";
+    }
+}
+
+MOELORA_API int moe_lora_version(void) { return 100; }
+
+MOELORA_API int64_t moe_lora_align_capacity(const moe_lora_dims* d) {
+    Layout L;
+    const int st = make_layout(d, &L);
+    return st == MOELORA_OK ? (int64_t)L.cap : (int64_t)st;
+}
+
+MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* d) {
+    Layout L;
+    return make_layout(d, &L) == MOELORA_OK ? L.total : 0;
+}
+
+MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_layout* out) {
+    if (!out) return MOELORA_EINVAL;
+    Layout L;
+    const int st = make_layout(d, &L);
+    if (st != MOELORA_OK) return st;
+    const bool lora = d->L > 0;
+    out->compact_ids = L.compact_ids;
+    out->compact_offset = L.compact_offset;
+    out->z1 = lora ? L.z1 : 0;
+    out->act = L.act;
+    out->z2 = lora ? L.z2 : 0;
+    out->pair_out = L.pair_out;
+    out->s1 = L.s1;
+    out->s2 = L.s2;
+    out->total = L.total;
+    return MOELORA_OK;
+}
+
+MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
+                               const int32_t* token_lora_ids, int32_t* sorted_ids,
+                               int32_t* tile_expert, int32_t* tile_lora, int32_t* num_post_padded,
+                               int32_t* bucket_count, int32_t* bucket_offset, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    Layout L;
+    int st = make_layout(d, &L);
+    if (st != MOELORA_OK) return st;
+    if (!sorted_ids || !tile_expert || !tile_lora || !num_post_padded || !bucket_count ||
+        !bucket_offset || !workspace)
+        return MOELORA_EINVAL;
+    if (d->T > 0 && (!topk_ids || !token_lora_ids)) return MOELORA_EINVAL;
+    if (workspace_bytes < L.total) return MOELORA_ENOSPC;
+    if (!aligned16(workspace)) return MOELORA_EUNSUPPORTED;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_setup(&dev)) != MOELORA_OK) return st;
+    AlignArgs a = make_align_args(d, L, topk_ids, token_lora_ids, workspace);
+    a.sorted_ids = sorted_ids;
+    a.tile_expert = tile_expert;
+    a.tile_lora = tile_lora;
+    a.num_post_padded = num_post_padded;
+    a.bucket_count = bucket_count;
+    a.bucket_offset = bucket_offset;
+    a.active_experts = nullptr;  // the standalone entry point skips the forward's work lists
+    const cudaError_t e = launch_align(a, align_hist_smem_bytes(d->E, d->L), (cudaStream_t)stream);
+    return e == cudaSuccess ? MOELORA_OK : MOELORA_ECUDA;
+}
+
+MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
+                                 const float* topk_weights, const int32_t* token_lora_ids,
+                                 const void* W1, const void* W2, const void* A1, const void* B1,
+                                 const void* A2, const void* B2, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    Layout L;
+    int st = make_layout(d, &L);
+    if (st != MOELORA_OK) return st;
+    if (!workspace || !W1 || !W2) return MOELORA_EINVAL;
+    if (d->T > 0 && (!x || !topk_ids || !topk_weights || !token_lora_ids || !out)) return MOELORA_EINVAL;
+    const bool has_lora = d->L > 0;
+    if (has_lora && (!A1 || !B1 || !A2 || !B2)) return MOELORA_EINVAL;
+    if (workspace_bytes < L.total) return MOELORA_ENOSPC;
+    const void* ptrs[] = {x, W1, W2, A1, B1, A2, B2, out, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MOELORA_EUNSUPPORTED;
+    DeviceInfo* dev = nullptr;
+    if ((st = device_setup(&dev)) != MOELORA_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    void* ws = workspace;
+    // programmatic dependent launch between the chained kernels; the legacy
+    // NULL stream gets plain stream order
+    const bool pdl = s != nullptr && s != cudaStreamLegacy;
+
+    AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
+    if (launch_align(aa, align_hist_smem_bytes(d->E, d->L), s) != cudaSuccess) return MOELORA_ECUDA;
+    if (d->T == 0) return MOELORA_OK;
+
+    const WsHeader* hdr = at<WsHeader>(ws, L.hdr);
+    const int sms = dev->sms;
+    const long lora_buckets_max = std::min<long>((long)d->E * d->L, L.P);
+
+    ShrinkArgs sh = {};
+    if (has_lora) {
+        sh.E = d->E; sh.L = d->L; sh.k = d->k; sh.r = d->r; sh.K = d->H; sh.P = (int)L.P;
+        sh.S = L.s1;
+        sh.in_is_x = 1;
+        sh.in = static_cast<const uint16_t*>(x);
+        sh.A = static_cast<const uint16_t*>(A1);
+        sh.lora_buckets = at<int32_t>(ws, L.lora_buckets);
+        sh.compact_offset = at<int32_t>(ws, L.compact_offset);
+        sh.compact_ids = at<int32_t>(ws, L.compact_ids);
+        sh.hdr = hdr;
+        sh.z = at<float>(ws, L.z1);
+        sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
+        const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
+        if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
+
+    GemvArgs g = {};
+    g.E = d->E; g.L = d->L; g.k = d->k; g.r = has_lora ? d->r : 0; g.I = d->I; g.H = d->H; g.P = (int)L.P;
+    g.lora_ids = token_lora_ids;
+    g.topk_weights = topk_weights;
+    g.active_experts = at<int32_t>(ws, L.active_experts);
+    g.compact_offset = at<int32_t>(ws, L.compact_offset);
+    g.compact_ids = at<int32_t>(ws, L.compact_ids);
+    g.hdr = hdr;
+    g.act_out = at<uint16_t>(ws, L.act);
+    g.pair_out = at<float>(ws, L.pair_out);
+    const long experts_max = std::min<long>(d->E, L.P);
+    const int grid_cap = sms * dev->gemv_bps;
+
+    // gate_up
+    g.gate_up = 1;
+    g.in = static_cast<const uint16_t*>(x);
+    g.W = static_cast<const uint16_t*>(W1);
+    g.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
+    g.zpart = has_lora ? at<float>(ws, L.z1) : nullptr;
+    g.S = L.s1;
+    g.kc = L.kc_gu;
+    {
+        const long per_cta = (kGemvThreads / 32) * (kGemvRows / 2);
+        g.max_tasks = (int)std::min<long>(experts_max * ((d->I + per_cta - 1) / per_cta), 1L << 30);
+        const int grid = std::max(1, std::min(g.max_tasks, grid_cap));
+        if (launch_gemv(g, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
+
+    if (has_lora) {
+        sh.K = d->I;
+        sh.S = L.s2;
+        sh.in_is_x = 0;
+        sh.in = at<uint16_t>(ws, L.act);
+        sh.A = static_cast<const uint16_t*>(A2);
+        sh.z = at<float>(ws, L.z2);
+        sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
+        const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
+        if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
+
+    // down
+    g.gate_up = 0;
+    g.in = at<uint16_t>(ws, L.act);
+    g.W = static_cast<const uint16_t*>(W2);
+    g.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
+    g.zpart = has_lora ? at<float>(ws, L.z2) : nullptr;
+    g.S = L.s2;
+    g.kc = L.kc_dn;
+    {
+        const long per_cta = (kGemvThreads / 32) * kGemvRows;
+        g.max_tasks = (int)std::min<long>(experts_max * ((d->H + per_cta - 1) / per_cta), 1L << 30);
+        const int grid = std::max(1, std::min(g.max_tasks, grid_cap));
+        if (launch_gemv(g, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
+
+    ReduceArgs ra = {};
+    ra.T = d->T; ra.k = d->k; ra.H = d->H; ra.E = d->E; ra.L = d->L;
+    ra.pair_out = at<float>(ws, L.pair_out);
+    ra.topk_ids = topk_ids;
+    ra.lora_ids = token_lora_ids;
+    ra.out = static_cast<uint16_t*>(out);
+    {
+        const long n = (long)d->T * (d->H / 4);
+        const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
+        if (launch_reduce(ra, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
+    return MOELORA_OK;
+}
+
+MOELORA_API int moe_lora_get_status(const void* workspace, void* stream) {
+    if (!workspace) return MOELORA_EINVAL;
+    int32_t status = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemcpyAsync(&status, workspace, sizeof(status), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return MOELORA_ECUDA;
+    }
+    return status == 0 ? MOELORA_OK : MOELORA_EDEVICE_ID;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// reduce.cu -- top-k weighted aggregation: out[t] = bf16(sum_j pair_out[t*k + j]).
+//
+// The router's k experts of a token are aggregated ("Efficiently serve dozens
+// of fine-tuned models with vLLM ...", section "Implementing multi-LoRA
+// inference for MoE models in vLLM"); the down kernel has already applied the
+// top-k weights, so this is a fixed-order sum over the token's slots (j = 0
+// .. k-1, deterministic) and one round-to-nearest-even to bf16.  Pairs that
+// carry an out-of-range id were left out upstream and are skipped here.
+// Four hidden elements per thread: 16-byte fp32 loads, 8-byte bf16 stores.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace moelora {
+
+namespace {
+
+__global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const int H4 = a.H >> 2;
+    const long n = (long)a.T * H4;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (long)gridDim.x * blockDim.x) {
+        const int t = (int)(idx / H4), h4 = (int)(idx % H4);
+        const int l = a.lora_ids[t];
+        const bool l_ok = l >= -1 && l < a.L;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < a.k; j++) {
+            const int p = t * a.k + j;
+            const int e = a.topk_ids[p];
+            if (l_ok && e >= 0 && e < a.E) {
+                const float4 v = reinterpret_cast<const float4*>(a.pair_out + (size_t)p * a.H)[h4];
+                s.x += v.x;
+                s.y += v.y;
+                s.z += v.z;
+                s.w += v.w;
+            }
+        }
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
+        o.y = (uint32_t)f32_to_bf16_rne(s.z) | ((uint32_t)f32_to_bf16_rne(s.w) << 16);
+        reinterpret_cast<uint2*>(a.out + (size_t)t * a.H)[h4] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reduce(const ReduceArgs& args, int grid, cudaStream_t stream, bool pdl) {
+    return launch_k(k_reduce, dim3(grid), dim3(256), 0, stream, pdl, args);
+}
+
+}  // namespace moelora

@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads and exports every declared symbol; its
+host-only entry points answer without a GPU (CPU only, no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lora_moe_layer_gb300 import binding as B
+from lora_moe_layer_gb300 import build as build_mod
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_lora.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MOELORA_API\s+[\w\s\*]+?\b(moe_lora_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert declared_symbols() == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(B.library_path())
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+
+
+def test_strerror_and_version(lib):
+    for code in (0, -1, -2, -3, -4, -5, 99):
+        assert isinstance(B.moe_lora_strerror(code), str) and B.moe_lora_strerror(code)
+    assert B.moe_lora_version() >= 100
+
+
+def test_align_capacity_formula(lib):
+    for (T, k, E, L, bm) in [(16, 4, 32, 8, 16), (2048, 4, 32, 8, 128), (1, 1, 1, 0, 1), (256, 8, 128, 16, 8)]:
+        d = B.dims(T, 64, 64, E, k, L, 8, bm)
+        P, NB = T * k, E * (L + 1)
+        assert B.moe_lora_align_capacity(d) == P + min(NB, P) * (bm - 1)
+
+
+def test_workspace_bytes_and_layout(lib):
+    d = B.dims(16, 2880, 2880, 32, 4, 8, 32)
+    n = B.moe_lora_workspace_bytes(d)
+    lay = B.moe_lora_workspace_layout(d)
+    assert n == lay["total"] > 0
+    P = 64
+    assert lay["s1"] == -(-2880 // 512) and lay["s2"] == -(-2880 // 512)
+    # regions are disjoint and inside the workspace
+    regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * lay["s1"] * P * 32),
+                      (lay["act"], 2 * P * 2880), (lay["z2"], 4 * lay["s2"] * P * 32),
+                      (lay["pair_out"], 4 * P * 2880)])
+    for (a, na), (b, _) in zip(regions, regions[1:]):
+        assert a + na <= b
+    assert regions[-1][0] + regions[-1][1] <= n
+    assert all(off % 256 == 0 for off, _ in regions)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(H=0), dict(E=0), dict(k=0), dict(T=-1), dict(L=-1), dict(block_m=3), dict(block_m=512),
+])
+def test_invalid_dims(lib, bad):
+    base = dict(T=4, H=64, I=64, E=4, k=2, L=2, r=8, block_m=0)
+    base.update(bad)
+    d = B.moe_lora_dims(*[base[n] for n in ("T", "H", "I", "E", "k", "L", "r", "block_m")])
+    assert B.moe_lora_workspace_bytes(d) == 0
+    assert B.moe_lora_align_capacity(d) == B.MOELORA_EINVAL
+
+
+@pytest.mark.parametrize("bad", [dict(H=60), dict(I=12), dict(r=12), dict(r=72)])
+def test_unsupported_dims(lib, bad):
+    base = dict(T=4, H=64, I=64, E=4, k=2, L=2, r=8, block_m=0)
+    base.update(bad)
+    d = B.moe_lora_dims(*[base[n] for n in ("T", "H", "I", "E", "k", "L", "r", "block_m")])
+    assert B.moe_lora_align_capacity(d) == B.MOELORA_EUNSUPPORTED
+
+
+def test_host_checks_return_before_any_launch(lib):
+    """Null pointers, a short workspace and misalignment are refused on the host
+    (fake addresses below are never dereferenced)."""
+    d = B.dims(4, 64, 64, 4, 2, 2, 8)
+    need = B.moe_lora_workspace_bytes(d)
+    f = 1 << 20  # an aligned fake address
+    args = [f] * 12
+    # x .. B2, out, workspace
+    def fwd(ptrs, wb):
+        return B.load().moe_lora_forward(ctypes.byref(d), *ptrs, wb, None)
+    assert fwd([f] * 5 + [None] + [f] * 6, need) == B.MOELORA_EINVAL          # W1 null
+    assert fwd([f] * 7 + [None] + [f] * 4, need) == B.MOELORA_EINVAL          # A1 null with L > 0
+    assert fwd(args, need - 1) == B.MOELORA_ENOSPC
+    assert fwd([f + 8] + [f] * 11, need) == B.MOELORA_EUNSUPPORTED            # misaligned x
+    assert B.load().moe_lora_align(ctypes.byref(d), f, f, None, f, f, f, f, f, f, need, None) == B.MOELORA_EINVAL
+    assert B.load().moe_lora_align(ctypes.byref(d), f, f, f, f, f, f, f, f, f, need - 1, None) == B.MOELORA_ENOSPC
+    assert B.load().moe_lora_get_status(None, None) == B.MOELORA_EINVAL
+
+
+def test_no_device_is_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    d = B.dims(4, 64, 64, 4, 2, 0, 0)
+    f = 1 << 20
+    st = B.load().moe_lora_forward(ctypes.byref(d), f, f, f, f, f, f, None, None, None, None, f, f,
+                                   B.moe_lora_workspace_bytes(d), None)
+    assert st == B.MOELORA_ECUDA

@@ -1,0 +1,260 @@
+"""moe_lora_forward on the GPU against the fp64 oracle.
+
+Bar: max|gpu - ref| / max|ref| <= 1e-2 on the layer output (bf16 I/O, fp32
+accumulation), per-kernel intermediates against the oracle's, and the exact
+invariants that hold for the GPU arithmetic too (zero B, weight scaling by 2,
+determinism, block_m independence, adapter swap).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lora_moe_layer_gb300 import binding as B
+from lora_moe_layer_gb300 import workloads as wl
+from lora_moe_layer_gb300.layer import DeviceLayer
+
+from gpu_helpers import TOL, norm_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run(layer, block_m=0):
+    dl = DeviceLayer(layer, "cuda", block_m=block_m)
+    B.check(dl.forward(), "moe_lora_forward")
+    st = dl.status()
+    return dl, st
+
+
+def check_layer(layer, tokens=None, block_m=0, tol=TOL):
+    dl, st = run(layer, block_m)
+    assert st == 0
+    got = dl.out_f64()
+    ref, inv = oracle.forward(layer, tokens=tokens)
+    assert inv == 0
+    sel = got if tokens is None else got[np.asarray(tokens)]
+    err = norm_err(sel, ref)
+    assert err <= tol, err
+    return dl, err
+
+
+# ------------------------------------------------------------------ small cases
+
+RAGGED = [
+    # T, H, I, E, k, L, r   -- H, I not multiples of the 256-element step; units not multiples of a CTA block
+    (37, 264, 136, 5, 3, 3, 24),
+    (9, 520, 200, 7, 2, 2, 64),
+    (64, 128, 72, 3, 2, 4, 8),
+    (5, 96, 1032, 4, 4, 1, 16),
+    (40, 256, 512, 9, 1, 0, 0),
+    (1, 64, 64, 2, 1, 1, 8),
+    (130, 200, 48, 1, 1, 3, 32),
+]
+
+
+@pytest.mark.parametrize("shape", RAGGED)
+def test_ragged_shapes(shape):
+    layer = wl.make_random(*shape, seed=7)
+    check_layer(layer)
+
+
+def test_config0():
+    check_layer(wl.make_config(0))
+
+
+@pytest.mark.parametrize("bm", [1, 8, 64, 128])
+def test_block_m_does_not_change_the_result(bm):
+    layer = wl.make_config(0)
+    a, _ = run(layer, 16)
+    b, _ = run(layer, bm)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_intermediates_config0():
+    layer = wl.make_config(0)
+    dl, st = run(layer)
+    assert st == 0
+    lay = B.moe_lora_workspace_layout(dl.d)
+    P, r, I, H = layer.P, layer.r, layer.I, layer.H
+    rows = dl.workspace_view("compact_ids", torch.int32, (P,)).cpu().numpy()
+    z1 = dl.workspace_view("z1", torch.float32, (lay["s1"], P, r)).sum(0).cpu().numpy().astype(np.float64)
+    act_bits = dl.workspace_view("act", torch.int16, (P, I)).cpu().numpy().view(np.uint16)
+    act = (act_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    pair_out = dl.workspace_view("pair_out", torch.float32, (P, H)).cpu().numpy().astype(np.float64)
+    for row, p in enumerate(rows):
+        ref = oracle.pair(layer, int(p))
+        t = p // layer.k
+        if layer.lora_ids[t] >= 0:
+            assert norm_err(z1[row], ref["z1"]) < 1e-5
+        assert norm_err(act[row], ref["act"]) < 8e-3
+        w = float(layer.topk_weights.flat[p])
+        assert norm_err(pair_out[p], w * ref["d"]) < 1e-2
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_zero_B_bit_identical_to_base_only():
+    layer = wl.make_config(0)
+    zb = dataclasses.replace(layer, B1=np.zeros_like(layer.B1), B2=np.zeros_like(layer.B2))
+    base = dataclasses.replace(layer, lora_ids=np.full_like(layer.lora_ids, -1))
+    a, _ = run(zb)
+    b, _ = run(base)
+    assert torch.equal(a.out.view(torch.int16), b.out.view(torch.int16))
+
+
+def test_base_only_tokens_match_a_layer_without_adapters():
+    layer = wl.make_config(0)
+    a, _ = run(layer)
+    nolora = dataclasses.replace(layer, L=0, r=0, A1=None, B1=None, A2=None, B2=None,
+                                 lora_ids=np.full_like(layer.lora_ids, -1))
+    b, _ = run(nolora)
+    m = torch.from_numpy(layer.lora_ids == -1).cuda()
+    assert torch.equal(a.out[m].view(torch.int16), b.out[m].view(torch.int16))
+
+
+def test_weights_times_two_doubles_output_exactly():
+    layer = wl.make_config(0)
+    a, _ = run(layer)
+    b, _ = run(dataclasses.replace(layer, topk_weights=layer.topk_weights * 2))
+    assert torch.equal(b.out.float(), 2 * a.out.float())
+
+
+def test_deterministic():
+    layer = wl.make_config(0)
+    dl, _ = run(layer)
+    first = dl.out.clone()
+    for _ in range(3):
+        B.check(dl.forward())
+        assert torch.equal(first.view(torch.int16), dl.out.view(torch.int16))
+
+
+def test_adapter_swap_swaps_outputs():
+    layer = wl.make_random(6, 64, 32, 3, 2, 2, 8, seed=21)
+    x, tk, tw, lo = layer.x.copy(), layer.topk_ids.copy(), layer.topk_weights.copy(), layer.lora_ids.copy()
+    x[1], tk[1], tw[1] = x[0], tk[0], tw[0]
+    lo[0], lo[1] = 0, 1
+    a, _ = run(dataclasses.replace(layer, x=x, topk_ids=tk, topk_weights=tw, lora_ids=lo))
+    lo2 = lo.copy()
+    lo2[0], lo2[1] = 1, 0
+    b, _ = run(dataclasses.replace(layer, x=x, topk_ids=tk, topk_weights=tw, lora_ids=lo2))
+    assert torch.equal(a.out[0].view(torch.int16), b.out[1].view(torch.int16))
+    assert torch.equal(a.out[1].view(torch.int16), b.out[0].view(torch.int16))
+
+
+def test_lora_delta_matches_oracle_delta():
+    """The adapter delta alone (forward minus the zero-B forward) against the
+    oracle's delta: a broken expand could hide under the 1e-2 output bar."""
+    layer = wl.make_config(0)
+    zb = dataclasses.replace(layer, B1=np.zeros_like(layer.B1), B2=np.zeros_like(layer.B2))
+    a, _ = run(layer)
+    b, _ = run(zb)
+    d_gpu = a.out_f64() - b.out_f64()
+    r1, _ = oracle.forward(layer)
+    r0, _ = oracle.forward(zb)
+    d_ref = r1 - r0
+    assert np.max(np.abs(d_ref)) > 0
+    assert norm_err(d_gpu, d_ref) < 5e-2
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_out_of_range_ids_are_flagged_and_left_out():
+    layer = wl.make_config(0)
+    tk = layer.topk_ids.copy()
+    tk[2, 1] = layer.E
+    tk[5, 0] = -2
+    lo = layer.lora_ids.copy()
+    lo[7] = layer.L
+    bad = dataclasses.replace(layer, topk_ids=tk, lora_ids=lo)
+    dl, st = run(bad)
+    assert st == B.MOELORA_EDEVICE_ID
+    ref, inv = oracle.forward(bad)
+    assert inv == 2 + layer.k
+    got = dl.out_f64()
+    assert norm_err(got, ref) <= TOL
+    assert np.all(got[7] == 0)
+    # the next clean forward on the same workspace reports OK again
+    dl.set_batch(layer.x, layer.topk_ids, layer.topk_weights, layer.lora_ids)
+    B.check(dl.forward())
+    assert dl.status() == 0
+
+
+def test_all_pairs_on_one_expert_and_all_base_only():
+    layer = wl.make_random(50, 128, 64, 6, 3, 2, 16, seed=4)
+    tk = np.tile(np.array([[5, 2, 0]], np.int32), (50, 1))
+    check_layer(dataclasses.replace(layer, topk_ids=tk))
+    check_layer(dataclasses.replace(layer, lora_ids=np.full(50, -1, np.int32)))
+
+
+def test_no_adapters_null_pointers():
+    layer = wl.make_random(12, 64, 64, 4, 2, 0, 0, seed=2)
+    assert layer.A1 is None
+    check_layer(layer)
+
+
+def test_empty_batch_is_ok():
+    layer = wl.make_random(3, 64, 64, 4, 2, 1, 8, seed=2)
+    dl = DeviceLayer(layer, "cuda")
+    d0 = B.dims(0, 64, 64, 4, 2, 1, 8)
+    ws = torch.empty(B.moe_lora_workspace_bytes(d0), dtype=torch.uint8, device="cuda")
+    st = B.moe_lora_forward(d0, None, None, None, None, dl.W1, dl.W2, dl.A1, dl.B1, dl.A2, dl.B2, None, ws)
+    assert st == 0 and B.moe_lora_get_status(ws) == 0
+
+
+def test_output_guard_bytes_untouched():
+    layer = wl.make_config(0)
+    dl = DeviceLayer(layer, "cuda")
+    buf = torch.full((layer.T * layer.H + 64,), 7, dtype=torch.int16, device="cuda")
+    out = buf[:layer.T * layer.H].view(torch.bfloat16).view(layer.T, layer.H)
+    B.check(dl.forward(out=out))
+    torch.cuda.synchronize()
+    assert (buf[layer.T * layer.H:] == 7).all()
+
+
+# ------------------------------------------------------------------ named workloads at full size
+
+@pytest.fixture(scope="module")
+def config1():
+    return wl.make_config(1)
+
+
+def test_config1_decode_full(config1):
+    check_layer(config1)
+
+
+def test_intermediates_config1(config1):
+    dl, st = run(config1)
+    lay = B.moe_lora_workspace_layout(dl.d)
+    P, r, I = config1.P, config1.r, config1.I
+    rows = dl.workspace_view("compact_ids", torch.int32, (P,)).cpu().numpy()
+    z1 = dl.workspace_view("z1", torch.float32, (lay["s1"], P, r)).sum(0).cpu().numpy()
+    z2 = dl.workspace_view("z2", torch.float32, (lay["s2"], P, r)).sum(0).cpu().numpy()
+    for row in range(0, P, 7):
+        ref = oracle.pair(config1, int(rows[row]))
+        assert norm_err(z1[row].astype(np.float64), ref["z1"]) < 1e-5
+        assert norm_err(z2[row].astype(np.float64), ref["z2"]) < 1e-2
+
+
+@pytest.mark.slow
+def test_config2_prefill_sampled():
+    layer = wl.make_config(2)
+    # two tokens of every 128-token sequence, first and last
+    tokens = sorted({s * 128 + o for s in range(16) for o in (0, 127)})
+    check_layer(layer, tokens=tokens)
+
+
+@pytest.mark.slow
+def test_config3_mixed_full():
+    layer = wl.make_config(3)
+    assert 0.45 <= layer.meta["hot_share"] <= 0.55
+    check_layer(layer)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("T", [1, 16, 256])
+def test_config4_dense(T):
+    layer = wl.make_config(4, T=T)
+    tokens = None if T <= 16 else list(range(0, T, 32))
+    check_layer(layer, tokens=tokens)
