@@ -81,7 +81,8 @@ def test_out_of_range_ids_flagged_and_left_out():
     topk = np.array([[0, 5], [1, -1], [1, 0], [2, 2]], np.int32)
     lora = np.array([0, 0, 7, -1], np.int32)
     status, ref = _compare(topk, lora, 3, 1, 2)
-    assert status == -5 and ref["invalid"] == 5
+    # t0 slot 1, t1 slot 1, and both slots of t2 (adapter 7 of 1)
+    assert status == -5 and ref["invalid"] == 4
 
 
 def test_status_resets_on_next_call():
