@@ -143,6 +143,28 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * moe_lora_forward with timing marks, for profiling the kernels one by one on
+ * the stream they run on.  kernel_events holds MOELORA_TRACE_EVENTS
+ * cudaEvent_t handles created by the caller (cudaEventCreate); event i is
+ * recorded on `stream` just before kernel slot i and the last one after the
+ * final kernel.  Kernel slots: 0 align, 1 gate_up shrink, 2 gate_up GEMV
+ * (+expand, SiLU*up), 3 down shrink, 4 down GEMV (+expand, x weight),
+ * 5 top-k reduce; a slot that has no kernel (no adapters) gets an empty
+ * interval.  The recorded events replace the programmatic launch overlap
+ * between consecutive kernels with plain stream order.  Same results and
+ * status codes as moe_lora_forward, plus MOELORA_EINVAL if kernel_events is
+ * NULL or n_events < MOELORA_TRACE_EVENTS.
+ */
+#define MOELORA_TRACE_EVENTS 7
+MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
+                                        const int32_t *topk_ids, const float *topk_weights,
+                                        const int32_t *token_lora_ids, const void *W1,
+                                        const void *W2, const void *A1, const void *B1,
+                                        const void *A2, const void *B2, void *out,
+                                        void *workspace, size_t workspace_bytes, void *stream,
+                                        void *const *kernel_events, int32_t n_events);
+
+/*
  * Waits for `stream`, then returns MOELORA_OK if the last align/forward that
  * used this workspace met no out-of-range id, MOELORA_EDEVICE_ID if it did,
  * or MOELORA_ECUDA if a CUDA call failed.  The only synchronising entry point.

@@ -25,7 +25,10 @@ MOELORA_EDEVICE_ID = -5
 # every symbol the header declares
 EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_workspace_bytes", "moe_lora_align", "moe_lora_forward",
-            "moe_lora_get_status", "moe_lora_workspace_layout")
+            "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced")
+MOELORA_TRACE_EVENTS = 7
+# kernel slots of one forward, in launch order
+KERNEL_SLOTS = ("align", "gate_up_shrink", "gate_up_gemv", "down_shrink", "down_gemv", "topk_reduce")
 
 
 class MoeLoraError(RuntimeError):
@@ -76,6 +79,8 @@ def load(path: Optional[str] = None):
     lib.moe_lora_align.argtypes = [D, V, V, V, V, V, V, V, V, V, SZ, V]
     lib.moe_lora_forward.restype = I32
     lib.moe_lora_forward.argtypes = [D] + [V] * 12 + [SZ, V]
+    lib.moe_lora_forward_traced.restype = I32
+    lib.moe_lora_forward_traced.argtypes = [D] + [V] * 12 + [SZ, V, ctypes.POINTER(V), ctypes.c_int32]
     lib.moe_lora_get_status.restype = I32
     lib.moe_lora_get_status.argtypes = [V, V]
     lib.moe_lora_workspace_layout.restype = I32
@@ -155,6 +160,26 @@ def moe_lora_forward(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids
     return load().moe_lora_forward(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                    _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
                                    _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb, _stream(stream))
+
+
+def moe_lora_forward_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2,
+                            B2, out, workspace, events, stream=None,
+                            workspace_bytes: Optional[int] = None) -> int:
+    """events: MOELORA_TRACE_EVENTS torch.cuda.Event objects (or raw cudaEvent_t ints)."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    handles = []
+    for ev in events:
+        if isinstance(ev, int):
+            handles.append(ev)
+        else:
+            if ev.cuda_event == 0:  # torch creates the event lazily
+                ev.record()
+            handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    return load().moe_lora_forward_traced(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                          _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
+                                          _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb,
+                                          _stream(stream), arr, len(handles))
 
 
 def moe_lora_get_status(workspace, stream=None) -> int:

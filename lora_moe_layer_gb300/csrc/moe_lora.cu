@@ -229,11 +229,27 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
     return e == cudaSuccess ? MOELORA_OK : MOELORA_ECUDA;
 }
 
-MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
-                                 const float* topk_weights, const int32_t* token_lora_ids,
-                                 const void* W1, const void* W2, const void* A1, const void* B1,
-                                 const void* A2, const void* B2, void* out, void* workspace,
-                                 size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Records event i (if given) just before kernel slot i of the forward; slot
+// 6 is after the last kernel.  Skipped kernels still get their event.
+struct Tracer {
+    void* const* ev;
+    int n;
+    cudaStream_t s;
+    bool ok = true;
+    void mark(int i) {
+        if (ev && i < n && ev[i] && cudaEventRecord((cudaEvent_t)ev[i], s) != cudaSuccess) ok = false;
+    }
+};
+
+int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
+                 const float* topk_weights, const int32_t* token_lora_ids, const void* W1,
+                 const void* W2, const void* A1, const void* B1, const void* A2, const void* B2,
+                 void* out, void* workspace, size_t workspace_bytes, void* stream,
+                 void* const* events, int n_events) {
     Layout L;
     int st = make_layout(d, &L);
     if (st != MOELORA_OK) return st;
@@ -253,15 +269,21 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
     // NULL stream gets plain stream order
     const bool pdl = s != nullptr && s != cudaStreamLegacy;
 
+    Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
+    tr.mark(0);
     if (launch_align(aa, align_hist_smem_bytes(d->E, d->L), s) != cudaSuccess) return MOELORA_ECUDA;
-    if (d->T == 0) return MOELORA_OK;
+    if (d->T == 0) {
+        for (int i = 1; i <= 6; i++) tr.mark(i);
+        return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
+    }
 
     const WsHeader* hdr = at<WsHeader>(ws, L.hdr);
     const int sms = dev->sms;
     const long lora_buckets_max = std::min<long>((long)d->E * d->L, L.P);
 
     ShrinkArgs sh = {};
+    tr.mark(1);
     if (has_lora) {
         sh.E = d->E; sh.L = d->L; sh.k = d->k; sh.r = d->r; sh.K = d->H; sh.P = (int)L.P;
         sh.S = L.s1;
@@ -299,6 +321,7 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
     g.zpart = has_lora ? at<float>(ws, L.z1) : nullptr;
     g.S = L.s1;
     g.kc = L.kc_gu;
+    tr.mark(2);
     {
         const long per_cta = (kGemvThreads / 32) * (kGemvRows / 2);
         g.max_tasks = (int)std::min<long>(experts_max * ((d->I + per_cta - 1) / per_cta), 1L << 30);
@@ -306,6 +329,7 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
         if (launch_gemv(g, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
+    tr.mark(3);
     if (has_lora) {
         sh.K = d->I;
         sh.S = L.s2;
@@ -326,6 +350,7 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
     g.zpart = has_lora ? at<float>(ws, L.z2) : nullptr;
     g.S = L.s2;
     g.kc = L.kc_dn;
+    tr.mark(4);
     {
         const long per_cta = (kGemvThreads / 32) * kGemvRows;
         g.max_tasks = (int)std::min<long>(experts_max * ((d->H + per_cta - 1) / per_cta), 1L << 30);
@@ -339,12 +364,39 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
     ra.topk_ids = topk_ids;
     ra.lora_ids = token_lora_ids;
     ra.out = static_cast<uint16_t*>(out);
+    tr.mark(5);
     {
         const long n = (long)d->T * (d->H / 4);
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_reduce(ra, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
-    return MOELORA_OK;
+    tr.mark(6);
+    return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
+                                 const float* topk_weights, const int32_t* token_lora_ids,
+                                 const void* W1, const void* W2, const void* A1, const void* B1,
+                                 const void* A2, const void* B2, void* out, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2, B2, out,
+                        workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+MOELORA_API int moe_lora_forward_traced(const moe_lora_dims* d, const void* x,
+                                        const int32_t* topk_ids, const float* topk_weights,
+                                        const int32_t* token_lora_ids, const void* W1,
+                                        const void* W2, const void* A1, const void* B1,
+                                        const void* A2, const void* B2, void* out, void* workspace,
+                                        size_t workspace_bytes, void* stream,
+                                        void* const* kernel_events, int32_t n_events) {
+    if (!kernel_events || n_events < MOELORA_TRACE_EVENTS) return MOELORA_EINVAL;
+    return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2, B2, out,
+                        workspace, workspace_bytes, stream, kernel_events, n_events);
 }
 
 MOELORA_API int moe_lora_get_status(const void* workspace, void* stream) {
