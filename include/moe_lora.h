@@ -172,6 +172,41 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
 MOELORA_API int moe_lora_get_status(const void *workspace, void *stream);
 
 /*
+ * moe_lora_forward for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it serves code that may not call
+ * cudaMalloc (which can wait for the whole device to go idle, so
+ * latency-bound loops avoid it), plugins whose host framework owns every
+ * device allocation and offers them none, or callers with no allocator at all.
+ *
+ * Same arguments, results and host-side status codes as moe_lora_forward,
+ * minus the workspace: the scratch is a buffer of
+ * MOELORA_NOALLOC_SCRATCH_BYTES (16 MiB) inside the library's device image,
+ * held by every GPU that loads the library until the process exits.  Nothing
+ * is allocated or freed by this call.
+ *   - Problems whose moe_lora_workspace_bytes(d) exceeds that size return
+ *     MOELORA_ENOSPC before anything is launched (e.g. the decode layer
+ *     T=16, H=I=2880, E=32, top-4, r=32 needs about 1.3 MiB).
+ *   - The first call on each device looks the buffer's device address up
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - All calls in the process share the one buffer per device, and each call
+ *     leaves its intermediates in it.  Calls whose work overlaps on the GPU
+ *     (two streams, or two host threads, of the same device) race on it:
+ *     order them on one stream or serialise them.  No part of the buffer has
+ *     to start at zero; every call rewrites what it reads.
+ *   - Out-of-range expert or adapter ids are still left out of the result, but
+ *     their status word lives in the shared buffer and is not reported; use
+ *     moe_lora_forward with a workspace where that status matters.
+ */
+#define MOELORA_NOALLOC_SCRATCH_BYTES (16u << 20)
+MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims *d, const void *x,
+                                         const int32_t *topk_ids, const float *topk_weights,
+                                         const int32_t *token_lora_ids, const void *W1,
+                                         const void *W2, const void *A1, const void *B1,
+                                         const void *A2, const void *B2, void *out,
+                                         void *stream);
+
+/*
  * Where the forward keeps its intermediates inside the workspace, for
  * diagnostics and per-kernel tests (byte offsets from the workspace start;
  * 0 bytes means absent).  Rows are the valid pairs in bucket order (the

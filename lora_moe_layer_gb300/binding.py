@@ -25,7 +25,9 @@ MOELORA_EDEVICE_ID = -5
 # every symbol the header declares
 EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_workspace_bytes", "moe_lora_align", "moe_lora_forward",
-            "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced")
+            "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced",
+            "moe_lora_forward_noalloc")
+MOELORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MOELORA_TRACE_EVENTS = 7
 # kernel slots of one forward, in launch order
 KERNEL_SLOTS = ("align", "gate_up_shrink", "gate_up_gemv", "down_shrink", "down_gemv", "topk_reduce")
@@ -81,6 +83,8 @@ def load(path: Optional[str] = None):
     lib.moe_lora_forward.argtypes = [D] + [V] * 12 + [SZ, V]
     lib.moe_lora_forward_traced.restype = I32
     lib.moe_lora_forward_traced.argtypes = [D] + [V] * 12 + [SZ, V, ctypes.POINTER(V), ctypes.c_int32]
+    lib.moe_lora_forward_noalloc.restype = I32
+    lib.moe_lora_forward_noalloc.argtypes = [D] + [V] * 12
     lib.moe_lora_get_status.restype = I32
     lib.moe_lora_get_status.argtypes = [V, V]
     lib.moe_lora_workspace_layout.restype = I32
@@ -180,6 +184,15 @@ def moe_lora_forward_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_l
                                           _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
                                           _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb,
                                           _stream(stream), arr, len(handles))
+
+
+def moe_lora_forward_noalloc(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2,
+                             B2, out, stream=None) -> int:
+    """moe_lora_forward on the library's built-in 16 MiB scratch buffer, for callers that
+    cannot allocate device memory (see include/moe_lora.h for the sharing rules)."""
+    return load().moe_lora_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                           _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
+                                           _ptr(A2), _ptr(B2), _ptr(out), _stream(stream))
 
 
 def moe_lora_get_status(workspace, stream=None) -> int:

@@ -399,6 +399,67 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims* d, const void* x,
                         workspace, workspace_bytes, stream, kernel_events, n_events);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward without any allocation.
+//
+// Some callers cannot obtain device memory for a workspace: code running where
+// cudaMalloc is off limits (it can block until the device is idle, so
+// latency-critical or real-time loops avoid it), plugins whose host framework
+// owns all device memory and exposes no allocator to them, or a caller with no
+// allocator of its own at all.  For them the forward can run on a scratch
+// buffer that lives inside this library: a file-scope array in device memory
+// of kNoAllocScratchBytes bytes, which every GPU that loads the library holds
+// until the process exits.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = MOELORA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device.  In host code the array's
+// name is only a host-side stand-in, so the address must come from the
+// runtime; it is looked up once per device, with that device current.
+void* g_noalloc_ptr[kMaxDevices];
+cudaError_t g_noalloc_err[kMaxDevices];
+std::once_flag g_noalloc_once[kMaxDevices];
+
+}  // namespace
+
+extern "C" {
+
+MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims* d, const void* x,
+                                         const int32_t* topk_ids, const float* topk_weights,
+                                         const int32_t* token_lora_ids, const void* W1,
+                                         const void* W2, const void* A1, const void* B1,
+                                         const void* A2, const void* B2, void* out,
+                                         void* stream) {
+    // host-side checks first, so a refused call touches no CUDA state
+    Layout L;
+    const int st = make_layout(d, &L);
+    if (st != MOELORA_OK) return st;
+    if (!W1 || !W2) return MOELORA_EINVAL;
+    if (d->T > 0 && (!x || !topk_ids || !topk_weights || !token_lora_ids || !out)) return MOELORA_EINVAL;
+    if (d->L > 0 && (!A1 || !B1 || !A2 || !B2)) return MOELORA_EINVAL;
+    if (L.total > kNoAllocScratchBytes) return MOELORA_ENOSPC;  // needs more than the built-in scratch
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOELORA_ECUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return MOELORA_EUNSUPPORTED;
+    std::call_once(g_noalloc_once[dev], [dev]() {
+        g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+    });
+    if (g_noalloc_err[dev] != cudaSuccess || g_noalloc_ptr[dev] == nullptr) return MOELORA_ECUDA;
+    // The forward overwrites every scratch byte it later reads (the status word
+    // and histograms are reset by its first kernel), so the previous call's
+    // leftovers need no clearing.
+    return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2, B2, out,
+                        g_noalloc_ptr[dev], kNoAllocScratchBytes, stream, nullptr, 0);
+}
+
 MOELORA_API int moe_lora_get_status(const void* workspace, void* stream) {
     if (!workspace) return MOELORA_EINVAL;
     int32_t status = 0;

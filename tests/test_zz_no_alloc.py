@@ -1,0 +1,53 @@
+"""moe_lora_forward_noalloc: the forward for callers that cannot allocate device
+memory (code that must not call cudaMalloc, plugins without access to their
+host's allocator), running on the library's own built-in scratch buffer.
+
+Checked through the C ABI against moe_lora_forward with a caller workspace, on
+two calls in a row with different problems (the second call reuses the buffer
+the first one left behind).  Collected last (file name) so that a stop at the
+first failure has already run every other test; it also passes alone.
+"""
+import numpy as np
+import pytest
+import torch
+
+from lora_moe_layer_gb300 import binding as B
+from lora_moe_layer_gb300 import workloads as wl
+from lora_moe_layer_gb300.layer import DeviceLayer
+
+from gpu_helpers import TOL, norm_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _noalloc(dl, out):
+    return B.moe_lora_forward_noalloc(dl.d, dl.x, dl.topk_ids, dl.topk_weights, dl.lora_ids, dl.W1, dl.W2,
+                                      dl.A1, dl.B1, dl.A2, dl.B2, out)
+
+
+def _bits_to_f64(t):
+    bits = t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def test_noalloc_matches_forward_on_two_calls_in_a_row():
+    layers = [wl.make_config(0), wl.make_random(37, 264, 136, 5, 3, 3, 24, seed=7)]
+    for layer in layers:  # call 1 and call 2 share the library's scratch buffer
+        dl = DeviceLayer(layer, "cuda")
+        B.check(dl.forward(), "moe_lora_forward")
+        ref = dl.out.clone()
+        out = torch.full_like(dl.out, float("nan"))
+        B.check(_noalloc(dl, out), "moe_lora_forward_noalloc")
+        torch.cuda.synchronize()
+        got, want = _bits_to_f64(out), _bits_to_f64(ref)
+        assert norm_err(got, want) <= TOL
+        # same kernels on the same inputs: the results agree bit for bit as well
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
+def test_noalloc_refuses_problems_larger_than_its_scratch():
+    d = B.dims(2048, 2880, 2880, 32, 4, 8, 32)
+    assert B.moe_lora_workspace_bytes(d) > B.MOELORA_NOALLOC_SCRATCH_BYTES
+    f = 1 << 20  # never dereferenced: the call returns before any launch
+    st = B.moe_lora_forward_noalloc(d, f, f, f, f, f, f, f, f, f, f, f)
+    assert st == B.MOELORA_ENOSPC
