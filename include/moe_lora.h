@@ -79,6 +79,7 @@ typedef struct moe_lora_dims {
 #define MOELORA_EUNSUPPORTED (-3)  /* valid but outside what the kernels handle (alignment, r > 64, ...) */
 #define MOELORA_ECUDA (-4)         /* a CUDA runtime call failed (e.g. no device) */
 #define MOELORA_EDEVICE_ID (-5)    /* the device met an out-of-range expert or adapter id */
+#define MOELORA_ETIMEOUT (-6)      /* a kernel gave up a bounded wait (its output is incomplete) */
 
 /* Human-readable message for a status code; never NULL. Host only. */
 MOELORA_API const char *moe_lora_strerror(int code);
@@ -147,15 +148,15 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
  * the stream they run on.  kernel_events holds MOELORA_TRACE_EVENTS
  * cudaEvent_t handles created by the caller (cudaEventCreate); event i is
  * recorded on `stream` just before kernel slot i and the last one after the
- * final kernel.  Kernel slots: 0 align, 1 gate_up shrink, 2 gate_up GEMV
- * (+expand, SiLU*up), 3 down shrink, 4 down GEMV (+expand, x weight),
- * 5 top-k reduce; a slot that has no kernel (no adapters) gets an empty
- * interval.  The recorded events replace the programmatic launch overlap
+ * final kernel.  Kernel slots: 0 align, 1 gather of x into bucket order,
+ * 2 gate_up LoRA shrink, 3 gate_up grouped GEMM (+expand, SiLU*up), 4 down
+ * LoRA shrink, 5 down grouped GEMM (+expand, x weight), 6 top-k reduce; a
+ * slot that has no kernel (no adapters) gets an empty interval.  The recorded events replace the programmatic launch overlap
  * between consecutive kernels with plain stream order.  Same results and
  * status codes as moe_lora_forward, plus MOELORA_EINVAL if kernel_events is
  * NULL or n_events < MOELORA_TRACE_EVENTS.
  */
-#define MOELORA_TRACE_EVENTS 7
+#define MOELORA_TRACE_EVENTS 8
 MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
                                         const int32_t *topk_ids, const float *topk_weights,
                                         const int32_t *token_lora_ids, const void *W1,
@@ -167,7 +168,10 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
 /*
  * Waits for `stream`, then returns MOELORA_OK if the last align/forward that
  * used this workspace met no out-of-range id, MOELORA_EDEVICE_ID if it did,
- * or MOELORA_ECUDA if a CUDA call failed.  The only synchronising entry point.
+ * MOELORA_ETIMEOUT if one of its kernels abandoned a bounded wait inside its
+ * copy pipeline (every wait in the library is bounded, so no kernel can spin
+ * forever; the output is then incomplete), or MOELORA_ECUDA if a CUDA call
+ * failed.  The only synchronising entry point.
  */
 MOELORA_API int moe_lora_get_status(const void *workspace, void *stream);
 
@@ -215,11 +219,11 @@ MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims *d, const void *x,
 typedef struct moe_lora_ws_layout {
     size_t compact_ids;      /* int32 [P]: pair id of each row */
     size_t compact_offset;   /* int32 [E*(L+1)+1]: first row of each bucket */
-    size_t z1;               /* float [S1][P][r]: gate_up shrink partials over S1 K-splits */
+    size_t z1;               /* float [P][r]: gate_up LoRA shrink A1 x per row (adapter rows only) */
     size_t act;              /* bf16 [P][I]: SiLU(gate)*up per row */
-    size_t z2;               /* float [S2][P][r]: down shrink partials over S2 K-splits */
+    size_t z2;               /* float [P][r]: down LoRA shrink A2 act per row (adapter rows only) */
     size_t pair_out;         /* float [P][H]: w * d per pair id p */
-    int32_t s1, s2;          /* K-split counts of the two shrinks */
+    int32_t s1, s2;          /* K-split counts the two shrinks used */
     size_t total;            /* == moe_lora_workspace_bytes */
 } moe_lora_ws_layout;
 

@@ -21,6 +21,7 @@ MOELORA_ENOSPC = -2
 MOELORA_EUNSUPPORTED = -3
 MOELORA_ECUDA = -4
 MOELORA_EDEVICE_ID = -5
+MOELORA_ETIMEOUT = -6
 
 # every symbol the header declares
 EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
@@ -28,9 +29,9 @@ EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced",
             "moe_lora_forward_noalloc")
 MOELORA_NOALLOC_SCRATCH_BYTES = 16 << 20
-MOELORA_TRACE_EVENTS = 7
+MOELORA_TRACE_EVENTS = 8
 # kernel slots of one forward, in launch order
-KERNEL_SLOTS = ("align", "gate_up_shrink", "gate_up_gemv", "down_shrink", "down_gemv", "topk_reduce")
+KERNEL_SLOTS = ("align", "gather_x", "gate_up_shrink", "gate_up_gemm", "down_shrink", "down_gemm", "topk_reduce")
 
 
 class MoeLoraError(RuntimeError):

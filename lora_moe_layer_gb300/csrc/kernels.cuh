@@ -1,6 +1,7 @@
 // kernels.cuh -- argument blocks and host launchers of the libmoelora kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,6 +29,8 @@ struct AlignArgs {
     int32_t* lora_buckets;     // [min(NB, P)]
     int32_t* scan_tmp;         // [max(E, NB) + 1]
     int* hist_global;          // [16 * NB] when the histogram does not fit in shared memory, else null
+    int* zero_ints;            // [n_zero] cleared for the kernels that follow (shrink counters), or null
+    int n_zero;
     WsHeader* hdr;
 };
 
@@ -49,7 +52,9 @@ struct ShrinkArgs {
     const int32_t* compact_offset;
     const int32_t* compact_ids;
     const WsHeader* hdr;
-    float* z;                   // [S][P][r]
+    float* z;                   // [S][P][r] split partials (scratch)
+    float* zfinal;              // [P][r] sum of the S partials, in split order
+    int* counters;              // [buckets] arrivals per bucket, zeroed by align
     int max_items;              // upper bound of buckets * S (host-known)
 };
 constexpr int kShrinkKC = 512;  // K elements per split
@@ -57,36 +62,38 @@ cudaError_t launch_shrink(const ShrinkArgs& args, int grid, cudaStream_t stream,
 cudaError_t init_shrink_attributes();
 int shrink_blocks_per_sm();
 
-// ----------------------------------------------------------------- gemv ----
-// Grouped GEMV over the active experts.  gate_up: act[row][i] =
-// SiLU(g_i) * g_{I+i} with g = W1[e] x + B1[l][e] z1.  down: pair_out[p][h]
-// = w_p * (W2[e] act[row] + B2[l][e] z2).
-struct GemvArgs {
+// ------------------------------------------------------------ tcgen05 GEMM ----
+// Grouped expert GEMM on the tensor cores (moe_gemm_tc.cu), weight rows on M.
+constexpr int kTcSmemLimit = 227 * 1024 - 1024;
+struct TcArgs {
+    CUtensorMap wmap;            // W1 as [E][2][I][H] (gate_up) or W2 [E][H][I]; box 64 (K) x 128 rows
+    CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16 rows
     int E, L, k, r, I, H, P;
-    int gate_up;                 // 1: gate_up (+ SiLU*mul), 0: down (+ weight)
-    const uint16_t* in;          // gate_up: x [T][H]; down: act [P][I]
-    const uint16_t* W;           // W1 [E][2I][H] or W2 [E][H][I]
-    const uint16_t* B;           // B1 [L][E][2I][r] or B2 [L][E][H][r] (null: no LoRA)
-    const float* zpart;          // [S][P][r] shrink partials (null: no LoRA)
-    int S;
-    const int32_t* lora_ids;     // [T]
-    const float* topk_weights;   // [T*k]
+    const uint16_t* B;           // B1 / B2 (null: no LoRA)
+    const float* z;              // final shrink output [P][r] (null: no LoRA)
+    const int32_t* lora_ids;
+    const float* topk_weights;
     const int32_t* active_experts;
     const int32_t* compact_offset;
     const int32_t* compact_ids;
-    const WsHeader* hdr;
-    uint16_t* act_out;           // gate_up output [P][I]
-    float* pair_out;             // down output [P][H] (indexed by pair id)
-    int kc;                      // K-chunk staged in shared memory
-    int max_tasks;
+    WsHeader* hdr;
+    uint16_t* act_out;           // gate_up: [P][I] bf16
+    float* pair_out;             // down: [P][H] fp32 by pair id
+    int nstages;
 };
-constexpr int kGemvThreads = 256;
-constexpr int kGemvMP = 8;       // pairs per pass
-constexpr int kGemvRows = 4;     // weight rows per warp
-int gemv_smem_bytes(int kc);
-cudaError_t launch_gemv(const GemvArgs& args, int grid, cudaStream_t stream, bool pdl);
-cudaError_t init_gemv_attributes();
-int gemv_blocks_per_sm(int smem_bytes);
+int tc_smem_bytes(bool gate_up, int bn, int nstages);
+int tc_plan_stages(bool gate_up, int bn);
+cudaError_t init_tc_attributes();
+cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl);
+
+struct GatherArgs {
+    int k, H;
+    const uint16_t* x;           // [T][H]
+    const int32_t* compact_ids;
+    const WsHeader* hdr;
+    uint16_t* out;               // [P][H] rows in bucket order
+};
+cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t stream, bool pdl);
 
 // --------------------------------------------------------------- reduce ----
 struct ReduceArgs {

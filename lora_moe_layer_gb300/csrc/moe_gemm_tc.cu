@@ -1,0 +1,393 @@
+// moe_gemm_tc.cu -- the grouped expert GEMMs on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), with the LoRA expand and the activation or
+// top-k weight in the epilogue.
+//
+// Layer math ("Efficiently serve dozens of fine-tuned models with vLLM on
+// Amazon SageMaker AI and Amazon Bedrock", section "Implementing multi-LoRA
+// inference for MoE models in vLLM", Figure 1), per routed pair:
+//   gate_up:  g = W1[e] x + B1[l][e] z1,  act = SiLU(g[0:I]) * g[I:2I]
+//   down:     d = W2[e] act + B2[l][e] z2, pair_out = w * d
+//
+// Operand order follows the swap-AB idea of the fused-MoE news item (its
+// first optimisation): the long weight dimension goes on the MMA's M side
+// (128 weight rows per task) and the expert's pairs on N (16..BN columns), so
+// a decode step with two or three pairs per expert still issues full-height
+// MMAs, and a prefill chunk fills N up to BN.  A task is (active expert,
+// 128-row weight tile, chunk of at most BN pairs).
+//
+// Warp roles (one CTA per SM, persistent over a contiguous task range):
+//   warp 0   TMA producer: per 64-wide K step, the weight tile (gate_up: the
+//            128 gate rows and the 128 matching up rows) and the pairs' rows
+//            (x or act in bucket order, 16-row boxes), all 128-byte swizzled,
+//            into a ring of shared-memory stages (full/empty mbarriers);
+//   warp 1   allocates TMEM; one thread issues tcgen05.mma (M=128, N=n_cols,
+//            K=16) into one of two TMEM accumulators (gate_up: a gate and an
+//            up accumulator, so a unit's gate and up values land in the same
+//            TMEM lane), and commits stage releases and accumulator
+//            completion to mbarriers;
+//   warps 2-5 epilogue: each thread owns one weight row (its TMEM lane), reads
+//            16 columns at a time, adds the LoRA expand B[l][e][row] . z[pair]
+//            on CUDA cores, and writes bf16 SiLU(gate)*up or fp32 w * d.
+// The two accumulators alternate, so one task's epilogue overlaps the next
+// task's MMAs.  Every wait is bounded (tma.cuh); on a timeout the CTA records
+// kStatusTimeout, drains its copies, frees TMEM and exits.
+#include "common.cuh"
+#include "kernels.cuh"
+#include "tc.cuh"
+
+namespace moelora {
+
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kBM = 128;                 // weight rows per task (MMA M)
+constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row
+constexpr int kATile = kBM * kBK * 2;    // 16 KiB
+constexpr int kBBoxRows = 16;
+constexpr int kBBox = kBBoxRows * kBK * 2;
+
+template <bool GATE_UP, int BN>
+struct TcShape {
+    static constexpr int kAB = GATE_UP ? 2 * kATile : kATile;  // weight bytes per stage
+    static constexpr int kStage = kAB + BN * kBK * 2;          // + pair rows
+    static constexpr int kAccCols = GATE_UP ? 2 * BN : BN;      // TMEM columns per accumulator set
+    static constexpr int kTmemCols = 2 * kAccCols <= 32 ? 32 : 2 * kAccCols;
+    static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM allocation");
+    static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
+};
+
+__device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
+
+// Walks the task sequence (active expert, weight tile, pair chunk) in order.
+template <int BN>
+struct TaskWalker {
+    int ai, mt, ch, e, q0, m_e, nch;
+    __device__ void load_expert(const TcArgs& a, int L1) {
+        e = a.active_experts[ai];
+        q0 = a.compact_offset[e * L1];
+        m_e = a.compact_offset[(e + 1) * L1] - q0;
+        nch = (m_e + BN - 1) / BN;
+    }
+    __device__ void seek(const TcArgs& a, int L1, int ntiles, int t, int n_active) {
+        int acc = 0;
+        for (ai = 0; ai < n_active; ai++) {
+            load_expert(a, L1);
+            const int cnt = ntiles * nch;
+            if (t < acc + cnt) {
+                const int loc = t - acc;
+                mt = loc / nch;
+                ch = loc % nch;
+                return;
+            }
+            acc += cnt;
+        }
+    }
+    __device__ void next(const TcArgs& a, int L1, int ntiles) {
+        if (++ch == nch) {
+            ch = 0;
+            if (++mt == ntiles) {
+                mt = 0;
+                ai++;
+                load_expert(a, L1);
+            }
+        }
+    }
+    __device__ int row0() const { return q0 + ch * BN; }              // first pair row of the chunk
+    __device__ int n_real() const { return min(BN, m_e - ch * BN); }
+    __device__ int n_cols() const { return (n_real() + 15) & ~15; }
+};
+
+// Epilogue state of one thread = one weight row of the tile: the row's LoRA B
+// (gate and up rows for gate_up) for the adapter of the current run of pairs.
+template <bool GATE_UP>
+struct EpiRow {
+    int e, w_row, cur_l;
+    bool row_ok;
+    size_t rows_per_expert;
+    uint4 bg[8], bu[8];  // r <= 64 bf16 each
+
+    __device__ void init(const TcArgs& a, int e_, int w_row_, bool row_ok_, size_t rpe) {
+        e = e_;
+        w_row = w_row_;
+        row_ok = row_ok_;
+        rows_per_expert = rpe;
+        cur_l = -2;
+    }
+
+    // one pair (compact row q) of this row: add the expand, apply the epilogue, store
+    __device__ __forceinline__ void column(const TcArgs& a, int q, float vg, float vu, bool has_lora) {
+        const int p = a.compact_ids[q];
+        const int l = a.lora_ids[p / a.k];
+        const int r = a.r;
+        if (has_lora && l >= 0 && row_ok) {
+            if (l != cur_l) {  // pairs come grouped by adapter: reload only at a run boundary
+                const size_t gbase = (((size_t)l * a.E + e) * rows_per_expert + w_row) * r;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    if (i * 8 < r) {
+                        bg[i] = ld_ro16(a.B + gbase + i * 8);
+                        if (GATE_UP) bu[i] = ld_ro16(a.B + gbase + (size_t)a.I * r + i * 8);
+                    }
+                }
+                cur_l = l;
+            }
+            const float* zq = a.z + (size_t)q * r;
+            float dg0 = 0.f, dg1 = 0.f, du0 = 0.f, du1 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if (i * 8 < r) {
+                    float zz[8];
+                    const float4 z0 = __ldcg(reinterpret_cast<const float4*>(zq + i * 8));
+                    const float4 z1 = __ldcg(reinterpret_cast<const float4*>(zq + i * 8 + 4));
+                    zz[0] = z0.x; zz[1] = z0.y; zz[2] = z0.z; zz[3] = z0.w;
+                    zz[4] = z1.x; zz[5] = z1.y; zz[6] = z1.z; zz[7] = z1.w;
+                    if (i & 1) dg1 = dot8(bg[i], zz, dg1);
+                    else dg0 = dot8(bg[i], zz, dg0);
+                    if (GATE_UP) {
+                        if (i & 1) du1 = dot8(bu[i], zz, du1);
+                        else du0 = dot8(bu[i], zz, du0);
+                    }
+                }
+            }
+            vg += dg0 + dg1;
+            vu += du0 + du1;
+        }
+        if (row_ok) {
+            if (GATE_UP)
+                a.act_out[(size_t)q * a.I + w_row] = f32_to_bf16_rne(silu_f(vg) * vu);
+            else
+                a.pair_out[(size_t)p * a.H + w_row] = a.topk_weights[p] * vg;
+        }
+    }
+};
+
+template <bool GATE_UP, int BN>
+__global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_constant__ TcArgs a) {
+    using S = TcShape<GATE_UP, BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int NS = a.nstages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)NS * S::kStage);
+    uint64_t* empty = full + NS;
+    uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
+    uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    __shared__ int s_total;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, S::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&a.wmap);
+        prefetch_tensormap(&a.xmap);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    pdl_wait();
+    pdl_trigger();
+
+    const int L1 = a.L + 1;
+    const int N_out = GATE_UP ? a.I : a.H;
+    const int K = GATE_UP ? a.H : a.I;
+    const int ntiles = (N_out + kBM - 1) / kBM;
+    const int nkb = (K + kBK - 1) / kBK;
+    const int n_active = a.hdr->n_active;
+    if (threadIdx.x == 0) {
+        int total = 0;
+        for (int ai = 0; ai < n_active; ai++) {
+            const int e = a.active_experts[ai];
+            const int m_e = a.compact_offset[(e + 1) * L1] - a.compact_offset[e * L1];
+            total += ntiles * ((m_e + BN - 1) / BN);
+        }
+        s_total = total;
+    }
+    __syncthreads();
+    const int total = s_total;
+    const int t_beg = (int)((long long)blockIdx.x * total / gridDim.x);
+    const int t_end = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
+    bool ok = true;
+
+    if (warp == 0) {
+        // -------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, last_par = 0;
+            TaskWalker<BN> tw;
+            if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
+            for (int t = t_beg; t < t_end && ok; t++) {
+                const int n_cols = tw.n_cols(), row0 = tw.row0(), e = tw.e;
+                const uint32_t bytes = S::kAB + (uint32_t)n_cols * kBK * 2;
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    uint8_t* dst = base + (size_t)stage * S::kStage;
+                    const int k0 = kb * kBK;
+                    if (GATE_UP) {
+                        tma_load_4d(dst, &a.wmap, &full[stage], k0, tw.mt * kBM, 0, e);
+                        tma_load_4d(dst + kATile, &a.wmap, &full[stage], k0, tw.mt * kBM, 1, e);
+                    } else {
+                        tma_load_3d(dst, &a.wmap, &full[stage], k0, tw.mt * kBM, e);
+                    }
+                    for (int g = 0; g < n_cols / kBBoxRows; g++)
+                        tma_load_2d(dst + S::kAB + g * kBBox, &a.xmap, &full[stage], k0, row0 + g * kBBoxRows);
+                    armed |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+                if (t + 1 < t_end) tw.next(a, L1, ntiles);
+            }
+            // every issued copy lands before the CTA may exit
+            for (int s = 0; s < NS; s++)
+                if ((armed >> s) & 1u) mbar_wait(&full[s], (last_par >> s) & 1u);
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            TaskWalker<BN> tw;
+            if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
+            for (int t = t_beg, it = 0; t < t_end && ok; t++, it++) {
+                const int b = it & 1;
+                if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
+                const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols());
+                for (int kb = 0; kb < nkb; kb++) {
+                    if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
+                    const uint32_t b_addr = a_addr + S::kAB;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; kk++) {
+                        const uint64_t bdesc = umma_desc_sw128(b_addr + kk * 32);
+                        const uint32_t acc = (kb | kk) != 0;
+                        umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
+                        if (GATE_UP)
+                            umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, acc);
+                    }
+                    umma_commit(&empty[stage]);  // stage reusable once these MMAs are done
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                umma_commit(&tfull[b]);          // accumulator complete
+                if (t + 1 < t_end) tw.next(a, L1, ntiles);
+            }
+        }
+    } else {
+        // -------------------------------------------------------------- epilogue
+        const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int row = qd * 32 + lane;          // weight row within the tile
+        const bool has_lora = a.B != nullptr && a.z != nullptr;
+        const size_t rows_per_expert = GATE_UP ? 2 * (size_t)a.I : (size_t)a.H;
+        TaskWalker<BN> tw;
+        if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
+        for (int t = t_beg, it = 0; t < t_end && ok; t++, it++) {
+            const int b = it & 1;
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) { ok = false; break; }
+            tc_fence_after();
+            const int e = tw.e, q0c = tw.row0(), n_real = tw.n_real(), n_cols = tw.n_cols();
+            const int w_row = tw.mt * kBM + row;
+            const bool row_ok = w_row < N_out;
+            const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * S::kAccCols);
+            EpiRow<GATE_UP> er;
+            er.init(a, e, w_row, row_ok, rows_per_expert);
+            for (int c0 = 0; c0 < n_cols; c0 += 16) {
+                float g[16], u[16];
+                tmem_ld16(t_lane + c0, g);
+                if (GATE_UP) tmem_ld16(t_lane + BN + c0, u);
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    if (c0 + c < n_real) er.column(a, q0c + c0 + c, g[c], GATE_UP ? u[c] : 0.f, has_lora);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            if (t + 1 < t_end) tw.next(a, L1, ntiles);
+        }
+    }
+
+    if (!ok) atomicOr(&a.hdr->status, kStatusTimeout);
+    // all roles done (every wait above is bounded): release TMEM
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, S::kTmemCols);
+}
+
+template <bool G, int BN>
+cudaError_t set_attr() {
+    return cudaFuncSetAttribute(k_moe_gemm_tc<G, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kTcSmemLimit);
+}
+
+// ---------------------------------------------------------------- gather
+// rows of x in bucket (compact) order, the B operand of the gate_up GEMM
+__global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const int n = a.hdr->n_valid;
+    const int c8 = a.H >> 3;
+    const long total = (long)n * c8;
+    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+        const int q = (int)(idx / c8), c = (int)(idx % c8);
+        const int t = a.compact_ids[q] / a.k;
+        *reinterpret_cast<uint4*>(a.out + (size_t)q * a.H + c * 8) = ld_ro16(a.x + (size_t)t * a.H + c * 8);
+    }
+}
+
+}  // namespace
+
+int tc_smem_bytes(bool gate_up, int bn, int nstages) {
+    const int ab = gate_up ? 2 * kATile : kATile;
+    const int stage = ab + bn * kBK * 2;
+    return 1024 + nstages * stage + (2 * nstages + 4) * 8 + 16;
+}
+
+int tc_plan_stages(bool gate_up, int bn) {
+    for (int ns = 8; ns >= 2; ns--)
+        if (tc_smem_bytes(gate_up, bn, ns) <= kTcSmemLimit) return ns;
+    return 0;
+}
+
+cudaError_t init_tc_attributes() {
+    cudaError_t e;
+    if ((e = set_attr<true, 64>()) != cudaSuccess) return e;
+    if ((e = set_attr<true, 128>()) != cudaSuccess) return e;
+    if ((e = set_attr<false, 64>()) != cudaSuccess) return e;
+    return set_attr<false, 256>();
+}
+
+cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl) {
+    const int smem = tc_smem_bytes(gate_up, bn, args.nstages);
+    const dim3 g(grid), b(kTcThreads);
+    if (gate_up) {
+        if (bn == 64) return launch_k(k_moe_gemm_tc<true, 64>, g, b, smem, stream, pdl, args);
+        return launch_k(k_moe_gemm_tc<true, 128>, g, b, smem, stream, pdl, args);
+    }
+    if (bn == 64) return launch_k(k_moe_gemm_tc<false, 64>, g, b, smem, stream, pdl, args);
+    return launch_k(k_moe_gemm_tc<false, 256>, g, b, smem, stream, pdl, args);
+}
+
+cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t stream, bool pdl) {
+    return launch_k(k_gather_rows, dim3(grid), dim3(256), 0, stream, pdl, args);
+}
+
+}  // namespace moelora

@@ -2,23 +2,28 @@
 // argument validation, workspace layout, per-device kernel set-up and the
 // launch sequence of one forward.
 //
-// One forward is six kernels on the caller's stream, chained with
+// One forward is seven kernels on the caller's stream, chained with
 // programmatic dependent launch so each can be resident before its
 // predecessor drains (the blog's PDL step, "Efficiently serve dozens of
 // fine-tuned models with vLLM ...", section "Execution optimizations"):
-//   align -> [gate_up shrink] -> gate_up GEMV (+expand, SiLU*up)
-//         -> [down shrink] -> down GEMV (+expand, x weight) -> top-k reduce.
+//   align -> gather x into bucket order -> [gate_up shrink]
+//         -> gate_up tcgen05 GEMM (+expand, SiLU*up) -> [down shrink]
+//         -> down tcgen05 GEMM (+expand, x weight) -> top-k reduce.
 // The shrinks are skipped when the layer has no adapters, and exit at once
 // when no token of the batch uses one (the blog's early exit, same section).
 // Nothing here allocates device memory or synchronises the host.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "kernels.cuh"
 #include "moe_lora.h"
+#include "tma.cuh"
 
 namespace moelora {
 namespace {
@@ -29,9 +34,11 @@ constexpr int kMaxDevices = 64;
 struct Layout {
     int bm;
     long P, NB, cap, tiles;
-    int s1, s2, kc_gu, kc_dn;
+    int s1, s2;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
-        compact_ids, active_experts, lora_buckets, scan_tmp, hist, z1, act, z2, pair_out, total;
+        compact_ids, active_experts, lora_buckets, scan_tmp, hist, counters, z1, z1f, xc, act, z2, z2f,
+        pair_out, total;
+    long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -70,8 +77,6 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     const int r = d->L > 0 ? d->r : 0;
     L->s1 = d->L > 0 ? (d->H + kShrinkKC - 1) / kShrinkKC : 0;
     L->s2 = d->L > 0 ? (d->I + kShrinkKC - 1) / kShrinkKC : 0;
-    L->kc_gu = std::min(d->H, 4096);
-    L->kc_dn = std::min(d->I, 4096);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
     L->hdr = take(sizeof(WsHeader));
@@ -86,9 +91,14 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
+    L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
+    L->counters = take(sizeof(int32_t) * 2 * L->nbl);
     L->z1 = take(sizeof(float) * (size_t)L->s1 * L->P * r);
+    L->z1f = take(sizeof(float) * (size_t)L->P * r);
+    L->xc = take(sizeof(uint16_t) * (size_t)L->P * d->H);
     L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
     L->z2 = take(sizeof(float) * (size_t)L->s2 * L->P * r);
+    L->z2f = take(sizeof(float) * (size_t)L->P * r);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
     L->total = o;
     return MOELORA_OK;
@@ -96,8 +106,6 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
 
 struct DeviceInfo {
     int sms = 0;
-    int gemv_bps_cache_smem = -1;
-    int gemv_bps = 1;
     cudaError_t init_err = cudaSuccess;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -115,8 +123,7 @@ int device_setup(DeviceInfo** out) {
         cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = init_align_attributes();
         if (e == cudaSuccess) e = init_shrink_attributes();
-        if (e == cudaSuccess) e = init_gemv_attributes();
-        if (e == cudaSuccess) info->gemv_bps = gemv_blocks_per_sm(gemv_smem_bytes(4096));
+        if (e == cudaSuccess) e = init_tc_attributes();
         info->init_err = e;
     });
     if (info->init_err != cudaSuccess) return MOELORA_ECUDA;
@@ -125,6 +132,60 @@ int device_setup(DeviceInfo** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// bf16 tiled tensor map, 128-byte swizzle, OOB elements read as zero
+bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                           strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// W1 [E][2I][H] viewed as [E][2][I][H]: boxes of 64 (K) x 128 units of one half
+bool encode_w1_map(CUtensorMap* map, const void* W1, int E, int I, int H) {
+    const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
+    const cuuint64_t strides[3] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)2 * I * H * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    return encode_bf16_map(map, W1, 4, dims, strides, box);
+}
+
+// W2 [E][H][I]: boxes of 64 (K) x 128 rows
+bool encode_w2_map(CUtensorMap* map, const void* W2, int E, int I, int H) {
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)I * 2, (cuuint64_t)H * I * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    return encode_bf16_map(map, W2, 3, dims, strides, box);
+}
+
+// pair rows [P][K] (x in bucket order, or act): boxes of 64 (K) x 16 rows
+bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, 16};
+    return encode_bf16_map(map, rows, 2, dims, strides, box);
+}
 
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
@@ -147,6 +208,8 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.lora_buckets = at<int32_t>(ws, L.lora_buckets);
     a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
+    a.zero_ints = at<int>(ws, L.counters);
+    a.n_zero = d->L > 0 ? (int)(2 * L.nbl) : 0;
     a.hdr = at<WsHeader>(ws, L.hdr);
     return a;
 }
@@ -166,6 +229,7 @@ MOELORA_API const char* moe_lora_strerror(int code) {
         case MOELORA_EUNSUPPORTED: return "unsupported size or alignment (H, I multiples of 8; r multiple of 8 <= 64; 16-byte aligned pointers)";
         case MOELORA_ECUDA: return "a CUDA runtime call failed";
         case MOELORA_EDEVICE_ID: return "the device met an expert or adapter id out of range; those pairs were left out";
+        case MOELORA_ETIMEOUT: return "a kernel gave up a bounded wait on its data pipeline; the result is incomplete";
         default: return "unknown status";
     }
 }
@@ -191,9 +255,9 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     const bool lora = d->L > 0;
     out->compact_ids = L.compact_ids;
     out->compact_offset = L.compact_offset;
-    out->z1 = lora ? L.z1 : 0;
+    out->z1 = lora ? L.z1f : 0;
     out->act = L.act;
-    out->z2 = lora ? L.z2 : 0;
+    out->z2 = lora ? L.z2f : 0;
     out->pair_out = L.pair_out;
     out->s1 = L.s1;
     out->s2 = L.s2;
@@ -274,16 +338,31 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tr.mark(0);
     if (launch_align(aa, align_hist_smem_bytes(d->E, d->L), s) != cudaSuccess) return MOELORA_ECUDA;
     if (d->T == 0) {
-        for (int i = 1; i <= 6; i++) tr.mark(i);
+        for (int i = 1; i < MOELORA_TRACE_EVENTS; i++) tr.mark(i);
         return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
     }
 
-    const WsHeader* hdr = at<WsHeader>(ws, L.hdr);
+    WsHeader* hdr = at<WsHeader>(ws, L.hdr);
     const int sms = dev->sms;
     const long lora_buckets_max = std::min<long>((long)d->E * d->L, L.P);
+    const long experts_max = std::min<long>(d->E, L.P);
+
+    // x rows in bucket order: the B operand of the gate_up GEMM
+    GatherArgs ga = {};
+    ga.k = d->k; ga.H = d->H;
+    ga.x = static_cast<const uint16_t*>(x);
+    ga.compact_ids = at<int32_t>(ws, L.compact_ids);
+    ga.hdr = hdr;
+    ga.out = at<uint16_t>(ws, L.xc);
+    tr.mark(1);
+    {
+        const long n = L.P * (d->H / 8);
+        const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
+        if (launch_gather_rows(ga, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+    }
 
     ShrinkArgs sh = {};
-    tr.mark(1);
+    tr.mark(2);
     if (has_lora) {
         sh.E = d->E; sh.L = d->L; sh.k = d->k; sh.r = d->r; sh.K = d->H; sh.P = (int)L.P;
         sh.S = L.s1;
@@ -295,41 +374,44 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         sh.compact_ids = at<int32_t>(ws, L.compact_ids);
         sh.hdr = hdr;
         sh.z = at<float>(ws, L.z1);
+        sh.zfinal = at<float>(ws, L.z1f);
+        sh.counters = at<int>(ws, L.counters);
         sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
         const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
         if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
-    GemvArgs g = {};
-    g.E = d->E; g.L = d->L; g.k = d->k; g.r = has_lora ? d->r : 0; g.I = d->I; g.H = d->H; g.P = (int)L.P;
-    g.lora_ids = token_lora_ids;
-    g.topk_weights = topk_weights;
-    g.active_experts = at<int32_t>(ws, L.active_experts);
-    g.compact_offset = at<int32_t>(ws, L.compact_offset);
-    g.compact_ids = at<int32_t>(ws, L.compact_ids);
-    g.hdr = hdr;
-    g.act_out = at<uint16_t>(ws, L.act);
-    g.pair_out = at<float>(ws, L.pair_out);
-    const long experts_max = std::min<long>(d->E, L.P);
-    const int grid_cap = sms * dev->gemv_bps;
+    // pair-chunk width: narrow when experts see few pairs (decode), wide otherwise
+    const long avg_pairs = (L.P + experts_max - 1) / experts_max;
+    TcArgs tc;
+    memset(&tc, 0, sizeof(tc));
+    tc.E = d->E; tc.L = d->L; tc.k = d->k; tc.r = has_lora ? d->r : 0; tc.I = d->I; tc.H = d->H;
+    tc.P = (int)L.P;
+    tc.lora_ids = token_lora_ids;
+    tc.topk_weights = topk_weights;
+    tc.active_experts = at<int32_t>(ws, L.active_experts);
+    tc.compact_offset = at<int32_t>(ws, L.compact_offset);
+    tc.compact_ids = at<int32_t>(ws, L.compact_ids);
+    tc.hdr = hdr;
+    tc.act_out = at<uint16_t>(ws, L.act);
+    tc.pair_out = at<float>(ws, L.pair_out);
 
-    // gate_up
-    g.gate_up = 1;
-    g.in = static_cast<const uint16_t*>(x);
-    g.W = static_cast<const uint16_t*>(W1);
-    g.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
-    g.zpart = has_lora ? at<float>(ws, L.z1) : nullptr;
-    g.S = L.s1;
-    g.kc = L.kc_gu;
-    tr.mark(2);
+    // gate_up on the tensor cores: W1 tiles x (x rows in bucket order)
     {
-        const long per_cta = (kGemvThreads / 32) * (kGemvRows / 2);
-        g.max_tasks = (int)std::min<long>(experts_max * ((d->I + per_cta - 1) / per_cta), 1L << 30);
-        const int grid = std::max(1, std::min(g.max_tasks, grid_cap));
-        if (launch_gemv(g, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        const int bn = avg_pairs <= 48 ? 64 : 128;
+        tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
+        tc.z = has_lora ? at<float>(ws, L.z1f) : nullptr;
+        tc.nstages = tc_plan_stages(true, bn);
+        if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H))
+            return MOELORA_ECUDA;
+        const long tasks = ((d->I + 127) / 128) * (experts_max + (L.P + bn - 1) / bn);
+        const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
+        tr.mark(3);
+        if (launch_moe_gemm_tc(tc, true, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
-    tr.mark(3);
+    tr.mark(4);
     if (has_lora) {
         sh.K = d->I;
         sh.S = L.s2;
@@ -337,25 +419,26 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         sh.in = at<uint16_t>(ws, L.act);
         sh.A = static_cast<const uint16_t*>(A2);
         sh.z = at<float>(ws, L.z2);
+        sh.zfinal = at<float>(ws, L.z2f);
+        sh.counters = at<int>(ws, L.counters) + L.nbl;
         sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
         const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
         if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
-    // down
-    g.gate_up = 0;
-    g.in = at<uint16_t>(ws, L.act);
-    g.W = static_cast<const uint16_t*>(W2);
-    g.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
-    g.zpart = has_lora ? at<float>(ws, L.z2) : nullptr;
-    g.S = L.s2;
-    g.kc = L.kc_dn;
-    tr.mark(4);
+    // down on the tensor cores: W2 tiles x act rows
     {
-        const long per_cta = (kGemvThreads / 32) * kGemvRows;
-        g.max_tasks = (int)std::min<long>(experts_max * ((d->H + per_cta - 1) / per_cta), 1L << 30);
-        const int grid = std::max(1, std::min(g.max_tasks, grid_cap));
-        if (launch_gemv(g, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        const int bn = avg_pairs <= 48 ? 64 : 256;
+        tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
+        tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
+        tc.nstages = tc_plan_stages(false, bn);
+        if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I))
+            return MOELORA_ECUDA;
+        const long tasks = ((d->H + 127) / 128) * (experts_max + (L.P + bn - 1) / bn);
+        const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
+        tr.mark(5);
+        if (launch_moe_gemm_tc(tc, false, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     ReduceArgs ra = {};
@@ -364,13 +447,13 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ra.topk_ids = topk_ids;
     ra.lora_ids = token_lora_ids;
     ra.out = static_cast<uint16_t*>(out);
-    tr.mark(5);
+    tr.mark(6);
     {
         const long n = (long)d->T * (d->H / 4);
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_reduce(ra, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
-    tr.mark(6);
+    tr.mark(7);
     return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
 }
 
@@ -469,7 +552,8 @@ MOELORA_API int moe_lora_get_status(const void* workspace, void* stream) {
         cudaGetLastError();
         return MOELORA_ECUDA;
     }
-    return status == 0 ? MOELORA_OK : MOELORA_EDEVICE_ID;
+    if (status == 0) return MOELORA_OK;
+    return (status & (kStatusBadExpert | kStatusBadLora)) ? MOELORA_EDEVICE_ID : MOELORA_ETIMEOUT;
 }
 
 }  // extern "C"

@@ -9,8 +9,10 @@
 // A[l][e] in shared memory once (coalesced 16-byte loads), then every warp
 // takes rows of the bucket, each lane holding 8 consecutive K elements per
 // 256-element step, and a shuffle reduce-scatter leaves one output per lane.
-// Partials are written to z[s][row][:] and summed in fixed s order by the
-// consumer, so the result is deterministic (no atomics).
+// Each split writes its partials to z[s][row][:]; the CTA that completes a
+// bucket's last split (an arrival counter per bucket decides which) sums the S
+// partials in split order into zfinal[row][:].  The order of the sum is fixed,
+// so the result is deterministic; only the choice of the summing CTA varies.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -26,6 +28,7 @@ __global__ void __launch_bounds__(kShrinkThreads) k_shrink(ShrinkArgs a) {
     extern __shared__ __align__(16) uint16_t a_slab[];  // [RP][kShrinkKC]
     pdl_wait();
     pdl_trigger();
+    __shared__ int s_last;
     const int n_items = a.hdr->n_lora_buckets * a.S;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int L1 = a.L + 1;
@@ -83,6 +86,22 @@ __global__ void __launch_bounds__(kShrinkThreads) k_shrink(ShrinkArgs a) {
                 const float thi = warp_reduce_scatter<32>(hi, lane);
                 if (lane < r) zrow[lane] = tlo;
                 if (32 + lane < r) zrow[32 + lane] = thi;
+            }
+        }
+
+        // split-K completion: the last split of this bucket to finish sums them all
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[bi], 1) == a.S - 1;
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            const int n = (row1 - row0) * r;
+            for (int idx = threadIdx.x; idx < n; idx += kShrinkThreads) {
+                const size_t off = (size_t)row0 * r + idx;
+                float v = 0.f;
+                for (int s2 = 0; s2 < a.S; s2++) v += __ldcg(a.z + (size_t)s2 * a.P * r + off);
+                a.zfinal[off] = v;
             }
         }
     }

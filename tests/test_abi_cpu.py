@@ -54,8 +54,8 @@ def test_workspace_bytes_and_layout(lib):
     P = 64
     assert lay["s1"] == -(-2880 // 512) and lay["s2"] == -(-2880 // 512)
     # regions are disjoint and inside the workspace
-    regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * lay["s1"] * P * 32),
-                      (lay["act"], 2 * P * 2880), (lay["z2"], 4 * lay["s2"] * P * 32),
+    regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * P * 32),
+                      (lay["act"], 2 * P * 2880), (lay["z2"], 4 * P * 32),
                       (lay["pair_out"], 4 * P * 2880)])
     for (a, na), (b, _) in zip(regions, regions[1:]):
         assert a + na <= b
