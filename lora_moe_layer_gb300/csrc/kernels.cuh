@@ -40,11 +40,12 @@ cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t str
 cudaError_t init_align_attributes();
 
 // --------------------------------------------------------------- shrink ----
-// z[s][row][0:r] = sum over the s-th K-split of A[l][e][0:r][k] * in(row)[k]
-// for every compact row of every (e, l >= 0) bucket.
+// z[row][0:r] = A[l][e][0:r][:] . in(row) for every compact row of every
+// (e, l >= 0) bucket, one warp per (bucket, 8 outputs, K-split) item.
 struct ShrinkArgs {
     int E, L, k, r, K, P;
     int S;                      // K-splits
+    int ks;                     // K elements per split (multiple of 256)
     int in_is_x;                // 1: in(row) = x[compact_ids[row] / k]; 0: in(row) = act[row]
     const uint16_t* in;         // x [T][K] or act [P][K]
     const uint16_t* A;          // [L][E][r][K]
@@ -52,15 +53,15 @@ struct ShrinkArgs {
     const int32_t* compact_offset;
     const int32_t* compact_ids;
     const WsHeader* hdr;
-    float* z;                   // [S][P][r] split partials (scratch)
-    float* zfinal;              // [P][r] sum of the S partials, in split order
-    int* counters;              // [buckets] arrivals per bucket, zeroed by align
-    int max_items;              // upper bound of buckets * S (host-known)
+    float* z;                   // [S][P][r] split partials (scratch, S > 1)
+    float* zfinal;              // [P][r] the shrink output
+    int* counters;              // [buckets * 8] arrivals per (bucket, group), zeroed by align
+    uint16_t* xc;               // when set: also copy x rows into bucket order [P][K] (gate_up launch)
 };
-constexpr int kShrinkKC = 512;  // K elements per split
+int shrink_splits(int K, long items_no_split);
+int shrink_split_len(int K, int S);
+int shrink_warps_per_block();
 cudaError_t launch_shrink(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl);
-cudaError_t init_shrink_attributes();
-int shrink_blocks_per_sm();
 
 // ------------------------------------------------------------ tcgen05 GEMM ----
 // Grouped expert GEMM on the tensor cores (moe_gemm_tc.cu), weight rows on M.

@@ -114,8 +114,10 @@ struct EpiRow {
         cur_l = -2;
     }
 
-    // one pair (compact row q) of this row: add the expand, apply the epilogue, store
-    __device__ __forceinline__ void column(const TcArgs& a, int q, float vg, float vu, bool has_lora) {
+    // one pair (compact row q, its z at zq) of this row: add the expand, apply
+    // the epilogue, store
+    __device__ __forceinline__ void column(const TcArgs& a, int q, const float* zq, float vg, float vu,
+                                           bool has_lora) {
         const int p = a.compact_ids[q];
         const int l = a.lora_ids[p / a.k];
         const int r = a.r;
@@ -131,7 +133,6 @@ struct EpiRow {
                 }
                 cur_l = l;
             }
-            const float* zq = a.z + (size_t)q * r;
             float dg0 = 0.f, dg1 = 0.f, du0 = 0.f, du1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -314,8 +315,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 tmem_ld16(t_lane + c0, g);
                 if (GATE_UP) tmem_ld16(t_lane + BN + c0, u);
 #pragma unroll
-                for (int c = 0; c < 16; c++)
-                    if (c0 + c < n_real) er.column(a, q0c + c0 + c, g[c], GATE_UP ? u[c] : 0.f, has_lora);
+                for (int c = 0; c < 16; c++) {
+                    if (c0 + c < n_real) {
+                        const int q = q0c + c0 + c;
+                        const float* zq = a.z + (size_t)q * a.r;
+                        er.column(a, q, zq, g[c], GATE_UP ? u[c] : 0.f, has_lora);
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -346,6 +352,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
     const int n = a.hdr->n_valid;
     const int c8 = a.H >> 3;
     const long total = (long)n * c8;
+#pragma unroll 4
     for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
         const int q = (int)(idx / c8), c = (int)(idx % c8);
         const int t = a.compact_ids[q] / a.k;

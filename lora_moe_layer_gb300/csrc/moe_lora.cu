@@ -34,7 +34,7 @@ constexpr int kMaxDevices = 64;
 struct Layout {
     int bm;
     long P, NB, cap, tiles;
-    int s1, s2;
+    int s1, s2, ks1, ks2;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
         compact_ids, active_experts, lora_buckets, scan_tmp, hist, counters, z1, z1f, xc, act, z2, z2f,
         pair_out, total;
@@ -75,8 +75,17 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->cap = L->P + std::min(L->NB, L->P) * (L->bm - 1);
     L->tiles = L->cap / L->bm;
     const int r = d->L > 0 ? d->r : 0;
-    L->s1 = d->L > 0 ? (d->H + kShrinkKC - 1) / kShrinkKC : 0;
-    L->s2 = d->L > 0 ? (d->I + kShrinkKC - 1) / kShrinkKC : 0;
+    L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
+    if (d->L > 0) {
+        const long items = L->nbl * (d->r / 8);
+        L->ks1 = shrink_split_len(d->H, shrink_splits(d->H, items));
+        L->ks2 = shrink_split_len(d->I, shrink_splits(d->I, items));
+        L->s1 = (d->H + L->ks1 - 1) / L->ks1;
+        L->s2 = (d->I + L->ks2 - 1) / L->ks2;
+    } else {
+        L->ks1 = L->ks2 = 0;
+        L->s1 = L->s2 = 0;
+    }
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
     L->hdr = take(sizeof(WsHeader));
@@ -91,13 +100,12 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
-    L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
-    L->counters = take(sizeof(int32_t) * 2 * L->nbl);
-    L->z1 = take(sizeof(float) * (size_t)L->s1 * L->P * r);
+    L->counters = take(sizeof(int32_t) * 16 * L->nbl);
+    L->z1 = take(sizeof(float) * (size_t)(L->s1 > 1 ? L->s1 : 0) * L->P * r);
     L->z1f = take(sizeof(float) * (size_t)L->P * r);
     L->xc = take(sizeof(uint16_t) * (size_t)L->P * d->H);
     L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
-    L->z2 = take(sizeof(float) * (size_t)L->s2 * L->P * r);
+    L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
     L->total = o;
@@ -122,7 +130,6 @@ int device_setup(DeviceInfo** out) {
     std::call_once(g_once[dev], [info, dev]() {
         cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = init_align_attributes();
-        if (e == cudaSuccess) e = init_shrink_attributes();
         if (e == cudaSuccess) e = init_tc_attributes();
         info->init_err = e;
     });
@@ -209,7 +216,7 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
     a.zero_ints = at<int>(ws, L.counters);
-    a.n_zero = d->L > 0 ? (int)(2 * L.nbl) : 0;
+    a.n_zero = d->L > 0 ? (int)(16 * L.nbl) : 0;
     a.hdr = at<WsHeader>(ws, L.hdr);
     return a;
 }
@@ -333,6 +340,11 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     // NULL stream gets plain stream order
     const bool pdl = s != nullptr && s != cudaStreamLegacy;
 
+    // pair-chunk width of the GEMMs: narrow when experts see few pairs (decode)
+    const long experts_max = std::min<long>(d->E, L.P);
+    const long avg_pairs = L.P > 0 ? (L.P + experts_max - 1) / experts_max : 0;
+    const bool narrow = avg_pairs <= 48;
+
     Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
     tr.mark(0);
@@ -345,7 +357,6 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     WsHeader* hdr = at<WsHeader>(ws, L.hdr);
     const int sms = dev->sms;
     const long lora_buckets_max = std::min<long>((long)d->E * d->L, L.P);
-    const long experts_max = std::min<long>(d->E, L.P);
 
     // x rows in bucket order: the B operand of the gate_up GEMM
     GatherArgs ga = {};
@@ -354,8 +365,9 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ga.compact_ids = at<int32_t>(ws, L.compact_ids);
     ga.hdr = hdr;
     ga.out = at<uint16_t>(ws, L.xc);
+    // with adapters the gate_up shrink kernel also does the gather (one launch)
     tr.mark(1);
-    {
+    if (!has_lora) {
         const long n = L.P * (d->H / 8);
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_gather_rows(ga, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
@@ -366,6 +378,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     if (has_lora) {
         sh.E = d->E; sh.L = d->L; sh.k = d->k; sh.r = d->r; sh.K = d->H; sh.P = (int)L.P;
         sh.S = L.s1;
+        sh.ks = L.ks1;
         sh.in_is_x = 1;
         sh.in = static_cast<const uint16_t*>(x);
         sh.A = static_cast<const uint16_t*>(A1);
@@ -376,13 +389,13 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         sh.z = at<float>(ws, L.z1);
         sh.zfinal = at<float>(ws, L.z1f);
         sh.counters = at<int>(ws, L.counters);
-        sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
-        const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
+        sh.xc = at<uint16_t>(ws, L.xc);
+        const long warps = lora_buckets_max * (d->r / 8) * sh.S;
+        const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
+        const int grid = (int)std::max<long>(sms, std::min<long>(blocks, (long)sms * 8));
         if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
-    // pair-chunk width: narrow when experts see few pairs (decode), wide otherwise
-    const long avg_pairs = (L.P + experts_max - 1) / experts_max;
     TcArgs tc;
     memset(&tc, 0, sizeof(tc));
     tc.E = d->E; tc.L = d->L; tc.k = d->k; tc.r = has_lora ? d->r : 0; tc.I = d->I; tc.H = d->H;
@@ -398,7 +411,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     // gate_up on the tensor cores: W1 tiles x (x rows in bucket order)
     {
-        const int bn = avg_pairs <= 48 ? 64 : 128;
+        const int bn = narrow ? 64 : 128;
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z1f) : nullptr;
         tc.nstages = tc_plan_stages(true, bn);
@@ -413,22 +426,25 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     tr.mark(4);
     if (has_lora) {
+        sh.xc = nullptr;
         sh.K = d->I;
         sh.S = L.s2;
+        sh.ks = L.ks2;
         sh.in_is_x = 0;
         sh.in = at<uint16_t>(ws, L.act);
         sh.A = static_cast<const uint16_t*>(A2);
         sh.z = at<float>(ws, L.z2);
         sh.zfinal = at<float>(ws, L.z2f);
-        sh.counters = at<int>(ws, L.counters) + L.nbl;
-        sh.max_items = (int)std::min<long>(lora_buckets_max * sh.S, 1L << 30);
-        const int grid = std::max(1, std::min(sh.max_items, sms * shrink_blocks_per_sm()));
+        sh.counters = at<int>(ws, L.counters) + 8 * L.nbl;
+        const long warps = lora_buckets_max * (d->r / 8) * sh.S;
+        const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
+        const int grid = (int)std::max<long>(1, std::min<long>(blocks, (long)sms * 8));
         if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     // down on the tensor cores: W2 tiles x act rows
     {
-        const int bn = avg_pairs <= 48 ? 64 : 256;
+        const int bn = narrow ? 64 : 256;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
         tc.nstages = tc_plan_stages(false, bn);
