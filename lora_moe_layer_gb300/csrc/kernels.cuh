@@ -82,8 +82,8 @@ struct TcArgs {
     float* pair_out;             // down: [P][H] fp32 by pair id
     int nstages;
 };
-int tc_smem_bytes(bool gate_up, int bn, int nstages);
-int tc_plan_stages(bool gate_up, int bn);
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages);
+int tc_plan_stages(bool gate_up, int bn, int r, int E);
 cudaError_t init_tc_attributes();
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl);
 

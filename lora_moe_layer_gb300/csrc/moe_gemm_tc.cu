@@ -25,9 +25,12 @@
 //            up accumulator, so a unit's gate and up values land in the same
 //            TMEM lane), and commits stage releases and accumulator
 //            completion to mbarriers;
-//   warps 2-5 epilogue: each thread owns one weight row (its TMEM lane), reads
-//            16 columns at a time, adds the LoRA expand B[l][e][row] . z[pair]
-//            on CUDA cores, and writes bf16 SiLU(gate)*up or fp32 w * d.
+//   warps 2-9 epilogue: each thread owns one weight row (its TMEM lane; two
+//            warps per lane quadrant take alternate 16-column chunks), adds the
+//            LoRA expand B[l][e][row] . z[pair] on CUDA cores, and writes bf16
+//            SiLU(gate)*up or fp32 w * d.  Per task the column metadata (pair,
+//            adapter, weight) and the chunk's z rows are first staged in
+//            shared memory, while the task's MMAs are still running.
 // The two accumulators alternate, so one task's epilogue overlaps the next
 // task's MMAs.  Every wait is bounded (tma.cuh); on a timeout the CTA records
 // kStatusTimeout, drains its copies, frees TMEM and exits.
@@ -39,7 +42,8 @@ namespace moelora {
 
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kEpiWarps = 8;             // two per TMEM lane quadrant, splitting the columns
+constexpr int kTcThreads = (2 + kEpiWarps) * 32;
 constexpr int kBM = 128;                 // weight rows per task (MMA M)
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row
 constexpr int kATile = kBM * kBK * 2;    // 16 KiB
@@ -58,43 +62,37 @@ struct TcShape {
 
 __device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
 
-// Walks the task sequence (active expert, weight tile, pair chunk) in order.
+// Task table built once per CTA in shared memory: for active expert a,
+// expert id, first pair row, pair count, and the exclusive prefix of its task
+// count (weight tiles x pair chunks).  A task index maps to (expert, tile,
+// chunk) by a binary search over the prefix.
+struct TaskTable {
+    int* e;    // [n_active]
+    int* q0;   // [n_active]
+    int* m;    // [n_active]
+    int* cum;  // [n_active + 1]
+};
+
 template <int BN>
-struct TaskWalker {
-    int ai, mt, ch, e, q0, m_e, nch;
-    __device__ void load_expert(const TcArgs& a, int L1) {
-        e = a.active_experts[ai];
-        q0 = a.compact_offset[e * L1];
-        m_e = a.compact_offset[(e + 1) * L1] - q0;
-        nch = (m_e + BN - 1) / BN;
-    }
-    __device__ void seek(const TcArgs& a, int L1, int ntiles, int t, int n_active) {
-        int acc = 0;
-        for (ai = 0; ai < n_active; ai++) {
-            load_expert(a, L1);
-            const int cnt = ntiles * nch;
-            if (t < acc + cnt) {
-                const int loc = t - acc;
-                mt = loc / nch;
-                ch = loc % nch;
-                return;
-            }
-            acc += cnt;
+struct Task {
+    int e, mt, q0c, n_real, n_cols;
+    __device__ void lookup(const TaskTable& tt, int n_active, int ntiles, int t) {
+        int lo = 0, hi = n_active;  // last a with cum[a] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tt.cum[mid] <= t) lo = mid;
+            else hi = mid;
         }
+        const int nch = (tt.m[lo] + BN - 1) / BN;
+        const int loc = t - tt.cum[lo];
+        mt = loc / nch;
+        const int ch = loc % nch;
+        (void)ntiles;
+        e = tt.e[lo];
+        q0c = tt.q0[lo] + ch * BN;
+        n_real = min(BN, tt.m[lo] - ch * BN);
+        n_cols = (n_real + 15) & ~15;
     }
-    __device__ void next(const TcArgs& a, int L1, int ntiles) {
-        if (++ch == nch) {
-            ch = 0;
-            if (++mt == ntiles) {
-                mt = 0;
-                ai++;
-                load_expert(a, L1);
-            }
-        }
-    }
-    __device__ int row0() const { return q0 + ch * BN; }              // first pair row of the chunk
-    __device__ int n_real() const { return min(BN, m_e - ch * BN); }
-    __device__ int n_cols() const { return (n_real() + 15) & ~15; }
 };
 
 // Epilogue state of one thread = one weight row of the tile: the row's LoRA B
@@ -114,12 +112,10 @@ struct EpiRow {
         cur_l = -2;
     }
 
-    // one pair (compact row q, its z at zq) of this row: add the expand, apply
-    // the epilogue, store
-    __device__ __forceinline__ void column(const TcArgs& a, int q, const float* zq, float vg, float vu,
-                                           bool has_lora) {
-        const int p = a.compact_ids[q];
-        const int l = a.lora_ids[p / a.k];
+    // one pair of this row (compact row q, pair id p, adapter l, top-k weight
+    // w, its z at zq): add the expand, apply the epilogue, store
+    __device__ __forceinline__ void column(const TcArgs& a, int q, int p, int l, float w, const float* zq, float vg,
+                                           float vu, bool has_lora) {
         const int r = a.r;
         if (has_lora && l >= 0 && row_ok) {
             if (l != cur_l) {  // pairs come grouped by adapter: reload only at a run boundary
@@ -138,8 +134,8 @@ struct EpiRow {
             for (int i = 0; i < 8; i++) {
                 if (i * 8 < r) {
                     float zz[8];
-                    const float4 z0 = __ldcg(reinterpret_cast<const float4*>(zq + i * 8));
-                    const float4 z1 = __ldcg(reinterpret_cast<const float4*>(zq + i * 8 + 4));
+                    const float4 z0 = *reinterpret_cast<const float4*>(zq + i * 8);
+                    const float4 z1 = *reinterpret_cast<const float4*>(zq + i * 8 + 4);
                     zz[0] = z0.x; zz[1] = z0.y; zz[2] = z0.z; zz[3] = z0.w;
                     zz[4] = z1.x; zz[5] = z1.y; zz[6] = z1.z; zz[7] = z1.w;
                     if (i & 1) dg1 = dot8(bg[i], zz, dg1);
@@ -157,7 +153,7 @@ struct EpiRow {
             if (GATE_UP)
                 a.act_out[(size_t)q * a.I + w_row] = f32_to_bf16_rne(silu_f(vg) * vu);
             else
-                a.pair_out[(size_t)p * a.H + w_row] = a.topk_weights[p] * vg;
+                a.pair_out[(size_t)p * a.H + w_row] = w * vg;
         }
     }
 };
@@ -168,12 +164,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)NS * S::kStage);
+    // epilogue staging: z rows [BN][r] fp32, then pair id / adapter / weight per column
+    float* zs = reinterpret_cast<float*>(base + (size_t)NS * S::kStage);
+    int* s_pair = reinterpret_cast<int*>(zs + (size_t)BN * a.r);
+    int* s_lora = s_pair + BN;
+    float* s_w = reinterpret_cast<float*>(s_lora + BN);
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_w + BN + ((BN * a.r) & 1 ? 1 : 0));
     uint64_t* empty = full + NS;
     uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
     uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-    __shared__ int s_total;
+    uint64_t* ebar = tempty + 2;    // epilogue rendezvous (kEpiWarps * 32 arrivals)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
+    TaskTable tt;
+    tt.e = reinterpret_cast<int*>(tmem_slot + 4);
+    tt.q0 = tt.e + a.E;
+    tt.m = tt.q0 + a.E;
+    tt.cum = tt.m + a.E;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -183,8 +189,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4);
+            mbar_init(&tempty[b], kEpiWarps);
         }
+        mbar_init(ebar, kEpiWarps * 32);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -209,19 +216,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     const int ntiles = (N_out + kBM - 1) / kBM;
     const int nkb = (K + kBK - 1) / kBK;
     const int n_active = a.hdr->n_active;
-    if (threadIdx.x == 0) {
-        int total = 0;
-        for (int ai = 0; ai < n_active; ai++) {
-            const int e = a.active_experts[ai];
-            const int m_e = a.compact_offset[(e + 1) * L1] - a.compact_offset[e * L1];
-            total += ntiles * ((m_e + BN - 1) / BN);
-        }
-        s_total = total;
+    // task table: independent loads across threads, then one warp scans the counts
+    for (int ai = threadIdx.x; ai < n_active; ai += kTcThreads) {
+        const int e = a.active_experts[ai];
+        const int q0 = a.compact_offset[e * L1];
+        const int m = a.compact_offset[(e + 1) * L1] - q0;
+        tt.e[ai] = e;
+        tt.q0[ai] = q0;
+        tt.m[ai] = m;
+        tt.cum[ai + 1] = ntiles * ((m + BN - 1) / BN);
     }
     __syncthreads();
-    const int total = s_total;
-    const int t_beg = (int)((long long)blockIdx.x * total / gridDim.x);
-    const int t_end = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < n_active; base += 32) {
+            const int i = base + lane;
+            int v = i < n_active ? tt.cum[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, v, o);
+                if (lane >= o) v += y;
+            }
+            if (i < n_active) tt.cum[i + 1] = carry + v;
+            carry += __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0) tt.cum[0] = 0;
+    }
+    __syncthreads();
+    const int total = tt.cum[n_active];
+    // tasks are dealt round-robin, so the pair chunks of one weight tile (and
+    // the tiles of one expert) stream on neighbouring CTAs at the same time and
+    // share their operands through L2
+    const int t_first = blockIdx.x, t_step = gridDim.x;
     bool ok = true;
 
     if (warp == 0) {
@@ -229,10 +255,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, armed = 0, last_par = 0;
-            TaskWalker<BN> tw;
-            if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
-            for (int t = t_beg; t < t_end && ok; t++) {
-                const int n_cols = tw.n_cols(), row0 = tw.row0(), e = tw.e;
+            for (int t = t_first; t < total && ok; t += t_step) {
+                Task<BN> tw;
+                tw.lookup(tt, n_active, ntiles, t);
+                const int n_cols = tw.n_cols, row0 = tw.q0c, e = tw.e;
                 const uint32_t bytes = S::kAB + (uint32_t)n_cols * kBK * 2;
                 for (int kb = 0; kb < nkb; kb++) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
@@ -251,7 +277,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
-                if (t + 1 < t_end) tw.next(a, L1, ntiles);
             }
             // every issued copy lands before the CTA may exit
             for (int s = 0; s < NS; s++)
@@ -262,14 +287,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            TaskWalker<BN> tw;
-            if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
-            for (int t = t_beg, it = 0; t < t_end && ok; t++, it++) {
+            for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+                Task<BN> tw;
+                tw.lookup(tt, n_active, ntiles, t);
                 const int b = it & 1;
                 if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
-                const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols());
+                const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols);
                 for (int kb = 0; kb < nkb; kb++) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
@@ -288,45 +313,67 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 }
                 if (!ok) break;
                 umma_commit(&tfull[b]);          // accumulator complete
-                if (t + 1 < t_end) tw.next(a, L1, ntiles);
             }
         }
     } else {
         // -------------------------------------------------------------- epilogue
+        const int ew = warp - 2;                 // 0 .. kEpiWarps-1
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
+        const int half = ew >> 2;                // which alternate 16-column chunks
         const int row = qd * 32 + lane;          // weight row within the tile
+        const int etid = ew * 32 + lane;
         const bool has_lora = a.B != nullptr && a.z != nullptr;
         const size_t rows_per_expert = GATE_UP ? 2 * (size_t)a.I : (size_t)a.H;
-        TaskWalker<BN> tw;
-        if (t_beg < t_end) tw.seek(a, L1, ntiles, t_beg, n_active);
-        for (int t = t_beg, it = 0; t < t_end && ok; t++, it++) {
+        const int r = a.r;
+        uint32_t epar = 0;
+        for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+            Task<BN> tw;
+            tw.lookup(tt, n_active, ntiles, t);
             const int b = it & 1;
+            const int e = tw.e, q0c = tw.q0c, n_real = tw.n_real, n_cols = tw.n_cols;
+            // stage this task's column data while its MMAs run (after everyone
+            // is done with the previous task's)
+            mbar_arrive(ebar);
+            if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
+            epar ^= 1;
+            for (int c = etid; c < n_real; c += kEpiWarps * 32) {
+                const int p = a.compact_ids[q0c + c];
+                s_pair[c] = p;
+                s_lora[c] = a.lora_ids[p / a.k];
+                s_w[c] = a.topk_weights[p];
+            }
+            if (has_lora) {
+                const float4* zsrc = reinterpret_cast<const float4*>(a.z + (size_t)q0c * r);
+                float4* zdst = reinterpret_cast<float4*>(zs);
+                for (int i = etid; i < n_real * r / 4; i += kEpiWarps * 32) zdst[i] = __ldcg(zsrc + i);
+            }
+            mbar_arrive(ebar);
+            if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
+            epar ^= 1;
+
             // warp-uniform outcome: the TMEM loads below are warp-collective
             if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) { ok = false; break; }
             tc_fence_after();
-            const int e = tw.e, q0c = tw.row0(), n_real = tw.n_real(), n_cols = tw.n_cols();
             const int w_row = tw.mt * kBM + row;
             const bool row_ok = w_row < N_out;
             const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * S::kAccCols);
             EpiRow<GATE_UP> er;
             er.init(a, e, w_row, row_ok, rows_per_expert);
-            for (int c0 = 0; c0 < n_cols; c0 += 16) {
+            for (int c0 = half * 16; c0 < n_cols; c0 += 32) {
                 float g[16], u[16];
                 tmem_ld16(t_lane + c0, g);
                 if (GATE_UP) tmem_ld16(t_lane + BN + c0, u);
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
-                    if (c0 + c < n_real) {
-                        const int q = q0c + c0 + c;
-                        const float* zq = a.z + (size_t)q * a.r;
-                        er.column(a, q, zq, g[c], GATE_UP ? u[c] : 0.f, has_lora);
-                    }
+                    const int cc = c0 + c;
+                    if (cc < n_real)
+                        er.column(a, q0c + cc, s_pair[cc], s_lora[cc], s_w[cc], zs + cc * r, g[c],
+                                  GATE_UP ? u[c] : 0.f, has_lora);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[b]);
-            if (t + 1 < t_end) tw.next(a, L1, ntiles);
         }
     }
 
@@ -362,15 +409,17 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
 
 }  // namespace
 
-int tc_smem_bytes(bool gate_up, int bn, int nstages) {
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages) {
     const int ab = gate_up ? 2 * kATile : kATile;
     const int stage = ab + bn * kBK * 2;
-    return 1024 + nstages * stage + (2 * nstages + 4) * 8 + 16;
+    const int staging = bn * r * 4 + 3 * bn * 4 + 8;
+    const int table = (4 * E + 1) * 4;
+    return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
 }
 
-int tc_plan_stages(bool gate_up, int bn) {
+int tc_plan_stages(bool gate_up, int bn, int r, int E) {
     for (int ns = 8; ns >= 2; ns--)
-        if (tc_smem_bytes(gate_up, bn, ns) <= kTcSmemLimit) return ns;
+        if (tc_smem_bytes(gate_up, bn, r, E, ns) <= kTcSmemLimit) return ns;
     return 0;
 }
 
@@ -383,7 +432,7 @@ cudaError_t init_tc_attributes() {
 }
 
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl) {
-    const int smem = tc_smem_bytes(gate_up, bn, args.nstages);
+    const int smem = tc_smem_bytes(gate_up, bn, args.r, args.E, args.nstages);
     const dim3 g(grid), b(kTcThreads);
     if (gate_up) {
         if (bn == 64) return launch_k(k_moe_gemm_tc<true, 64>, g, b, smem, stream, pdl, args);

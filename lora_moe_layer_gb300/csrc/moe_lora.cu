@@ -414,7 +414,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         const int bn = narrow ? 64 : 128;
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z1f) : nullptr;
-        tc.nstages = tc_plan_stages(true, bn);
+        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E);
+        if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H))
             return MOELORA_ECUDA;
@@ -447,7 +448,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         const int bn = narrow ? 64 : 256;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
-        tc.nstages = tc_plan_stages(false, bn);
+        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E);
+        if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I))
             return MOELORA_ECUDA;
