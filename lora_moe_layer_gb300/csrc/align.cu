@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     if (threadIdx.x == 0) hdr->status = 0;
     for (int i = threadIdx.x; i < kAlignWarps * NB; i += kAlignThreads) hist[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero; i += kAlignThreads) a.zero_ints[i] = 0;
+    for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
     __syncthreads();
 
     // each warp owns pairs [seg_beg, seg_end), walked 32 at a time

@@ -31,6 +31,8 @@ struct AlignArgs {
     int* hist_global;          // [16 * NB] when the histogram does not fit in shared memory, else null
     int* zero_ints;            // [n_zero] cleared for the kernels that follow (shrink counters), or null
     int n_zero;
+    int* zero_ints2;           // [n_zero2] second region (GEMM split-K counters), or null
+    int n_zero2;
     WsHeader* hdr;
 };
 
@@ -81,6 +83,9 @@ struct TcArgs {
     uint16_t* act_out;           // gate_up: [P][I] bf16
     float* pair_out;             // down: [P][H] fp32 by pair id
     int nstages;
+    int ksplit;                  // K-splits per weight tile (1: none)
+    float* part;                 // split-K partial tiles [tiles][ksplit][acc columns][128]
+    int* tile_counters;          // [tiles] split arrivals, zeroed by align
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages);
 int tc_plan_stages(bool gate_up, int bn, int r, int E);

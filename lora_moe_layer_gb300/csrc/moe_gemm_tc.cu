@@ -76,18 +76,21 @@ struct TaskTable {
 template <int BN>
 struct Task {
     int e, mt, q0c, n_real, n_cols;
-    __device__ void lookup(const TaskTable& tt, int n_active, int ntiles, int t) {
-        int lo = 0, hi = n_active;  // last a with cum[a] <= t
+    int tile;       // (expert, weight tile, pair chunk) index, for split-K partials
+    int split;      // K-split of this task
+    __device__ void lookup(const TaskTable& tt, int n_active, int ksplit, int t) {
+        tile = t / ksplit;
+        split = t % ksplit;
+        int lo = 0, hi = n_active;  // last a with cum[a] <= tile
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (tt.cum[mid] <= t) lo = mid;
+            if (tt.cum[mid] <= tile) lo = mid;
             else hi = mid;
         }
         const int nch = (tt.m[lo] + BN - 1) / BN;
-        const int loc = t - tt.cum[lo];
+        const int loc = tile - tt.cum[lo];
         mt = loc / nch;
         const int ch = loc % nch;
-        (void)ntiles;
         e = tt.e[lo];
         q0c = tt.q0[lo] + ch * BN;
         n_real = min(BN, tt.m[lo] - ch * BN);
@@ -167,9 +170,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     // epilogue staging: z rows [BN][r] fp32, then pair id / adapter / weight per column
     float* zs = reinterpret_cast<float*>(base + (size_t)NS * S::kStage);
     int* s_pair = reinterpret_cast<int*>(zs + (size_t)BN * a.r);
-    int* s_lora = s_pair + BN;
+    int* s_lora = s_pair + BN + 1;  // s_pair[BN] carries the split-K verdict
     float* s_w = reinterpret_cast<float*>(s_lora + BN);
-    uint64_t* full = reinterpret_cast<uint64_t*>(s_w + BN + ((BN * a.r) & 1 ? 1 : 0));
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_w + BN + 1);
     uint64_t* empty = full + NS;
     uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
     uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
@@ -243,7 +246,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) tt.cum[0] = 0;
     }
     __syncthreads();
-    const int total = tt.cum[n_active];
+    const int ksplit = a.ksplit;
+    const int total = tt.cum[n_active] * ksplit;
     // tasks are dealt round-robin, so the pair chunks of one weight tile (and
     // the tiles of one expert) stream on neighbouring CTAs at the same time and
     // share their operands through L2
@@ -257,10 +261,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             uint32_t phase = 0, armed = 0, last_par = 0;
             for (int t = t_first; t < total && ok; t += t_step) {
                 Task<BN> tw;
-                tw.lookup(tt, n_active, ntiles, t);
+                tw.lookup(tt, n_active, ksplit, t);
                 const int n_cols = tw.n_cols, row0 = tw.q0c, e = tw.e;
                 const uint32_t bytes = S::kAB + (uint32_t)n_cols * kBK * 2;
-                for (int kb = 0; kb < nkb; kb++) {
+                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t* dst = base + (size_t)stage * S::kStage;
@@ -289,13 +294,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             uint32_t phase = 0;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
                 Task<BN> tw;
-                tw.lookup(tt, n_active, ntiles, t);
+                tw.lookup(tt, n_active, ksplit, t);
                 const int b = it & 1;
                 if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
                 const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols);
-                for (int kb = 0; kb < nkb; kb++) {
+                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
@@ -303,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++) {
                         const uint64_t bdesc = umma_desc_sw128(b_addr + kk * 32);
-                        const uint32_t acc = (kb | kk) != 0;
+                        const uint32_t acc = (kb != kb0) || (kk != 0);
                         umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
                         if (GATE_UP)
                             umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, acc);
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         uint32_t epar = 0;
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
             Task<BN> tw;
-            tw.lookup(tt, n_active, ntiles, t);
+            tw.lookup(tt, n_active, ksplit, t);
             const int b = it & 1;
             const int e = tw.e, q0c = tw.q0c, n_real = tw.n_real, n_cols = tw.n_cols;
             // stage this task's column data while its MMAs run (after everyone
@@ -357,12 +363,75 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             const int w_row = tw.mt * kBM + row;
             const bool row_ok = w_row < N_out;
             const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * S::kAccCols);
+            // split-K: partial tiles go to global memory; the split that arrives
+            // last adds the others' partials (in split order) to its own
+            bool finish = true;
+            float* part_tile = nullptr;
+            if (ksplit > 1) {
+                part_tile = a.part + (size_t)tw.tile * ksplit * S::kAccCols * kBM;
+                float* mine = part_tile + (size_t)tw.split * S::kAccCols * kBM;
+                for (int c0 = half * 16; c0 < n_cols; c0 += 32) {
+                    float g[16];
+                    tmem_ld16(t_lane + c0, g);
+#pragma unroll
+                    for (int c = 0; c < 16; c++) mine[(size_t)(c0 + c) * kBM + row] = g[c];
+                    if (GATE_UP) {
+                        tmem_ld16(t_lane + BN + c0, g);
+#pragma unroll
+                        for (int c = 0; c < 16; c++) mine[(size_t)(BN + c0 + c) * kBM + row] = g[c];
+                    }
+                }
+                __threadfence();
+                mbar_arrive(ebar);
+                if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
+                epar ^= 1;
+                if (etid == 0) s_pair[BN] = atomicAdd(&a.tile_counters[tw.tile], 1) == ksplit - 1;
+                mbar_arrive(ebar);
+                if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
+                epar ^= 1;
+                finish = s_pair[BN] != 0;
+                if (finish) __threadfence();
+            }
             EpiRow<GATE_UP> er;
             er.init(a, e, w_row, row_ok, rows_per_expert);
-            for (int c0 = half * 16; c0 < n_cols; c0 += 32) {
+            for (int c0 = half * 16; finish && c0 < n_cols; c0 += 32) {
                 float g[16], u[16];
                 tmem_ld16(t_lane + c0, g);
                 if (GATE_UP) tmem_ld16(t_lane + BN + c0, u);
+                if (ksplit > 1) {
+                    // own split from TMEM, the others from their partial tiles,
+                    // summed in split order; one split's 16 columns load at once
+                    float sg[16], su[16];
+#pragma unroll
+                    for (int c = 0; c < 16; c++) sg[c] = su[c] = 0.f;
+                    for (int sp = 0; sp < ksplit; sp++) {
+                        float vg[16], vu[16];
+                        if (sp == tw.split) {
+#pragma unroll
+                            for (int c = 0; c < 16; c++) {
+                                vg[c] = g[c];
+                                vu[c] = GATE_UP ? u[c] : 0.f;
+                            }
+                        } else {
+                            const float* ps = part_tile + (size_t)sp * S::kAccCols * kBM + (size_t)c0 * kBM + row;
+#pragma unroll
+                            for (int c = 0; c < 16; c++) {
+                                vg[c] = __ldcg(ps + (size_t)c * kBM);
+                                vu[c] = GATE_UP ? __ldcg(ps + (size_t)(BN + c) * kBM) : 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int c = 0; c < 16; c++) {
+                            sg[c] += vg[c];
+                            su[c] += vu[c];
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; c++) {
+                        g[c] = sg[c];
+                        if (GATE_UP) u[c] = su[c];
+                    }
+                }
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     const int cc = c0 + c;
@@ -412,7 +481,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages) {
     const int ab = gate_up ? 2 * kATile : kATile;
     const int stage = ab + bn * kBK * 2;
-    const int staging = bn * r * 4 + 3 * bn * 4 + 8;
+    const int staging = bn * r * 4 + 3 * (bn + 1) * 4 + 8;
     const int table = (4 * E + 1) * 4;
     return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
 }

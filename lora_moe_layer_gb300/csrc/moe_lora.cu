@@ -37,7 +37,10 @@ struct Layout {
     int s1, s2, ks1, ks2;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
         compact_ids, active_experts, lora_buckets, scan_tmp, hist, counters, z1, z1f, xc, act, z2, z2f,
-        pair_out, total;
+        pair_out, tc_part, tc_counters, total;
+    // tensor-core GEMM plan (shared by the launch code and the workspace size)
+    int bn_gu, bn_dn, ks_gu, ks_dn;
+    long tiles_gu, tiles_dn;
     long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
 };
 
@@ -64,6 +67,45 @@ int check_dims(const moe_lora_dims* d) {
     const long long nonempty = std::min(NB, P);
     if (P + nonempty * (bm - 1) > (1LL << 30)) return MOELORA_EUNSUPPORTED;
     return MOELORA_OK;
+}
+
+// K-splits for a GEMM whose weight tiles alone would leave SMs idle: the
+// smallest split count whose task count fills the SMs' waves to >= 90%,
+// keeping >= 512 K-elements per split.  Sized for a 152-SM GB300; on other
+// parts it only changes the balance, not the result.
+int pick_ksplit(long tiles, int K) {
+    constexpr long kSms = 152;
+    if (tiles >= 2 * kSms) return 1;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int ks = 1; ks <= 8 && K / ks >= 512; ks++) {
+        const long tasks = tiles * ks;
+        const long waves = (tasks + kSms - 1) / kSms;
+        const double eff = (double)tasks / (double)(waves * kSms);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = ks;
+        }
+        if (eff >= 0.9) return ks;
+    }
+    return best;
+}
+
+void plan_gemms(const moe_lora_dims* d, Layout* L) {
+    const long experts_max = std::max<long>(1, std::min<long>(d->E, L->P));
+    const long avg_pairs = L->P > 0 ? (L->P + experts_max - 1) / experts_max : 0;
+    const bool narrow = avg_pairs <= 48;
+    L->bn_gu = narrow ? 64 : 128;
+    L->bn_dn = narrow ? 64 : 256;
+    const long nt_gu = (d->I + 127) / 128, nt_dn = (d->H + 127) / 128;
+    // upper bounds on the (expert, tile, chunk) count, for workspace sizing
+    L->tiles_gu = nt_gu * (experts_max + (L->P + L->bn_gu - 1) / L->bn_gu);
+    L->tiles_dn = nt_dn * (experts_max + (L->P + L->bn_dn - 1) / L->bn_dn);
+    // expected counts with the pairs spread evenly, for the split choice
+    const long est_gu = nt_gu * experts_max * ((avg_pairs + L->bn_gu - 1) / L->bn_gu);
+    const long est_dn = nt_dn * experts_max * ((avg_pairs + L->bn_dn - 1) / L->bn_dn);
+    L->ks_gu = pick_ksplit(est_gu, d->H);
+    L->ks_dn = pick_ksplit(est_dn, d->I);
 }
 
 int make_layout(const moe_lora_dims* d, Layout* L) {
@@ -108,6 +150,11 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
+    plan_gemms(d, L);
+    const size_t part_gu = L->ks_gu > 1 ? (size_t)L->tiles_gu * L->ks_gu * 2 * L->bn_gu * 128 : 0;
+    const size_t part_dn = L->ks_dn > 1 ? (size_t)L->tiles_dn * L->ks_dn * L->bn_dn * 128 : 0;
+    L->tc_part = take(sizeof(float) * std::max(part_gu, part_dn));
+    L->tc_counters = take(sizeof(int32_t) * (L->tiles_gu + L->tiles_dn));
     L->total = o;
     return MOELORA_OK;
 }
@@ -217,6 +264,8 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
     a.zero_ints = at<int>(ws, L.counters);
     a.n_zero = d->L > 0 ? (int)(16 * L.nbl) : 0;
+    a.zero_ints2 = at<int>(ws, L.tc_counters);
+    a.n_zero2 = (L.ks_gu > 1 || L.ks_dn > 1) ? (int)(L.tiles_gu + L.tiles_dn) : 0;
     a.hdr = at<WsHeader>(ws, L.hdr);
     return a;
 }
@@ -340,10 +389,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     // NULL stream gets plain stream order
     const bool pdl = s != nullptr && s != cudaStreamLegacy;
 
-    // pair-chunk width of the GEMMs: narrow when experts see few pairs (decode)
     const long experts_max = std::min<long>(d->E, L.P);
-    const long avg_pairs = L.P > 0 ? (L.P + experts_max - 1) / experts_max : 0;
-    const bool narrow = avg_pairs <= 48;
 
     Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
@@ -411,7 +457,10 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     // gate_up on the tensor cores: W1 tiles x (x rows in bucket order)
     {
-        const int bn = narrow ? 64 : 128;
+        const int bn = L.bn_gu;
+        tc.ksplit = L.ks_gu;
+        tc.part = at<float>(ws, L.tc_part);
+        tc.tile_counters = at<int>(ws, L.tc_counters);
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z1f) : nullptr;
         tc.nstages = tc_plan_stages(true, bn, tc.r, d->E);
@@ -419,7 +468,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H))
             return MOELORA_ECUDA;
-        const long tasks = ((d->I + 127) / 128) * (experts_max + (L.P + bn - 1) / bn);
+        const long tasks = L.tiles_gu * L.ks_gu;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
         tr.mark(3);
         if (launch_moe_gemm_tc(tc, true, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
@@ -445,7 +494,9 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     // down on the tensor cores: W2 tiles x act rows
     {
-        const int bn = narrow ? 64 : 256;
+        const int bn = L.bn_dn;
+        tc.ksplit = L.ks_dn;
+        tc.tile_counters = at<int>(ws, L.tc_counters) + L.tiles_gu;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
         tc.nstages = tc_plan_stages(false, bn, tc.r, d->E);
@@ -453,7 +504,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I))
             return MOELORA_ECUDA;
-        const long tasks = ((d->H + 127) / 128) * (experts_max + (L.P + bn - 1) / bn);
+        const long tasks = L.tiles_dn * L.ks_dn;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
         tr.mark(5);
         if (launch_moe_gemm_tc(tc, false, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;

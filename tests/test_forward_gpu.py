@@ -55,6 +55,10 @@ RAGGED = [
     (24, 264, 136, 40, 2, 3, 24),
     (30, 520, 200, 24, 3, 2, 64),
     (16, 128, 96, 64, 4, 5, 8),
+    # one expert, few weight tiles: the GEMMs split K across CTAs
+    (3, 1024, 2048, 1, 1, 4, 16),
+    (5, 1032, 1544, 1, 1, 2, 8),
+    (2, 2048, 512, 2, 1, 1, 64),
 ]
 
 
