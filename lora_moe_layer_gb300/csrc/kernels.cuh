@@ -57,13 +57,17 @@ struct ShrinkArgs {
     const WsHeader* hdr;
     float* z;                   // [S][P][r] split partials (scratch, S > 1)
     float* zfinal;              // [P][r] the shrink output
-    int* counters;              // [buckets * 8] arrivals per (bucket, group), zeroed by align
+    int* counters;              // arrivals per (bucket, group) [buckets * 8] or per bucket, zeroed by align
     uint16_t* xc;               // when set: also copy x rows into bucket order [P][K] (gate_up launch)
 };
 int shrink_splits(int K, long items_no_split);
 int shrink_split_len(int K, int S);
 int shrink_warps_per_block();
 cudaError_t launch_shrink(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl);
+// wide buckets: one CTA per (bucket, 512-wide K split), A staged in shared memory
+int shrink_slab_splits(int K);
+cudaError_t init_shrink_attributes();
+cudaError_t launch_shrink_slab(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl);
 
 // ------------------------------------------------------------ tcgen05 GEMM ----
 // Grouped expert GEMM on the tensor cores (moe_gemm_tc.cu), weight rows on M.

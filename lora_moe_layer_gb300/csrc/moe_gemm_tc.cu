@@ -115,23 +115,28 @@ struct EpiRow {
         cur_l = -2;
     }
 
+    // this row of B[l][e] (and its up row for gate_up) for adapter l: runs once
+    // per adapter run
+    __device__ __forceinline__ void reload(const TcArgs& a, int l) {
+        const int r = a.r;
+        const size_t gbase = (((size_t)l * a.E + e) * rows_per_expert + w_row) * r;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            if (i * 8 < r) {
+                bg[i] = ld_ro16(a.B + gbase + i * 8);
+                if (GATE_UP) bu[i] = ld_ro16(a.B + gbase + (size_t)a.I * r + i * 8);
+            }
+        }
+        cur_l = l;
+    }
+
     // one pair of this row (compact row q, pair id p, adapter l, top-k weight
     // w, its z at zq): add the expand, apply the epilogue, store
     __device__ __forceinline__ void column(const TcArgs& a, int q, int p, int l, float w, const float* zq, float vg,
                                            float vu, bool has_lora) {
         const int r = a.r;
         if (has_lora && l >= 0 && row_ok) {
-            if (l != cur_l) {  // pairs come grouped by adapter: reload only at a run boundary
-                const size_t gbase = (((size_t)l * a.E + e) * rows_per_expert + w_row) * r;
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    if (i * 8 < r) {
-                        bg[i] = ld_ro16(a.B + gbase + i * 8);
-                        if (GATE_UP) bu[i] = ld_ro16(a.B + gbase + (size_t)a.I * r + i * 8);
-                    }
-                }
-                cur_l = l;
-            }
+            if (l != cur_l) reload(a, l);  // pairs come grouped by adapter: once per run
             float dg0 = 0.f, dg1 = 0.f, du0 = 0.f, du1 = 0.f;
 #pragma unroll
             for (int i = 0; i < 8; i++) {
@@ -395,49 +400,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             EpiRow<GATE_UP> er;
             er.init(a, e, w_row, row_ok, rows_per_expert);
             for (int c0 = half * 16; finish && c0 < n_cols; c0 += 32) {
-                float g[16], u[16];
-                tmem_ld16(t_lane + c0, g);
-                if (GATE_UP) tmem_ld16(t_lane + BN + c0, u);
-                if (ksplit > 1) {
-                    // own split from TMEM, the others from their partial tiles,
-                    // summed in split order; one split's 16 columns load at once
-                    float sg[16], su[16];
+                // columns in groups of four keep the loop small (instruction cache)
+                for (int c4 = c0; c4 < c0 + 16 && c4 < n_real; c4 += 4) {
+                    float g4[4], u4[4];
+                    if (ksplit == 1) {
+                        tmem_ld4(t_lane + c4, g4);
+                        if (GATE_UP) tmem_ld4(t_lane + BN + c4, u4);
+                    } else {
+                        // every split's partial (this one's included), added in split order
 #pragma unroll
-                    for (int c = 0; c < 16; c++) sg[c] = su[c] = 0.f;
-                    for (int sp = 0; sp < ksplit; sp++) {
-                        float vg[16], vu[16];
-                        if (sp == tw.split) {
+                        for (int c = 0; c < 4; c++) g4[c] = u4[c] = 0.f;
+                        for (int sp = 0; sp < ksplit; sp++) {
+                            const float* ps = part_tile + (size_t)sp * S::kAccCols * kBM + row;
 #pragma unroll
-                            for (int c = 0; c < 16; c++) {
-                                vg[c] = g[c];
-                                vu[c] = GATE_UP ? u[c] : 0.f;
+                            for (int c = 0; c < 4; c++) {
+                                g4[c] += __ldcg(ps + (size_t)(c4 + c) * kBM);
+                                if (GATE_UP) u4[c] += __ldcg(ps + (size_t)(BN + c4 + c) * kBM);
                             }
-                        } else {
-                            const float* ps = part_tile + (size_t)sp * S::kAccCols * kBM + (size_t)c0 * kBM + row;
-#pragma unroll
-                            for (int c = 0; c < 16; c++) {
-                                vg[c] = __ldcg(ps + (size_t)c * kBM);
-                                vu[c] = GATE_UP ? __ldcg(ps + (size_t)(BN + c) * kBM) : 0.f;
-                            }
-                        }
-#pragma unroll
-                        for (int c = 0; c < 16; c++) {
-                            sg[c] += vg[c];
-                            su[c] += vu[c];
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < 16; c++) {
-                        g[c] = sg[c];
-                        if (GATE_UP) u[c] = su[c];
+                    for (int c = 0; c < 4; c++) {
+                        const int cc = c4 + c;
+                        if (cc < n_real)
+                            er.column(a, q0c + cc, s_pair[cc], s_lora[cc], s_w[cc], zs + cc * r, g4[c],
+                                      GATE_UP ? u4[c] : 0.f, has_lora);
                     }
-                }
-#pragma unroll
-                for (int c = 0; c < 16; c++) {
-                    const int cc = c0 + c;
-                    if (cc < n_real)
-                        er.column(a, q0c + cc, s_pair[cc], s_lora[cc], s_w[cc], zs + cc * r, g[c],
-                                  GATE_UP ? u[c] : 0.f, has_lora);
                 }
             }
             tc_fence_before();

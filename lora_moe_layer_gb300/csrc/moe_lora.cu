@@ -35,6 +35,7 @@ struct Layout {
     int bm;
     long P, NB, cap, tiles;
     int s1, s2, ks1, ks2;
+    bool wide_shrink;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
         compact_ids, active_experts, lora_buckets, scan_tmp, hist, counters, z1, z1f, xc, act, z2, z2f,
         pair_out, tc_part, tc_counters, total;
@@ -118,7 +119,14 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->tiles = L->cap / L->bm;
     const int r = d->L > 0 ? d->r : 0;
     L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
-    if (d->L > 0) {
+    // wide buckets (prefill: several rows per (expert, adapter)) use the
+    // shared-memory slab shrink, narrow ones (decode) the warp-per-item shrink
+    L->wide_shrink = d->L > 0 && L->P >= 4 * std::max<long>(1, std::min(L->NB, L->P));
+    if (d->L > 0 && L->wide_shrink) {
+        L->ks1 = L->ks2 = 512;
+        L->s1 = shrink_slab_splits(d->H);
+        L->s2 = shrink_slab_splits(d->I);
+    } else if (d->L > 0) {
         const long items = L->nbl * (d->r / 8);
         L->ks1 = shrink_split_len(d->H, shrink_splits(d->H, items));
         L->ks2 = shrink_split_len(d->I, shrink_splits(d->I, items));
@@ -178,6 +186,7 @@ int device_setup(DeviceInfo** out) {
         cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = init_align_attributes();
         if (e == cudaSuccess) e = init_tc_attributes();
+        if (e == cudaSuccess) e = init_shrink_attributes();
         info->init_err = e;
     });
     if (info->init_err != cudaSuccess) return MOELORA_ECUDA;
@@ -365,6 +374,20 @@ struct Tracer {
     }
 };
 
+// the shrink variant the layout planned for, with a grid that covers its items
+cudaError_t launch_any_shrink(const ShrinkArgs& sh, const Layout& L, long lora_buckets_max, int sms,
+                              cudaStream_t s, bool pdl, bool gather) {
+    if (L.wide_shrink) {
+        const long items = lora_buckets_max * sh.S;
+        const int grid = (int)std::max<long>(gather ? sms : 1, std::min<long>(items, (long)sms * 4));
+        return launch_shrink_slab(sh, grid, s, pdl);
+    }
+    const long warps = lora_buckets_max * (sh.r / 8) * sh.S;
+    const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
+    const int grid = (int)std::max<long>(gather ? sms : 1, std::min<long>(blocks, (long)sms * 8));
+    return launch_shrink(sh, grid, s, pdl);
+}
+
 int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
                  const float* topk_weights, const int32_t* token_lora_ids, const void* W1,
                  const void* W2, const void* A1, const void* B1, const void* A2, const void* B2,
@@ -436,10 +459,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         sh.zfinal = at<float>(ws, L.z1f);
         sh.counters = at<int>(ws, L.counters);
         sh.xc = at<uint16_t>(ws, L.xc);
-        const long warps = lora_buckets_max * (d->r / 8) * sh.S;
-        const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
-        const int grid = (int)std::max<long>(sms, std::min<long>(blocks, (long)sms * 8));
-        if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        if (launch_any_shrink(sh, L, lora_buckets_max, sms, s, pdl, true) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     TcArgs tc;
@@ -486,10 +506,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         sh.z = at<float>(ws, L.z2);
         sh.zfinal = at<float>(ws, L.z2f);
         sh.counters = at<int>(ws, L.counters) + 8 * L.nbl;
-        const long warps = lora_buckets_max * (d->r / 8) * sh.S;
-        const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
-        const int grid = (int)std::max<long>(1, std::min<long>(blocks, (long)sms * 8));
-        if (launch_shrink(sh, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        if (launch_any_shrink(sh, L, lora_buckets_max, sms, s, pdl, false) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     // down on the tensor cores: W2 tiles x act rows

@@ -16,8 +16,10 @@
 // adds the partials in split order, so the result is deterministic.  No shared
 // memory and no block-wide barrier: warps run independently.
 //
-// The gate_up launch also copies x rows into bucket order (the B operand of
-// the gate_up GEMM), so the forward needs no separate gather launch.
+// For wide buckets (tens of rows) a second kernel below stages A in shared
+// memory per CTA instead.  The gate_up launch of either also copies x rows
+// into bucket order (the B operand of the gate_up GEMM), so the forward needs
+// no separate gather launch.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -38,6 +40,53 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRB = 1;  // bucket rows per pass
 
+// x rows into bucket order (the gate_up GEMM's B operand), four copies in
+// flight per thread, grid-strided over all CTAs of the launch
+__device__ void gather_rows(const ShrinkArgs& a) {
+    const int K = a.K;
+    const int c8 = K >> 3;
+    const long total = (long)a.hdr->n_valid * c8;
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i0 = (long)blockIdx.x * blockDim.x + threadIdx.x; i0 < total; i0 += 4 * stride) {
+        uint4 v[4];
+        long dst[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const long idx = i0 + u * stride;
+            dst[u] = -1;
+            if (idx < total) {
+                const int q = (int)(idx / c8), c = (int)(idx % c8);
+                dst[u] = (long)q * K + c * 8;
+                v[u] = ld_ro16(a.in + (size_t)(a.compact_ids[q] / a.k) * K + c * 8);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++)
+            if (dst[u] >= 0) *reinterpret_cast<uint4*>(a.xc + dst[u]) = v[u];
+    }
+}
+
+// z rows of one (bucket, output group) completed by the last split: the S
+// partials added in split order, loads in batches of 8
+__device__ __forceinline__ void finish_split(const ShrinkArgs& a, int row0, int row1, int col0, int ncol, int tid,
+                                             int nthreads) {
+    const int r = a.r, S = a.S;
+    const int n = (row1 - row0) * ncol;
+    for (int idx = tid; idx < n; idx += nthreads) {
+        const size_t off = (size_t)(row0 + idx / ncol) * r + col0 + idx % ncol;
+        float v = 0.f;
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float part[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) part[u] = s0 + u < S ? __ldcg(a.z + (size_t)(s0 + u) * a.P * r + off) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 8; u++)
+                if (s0 + u < S) v += part[u];
+        }
+        a.zfinal[off] = v;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 2) k_shrink(ShrinkArgs a) {
     pdl_wait();
     pdl_trigger();
@@ -46,29 +95,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_shrink(ShrinkArgs a) {
     const int r = a.r;
     const int K = a.K;
 
-    if (a.xc) {
-        // x rows into bucket order, four copies in flight per thread
-        const int c8 = K >> 3;
-        const long total = (long)a.hdr->n_valid * c8;
-        const long stride = (long)gridDim.x * kThreads;
-        for (long i0 = (long)blockIdx.x * kThreads + threadIdx.x; i0 < total; i0 += 4 * stride) {
-            uint4 v[4];
-            long dst[4];
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-                const long idx = i0 + u * stride;
-                dst[u] = -1;
-                if (idx < total) {
-                    const int q = (int)(idx / c8), c = (int)(idx % c8);
-                    dst[u] = (long)q * K + c * 8;
-                    v[u] = ld_ro16(a.in + (size_t)(a.compact_ids[q] / a.k) * K + c * 8);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; u++)
-                if (dst[u] >= 0) *reinterpret_cast<uint4*>(a.xc + dst[u]) = v[u];
-        }
-    }
+    if (a.xc) gather_rows(a);
 
     const int groups = r >> 3;
     const int S = a.S;
@@ -149,27 +176,138 @@ __global__ void __launch_bounds__(kThreads, 2) k_shrink(ShrinkArgs a) {
             last = __shfl_sync(kFull, last, 0);
             if (last) {
                 __threadfence();
-                const int n = (row1 - row0) * 8;
-                for (int idx = lane; idx < n; idx += 32) {
-                    const size_t off = (size_t)(row0 + idx / 8) * r + g * 8 + (idx & 7);
-                    float v = 0.f;
-                    for (int s0 = 0; s0 < S; s0 += 8) {  // loads in batches of 8, sums in split order
-                        float part[8];
-#pragma unroll
-                        for (int u = 0; u < 8; u++)
-                            part[u] = s0 + u < S ? __ldcg(a.z + (size_t)(s0 + u) * a.P * r + off) : 0.f;
-#pragma unroll
-                        for (int u = 0; u < 8; u++)
-                            if (s0 + u < S) v += part[u];
-                    }
-                    a.zfinal[off] = v;
-                }
+                finish_split(a, row0, row1, g * 8, 8, lane, 32);
             }
         }
     }
 }
 
+// ---------------------------------------------------------------------------
+// Wide buckets (prefill: tens of rows per (expert, adapter)): one CTA per
+// (bucket, K-split of kSlabK elements) stages the r x kSlabK slab of A[l][e]
+// in shared memory once (eight 16-byte loads in flight per thread), and its
+// eight warps share the bucket's rows: per row, lanes side by side along K,
+// every A row read from shared memory, then a reduce-scatter.  Split-K
+// partials are finished by the last CTA of the bucket, in split order.
+constexpr int kSlabK = 512;
+
+template <int RP>  // rank rounded up to a power of two (8, 16, 32, 64)
+__global__ void __launch_bounds__(kThreads) k_shrink_slab(ShrinkArgs a) {
+    extern __shared__ __align__(16) uint16_t slab[];  // [RP][kSlabK]
+    __shared__ int s_last;
+    pdl_wait();
+    pdl_trigger();
+    if (a.xc) gather_rows(a);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L1 = a.L + 1;
+    const int r = a.r, K = a.K, S = a.S;
+    const int n_items = a.hdr->n_lora_buckets * S;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int bi = item / S, s = item % S;
+        const int b = a.lora_buckets[bi];
+        const int e = b / L1, l = b % L1 - 1;
+        const int row0 = a.compact_offset[b], row1 = a.compact_offset[b + 1];
+        const int k0 = s * kSlabK;
+        const int kc = min(kSlabK, K - k0);
+        const int chunks = kc >> 3;
+        const uint16_t* abase = a.A + ((size_t)(l * a.E + e) * r) * K + k0;
+
+        __syncthreads();  // the previous item's slab is no longer read
+        const int n16 = r * chunks;
+        for (int c0 = threadIdx.x; c0 < n16; c0 += 8 * kThreads) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int c = c0 + u * kThreads;
+                if (c < n16) v[u] = ld_stream16(abase + (size_t)(c / chunks) * K + (c % chunks) * 8);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int c = c0 + u * kThreads;
+                if (c < n16) *reinterpret_cast<uint4*>(slab + (c / chunks) * kSlabK + (c % chunks) * 8) = v[u];
+            }
+        }
+        __syncthreads();
+
+        for (int row = row0 + warp; row < row1; row += kWarps) {
+            const uint16_t* in = (a.in_is_x ? a.in + (size_t)(a.compact_ids[row] / a.k) * K : a.in + (size_t)row * K) + k0;
+            uint4 xin[kSlabK / 256];
+#pragma unroll
+            for (int u = 0; u < kSlabK / 256; u++) {
+                const int c = lane + 32 * u;
+                xin[u] = make_uint4(0, 0, 0, 0);
+                if (c < chunks) xin[u] = a.in_is_x ? ld_ro16(in + c * 8) : ld_cg16(in + c * 8);
+            }
+            float acc[RP];
+#pragma unroll
+            for (int i = 0; i < RP; i++) acc[i] = 0.f;
+#pragma unroll
+            for (int u = 0; u < kSlabK / 256; u++) {
+                const int c = lane + 32 * u;
+                if (c < chunks) {
+                    float xv[8];
+                    unpack8(xin[u], xv);
+#pragma unroll
+                    for (int rr = 0; rr < RP; rr++)
+                        if (rr < r) acc[rr] = dot8(*reinterpret_cast<const uint4*>(slab + rr * kSlabK + c * 8), xv, acc[rr]);
+                }
+            }
+            float* dst = (S == 1 ? a.zfinal : a.z + (size_t)s * a.P * r) + (size_t)row * r;
+            if constexpr (RP <= 32) {
+                const float tot = warp_reduce_scatter<RP>(acc, lane);
+                const int idx = lane / (32 / RP);
+                if (lane % (32 / RP) == 0 && idx < r) dst[idx] = tot;
+            } else {
+                float lo[32], hi[32];
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    lo[i] = acc[i];
+                    hi[i] = acc[32 + i];
+                }
+                const float tlo = warp_reduce_scatter<32>(lo, lane);
+                const float thi = warp_reduce_scatter<32>(hi, lane);
+                if (lane < r) dst[lane] = tlo;
+                if (32 + lane < r) dst[32 + lane] = thi;
+            }
+        }
+
+        if (S > 1) {
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_last = atomicAdd(&a.counters[bi], 1) == S - 1;
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                finish_split(a, row0, row1, 0, r, threadIdx.x, kThreads);
+            }
+        }
+    }
+}
+
+template <int RP>
+cudaError_t slab_attr() {
+    return cudaFuncSetAttribute(k_shrink_slab<RP>, cudaFuncAttributeMaxDynamicSharedMemorySize, RP * kSlabK * 2);
+}
+
 }  // namespace
+
+cudaError_t init_shrink_attributes() {
+    cudaError_t e;
+    if ((e = slab_attr<8>()) != cudaSuccess) return e;
+    if ((e = slab_attr<16>()) != cudaSuccess) return e;
+    if ((e = slab_attr<32>()) != cudaSuccess) return e;
+    return slab_attr<64>();
+}
+
+int shrink_slab_splits(int K) { return (K + kSlabK - 1) / kSlabK; }
+
+cudaError_t launch_shrink_slab(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl) {
+    const dim3 g(grid), b(kThreads);
+    if (args.r <= 8) return launch_k(k_shrink_slab<8>, g, b, 8 * kSlabK * 2, stream, pdl, args);
+    if (args.r <= 16) return launch_k(k_shrink_slab<16>, g, b, 16 * kSlabK * 2, stream, pdl, args);
+    if (args.r <= 32) return launch_k(k_shrink_slab<32>, g, b, 32 * kSlabK * 2, stream, pdl, args);
+    return launch_k(k_shrink_slab<64>, g, b, 64 * kSlabK * 2, stream, pdl, args);
+}
 
 int shrink_splits(int K, long items_no_split) {
     // about 2048 warps in flight (a GB300 holds ~9700), in K slices of 256 or more
