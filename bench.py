@@ -191,7 +191,7 @@ def run_ours(args, rank, world, local_rank):
     dl = DeviceLayer(layer, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    kernels_per_forward = 7 if layer.L > 0 else 5
+    kernels_per_forward = 5  # align, gather, gate_up, down, reduce
 
     def fwd():
         st = dl.forward(stream=stream)

@@ -149,14 +149,14 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
  * cudaEvent_t handles created by the caller (cudaEventCreate); event i is
  * recorded on `stream` just before kernel slot i and the last one after the
  * final kernel.  Kernel slots: 0 align, 1 gather of x into bucket order,
- * 2 gate_up LoRA shrink, 3 gate_up grouped GEMM (+expand, SiLU*up), 4 down
- * LoRA shrink, 5 down grouped GEMM (+expand, x weight), 6 top-k reduce; a
- * slot that has no kernel (no adapters) gets an empty interval.  The recorded events replace the programmatic launch overlap
- * between consecutive kernels with plain stream order.  Same results and
- * status codes as moe_lora_forward, plus MOELORA_EINVAL if kernel_events is
- * NULL or n_events < MOELORA_TRACE_EVENTS.
+ * 2 gate_up tcgen05 kernel (LoRA shrink items, grouped GEMM, expand,
+ * SiLU*up), 3 down tcgen05 kernel (LoRA shrink items, grouped GEMM, expand,
+ * x weight), 4 top-k reduce.  The recorded events replace the programmatic
+ * launch overlap between consecutive kernels with plain stream order.  Same
+ * results and status codes as moe_lora_forward, plus MOELORA_EINVAL if
+ * kernel_events is NULL or n_events < MOELORA_TRACE_EVENTS.
  */
-#define MOELORA_TRACE_EVENTS 8
+#define MOELORA_TRACE_EVENTS 6
 MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
                                         const int32_t *topk_ids, const float *topk_weights,
                                         const int32_t *token_lora_ids, const void *W1,

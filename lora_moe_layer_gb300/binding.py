@@ -29,9 +29,9 @@ EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced",
             "moe_lora_forward_noalloc")
 MOELORA_NOALLOC_SCRATCH_BYTES = 16 << 20
-MOELORA_TRACE_EVENTS = 8
+MOELORA_TRACE_EVENTS = 6
 # kernel slots of one forward, in launch order
-KERNEL_SLOTS = ("align", "gather_x", "gate_up_shrink", "gate_up_gemm", "down_shrink", "down_gemm", "topk_reduce")
+KERNEL_SLOTS = ("align", "gather_x", "gate_up_gemm", "down_gemm", "topk_reduce")
 
 
 class MoeLoraError(RuntimeError):

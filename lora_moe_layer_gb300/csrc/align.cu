@@ -222,6 +222,30 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         for (int b = threadIdx.x; b < NB; b += kAlignThreads)
             if ((b % L1) != 0 && cnt[b] > 0) a.lora_buckets[a.scan_tmp[b]] = b;
         if (threadIdx.x == 0) hdr->n_lora_buckets = a.scan_tmp[NB];
+        __syncthreads();
+        if (a.st_tasks) {
+            // shrink tasks: st_G consecutive adapter buckets per group; a group's
+            // rows are contiguous in bucket order and split into chunks of st_BN
+            const int n = a.scan_tmp[NB];
+            __syncthreads();
+            const int G = a.st_G, BN = a.st_BN;
+            const int ng = (n + G - 1) / G;
+            const int* lb = a.lora_buckets;
+            auto rows = [&](int g) {
+                const int j1 = min(n, g * G + G) - 1;
+                return make_int2(coff[lb[g * G]], coff[lb[j1] + 1]);
+            };
+            block_scan_items(
+                ng, [&](int g) { const int2 q = rows(g); return make_int2((q.y - q.x + BN - 1) / BN, 0); },
+                a.scan_tmp, nullptr, sw);
+            __syncthreads();
+            for (int g = threadIdx.x; g < ng; g += kAlignThreads) {
+                const int2 q = rows(g);
+                int at = a.scan_tmp[g];
+                for (int q0 = q.x; q0 < q.y; q0 += BN) a.st_tasks[at++] = make_int4(g, q0, min(BN, q.y - q0), 0);
+            }
+            if (threadIdx.x == 0) hdr->n_shrink_tasks = a.scan_tmp[ng];
+        }
     }
     pdl_trigger();
 }

@@ -17,7 +17,8 @@ struct WsHeader {
     int32_t n_valid;          // valid pairs (= rows of the compact order)
     int32_t n_active;         // experts with at least one valid pair
     int32_t n_lora_buckets;   // (expert, adapter >= 0) buckets with at least one pair
-    int32_t reserved[59];
+    int32_t n_shrink_tasks;   // entries of the LoRA shrink task list
+    int32_t reserved[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte block");
 

@@ -33,6 +33,10 @@ struct AlignArgs {
     int n_zero;
     int* zero_ints2;           // [n_zero2] second region (GEMM split-K counters), or null
     int n_zero2;
+    // LoRA shrink task list (null: none): buckets of lora_buckets in groups of
+    // st_G, each group's rows in chunks of at most st_BN, as (group, first row, rows, 0)
+    int4* st_tasks;
+    int st_G, st_BN;
     WsHeader* hdr;
 };
 
@@ -41,43 +45,24 @@ long align_hist_global_ints(int E, int L);
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream);
 cudaError_t init_align_attributes();
 
-// --------------------------------------------------------------- shrink ----
-// z[row][0:r] = A[l][e][0:r][:] . in(row) for every compact row of every
-// (e, l >= 0) bucket, one warp per (bucket, 8 outputs, K-split) item.
-struct ShrinkArgs {
-    int E, L, k, r, K, P;
-    int S;                      // K-splits
-    int ks;                     // K elements per split (multiple of 256)
-    int in_is_x;                // 1: in(row) = x[compact_ids[row] / k]; 0: in(row) = act[row]
-    const uint16_t* in;         // x [T][K] or act [P][K]
-    const uint16_t* A;          // [L][E][r][K]
-    const int32_t* lora_buckets;
-    const int32_t* compact_offset;
-    const int32_t* compact_ids;
-    const WsHeader* hdr;
-    float* z;                   // [S][P][r] split partials (scratch, S > 1)
-    float* zfinal;              // [P][r] the shrink output
-    int* counters;              // arrivals per (bucket, group) [buckets * 8] or per bucket, zeroed by align
-    uint16_t* xc;               // when set: also copy x rows into bucket order [P][K] (gate_up launch)
-};
-int shrink_splits(int K, long items_no_split);
-int shrink_split_len(int K, int S);
-int shrink_warps_per_block();
-cudaError_t launch_shrink(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl);
-// wide buckets: one CTA per (bucket, 512-wide K split), A staged in shared memory
-int shrink_slab_splits(int K);
-cudaError_t init_shrink_attributes();
-cudaError_t launch_shrink_slab(const ShrinkArgs& args, int grid, cudaStream_t stream, bool pdl);
-
 // ------------------------------------------------------------ tcgen05 GEMM ----
 // Grouped expert GEMM on the tensor cores (moe_gemm_tc.cu), weight rows on M.
 constexpr int kTcSmemLimit = 227 * 1024 - 1024;
 struct TcArgs {
     CUtensorMap wmap;            // W1 as [E][2][I][H] (gate_up) or W2 [E][H][I]; box 64 (K) x 128 rows
     CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16 rows
+    CUtensorMap amap;            // LoRA A (A1 / A2) as [L*E*r][K]; box 64 (K) x r rows
     int E, L, k, r, I, H, P;
     const uint16_t* B;           // B1 / B2 (null: no LoRA)
-    const float* z;              // final shrink output [P][r] (null: no LoRA)
+    float* z;                    // shrink output [P][r], written by the shrink items (null: no LoRA)
+    // LoRA shrink items, run first (the GEMM epilogues wait for all of them):
+    // align's task list, G adapter buckets per task, K-split into sh_ks parts
+    const int4* sh_tasks;
+    int sh_G, sh_ks;
+    const int32_t* lora_buckets;
+    float* zpart;                // [sh_ks][P][r] split partials (sh_ks > 1)
+    int* sh_counters;            // [tasks] split arrivals, zeroed by align
+    int* zdone;                  // shrink tasks finished, zeroed by align
     const int32_t* lora_ids;
     const float* topk_weights;
     const int32_t* active_experts;

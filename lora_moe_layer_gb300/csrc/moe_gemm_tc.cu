@@ -15,7 +15,20 @@
 // MMAs, and a prefill chunk fills N up to BN.  A task is (active expert,
 // 128-row weight tile, chunk of at most BN pairs).
 //
-// Warp roles (one CTA per SM, persistent over a contiguous task range):
+// The LoRA shrink of the same projection (z = A[l][e] . in, the blog's
+// skinny split-K GEMM, section "Kernel optimizations") runs in the same launch
+// as "shrink items" ahead of the GEMM tasks: an item stacks the A matrices of
+// G = 128 / r consecutive (expert, adapter) buckets on M (slot s = rows
+// s*r .. s*r+r-1) against those buckets' pairs -- a contiguous run of rows in
+// bucket order -- on N, and each pair keeps its own slot's r rows (the cross
+// terms cost tensor time only).  K is split across items when the buckets are
+// few; the split that arrives last adds the partials in split order
+// (deterministic).  Every CTA runs its shrink items before its GEMM tasks, and
+// a GEMM epilogue reads z only after a device counter shows every shrink task
+// finished, so the shrink hides under the weight streaming instead of being a
+// launch of its own.
+//
+// Warp roles (one CTA per SM, persistent; items dealt round-robin):
 //   warp 0   TMA producer: per 64-wide K step, the weight tile (gate_up: the
 //            128 gate rows and the 128 matching up rows) and the pairs' rows
 //            (x or act in bucket order, 16-row boxes), all 128-byte swizzled,
@@ -166,18 +179,125 @@ struct EpiRow {
     }
 };
 
+// ---------------------------------------------------------------- shrink items
+constexpr int kMaxSlots = 16;  // adapter buckets per shrink item: 128 / r with r >= 8
+
+// shrink item t: task t / sh_ks of align's list (G buckets from bucket-list
+// index j0, pair rows q0c .. q0c + n_real), K-split sp
+struct ShItem {
+    int i, sp, j0, nb, q0c, n_real, n_cols;
+    __device__ void load(const TcArgs& a, int t, int n_lora) {
+        i = t / a.sh_ks;
+        sp = t % a.sh_ks;
+        const int4 v = __ldcg(a.sh_tasks + i);
+        j0 = v.x * a.sh_G;
+        nb = min(a.sh_G, n_lora - j0);
+        q0c = v.y;
+        n_real = v.z;
+        n_cols = (n_real + 15) & ~15;
+    }
+};
+
+// spin (bounded) until *p >= target; 1 on success
+__device__ __forceinline__ int wait_count(const int* p, int target) {
+    for (uint32_t i = 0; i < kWaitRounds; i++) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return 1;
+        __nanosleep(64);
+    }
+    return 0;
+}
+
+// Epilogue of shrink item t: each thread is one TMEM lane = (slot, rank
+// index) row and stores z for the pairs of its slot; the two warps of a lane
+// quadrant take alternate 4-column groups.  With a K-split, the split that
+// arrives last sums all partials in split order.  The item then counts
+// itself in zdone.  False on a timeout (warp-uniform).
+template <typename Rdv>
+__device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int it, uint32_t tmem_base,
+                                uint32_t acc_cols, int qd, int half, int lane, int etid, int* s_cb, int* s_ce,
+                                int* s_misc, uint64_t* tfull, uint64_t* tempty, Rdv& rendezvous) {
+    ShItem sh;
+    sh.load(a, t, n_lora);
+    const int r = a.r;
+    // slot column ranges (after everyone is done with the previous item's staging)
+    if (!rendezvous()) return false;
+    if (etid < sh.nb) {
+        const int bk = a.lora_buckets[sh.j0 + etid];
+        s_cb[etid] = min(max(a.compact_offset[bk] - sh.q0c, 0), sh.n_real);
+        s_ce[etid] = min(max(a.compact_offset[bk + 1] - sh.q0c, 0), sh.n_real);
+    }
+    if (!rendezvous()) return false;
+    const int row = qd * 32 + lane;
+    const int my_s = row / r, j = row % r;
+    const int s_lo = (qd * 32) / r, s_hi = min((qd * 32 + 31) / r, sh.nb - 1);
+    const bool mine = my_s < sh.nb;
+    const int mcb = mine ? s_cb[my_s] : 0, mce = mine ? s_ce[my_s] : 0;
+    const int clo = s_lo < sh.nb ? s_cb[s_lo] : 0;
+    const int chi = s_lo < sh.nb ? s_ce[s_hi] : 0;
+    float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
+
+    if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) return false;
+    tc_fence_after();
+    const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)b * acc_cols;
+    for (int c4 = (clo & ~3) + 4 * half; c4 < chi; c4 += 8) {
+        float v[4];
+        tmem_ld4(t_lane + c4, v);
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            const int cc = c4 + c;
+            if (cc >= mcb && cc < mce) dst[(size_t)(sh.q0c + cc) * r + j] = v[c];
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[b]);
+    __threadfence();
+    if (!rendezvous()) return false;
+    if (a.sh_ks > 1) {
+        if (etid == 0) s_misc[1] = atomicAdd(&a.sh_counters[sh.i], 1) == a.sh_ks - 1;
+        if (!rendezvous()) return false;
+        if (!s_misc[1]) return true;
+        // one flat pass over the rows the item's slots cover (rows of base-only
+        // pairs in between get a sum nobody reads)
+        __threadfence();
+        const int lo = s_cb[0], hi = s_ce[sh.nb - 1];
+        const size_t beg = (size_t)(sh.q0c + lo) * r;
+        const int n4 = (hi - lo) * r / 4;
+        const float4* src = reinterpret_cast<const float4*>(a.zpart + beg);
+        float4* out = reinterpret_cast<float4*>(a.z + beg);
+        const size_t split4 = (size_t)a.P * r / 4;
+        for (int i4 = etid; i4 < n4; i4 += kEpiWarps * 32) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int q = 0; q < a.sh_ks; q++) {
+                const float4 v = __ldcg(src + q * split4 + i4);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            out[i4] = acc;
+        }
+        __threadfence();
+        if (!rendezvous()) return false;
+    }
+    if (etid == 0) atomicAdd(a.zdone, 1);
+    return true;
+}
+
 template <bool GATE_UP, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_constant__ TcArgs a) {
     using S = TcShape<GATE_UP, BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
-    // epilogue staging: z rows [BN][r] fp32, then pair id / adapter / weight per column
+    // epilogue staging: z rows [BN][r] fp32, then pair id / adapter / weight per
+    // column (a shrink item keeps its slots' column ranges in s_pair / s_lora)
     float* zs = reinterpret_cast<float*>(base + (size_t)NS * S::kStage);
     int* s_pair = reinterpret_cast<int*>(zs + (size_t)BN * a.r);
-    int* s_lora = s_pair + BN + 1;  // s_pair[BN] carries the split-K verdict
+    int* s_lora = s_pair + BN;
     float* s_w = reinterpret_cast<float*>(s_lora + BN);
-    uint64_t* full = reinterpret_cast<uint64_t*>(s_w + BN + 1);
+    int* s_misc = reinterpret_cast<int*>(s_w + BN);  // [4] verdicts shared by the epilogue warps
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_misc + 4);
     uint64_t* empty = full + NS;
     uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
     uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
@@ -209,6 +329,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&a.wmap);
         prefetch_tensormap(&a.xmap);
+        if (a.sh_tasks) prefetch_tensormap(&a.amap);
     }
     tc_fence_before();
     __syncthreads();
@@ -218,7 +339,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     pdl_wait();
     pdl_trigger();
 
-    const int L1 = a.L + 1;
     const int N_out = GATE_UP ? a.I : a.H;
     const int K = GATE_UP ? a.H : a.I;
     const int ntiles = (N_out + kBM - 1) / kBM;
@@ -226,6 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     const int n_active = a.hdr->n_active;
     // task table: independent loads across threads, then one warp scans the counts
     for (int ai = threadIdx.x; ai < n_active; ai += kTcThreads) {
+        const int L1 = a.L + 1;
         const int e = a.active_experts[ai];
         const int q0 = a.compact_offset[e * L1];
         const int m = a.compact_offset[(e + 1) * L1] - q0;
@@ -252,7 +373,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     }
     __syncthreads();
     const int ksplit = a.ksplit;
-    const int total = tt.cum[n_active] * ksplit;
+    // shrink items first, then the GEMM tasks
+    const bool shrink = a.sh_tasks != nullptr && a.r > 0;
+    const int sh_ks = a.sh_ks;
+    const int n_sh_tasks = shrink ? a.hdr->n_shrink_tasks : 0;
+    const int n_sh = n_sh_tasks * sh_ks;
+    const int n_lora = shrink ? a.hdr->n_lora_buckets : 0;
+    const int L1 = a.L + 1;
+    const int total = n_sh + tt.cum[n_active] * ksplit;
     // tasks are dealt round-robin, so the pair chunks of one weight tile (and
     // the tiles of one expert) stream on neighbouring CTAs at the same time and
     // share their operands through L2
@@ -264,9 +392,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, armed = 0, last_par = 0;
+            int arow[kMaxSlots];
             for (int t = t_first; t < total && ok; t += t_step) {
+                if (t < n_sh) {
+                    // shrink item: one r-row box per slot, then the pair rows
+                    ShItem sh;
+                    sh.load(a, t, n_lora);
+                    for (int q = 0; q < sh.nb; q++) {
+                        const int b = a.lora_buckets[sh.j0 + q];
+                        arow[q] = ((b % L1 - 1) * a.E + b / L1) * a.r;  // first row of A[l][e]
+                    }
+                    const uint32_t bytes = (uint32_t)(sh.nb * a.r + sh.n_cols) * kBK * 2;
+                    const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
+                    for (int kb = kb0; kb < kb1; kb++) {
+                        if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&full[stage], bytes);
+                        uint8_t* dst = base + (size_t)stage * S::kStage;
+                        const int k0 = kb * kBK;
+                        for (int q = 0; q < sh.nb; q++)
+                            tma_load_2d(dst + q * a.r * kBK * 2, &a.amap, &full[stage], k0, arow[q]);
+                        for (int g = 0; g < sh.n_cols / kBBoxRows; g++)
+                            tma_load_2d(dst + kATile + g * kBBox, &a.xmap, &full[stage], k0, sh.q0c + g * kBBoxRows);
+                        armed |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                    continue;
+                }
                 Task<BN> tw;
-                tw.lookup(tt, n_active, ksplit, t);
+                tw.lookup(tt, n_active, ksplit, t - n_sh);
                 const int n_cols = tw.n_cols, row0 = tw.q0c, e = tw.e;
                 const uint32_t bytes = S::kAB + (uint32_t)n_cols * kBK * 2;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
@@ -298,12 +452,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             int stage = 0;
             uint32_t phase = 0;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-                Task<BN> tw;
-                tw.lookup(tt, n_active, ksplit, t);
                 const int b = it & 1;
                 if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
+                if (t < n_sh) {
+                    // shrink item: stacked adapter rows x pair rows, N up to the buffer's columns
+                    ShItem sh;
+                    sh.load(a, t, n_lora);
+                    const uint32_t idesc = umma_idesc_bf16_f32(kBM, sh.n_cols);
+                    const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
+                    for (int kb = kb0; kb < kb1; kb++) {
+                        if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; kk++)
+                            umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32),
+                                      umma_desc_sw128(a_addr + kATile + kk * 32), idesc, (kb != kb0) || (kk != 0));
+                        umma_commit(&empty[stage]);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    umma_commit(&tfull[b]);
+                    continue;
+                }
+                Task<BN> tw;
+                tw.lookup(tt, n_active, ksplit, t - n_sh);
                 const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -337,16 +512,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         const size_t rows_per_expert = GATE_UP ? 2 * (size_t)a.I : (size_t)a.H;
         const int r = a.r;
         uint32_t epar = 0;
+        bool z_ready = !has_lora;
+        // all epilogue warps meet here (bounded); false on timeout, warp-uniform
+        auto rendezvous = [&]() {
+            mbar_arrive(ebar);
+            const bool r_ok = __all_sync(kFull, mbar_wait(ebar, epar));
+            epar ^= 1;
+            return r_ok;
+        };
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-            Task<BN> tw;
-            tw.lookup(tt, n_active, ksplit, t);
             const int b = it & 1;
+            if (t < n_sh) {
+                if (!shrink_epilogue(a, t, n_lora, b, it, tmem_base, S::kAccCols, qd, half, lane, etid, s_pair,
+                                     s_lora, s_misc, tfull, tempty, rendezvous)) { ok = false; break; }
+                continue;
+            }
+            Task<BN> tw;
+            tw.lookup(tt, n_active, ksplit, t - n_sh);
             const int e = tw.e, q0c = tw.q0c, n_real = tw.n_real, n_cols = tw.n_cols;
+            // z is complete once every shrink task has finished (they run first on every CTA)
+            if (!z_ready && etid == 0) s_misc[0] = wait_count(a.zdone, n_sh_tasks);
             // stage this task's column data while its MMAs run (after everyone
             // is done with the previous task's)
-            mbar_arrive(ebar);
-            if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
-            epar ^= 1;
+            if (!rendezvous()) { ok = false; break; }
+            if (!z_ready) {
+                if (!s_misc[0]) { ok = false; break; }
+                __threadfence();
+                z_ready = true;
+            }
             for (int c = etid; c < n_real; c += kEpiWarps * 32) {
                 const int p = a.compact_ids[q0c + c];
                 s_pair[c] = p;
@@ -358,9 +551,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 float4* zdst = reinterpret_cast<float4*>(zs);
                 for (int i = etid; i < n_real * r / 4; i += kEpiWarps * 32) zdst[i] = __ldcg(zsrc + i);
             }
-            mbar_arrive(ebar);
-            if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
-            epar ^= 1;
+            if (!rendezvous()) { ok = false; break; }
 
             // warp-uniform outcome: the TMEM loads below are warp-collective
             if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) { ok = false; break; }
@@ -387,14 +578,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     }
                 }
                 __threadfence();
-                mbar_arrive(ebar);
-                if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
-                epar ^= 1;
-                if (etid == 0) s_pair[BN] = atomicAdd(&a.tile_counters[tw.tile], 1) == ksplit - 1;
-                mbar_arrive(ebar);
-                if (!__all_sync(kFull, mbar_wait(ebar, epar))) { ok = false; break; }
-                epar ^= 1;
-                finish = s_pair[BN] != 0;
+                if (!rendezvous()) { ok = false; break; }
+                if (etid == 0) s_misc[1] = atomicAdd(&a.tile_counters[tw.tile], 1) == ksplit - 1;
+                if (!rendezvous()) { ok = false; break; }
+                finish = s_misc[1] != 0;
                 if (finish) __threadfence();
             }
             EpiRow<GATE_UP> er;
@@ -469,7 +656,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages) {
     const int ab = gate_up ? 2 * kATile : kATile;
     const int stage = ab + bn * kBK * 2;
-    const int staging = bn * r * 4 + 3 * (bn + 1) * 4 + 8;
+    const int staging = bn * r * 4 + 3 * bn * 4 + 16;
     const int table = (4 * E + 1) * 4;
     return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
 }

@@ -2,15 +2,16 @@
 // argument validation, workspace layout, per-device kernel set-up and the
 // launch sequence of one forward.
 //
-// One forward is seven kernels on the caller's stream, chained with
+// One forward is five kernels on the caller's stream, chained with
 // programmatic dependent launch so each can be resident before its
 // predecessor drains (the blog's PDL step, "Efficiently serve dozens of
 // fine-tuned models with vLLM ...", section "Execution optimizations"):
-//   align -> gather x into bucket order -> [gate_up shrink]
-//         -> gate_up tcgen05 GEMM (+expand, SiLU*up) -> [down shrink]
-//         -> down tcgen05 GEMM (+expand, x weight) -> top-k reduce.
-// The shrinks are skipped when the layer has no adapters, and exit at once
-// when no token of the batch uses one (the blog's early exit, same section).
+//   align -> gather x into bucket order
+//         -> gate_up tcgen05 kernel (LoRA shrink items, then W1 tiles + expand, SiLU*up)
+//         -> down tcgen05 kernel (LoRA shrink items, then W2 tiles + expand, x weight)
+//         -> top-k reduce.
+// A layer without adapters, or a batch without adapter tokens, has no shrink
+// items (the blog's early exit, same section).
 // Nothing here allocates device memory or synchronises the host.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -18,6 +19,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -34,11 +36,13 @@ constexpr int kMaxDevices = 64;
 struct Layout {
     int bm;
     long P, NB, cap, tiles;
-    int s1, s2, ks1, ks2;
-    bool wide_shrink;
+    // LoRA shrink plan: K-splits of the two shrinks, adapter buckets per task,
+    // pairs per task, and the task-list bound
+    int s1, s2, st_G, st_bn;
+    long st_tasks_max;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
-        compact_ids, active_experts, lora_buckets, scan_tmp, hist, counters, z1, z1f, xc, act, z2, z2f,
-        pair_out, tc_part, tc_counters, total;
+        compact_ids, active_experts, lora_buckets, scan_tmp, hist, st_tasks, counters, z1, z1f, xc, act, z2,
+        z2f, pair_out, tc_part, tc_counters, total;
     // tensor-core GEMM plan (shared by the launch code and the workspace size)
     int bn_gu, bn_dn, ks_gu, ks_dn;
     long tiles_gu, tiles_dn;
@@ -92,6 +96,38 @@ int pick_ksplit(long tiles, int K) {
     return best;
 }
 
+// K-splits of a shrink: enough (task, split) items for one wave of SMs, at
+// least two 64-wide K steps per split.
+int pick_shrink_split(long est_tasks, int K) {
+    constexpr long kSms = 152;
+    const int nkb = (K + 63) / 64;
+    if (est_tasks >= kSms) return 1;
+    const long want = (kSms + std::max<long>(est_tasks, 1) - 1) / std::max<long>(est_tasks, 1);
+    return (int)std::max<long>(1, std::min<long>({want, (long)std::max(1, nkb / 2), 32L}));
+}
+
+// Shrink plan from the expected number of touched (expert, adapter) buckets
+// when the pairs spread uniformly over the E*L of them.
+void plan_shrinks(const moe_lora_dims* d, Layout* L) {
+    if (d->L <= 0) {
+        L->s1 = L->s2 = 0;
+        L->st_G = L->st_bn = 0;
+        L->st_tasks_max = 0;
+        return;
+    }
+    L->st_G = 128 / d->r;
+    const double nbl = (double)d->E * d->L;
+    const double est_buckets = std::max(1.0, nbl * (1.0 - std::exp(-(double)L->P / nbl)));
+    const long est_groups = std::max<long>(1, (long)std::ceil(est_buckets / L->st_G));
+    const long rows_per_group = (L->P + est_groups - 1) / est_groups;
+    // an item's pairs fit one TMEM accumulator buffer of both GEMM kernels
+    L->st_bn = std::min(2 * L->bn_gu, L->bn_dn);
+    const long est_tasks = est_groups * ((rows_per_group + L->st_bn - 1) / L->st_bn);
+    L->s1 = pick_shrink_split(est_tasks, d->H);
+    L->s2 = pick_shrink_split(est_tasks, d->I);
+    L->st_tasks_max = (L->nbl + L->st_G - 1) / L->st_G + (L->P + L->st_bn - 1) / L->st_bn;
+}
+
 void plan_gemms(const moe_lora_dims* d, Layout* L) {
     const long experts_max = std::max<long>(1, std::min<long>(d->E, L->P));
     const long avg_pairs = L->P > 0 ? (L->P + experts_max - 1) / experts_max : 0;
@@ -119,23 +155,8 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->tiles = L->cap / L->bm;
     const int r = d->L > 0 ? d->r : 0;
     L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
-    // wide buckets (prefill: several rows per (expert, adapter)) use the
-    // shared-memory slab shrink, narrow ones (decode) the warp-per-item shrink
-    L->wide_shrink = d->L > 0 && L->P >= 4 * std::max<long>(1, std::min(L->NB, L->P));
-    if (d->L > 0 && L->wide_shrink) {
-        L->ks1 = L->ks2 = 512;
-        L->s1 = shrink_slab_splits(d->H);
-        L->s2 = shrink_slab_splits(d->I);
-    } else if (d->L > 0) {
-        const long items = L->nbl * (d->r / 8);
-        L->ks1 = shrink_split_len(d->H, shrink_splits(d->H, items));
-        L->ks2 = shrink_split_len(d->I, shrink_splits(d->I, items));
-        L->s1 = (d->H + L->ks1 - 1) / L->ks1;
-        L->s2 = (d->I + L->ks2 - 1) / L->ks2;
-    } else {
-        L->ks1 = L->ks2 = 0;
-        L->s1 = L->s2 = 0;
-    }
+    plan_gemms(d, L);
+    plan_shrinks(d, L);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
     L->hdr = take(sizeof(WsHeader));
@@ -150,7 +171,9 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
-    L->counters = take(sizeof(int32_t) * 16 * L->nbl);
+    L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
+    // split arrivals of the two shrinks' tasks, then the two finished-task counts
+    L->counters = take(sizeof(int32_t) * (2 * std::max<long>(L->st_tasks_max, 1) + 2));
     L->z1 = take(sizeof(float) * (size_t)(L->s1 > 1 ? L->s1 : 0) * L->P * r);
     L->z1f = take(sizeof(float) * (size_t)L->P * r);
     L->xc = take(sizeof(uint16_t) * (size_t)L->P * d->H);
@@ -158,7 +181,6 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
-    plan_gemms(d, L);
     const size_t part_gu = L->ks_gu > 1 ? (size_t)L->tiles_gu * L->ks_gu * 2 * L->bn_gu * 128 : 0;
     const size_t part_dn = L->ks_dn > 1 ? (size_t)L->tiles_dn * L->ks_dn * L->bn_dn * 128 : 0;
     L->tc_part = take(sizeof(float) * std::max(part_gu, part_dn));
@@ -186,7 +208,6 @@ int device_setup(DeviceInfo** out) {
         cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = init_align_attributes();
         if (e == cudaSuccess) e = init_tc_attributes();
-        if (e == cudaSuccess) e = init_shrink_attributes();
         info->init_err = e;
     });
     if (info->init_err != cudaSuccess) return MOELORA_ECUDA;
@@ -242,6 +263,14 @@ bool encode_w2_map(CUtensorMap* map, const void* W2, int E, int I, int H) {
     return encode_bf16_map(map, W2, 3, dims, strides, box);
 }
 
+// adapter matrices A [L][E][r][K] as [L*E*r][K]: boxes of 64 (K) x r rows
+bool encode_adapter_map(CUtensorMap* map, const void* A, int L, int E, int r, int K) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)L * E * r};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)r};
+    return encode_bf16_map(map, A, 2, dims, strides, box);
+}
+
 // pair rows [P][K] (x in bucket order, or act): boxes of 64 (K) x 16 rows
 bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
@@ -272,7 +301,10 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
     a.zero_ints = at<int>(ws, L.counters);
-    a.n_zero = d->L > 0 ? (int)(16 * L.nbl) : 0;
+    a.n_zero = d->L > 0 ? (int)(2 * L.st_tasks_max + 2) : 0;
+    a.st_tasks = d->L > 0 ? at<int4>(ws, L.st_tasks) : nullptr;
+    a.st_G = L.st_G;
+    a.st_BN = L.st_bn;
     a.zero_ints2 = at<int>(ws, L.tc_counters);
     a.n_zero2 = (L.ks_gu > 1 || L.ks_dn > 1) ? (int)(L.tiles_gu + L.tiles_dn) : 0;
     a.hdr = at<WsHeader>(ws, L.hdr);
@@ -363,7 +395,7 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
 namespace {
 
 // Records event i (if given) just before kernel slot i of the forward; slot
-// 6 is after the last kernel.  Skipped kernels still get their event.
+// 5 is after the last kernel.  Skipped kernels still get their event.
 struct Tracer {
     void* const* ev;
     int n;
@@ -373,20 +405,6 @@ struct Tracer {
         if (ev && i < n && ev[i] && cudaEventRecord((cudaEvent_t)ev[i], s) != cudaSuccess) ok = false;
     }
 };
-
-// the shrink variant the layout planned for, with a grid that covers its items
-cudaError_t launch_any_shrink(const ShrinkArgs& sh, const Layout& L, long lora_buckets_max, int sms,
-                              cudaStream_t s, bool pdl, bool gather) {
-    if (L.wide_shrink) {
-        const long items = lora_buckets_max * sh.S;
-        const int grid = (int)std::max<long>(gather ? sms : 1, std::min<long>(items, (long)sms * 4));
-        return launch_shrink_slab(sh, grid, s, pdl);
-    }
-    const long warps = lora_buckets_max * (sh.r / 8) * sh.S;
-    const long blocks = (warps + shrink_warps_per_block() - 1) / shrink_warps_per_block();
-    const int grid = (int)std::max<long>(gather ? sms : 1, std::min<long>(blocks, (long)sms * 8));
-    return launch_shrink(sh, grid, s, pdl);
-}
 
 int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
                  const float* topk_weights, const int32_t* token_lora_ids, const void* W1,
@@ -412,8 +430,6 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     // NULL stream gets plain stream order
     const bool pdl = s != nullptr && s != cudaStreamLegacy;
 
-    const long experts_max = std::min<long>(d->E, L.P);
-
     Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
     tr.mark(0);
@@ -425,41 +441,19 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     WsHeader* hdr = at<WsHeader>(ws, L.hdr);
     const int sms = dev->sms;
-    const long lora_buckets_max = std::min<long>((long)d->E * d->L, L.P);
 
-    // x rows in bucket order: the B operand of the gate_up GEMM
+    // x rows in bucket order: the B operand of the gate_up shrink and GEMM
     GatherArgs ga = {};
     ga.k = d->k; ga.H = d->H;
     ga.x = static_cast<const uint16_t*>(x);
     ga.compact_ids = at<int32_t>(ws, L.compact_ids);
     ga.hdr = hdr;
     ga.out = at<uint16_t>(ws, L.xc);
-    // with adapters the gate_up shrink kernel also does the gather (one launch)
     tr.mark(1);
-    if (!has_lora) {
+    {
         const long n = L.P * (d->H / 8);
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_gather_rows(ga, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
-    }
-
-    ShrinkArgs sh = {};
-    tr.mark(2);
-    if (has_lora) {
-        sh.E = d->E; sh.L = d->L; sh.k = d->k; sh.r = d->r; sh.K = d->H; sh.P = (int)L.P;
-        sh.S = L.s1;
-        sh.ks = L.ks1;
-        sh.in_is_x = 1;
-        sh.in = static_cast<const uint16_t*>(x);
-        sh.A = static_cast<const uint16_t*>(A1);
-        sh.lora_buckets = at<int32_t>(ws, L.lora_buckets);
-        sh.compact_offset = at<int32_t>(ws, L.compact_offset);
-        sh.compact_ids = at<int32_t>(ws, L.compact_ids);
-        sh.hdr = hdr;
-        sh.z = at<float>(ws, L.z1);
-        sh.zfinal = at<float>(ws, L.z1f);
-        sh.counters = at<int>(ws, L.counters);
-        sh.xc = at<uint16_t>(ws, L.xc);
-        if (launch_any_shrink(sh, L, lora_buckets_max, sms, s, pdl, true) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     TcArgs tc;
@@ -474,6 +468,12 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tc.hdr = hdr;
     tc.act_out = at<uint16_t>(ws, L.act);
     tc.pair_out = at<float>(ws, L.pair_out);
+    int* sh_counters = at<int>(ws, L.counters);
+    if (has_lora) {
+        tc.sh_tasks = at<int4>(ws, L.st_tasks);
+        tc.sh_G = L.st_G;
+        tc.lora_buckets = at<int32_t>(ws, L.lora_buckets);
+    }
 
     // gate_up on the tensor cores: W1 tiles x (x rows in bucket order)
     {
@@ -483,30 +483,20 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.tile_counters = at<int>(ws, L.tc_counters);
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z1f) : nullptr;
+        tc.zpart = at<float>(ws, L.z1);
+        tc.sh_ks = L.s1;
+        tc.sh_counters = sh_counters;
+        tc.zdone = sh_counters + 2 * L.st_tasks_max;
         tc.nstages = tc_plan_stages(true, bn, tc.r, d->E);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H))
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H) ||
+            (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)))
             return MOELORA_ECUDA;
-        const long tasks = L.tiles_gu * L.ks_gu;
+        const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
-        tr.mark(3);
+        tr.mark(2);
         if (launch_moe_gemm_tc(tc, true, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
-    }
-
-    tr.mark(4);
-    if (has_lora) {
-        sh.xc = nullptr;
-        sh.K = d->I;
-        sh.S = L.s2;
-        sh.ks = L.ks2;
-        sh.in_is_x = 0;
-        sh.in = at<uint16_t>(ws, L.act);
-        sh.A = static_cast<const uint16_t*>(A2);
-        sh.z = at<float>(ws, L.z2);
-        sh.zfinal = at<float>(ws, L.z2f);
-        sh.counters = at<int>(ws, L.counters) + 8 * L.nbl;
-        if (launch_any_shrink(sh, L, lora_buckets_max, sms, s, pdl, false) != cudaSuccess) return MOELORA_ECUDA;
     }
 
     // down on the tensor cores: W2 tiles x act rows
@@ -516,14 +506,19 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.tile_counters = at<int>(ws, L.tc_counters) + L.tiles_gu;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
+        tc.zpart = at<float>(ws, L.z2);
+        tc.sh_ks = L.s2;
+        tc.sh_counters = sh_counters + L.st_tasks_max;
+        tc.zdone = sh_counters + 2 * L.st_tasks_max + 1;
         tc.nstages = tc_plan_stages(false, bn, tc.r, d->E);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I))
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I) ||
+            (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)))
             return MOELORA_ECUDA;
-        const long tasks = L.tiles_dn * L.ks_dn;
+        const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
-        tr.mark(5);
+        tr.mark(3);
         if (launch_moe_gemm_tc(tc, false, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 
@@ -533,13 +528,13 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ra.topk_ids = topk_ids;
     ra.lora_ids = token_lora_ids;
     ra.out = static_cast<uint16_t*>(out);
-    tr.mark(6);
+    tr.mark(4);
     {
         const long n = (long)d->T * (d->H / 4);
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_reduce(ra, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
-    tr.mark(7);
+    tr.mark(5);
     return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
 }
 

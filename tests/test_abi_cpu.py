@@ -52,7 +52,10 @@ def test_workspace_bytes_and_layout(lib):
     lay = B.moe_lora_workspace_layout(d)
     assert n == lay["total"] > 0
     P = 64
-    assert lay["s1"] == -(-2880 // 512) and lay["s2"] == -(-2880 // 512)
+    # the shrinks split K across CTAs (a decode batch has too few adapter
+    # buckets to fill the SMs), keeping at least two 64-wide K steps per split
+    for s in (lay["s1"], lay["s2"]):
+        assert 1 < s <= min(32, (2880 // 64) // 2)
     # regions are disjoint and inside the workspace
     regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * P * 32),
                       (lay["act"], 2 * P * 2880), (lay["z2"], 4 * P * 32),
