@@ -52,6 +52,8 @@ struct TcArgs {
     CUtensorMap wmap;            // W1 as [E][2][I][H] (gate_up) or W2 [E][H][I]; box 64 (K) x 128 rows
     CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16 rows
     CUtensorMap amap;            // LoRA A (A1 / A2) as [L*E*r][K]; box 64 (K) x r rows
+    CUtensorMap bmap;            // LoRA B: B1 as {r, I, 2, E, L} / B2 as {r, H, E, L}; box 64 x 128 rows
+    CUtensorMap zxmap;           // zexp [P][L*64] bf16; box 64 x pair rows
     int E, L, k, r, I, H, P;
     const uint16_t* B;           // B1 / B2 (null: no LoRA)
     float* z;                    // shrink output [P][r], written by the shrink items (null: no LoRA)
@@ -63,6 +65,8 @@ struct TcArgs {
     float* zpart;                // [sh_ks][P][r] split partials (sh_ks > 1)
     int* sh_counters;            // [tasks] split arrivals, zeroed by align
     int* zdone;                  // shrink tasks finished, zeroed by align
+    int tc_expand;               // 1: LoRA expand as extra tensor-core K-blocks; 0: CUDA cores in the epilogue
+    uint16_t* zexp;              // [P][L*64] bf16: a pair's z in its adapter's 64-column slot, zeros elsewhere
     const int32_t* lora_ids;
     const float* topk_weights;
     const int32_t* active_experts;
@@ -76,8 +80,8 @@ struct TcArgs {
     float* part;                 // split-K partial tiles [tiles][ksplit][acc columns][128]
     int* tile_counters;          // [tiles] split arrivals, zeroed by align
 };
-int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages);
-int tc_plan_stages(bool gate_up, int bn, int r, int E);
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand);
+int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand);
 cudaError_t init_tc_attributes();
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl);
 
@@ -87,6 +91,9 @@ struct GatherArgs {
     const int32_t* compact_ids;
     const WsHeader* hdr;
     uint16_t* out;               // [P][H] rows in bucket order
+    uint16_t* zexp1;             // [P][zx_cols] zeroed here (null: none)
+    uint16_t* zexp2;
+    int zx_cols;
 };
 cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t stream, bool pdl);
 

@@ -60,8 +60,11 @@ constexpr int kTcThreads = (2 + kEpiWarps) * 32;
 constexpr int kBM = 128;                 // weight rows per task (MMA M)
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row
 constexpr int kATile = kBM * kBK * 2;    // 16 KiB
-constexpr int kBBoxRows = 16;
-constexpr int kBBox = kBBoxRows * kBK * 2;
+// pair rows per TMA box: 16 for decode-sized chunks, 64 when chunks are wide
+// (fewer, larger copies keep the TMA issue rate off the critical path)
+template <int BN>
+constexpr int kRowsFor = BN >= 128 ? 64 : 16;
+constexpr int kMisc = 20;  // shared verdicts [0..3] and shrink-slot adapters [4..19]
 
 template <bool GATE_UP, int BN>
 struct TcShape {
@@ -80,6 +83,7 @@ __device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u));
 // count (weight tiles x pair chunks).  A task index maps to (expert, tile,
 // chunk) by a binary search over the prefix.
 struct TaskTable {
+    unsigned long long* amask;  // [n_active] adapters (< 64) with pairs on the expert
     int* e;    // [n_active]
     int* q0;   // [n_active]
     int* m;    // [n_active]
@@ -88,7 +92,7 @@ struct TaskTable {
 
 template <int BN>
 struct Task {
-    int e, mt, q0c, n_real, n_cols;
+    int ai, e, mt, q0c, n_real, n_cols;
     int tile;       // (expert, weight tile, pair chunk) index, for split-K partials
     int split;      // K-split of this task
     __device__ void lookup(const TaskTable& tt, int n_active, int ksplit, int t) {
@@ -100,6 +104,7 @@ struct Task {
             if (tt.cum[mid] <= tile) lo = mid;
             else hi = mid;
         }
+        ai = lo;
         const int nch = (tt.m[lo] + BN - 1) / BN;
         const int loc = tile - tt.cum[lo];
         mt = loc / nch;
@@ -179,6 +184,34 @@ struct EpiRow {
     }
 };
 
+// Adapters whose LoRA expand a GEMM task adds on the tensor cores: the pairs of
+// a chunk come sorted by adapter, so they span the adapters la .. lb of its
+// first and last pair; of those, the ones with pairs on the expert (mask, known
+// for ids < 64) each get one extra K-block: A = the adapter's B rows (TMA reads
+// zeros beyond r), B = zexp rows, whose 64-column slot of this adapter holds
+// the pair's z for pairs of that adapter and zeros for all others.
+struct ExpandRange {
+    int la, lb, p0, p1;
+    unsigned long long mask;
+    // pair ids of the chunk's first and last row (issued early), then their adapters
+    __device__ void begin(const TcArgs& a, int q0c, int n_real) {
+        p0 = a.compact_ids[q0c];
+        p1 = a.compact_ids[q0c + n_real - 1];
+    }
+    __device__ void finish(const TcArgs& a, unsigned long long m) {
+        la = max(a.lora_ids[p0 / a.k], 0);
+        lb = a.lora_ids[p1 / a.k];
+        mask = a.L <= 64 ? m : ~0ull;  // no per-expert mask beyond 64 adapters
+    }
+    __device__ void none() { la = 0; lb = -1; mask = 0; }
+    __device__ bool has(int l) const { return l >= 64 || ((mask >> l) & 1ull); }
+    __device__ int count() const {
+        int n = 0;
+        for (int l = la; l <= lb; l++) n += has(l) ? 1 : 0;
+        return n;
+    }
+};
+
 // ---------------------------------------------------------------- shrink items
 constexpr int kMaxSlots = 16;  // adapter buckets per shrink item: 128 / r with r >= 8
 
@@ -223,10 +256,12 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
     const int r = a.r;
     // slot column ranges (after everyone is done with the previous item's staging)
     if (!rendezvous()) return false;
+    int* s_sl = s_misc + 4;  // adapter of each slot
     if (etid < sh.nb) {
         const int bk = a.lora_buckets[sh.j0 + etid];
         s_cb[etid] = min(max(a.compact_offset[bk] - sh.q0c, 0), sh.n_real);
         s_ce[etid] = min(max(a.compact_offset[bk + 1] - sh.q0c, 0), sh.n_real);
+        s_sl[etid] = bk % (a.L + 1) - 1;
     }
     if (!rendezvous()) return false;
     const int row = qd * 32 + lane;
@@ -237,6 +272,9 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
     const int clo = s_lo < sh.nb ? s_cb[s_lo] : 0;
     const int chi = s_lo < sh.nb ? s_ce[s_hi] : 0;
     float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
+    // bf16 copy for the tensor-core expand: row q, slot of adapter l
+    const size_t zx_cols = (size_t)a.L * 64;
+    uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + s_sl[my_s] * 64 + j : nullptr;
 
     if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) return false;
     tc_fence_after();
@@ -247,7 +285,10 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
 #pragma unroll
         for (int c = 0; c < 4; c++) {
             const int cc = c4 + c;
-            if (cc >= mcb && cc < mce) dst[(size_t)(sh.q0c + cc) * r + j] = v[c];
+            if (cc >= mcb && cc < mce) {
+                dst[(size_t)(sh.q0c + cc) * r + j] = v[c];
+                if (zx) zx[(size_t)(sh.q0c + cc) * zx_cols] = f32_to_bf16_rne(v[c]);
+            }
         }
     }
     tc_fence_before();
@@ -276,6 +317,19 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
                 acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
             }
             out[i4] = acc;
+            if (a.zexp) {
+                const int q = (int)((beg + (size_t)i4 * 4) / r), kk = (int)((beg + (size_t)i4 * 4) % r);
+                const int c = q - sh.q0c;
+                int l = -1;
+                for (int u = 0; u < sh.nb; u++)
+                    if (c >= s_cb[u] && c < s_ce[u]) l = s_sl[u];
+                if (l >= 0) {
+                    uint2 pk;
+                    pk.x = (uint32_t)f32_to_bf16_rne(acc.x) | ((uint32_t)f32_to_bf16_rne(acc.y) << 16);
+                    pk.y = (uint32_t)f32_to_bf16_rne(acc.z) | ((uint32_t)f32_to_bf16_rne(acc.w) << 16);
+                    *reinterpret_cast<uint2*>(a.zexp + (size_t)q * zx_cols + l * 64 + kk) = pk;
+                }
+            }
         }
         __threadfence();
         if (!rendezvous()) return false;
@@ -287,24 +341,26 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
 template <bool GATE_UP, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_constant__ TcArgs a) {
     using S = TcShape<GATE_UP, BN>;
+    constexpr int kRows = kRowsFor<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
     // epilogue staging: z rows [BN][r] fp32, then pair id / adapter / weight per
     // column (a shrink item keeps its slots' column ranges in s_pair / s_lora)
     float* zs = reinterpret_cast<float*>(base + (size_t)NS * S::kStage);
-    int* s_pair = reinterpret_cast<int*>(zs + (size_t)BN * a.r);
+    int* s_pair = reinterpret_cast<int*>(zs + (a.tc_expand ? 0 : (size_t)BN * a.r));
     int* s_lora = s_pair + BN;
     float* s_w = reinterpret_cast<float*>(s_lora + BN);
-    int* s_misc = reinterpret_cast<int*>(s_w + BN);  // [4] verdicts shared by the epilogue warps
-    uint64_t* full = reinterpret_cast<uint64_t*>(s_misc + 4);
+    int* s_misc = reinterpret_cast<int*>(s_w + BN);  // [kMisc] shared by the epilogue warps
+    uint64_t* full = reinterpret_cast<uint64_t*>(s_misc + kMisc);
     uint64_t* empty = full + NS;
     uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
     uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
     uint64_t* ebar = tempty + 2;    // epilogue rendezvous (kEpiWarps * 32 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
     TaskTable tt;
-    tt.e = reinterpret_cast<int*>(tmem_slot + 4);
+    tt.amask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
+    tt.e = reinterpret_cast<int*>(tt.amask + a.E);
     tt.q0 = tt.e + a.E;
     tt.m = tt.q0 + a.E;
     tt.cum = tt.m + a.E;
@@ -330,6 +386,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         prefetch_tensormap(&a.wmap);
         prefetch_tensormap(&a.xmap);
         if (a.sh_tasks) prefetch_tensormap(&a.amap);
+        if (a.tc_expand) {
+            prefetch_tensormap(&a.bmap);
+            prefetch_tensormap(&a.zxmap);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -354,8 +414,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         tt.q0[ai] = q0;
         tt.m[ai] = m;
         tt.cum[ai + 1] = ntiles * ((m + BN - 1) / BN);
+        tt.amask[ai] = 0ull;
     }
     __syncthreads();
+    if (a.tc_expand && a.L <= 64) {
+        // adapters with pairs on each active expert
+        for (int w = threadIdx.x; w < n_active * a.L; w += kTcThreads) {
+            const int ai = w / a.L, l = w % a.L;
+            const int b = tt.e[ai] * (a.L + 1) + l + 1;
+            if (a.compact_offset[b + 1] > a.compact_offset[b]) atomicOr(&tt.amask[ai], 1ull << l);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         int carry = 0;
         for (int base = 0; base < n_active; base += 32) {
@@ -375,6 +445,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     const int ksplit = a.ksplit;
     // shrink items first, then the GEMM tasks
     const bool shrink = a.sh_tasks != nullptr && a.r > 0;
+    const bool expand = a.tc_expand != 0 && a.r > 0;
     const int sh_ks = a.sh_ks;
     const int n_sh_tasks = shrink ? a.hdr->n_shrink_tasks : 0;
     const int n_sh = n_sh_tasks * sh_ks;
@@ -392,6 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, armed = 0, last_par = 0;
+            bool z_seen = false;
             int arow[kMaxSlots];
             for (int t = t_first; t < total && ok; t += t_step) {
                 if (t < n_sh) {
@@ -402,7 +474,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                         const int b = a.lora_buckets[sh.j0 + q];
                         arow[q] = ((b % L1 - 1) * a.E + b / L1) * a.r;  // first row of A[l][e]
                     }
-                    const uint32_t bytes = (uint32_t)(sh.nb * a.r + sh.n_cols) * kBK * 2;
+                    const int sh_box = (sh.n_cols + kRows - 1) / kRows;
+                    const uint32_t bytes = (uint32_t)(sh.nb * a.r + sh_box * kRows) * kBK * 2;
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
@@ -411,8 +484,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                         const int k0 = kb * kBK;
                         for (int q = 0; q < sh.nb; q++)
                             tma_load_2d(dst + q * a.r * kBK * 2, &a.amap, &full[stage], k0, arow[q]);
-                        for (int g = 0; g < sh.n_cols / kBBoxRows; g++)
-                            tma_load_2d(dst + kATile + g * kBBox, &a.xmap, &full[stage], k0, sh.q0c + g * kBBoxRows);
+                        for (int g = 0; g < sh_box; g++)
+                            tma_load_2d(dst + kATile + g * kRows * kBK * 2, &a.xmap, &full[stage], k0, sh.q0c + g * kRows);
                         armed |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
                         if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -422,9 +495,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 Task<BN> tw;
                 tw.lookup(tt, n_active, ksplit, t - n_sh);
                 const int n_cols = tw.n_cols, row0 = tw.q0c, e = tw.e;
-                const uint32_t bytes = S::kAB + (uint32_t)n_cols * kBK * 2;
+                const int n_box = (n_cols + kRows - 1) / kRows;
+                const uint32_t bytes = S::kAB + (uint32_t)n_box * kRows * kBK * 2;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                // LoRA expand K-blocks of this task (last K-split only): the pair ids
+                // are fetched now, their adapters just before the last base stage
+                ExpandRange xr;
+                xr.none();
+                const bool with_x = expand && tw.split == ksplit - 1;
+                if (with_x) xr.begin(a, row0, tw.n_real);
+                int n_x = 0;
                 for (int kb = kb0; kb < kb1; kb++) {
+                    if (with_x && kb == kb1 - 1) {
+                        xr.finish(a, tt.amask[tw.ai]);
+                        n_x = xr.count();
+                    }
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t* dst = base + (size_t)stage * S::kStage;
@@ -435,8 +520,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     } else {
                         tma_load_3d(dst, &a.wmap, &full[stage], k0, tw.mt * kBM, e);
                     }
-                    for (int g = 0; g < n_cols / kBBoxRows; g++)
-                        tma_load_2d(dst + S::kAB + g * kBBox, &a.xmap, &full[stage], k0, row0 + g * kBBoxRows);
+                    for (int g = 0; g < n_box; g++)
+                        tma_load_2d(dst + S::kAB + g * kRows * kBK * 2, &a.xmap, &full[stage], k0, row0 + g * kRows);
+                    armed |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+                // the expand reads zexp: wait once until every shrink task is done
+                if (ok && n_x > 0 && !z_seen) {
+                    if (!wait_count(a.zdone, n_sh_tasks)) { ok = false; break; }
+                    // the shrink items' generic stores before the TMA (async proxy) reads
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    z_seen = true;
+                }
+                for (int l = xr.la; ok && l <= xr.lb; l++) {
+                    if (!xr.has(l)) continue;
+                    if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    uint8_t* dst = base + (size_t)stage * S::kStage;
+                    if (GATE_UP) {
+                        tma_load_5d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l);
+                        tma_load_5d(dst + kATile, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l);
+                    } else {
+                        tma_load_4d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l);
+                    }
+                    for (int g = 0; g < n_box; g++)
+                        tma_load_2d(dst + S::kAB + g * kRows * kBK * 2, &a.zxmap, &full[stage], l * 64, row0 + g * kRows);
                     armed |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -448,16 +557,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         }
     } else if (warp == 1) {
         // -------------------------------------------------------------- MMA issuer
+        // Walks the same item sequence as the producer (shrink items, then GEMM
+        // tasks with their expand K-blocks); task data comes from the shared
+        // table, so the per-stage path is MMA issue only.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
+            const int xsteps = (a.r + 15) / 16;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
                 const int b = it & 1;
                 if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
                 if (t < n_sh) {
-                    // shrink item: stacked adapter rows x pair rows, N up to the buffer's columns
                     ShItem sh;
                     sh.load(a, t, n_lora);
                     const uint32_t idesc = umma_idesc_bf16_f32(kBM, sh.n_cols);
@@ -481,6 +593,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 tw.lookup(tt, n_active, ksplit, t - n_sh);
                 const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                ExpandRange xr;
+                xr.none();
+                if (expand && tw.split == ksplit - 1) {
+                    // the expand's adapters (same rule as the producer), looked up while
+                    // the first stage is in flight
+                    xr.begin(a, tw.q0c, tw.n_real);
+                    xr.finish(a, tt.amask[tw.ai]);
+                }
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
@@ -494,11 +614,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                         if (GATE_UP)
                             umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, acc);
                     }
-                    umma_commit(&empty[stage]);  // stage reusable once these MMAs are done
+                    umma_commit(&empty[stage]);
+                    if (++stage == NS) { stage = 0; phase ^= 1; }
+                }
+                for (int l = xr.la; l <= xr.lb && ok; l++) {
+                    if (!xr.has(l)) continue;
+                    if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
+                    const uint32_t b_addr = a_addr + S::kAB;
+                    for (int kk = 0; kk < xsteps; kk++) {
+                        const uint64_t bdesc = umma_desc_sw128(b_addr + kk * 32);
+                        umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32), bdesc, idesc, 1u);
+                        if (GATE_UP)
+                            umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, 1u);
+                    }
+                    umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
-                umma_commit(&tfull[b]);          // accumulator complete
+                umma_commit(&tfull[b]);
             }
         }
     } else {
@@ -508,7 +643,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         const int half = ew >> 2;                // which alternate 16-column chunks
         const int row = qd * 32 + lane;          // weight row within the tile
         const int etid = ew * 32 + lane;
-        const bool has_lora = a.B != nullptr && a.z != nullptr;
+        // the CUDA-core expand runs here only when the tensor cores do not take it
+        const bool has_lora = a.B != nullptr && a.z != nullptr && !a.tc_expand;
         const size_t rows_per_expert = GATE_UP ? 2 * (size_t)a.I : (size_t)a.H;
         const int r = a.r;
         uint32_t epar = 0;
@@ -643,27 +779,38 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
     const int n = a.hdr->n_valid;
     const int c8 = a.H >> 3;
     const long total = (long)n * c8;
+    const long stride = (long)gridDim.x * blockDim.x;
+    const long first = (long)blockIdx.x * blockDim.x + threadIdx.x;
 #pragma unroll 4
-    for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += (long)gridDim.x * blockDim.x) {
+    for (long idx = first; idx < total; idx += stride) {
         const int q = (int)(idx / c8), c = (int)(idx % c8);
         const int t = a.compact_ids[q] / a.k;
         *reinterpret_cast<uint4*>(a.out + (size_t)q * a.H + c * 8) = ld_ro16(a.x + (size_t)t * a.H + c * 8);
+    }
+    // zexp rows start as zeros; the shrink items fill each pair's own slot
+    if (a.zexp1) {
+        const long nz = (long)n * a.zx_cols / 8;
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        for (long i = first; i < nz; i += stride) {
+            reinterpret_cast<uint4*>(a.zexp1)[i] = zero;
+            reinterpret_cast<uint4*>(a.zexp2)[i] = zero;
+        }
     }
 }
 
 }  // namespace
 
-int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages) {
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand) {
     const int ab = gate_up ? 2 * kATile : kATile;
     const int stage = ab + bn * kBK * 2;
-    const int staging = bn * r * 4 + 3 * bn * 4 + 16;
-    const int table = (4 * E + 1) * 4;
+    const int staging = (tc_expand ? 0 : bn * r * 4) + 3 * bn * 4 + kMisc * 4;
+    const int table = 8 * E + (4 * E + 1) * 4;
     return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
 }
 
-int tc_plan_stages(bool gate_up, int bn, int r, int E) {
+int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand) {
     for (int ns = 8; ns >= 2; ns--)
-        if (tc_smem_bytes(gate_up, bn, r, E, ns) <= kTcSmemLimit) return ns;
+        if (tc_smem_bytes(gate_up, bn, r, E, ns, tc_expand) <= kTcSmemLimit) return ns;
     return 0;
 }
 
@@ -676,7 +823,7 @@ cudaError_t init_tc_attributes() {
 }
 
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl) {
-    const int smem = tc_smem_bytes(gate_up, bn, args.r, args.E, args.nstages);
+    const int smem = tc_smem_bytes(gate_up, bn, args.r, args.E, args.nstages, args.tc_expand != 0);
     const dim3 g(grid), b(kTcThreads);
     if (gate_up) {
         if (bn == 64) return launch_k(k_moe_gemm_tc<true, 64>, g, b, smem, stream, pdl, args);

@@ -31,6 +31,7 @@ namespace moelora {
 namespace {
 
 constexpr int kDefaultBlockM = 16;
+constexpr long kMaxZexpSlots = 1L << 17;  // pairs x adapters: 16 MiB per zexp buffer
 constexpr int kMaxDevices = 64;
 
 struct Layout {
@@ -42,7 +43,9 @@ struct Layout {
     long st_tasks_max;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
         compact_ids, active_experts, lora_buckets, scan_tmp, hist, st_tasks, counters, z1, z1f, xc, act, z2,
-        z2f, pair_out, tc_part, tc_counters, total;
+        z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
+    // LoRA expand on the tensor cores (zexp buffers bounded), else on CUDA cores
+    bool tc_expand;
     // tensor-core GEMM plan (shared by the launch code and the workspace size)
     int bn_gu, bn_dn, ks_gu, ks_dn;
     long tiles_gu, tiles_dn;
@@ -128,6 +131,15 @@ void plan_shrinks(const moe_lora_dims* d, Layout* L) {
     L->st_tasks_max = (L->nbl + L->st_G - 1) / L->st_G + (L->P + L->st_bn - 1) / L->st_bn;
 }
 
+// Expected distinct adapters among one expert's pairs (capped at a 256-pair
+// chunk), with pairs spread evenly over experts and adapters drawn uniformly.
+double expected_adapters_per_chunk(const moe_lora_dims* d, long P) {
+    if (d->L <= 0 || P <= 0) return 0.0;
+    const double experts = (double)std::max<long>(1, std::min<long>(d->E, P));
+    const double pairs = std::min(256.0, (double)P / experts);
+    return d->L * (1.0 - std::pow(1.0 - 1.0 / d->L, pairs));
+}
+
 void plan_gemms(const moe_lora_dims* d, Layout* L) {
     const long experts_max = std::max<long>(1, std::min<long>(d->E, L->P));
     const long avg_pairs = L->P > 0 ? (L->P + experts_max - 1) / experts_max : 0;
@@ -180,6 +192,15 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
     L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
+    // zexp: per pair L slots of 64 bf16.  The tensor-core expand pays one K
+    // block per adapter of a chunk; it is used when chunks are expected to mix
+    // several adapters (the CUDA-core expand then reloads B rows per adapter run)
+    // and while zexp stays small (it is rewritten every forward).
+    L->tc_expand = d->L > 0 && L->P * (long)d->L <= kMaxZexpSlots &&
+                   expected_adapters_per_chunk(d, L->P) >= 4.0;
+    const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * d->L * 64 : 0;
+    L->zexp1 = take(zx);
+    L->zexp2 = take(zx);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
     const size_t part_gu = L->ks_gu > 1 ? (size_t)L->tiles_gu * L->ks_gu * 2 * L->bn_gu * 128 : 0;
     const size_t part_dn = L->ks_dn > 1 ? (size_t)L->tiles_dn * L->ks_dn * L->bn_dn * 128 : 0;
@@ -271,12 +292,31 @@ bool encode_adapter_map(CUtensorMap* map, const void* A, int L, int E, int r, in
     return encode_bf16_map(map, A, 2, dims, strides, box);
 }
 
-// pair rows [P][K] (x in bucket order, or act): boxes of 64 (K) x 16 rows
-bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K) {
+// pair rows [P][K] (x in bucket order, act, or zexp): boxes of 64 (K) x
+// box_rows rows (16 for decode-sized chunks, 64 for wide ones)
+bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K, int box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     return encode_bf16_map(map, rows, 2, dims, strides, box);
+}
+int pair_box_rows(int bn) { return bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
+
+// B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of 64 (K; zeros beyond r) x 128 units of one half
+bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r) {
+    const cuuint64_t dims[5] = {(cuuint64_t)r, (cuuint64_t)I, 2, (cuuint64_t)E, (cuuint64_t)L};
+    const cuuint64_t strides[4] = {(cuuint64_t)r * 2, (cuuint64_t)I * r * 2, (cuuint64_t)2 * I * r * 2,
+                                   (cuuint64_t)E * 2 * I * r * 2};
+    const cuuint32_t box[5] = {64, 128, 1, 1, 1};
+    return encode_bf16_map(map, B1, 5, dims, strides, box);
+}
+
+// B2 [L][E][H][r] as {r, H, E, L}: boxes of 64 (K; zeros beyond r) x 128 rows
+bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r) {
+    const cuuint64_t dims[4] = {(cuuint64_t)r, (cuuint64_t)H, (cuuint64_t)E, (cuuint64_t)L};
+    const cuuint64_t strides[3] = {(cuuint64_t)r * 2, (cuuint64_t)H * r * 2, (cuuint64_t)E * H * r * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    return encode_bf16_map(map, B2, 4, dims, strides, box);
 }
 
 template <typename T>
@@ -449,6 +489,11 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ga.compact_ids = at<int32_t>(ws, L.compact_ids);
     ga.hdr = hdr;
     ga.out = at<uint16_t>(ws, L.xc);
+    if (L.tc_expand) {
+        ga.zexp1 = at<uint16_t>(ws, L.zexp1);
+        ga.zexp2 = at<uint16_t>(ws, L.zexp2);
+        ga.zx_cols = d->L * 64;
+    }
     tr.mark(1);
     {
         const long n = L.P * (d->H / 8);
@@ -469,6 +514,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tc.act_out = at<uint16_t>(ws, L.act);
     tc.pair_out = at<float>(ws, L.pair_out);
     int* sh_counters = at<int>(ws, L.counters);
+    tc.tc_expand = L.tc_expand ? 1 : 0;
     if (has_lora) {
         tc.sh_tasks = at<int4>(ws, L.st_tasks);
         tc.sh_G = L.st_G;
@@ -487,11 +533,15 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.sh_ks = L.s1;
         tc.sh_counters = sh_counters;
         tc.zdone = sh_counters + 2 * L.st_tasks_max;
-        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E);
+        tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp1) : nullptr;
+        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+        const int rows = pair_box_rows(bn);
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H) ||
-            (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)))
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
+            (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
+            (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
+                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, d->L * 64, rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
@@ -510,11 +560,15 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.sh_ks = L.s2;
         tc.sh_counters = sh_counters + L.st_tasks_max;
         tc.zdone = sh_counters + 2 * L.st_tasks_max + 1;
-        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E);
+        tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp2) : nullptr;
+        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+        const int rows = pair_box_rows(bn);
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I) ||
-            (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)))
+            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
+            (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
+            (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
+                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, d->L * 64, rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));

@@ -59,6 +59,15 @@ RAGGED = [
     (3, 1024, 2048, 1, 1, 4, 16),
     (5, 1032, 1544, 1, 1, 2, 8),
     (2, 2048, 512, 2, 1, 1, 64),
+    # more than 64 adapters: the tensor-core expand runs without per-expert adapter masks
+    (40, 128, 96, 3, 2, 70, 8),
+    # pairs x adapters beyond the zexp bound: the expand falls back to CUDA cores
+    (2100, 64, 64, 4, 1, 64, 8),
+    # wide chunks mixing several adapters (prefill-like): 64-row pair boxes, the
+    # LoRA expand as tensor-core K blocks (r not a power of two; r = 64 with ragged I)
+    (600, 128, 136, 2, 2, 5, 32),
+    (200, 264, 136, 3, 2, 6, 24),
+    (300, 96, 1032, 2, 1, 8, 64),
 ]
 
 
@@ -151,12 +160,18 @@ def test_adapter_swap_swaps_outputs():
     assert torch.equal(a.out[1].view(torch.int16), b.out[0].view(torch.int16))
 
 
-@pytest.mark.parametrize("which", ["config0", "many_experts"])
+@pytest.mark.parametrize("which", ["config0", "many_experts", "mixed_chunks"])
 def test_lora_delta_matches_oracle_delta(which):
     """The adapter delta alone (forward minus the zero-B forward) against the
     oracle's delta: a broken expand could hide under the 1e-2 output bar.  The
-    second layer has enough experts for the shrink to run inside the GEMMs."""
-    layer = wl.make_config(0) if which == "config0" else wl.make_random(24, 264, 136, 40, 2, 3, 24, seed=8)
+    first two layers take the CUDA-core expand, the third (several adapters
+    per expert chunk) the tensor-core one."""
+    if which == "config0":
+        layer = wl.make_config(0)
+    elif which == "many_experts":
+        layer = wl.make_random(24, 264, 136, 40, 2, 3, 24, seed=8)
+    else:
+        layer = wl.make_random(300, 128, 136, 2, 2, 6, 32, seed=9)
     zb = dataclasses.replace(layer, B1=np.zeros_like(layer.B1), B2=np.zeros_like(layer.B2))
     a, _ = run(layer)
     b, _ = run(zb)
