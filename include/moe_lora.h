@@ -219,11 +219,10 @@ MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims *d, const void *x,
 typedef struct moe_lora_ws_layout {
     size_t compact_ids;      /* int32 [P]: pair id of each row */
     size_t compact_offset;   /* int32 [E*(L+1)+1]: first row of each bucket */
-    size_t z1;               /* float [P][r]: gate_up LoRA shrink A1 x per row (adapter rows only;
-                                written when the shrink runs as its own kernel, i.e. when few
-                                experts share the batch or experts see many pairs each) */
+    size_t z1;               /* float [P][r]: gate_up LoRA shrink A1 x per row (rows of
+                                adapter pairs only; other rows are left undefined) */
     size_t act;              /* bf16 [P][I]: SiLU(gate)*up per row */
-    size_t z2;               /* float [P][r]: down LoRA shrink A2 act per row (same condition) */
+    size_t z2;               /* float [P][r]: down LoRA shrink A2 act per row (same rows) */
     size_t pair_out;         /* float [P][H]: w * d per pair id p */
     int32_t s1, s2;          /* K-split counts the two shrinks used */
     size_t total;            /* == moe_lora_workspace_bytes */

@@ -250,17 +250,22 @@ def test_config1_decode_full(config1):
 
 
 def test_intermediates_config1(config1):
-    """act and the weighted pair outputs of the decode layer against the oracle
-    (its LoRA shrinks run inside the GEMMs, so z is not kept in the workspace)."""
+    """z1, z2, act and the weighted pair outputs of the decode layer against the
+    oracle (its shrinks split K across CTAs and finish in the last split)."""
     dl, st = run(config1)
-    P, I, H = config1.P, config1.I, config1.H
+    P, I, H, r = config1.P, config1.I, config1.H, config1.r
     rows = dl.workspace_view("compact_ids", torch.int32, (P,)).cpu().numpy()
+    z1 = dl.workspace_view("z1", torch.float32, (P, r)).cpu().numpy().astype(np.float64)
+    z2 = dl.workspace_view("z2", torch.float32, (P, r)).cpu().numpy().astype(np.float64)
     act_bits = dl.workspace_view("act", torch.int16, (P, I)).cpu().numpy().view(np.uint16)
     act = (act_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     pair_out = dl.workspace_view("pair_out", torch.float32, (P, H)).cpu().numpy().astype(np.float64)
     for row in range(0, P, 7):
         p = int(rows[row])
         ref = oracle.pair(config1, p)
+        assert norm_err(z1[row], ref["z1"]) < 1e-5
+        # z2 is A2 applied to the bf16 act of the GPU, so it inherits act's rounding
+        assert norm_err(z2[row], ref["z2"]) < 8e-3
         assert norm_err(act[row], ref["act"]) < 8e-3
         assert norm_err(pair_out[p], float(config1.topk_weights.flat[p]) * ref["d"]) < 1e-2
 
