@@ -67,6 +67,8 @@ struct TcArgs {
     int* zdone;                  // shrink tasks finished, zeroed by align
     int tc_expand;               // 1: LoRA expand as extra tensor-core K-blocks; 0: CUDA cores in the epilogue
     uint16_t* zexp;              // [P][L*64] bf16: a pair's z in its adapter's 64-column slot, zeros elsewhere
+    int chunk_masks;             // 1: per-(expert, pair chunk) adapter masks in shared memory (L <= 64)
+    int max_chunks;              // bound on (expert, pair chunk) count, for the mask table
     const int32_t* lora_ids;
     const float* topk_weights;
     const int32_t* active_experts;
@@ -80,8 +82,8 @@ struct TcArgs {
     float* part;                 // split-K partial tiles [tiles][ksplit][acc columns][128]
     int* tile_counters;          // [tiles] split arrivals, zeroed by align
 };
-int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand);
-int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand);
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
+int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks);
 cudaError_t init_tc_attributes();
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl);
 

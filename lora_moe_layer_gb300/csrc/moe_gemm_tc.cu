@@ -83,7 +83,7 @@ __device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u));
 // count (weight tiles x pair chunks).  A task index maps to (expert, tile,
 // chunk) by a binary search over the prefix.
 struct TaskTable {
-    unsigned long long* amask;  // [n_active] adapters (< 64) with pairs on the expert
+    unsigned long long* cmask;  // [chunks] adapters (< 64) with pairs in each (expert, pair chunk)
     int* e;    // [n_active]
     int* q0;   // [n_active]
     int* m;    // [n_active]
@@ -93,9 +93,10 @@ struct TaskTable {
 template <int BN>
 struct Task {
     int ai, e, mt, q0c, n_real, n_cols;
+    int chunk;      // (expert, pair chunk) index, for the chunk's adapter mask
     int tile;       // (expert, weight tile, pair chunk) index, for split-K partials
     int split;      // K-split of this task
-    __device__ void lookup(const TaskTable& tt, int n_active, int ksplit, int t) {
+    __device__ void lookup(const TaskTable& tt, int n_active, int ksplit, int ntiles, int t) {
         tile = t / ksplit;
         split = t % ksplit;
         int lo = 0, hi = n_active;  // last a with cum[a] <= tile
@@ -109,6 +110,7 @@ struct Task {
         const int loc = tile - tt.cum[lo];
         mt = loc / nch;
         const int ch = loc % nch;
+        chunk = tt.cum[lo] / ntiles + ch;
         e = tt.e[lo];
         q0c = tt.q0[lo] + ch * BN;
         n_real = min(BN, tt.m[lo] - ch * BN);
@@ -184,30 +186,65 @@ struct EpiRow {
     }
 };
 
-// Adapters whose LoRA expand a GEMM task adds on the tensor cores: the pairs of
-// a chunk come sorted by adapter, so they span the adapters la .. lb of its
-// first and last pair; of those, the ones with pairs on the expert (mask, known
-// for ids < 64) each get one extra K-block: A = the adapter's B rows (TMA reads
-// zeros beyond r), B = zexp rows, whose 64-column slot of this adapter holds
-// the pair's z for pairs of that adapter and zeros for all others.
+// LoRA expand on the tensor cores: one 64-wide K block per adapter l, whose A
+// tile is that adapter's B rows (a 64-element TMA box over the r-wide rows reads
+// zeros beyond r) and whose B tile is zexp rows, where a pair's z sits in its
+// adapter's 64-wide slot and all other slots are zero.
+
+// The expand blocks of one GEMM task: one per adapter with pairs in the task's
+// chunk, dealt to the task's K-splits by jb mod ksplit so a split-K task
+// spreads its expand work too.  With up to 64 adapters the set comes from the
+// chunk's adapter mask built at kernel start and is walked by its set bits, so
+// the single MMA-issuing thread spends a few instructions per task on it.
+// Beyond that, the pairs of a chunk (sorted by adapter) span the adapters la ..
+// lb of its first and last pair, read from global memory, and every adapter of
+// the span gets a block (zexp zeros make the absent ones add nothing).
 struct ExpandRange {
-    int la, lb, p0, p1;
-    unsigned long long mask;
+    int la, lb, p0, p1, split, ksplit;
+    bool wide;
+    unsigned long long bits;   // blocks of this split (ids < 64)
+    __device__ void from_mask(unsigned long long m, int split_, int ksplit_) {
+        la = 0;
+        lb = -1;
+        split = split_;
+        ksplit = ksplit_;
+        wide = false;
+        bits = m;
+        if (ksplit > 1) {
+            unsigned long long mine = 0;
+            for (int jb = split; jb < 64; jb += ksplit) mine |= 1ull << jb;
+            bits &= mine;
+        }
+    }
     // pair ids of the chunk's first and last row (issued early), then their adapters
     __device__ void begin(const TcArgs& a, int q0c, int n_real) {
         p0 = a.compact_ids[q0c];
         p1 = a.compact_ids[q0c + n_real - 1];
     }
-    __device__ void finish(const TcArgs& a, unsigned long long m) {
+    __device__ void finish_wide(const TcArgs& a, int split_, int ksplit_) {
         la = max(a.lora_ids[p0 / a.k], 0);
         lb = a.lora_ids[p1 / a.k];
-        mask = a.L <= 64 ? m : ~0ull;  // no per-expert mask beyond 64 adapters
+        split = split_;
+        ksplit = ksplit_;
+        wide = true;
+        bits = 0;
     }
-    __device__ void none() { la = 0; lb = -1; mask = 0; }
-    __device__ bool has(int l) const { return l >= 64 || ((mask >> l) & 1ull); }
+    __device__ void none() { la = 0; lb = -1; split = 0; ksplit = 1; wide = false; bits = 0; }
+    // first block >= jb of this task's split, or -1
+    __device__ int next(int jb) const {
+        if (!wide) {
+            if (jb >= 64) return -1;
+            const unsigned long long rest = bits & (~0ull << jb);
+            return rest ? __ffsll((long long)rest) - 1 : -1;
+        }
+        for (jb = max(jb, la); jb <= lb; jb++)
+            if (jb % ksplit == split) return jb;
+        return -1;
+    }
     __device__ int count() const {
+        if (!wide) return __popcll(bits);
         int n = 0;
-        for (int l = la; l <= lb; l++) n += has(l) ? 1 : 0;
+        for (int jb = next(0); jb >= 0; jb = next(jb + 1)) n++;
         return n;
     }
 };
@@ -272,7 +309,7 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
     const int clo = s_lo < sh.nb ? s_cb[s_lo] : 0;
     const int chi = s_lo < sh.nb ? s_ce[s_hi] : 0;
     float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
-    // bf16 copy for the tensor-core expand: row q, slot of adapter l
+    // bf16 copy for the tensor-core expand: row q, the 64-wide slot of adapter l
     const size_t zx_cols = (size_t)a.L * 64;
     uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + s_sl[my_s] * 64 + j : nullptr;
 
@@ -359,8 +396,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     uint64_t* ebar = tempty + 2;    // epilogue rendezvous (kEpiWarps * 32 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
     TaskTable tt;
-    tt.amask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
-    tt.e = reinterpret_cast<int*>(tt.amask + a.E);
+    tt.cmask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
+    tt.e = reinterpret_cast<int*>(tt.cmask + (a.chunk_masks ? a.max_chunks : 0));
     tt.q0 = tt.e + a.E;
     tt.m = tt.q0 + a.E;
     tt.cum = tt.m + a.E;
@@ -414,18 +451,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         tt.q0[ai] = q0;
         tt.m[ai] = m;
         tt.cum[ai + 1] = ntiles * ((m + BN - 1) / BN);
-        tt.amask[ai] = 0ull;
     }
     __syncthreads();
-    if (a.tc_expand && a.L <= 64) {
-        // adapters with pairs on each active expert
-        for (int w = threadIdx.x; w < n_active * a.L; w += kTcThreads) {
-            const int ai = w / a.L, l = w % a.L;
-            const int b = tt.e[ai] * (a.L + 1) + l + 1;
-            if (a.compact_offset[b + 1] > a.compact_offset[b]) atomicOr(&tt.amask[ai], 1ull << l);
-        }
-        __syncthreads();
-    }
     if (warp == 0) {
         int carry = 0;
         for (int base = 0; base < n_active; base += 32) {
@@ -442,6 +469,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) tt.cum[0] = 0;
     }
     __syncthreads();
+    if (a.chunk_masks) {
+        // adapters with pairs in each (expert, pair chunk): one item per (expert,
+        // adapter) bucket, OR-ed into the chunks the bucket's rows fall in
+        const int n_chunks = tt.cum[n_active] / ntiles;
+        for (int c = threadIdx.x; c < n_chunks; c += kTcThreads) tt.cmask[c] = 0ull;
+        __syncthreads();
+        for (int w = threadIdx.x; w < n_active * a.L; w += kTcThreads) {
+            const int ai = w / a.L, l = w % a.L;
+            const int b = tt.e[ai] * (a.L + 1) + l + 1;
+            const int lo = a.compact_offset[b] - tt.q0[ai], hi = a.compact_offset[b + 1] - tt.q0[ai];
+            const int c0 = tt.cum[ai] / ntiles;
+            for (int ch = lo / BN; hi > lo && ch <= (hi - 1) / BN; ch++) atomicOr(&tt.cmask[c0 + ch], 1ull << l);
+        }
+        __syncthreads();
+    }
     const int ksplit = a.ksplit;
     // shrink items first, then the GEMM tasks
     const bool shrink = a.sh_tasks != nullptr && a.r > 0;
@@ -493,21 +535,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     continue;
                 }
                 Task<BN> tw;
-                tw.lookup(tt, n_active, ksplit, t - n_sh);
+                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
                 const int n_cols = tw.n_cols, row0 = tw.q0c, e = tw.e;
                 const int n_box = (n_cols + kRows - 1) / kRows;
                 const uint32_t bytes = S::kAB + (uint32_t)n_box * kRows * kBK * 2;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                // LoRA expand K-blocks of this task (last K-split only): the pair ids
-                // are fetched now, their adapters just before the last base stage
+                // LoRA expand K-blocks of this task's split (without chunk masks the
+                // pair ids are fetched now, their adapters before the last base stage)
                 ExpandRange xr;
                 xr.none();
-                const bool with_x = expand && tw.split == ksplit - 1;
-                if (with_x) xr.begin(a, row0, tw.n_real);
                 int n_x = 0;
+                if (expand && a.chunk_masks) {
+                    xr.from_mask(tt.cmask[tw.chunk], tw.split, ksplit);
+                    n_x = xr.count();
+                } else if (expand) {
+                    xr.begin(a, row0, tw.n_real);
+                }
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (with_x && kb == kb1 - 1) {
-                        xr.finish(a, tt.amask[tw.ai]);
+                    if (expand && !a.chunk_masks && kb == kb1 - 1) {
+                        xr.finish_wide(a, tw.split, ksplit);
                         n_x = xr.count();
                     }
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
@@ -533,19 +579,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     z_seen = true;
                 }
-                for (int l = xr.la; ok && l <= xr.lb; l++) {
-                    if (!xr.has(l)) continue;
+                for (int jb = n_x > 0 ? xr.next(0) : -1; ok && jb >= 0; jb = xr.next(jb + 1)) {
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[stage], bytes);
                     uint8_t* dst = base + (size_t)stage * S::kStage;
+                    const int l0 = jb;
+                    // B rows of adapter l0 (one adapter per block): coordinates
+                    // (k, unit, half, expert, adapter) / (k, row, expert, adapter)
                     if (GATE_UP) {
-                        tma_load_5d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l);
-                        tma_load_5d(dst + kATile, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l);
+                        tma_load_5d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l0);
+                        tma_load_5d(dst + kATile, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l0);
                     } else {
-                        tma_load_4d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l);
+                        tma_load_4d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l0);
                     }
                     for (int g = 0; g < n_box; g++)
-                        tma_load_2d(dst + S::kAB + g * kRows * kBK * 2, &a.zxmap, &full[stage], l * 64, row0 + g * kRows);
+                        tma_load_2d(dst + S::kAB + g * kRows * kBK * 2, &a.zxmap, &full[stage], jb * kBK, row0 + g * kRows);
                     armed |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -563,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            const int xsteps = (a.r + 15) / 16;
+            const int xsteps = (a.r + 15) / 16;  // K steps of an expand block
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
                 const int b = it & 1;
                 if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
@@ -590,16 +638,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     continue;
                 }
                 Task<BN> tw;
-                tw.lookup(tt, n_active, ksplit, t - n_sh);
+                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
                 const uint32_t idesc = umma_idesc_bf16_f32(kBM, tw.n_cols);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 ExpandRange xr;
                 xr.none();
-                if (expand && tw.split == ksplit - 1) {
-                    // the expand's adapters (same rule as the producer), looked up while
+                if (expand && a.chunk_masks) {
+                    xr.from_mask(tt.cmask[tw.chunk], tw.split, ksplit);
+                } else if (expand) {
+                    // the expand blocks (same rule as the producer), looked up while
                     // the first stage is in flight
                     xr.begin(a, tw.q0c, tw.n_real);
-                    xr.finish(a, tt.amask[tw.ai]);
+                    xr.finish_wide(a, tw.split, ksplit);
                 }
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
@@ -617,8 +667,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
-                for (int l = xr.la; l <= xr.lb && ok; l++) {
-                    if (!xr.has(l)) continue;
+                for (int jb = xr.next(0); jb >= 0 && ok; jb = xr.next(jb + 1)) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
@@ -664,7 +713,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 continue;
             }
             Task<BN> tw;
-            tw.lookup(tt, n_active, ksplit, t - n_sh);
+            tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
             const int e = tw.e, q0c = tw.q0c, n_real = tw.n_real, n_cols = tw.n_cols;
             // z is complete once every shrink task has finished (they run first on every CTA)
             if (!z_ready && etid == 0) s_misc[0] = wait_count(a.zdone, n_sh_tasks);
@@ -800,17 +849,17 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
 
 }  // namespace
 
-int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand) {
+int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks) {
     const int ab = gate_up ? 2 * kATile : kATile;
     const int stage = ab + bn * kBK * 2;
     const int staging = (tc_expand ? 0 : bn * r * 4) + 3 * bn * 4 + kMisc * 4;
-    const int table = 8 * E + (4 * E + 1) * 4;
+    const int table = 8 * mask_chunks + (4 * E + 1) * 4;
     return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
 }
 
-int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand) {
+int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks) {
     for (int ns = 8; ns >= 2; ns--)
-        if (tc_smem_bytes(gate_up, bn, r, E, ns, tc_expand) <= kTcSmemLimit) return ns;
+        if (tc_smem_bytes(gate_up, bn, r, E, ns, tc_expand, mask_chunks) <= kTcSmemLimit) return ns;
     return 0;
 }
 
@@ -823,7 +872,8 @@ cudaError_t init_tc_attributes() {
 }
 
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl) {
-    const int smem = tc_smem_bytes(gate_up, bn, args.r, args.E, args.nstages, args.tc_expand != 0);
+    const int smem = tc_smem_bytes(gate_up, bn, args.r, args.E, args.nstages, args.tc_expand != 0,
+                                   args.chunk_masks ? args.max_chunks : 0);
     const dim3 g(grid), b(kTcThreads);
     if (gate_up) {
         if (bn == 64) return launch_k(k_moe_gemm_tc<true, 64>, g, b, smem, stream, pdl, args);

@@ -31,8 +31,12 @@ namespace moelora {
 namespace {
 
 constexpr int kDefaultBlockM = 16;
-constexpr long kMaxZexpSlots = 1L << 17;  // pairs x adapters: 16 MiB per zexp buffer
+constexpr long kMaxZexpElems = 1L << 23;  // bf16 elements per zexp buffer (16 MiB)
+
+// zexp columns: one 64-wide slot per adapter (the expand's K block of that adapter)
+long zexp_cols(int L, int /*r*/) { return (long)L * 64; }
 constexpr int kMaxDevices = 64;
+constexpr int kMaxChunkMasks = 2048;  // 16 KiB of shared memory for the expand's chunk masks
 
 struct Layout {
     int bm;
@@ -192,13 +196,14 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
     L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
-    // zexp: per pair L slots of 64 bf16.  The tensor-core expand pays one K
-    // block per adapter of a chunk; it is used when chunks are expected to mix
-    // several adapters (the CUDA-core expand then reloads B rows per adapter run)
-    // and while zexp stays small (it is rewritten every forward).
-    L->tc_expand = d->L > 0 && L->P * (long)d->L <= kMaxZexpSlots &&
+    // zexp: per pair, one 64-wide slot per adapter.  The tensor-core expand
+    // pays one K block per adapter of a chunk; it is used when chunks are
+    // expected to mix several adapters (the CUDA-core expand then reloads B rows
+    // per adapter run) and while zexp stays small (it is rewritten every
+    // forward).
+    L->tc_expand = d->L > 0 && L->P * zexp_cols(d->L, d->r) <= kMaxZexpElems &&
                    expected_adapters_per_chunk(d, L->P) >= 4.0;
-    const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * d->L * 64 : 0;
+    const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * zexp_cols(d->L, d->r) : 0;
     L->zexp1 = take(zx);
     L->zexp2 = take(zx);
     L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
@@ -302,7 +307,8 @@ bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K, int box_
 }
 int pair_box_rows(int bn) { return bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
 
-// B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of 64 (K; zeros beyond r) x 128 units of one half
+// B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of 64 (K; zeros beyond r) x 128
+// units of one half, for one adapter (strides increase with the dimension)
 bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r) {
     const cuuint64_t dims[5] = {(cuuint64_t)r, (cuuint64_t)I, 2, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[4] = {(cuuint64_t)r * 2, (cuuint64_t)I * r * 2, (cuuint64_t)2 * I * r * 2,
@@ -492,7 +498,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     if (L.tc_expand) {
         ga.zexp1 = at<uint16_t>(ws, L.zexp1);
         ga.zexp2 = at<uint16_t>(ws, L.zexp2);
-        ga.zx_cols = d->L * 64;
+        ga.zx_cols = (int)zexp_cols(d->L, d->r);
     }
     tr.mark(1);
     {
@@ -515,6 +521,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tc.pair_out = at<float>(ws, L.pair_out);
     int* sh_counters = at<int>(ws, L.counters);
     tc.tc_expand = L.tc_expand ? 1 : 0;
+    const long experts_bound = std::max<long>(1, std::min<long>(d->E, L.P));
     if (has_lora) {
         tc.sh_tasks = at<int4>(ws, L.st_tasks);
         tc.sh_G = L.st_G;
@@ -534,14 +541,16 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.sh_counters = sh_counters;
         tc.zdone = sh_counters + 2 * L.st_tasks_max;
         tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp1) : nullptr;
-        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand);
+        tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
+        tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
+        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         const int rows = pair_box_rows(bn);
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
-                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, d->L * 64, rows))))
+                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, (int)zexp_cols(d->L, d->r), rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
@@ -561,14 +570,16 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.sh_counters = sh_counters + L.st_tasks_max;
         tc.zdone = sh_counters + 2 * L.st_tasks_max + 1;
         tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp2) : nullptr;
-        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand);
+        tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
+        tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
+        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
         const int rows = pair_box_rows(bn);
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
-                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, d->L * 64, rows))))
+                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, (int)zexp_cols(d->L, d->r), rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));

@@ -61,8 +61,11 @@ RAGGED = [
     (2, 2048, 512, 2, 1, 1, 64),
     # more than 64 adapters: the tensor-core expand runs without per-expert adapter masks
     (40, 128, 96, 3, 2, 70, 8),
-    # pairs x adapters beyond the zexp bound: the expand falls back to CUDA cores
-    (2100, 64, 64, 4, 1, 64, 8),
+    # pairs x adapter slots beyond the zexp bound: the expand falls back to CUDA cores
+    (2100, 64, 64, 4, 1, 64, 64),
+    # r = 8 and r = 16: eight and four adapters packed per expand K block
+    (160, 128, 96, 2, 2, 11, 8),
+    (160, 128, 96, 2, 2, 7, 16),
     # wide chunks mixing several adapters (prefill-like): 64-row pair boxes, the
     # LoRA expand as tensor-core K blocks (r not a power of two; r = 64 with ragged I)
     (600, 128, 136, 2, 2, 5, 32),
