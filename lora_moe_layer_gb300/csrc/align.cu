@@ -9,14 +9,18 @@
 // b = e*(L+1) + (l+1): buckets in ascending b, pairs in ascending p inside a
 // bucket, each non-empty bucket padded to a multiple of block_m.
 //
-// One CTA of 16 warps.  Each warp owns a contiguous segment of pairs and keeps
-// a per-bucket histogram row (shared memory when it fits, else the workspace).
-// Pass 1 counts with warp match-any + popc (one leader per distinct key per
-// 32 pairs); the histogram rows are then turned into per-warp exclusive
-// prefixes, bucket sizes are scanned (warp shuffles) into padded and compact
-// offsets, and pass 2 places every pair at
+// One CTA of 16 warps.  First every thread computes bucket keys for a strided
+// share of the pairs (independent loads, many in flight) into shared memory
+// when they fit, else the workspace.  Each warp then owns a contiguous segment
+// of pairs and keeps a per-bucket histogram row (shared memory when it fits,
+// else the workspace).  Pass 1 counts with warp match-any + popc (one leader
+// per distinct key per 32 pairs); the histogram rows are then turned into
+// per-warp exclusive prefixes, bucket sizes are scanned (warp shuffles) into
+// padded and compact offsets, and pass 2 places every pair at
 //     offset[b] + (pairs of b in earlier warps) + (earlier lanes of b in this step).
 // Walking each segment in order and the warps in order keeps ascending p.
+// The padded outputs (sentinels, per-tile expert and adapter) are written only
+// for the standalone entry point; the forward works on the compact order.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -101,13 +105,36 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     const int P = a.T * a.k;
     const int L1 = a.L + 1;
     const int NB = a.E * L1;
-    int* hist = a.hist_global ? a.hist_global : smem_hist;  // [kAlignWarps][NB]
+    // shared memory: [histogram][bucket tables][pair keys], each part optional
+    int* sm = smem_hist;
+    int* hist = a.hist_global ? a.hist_global : sm;  // [kAlignWarps][NB]
+    if (!a.hist_global) sm += kAlignWarps * NB;
+    // bucket sizes and padded / compact offsets; later steps read them from here
+    int* cnt_t = a.tabs_in_smem ? sm : a.bucket_count;
+    int* boff_t = a.tabs_in_smem ? sm + NB : a.bucket_offset;
+    int* coff_t = a.tabs_in_smem ? sm + 2 * NB + 1 : a.compact_offset;
+    if (a.tabs_in_smem) sm += 3 * NB + 2;
+    // bucket key of every pair (-1: left out)
+    int* keys = a.keys_in_smem ? sm : a.keys_global;
     WsHeader* hdr = a.hdr;
 
     if (threadIdx.x == 0) hdr->status = 0;
     for (int i = threadIdx.x; i < kAlignWarps * NB; i += kAlignThreads) hist[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero; i += kAlignThreads) a.zero_ints[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
+    {
+        int bad = 0;
+#pragma unroll 4
+        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
+            const int e = a.topk_ids[p];
+            const int l = a.lora_ids[p / a.k];
+            const bool e_ok = e >= 0 && e < a.E;
+            const bool l_ok = l >= -1 && l < a.L;
+            keys[p] = e_ok && l_ok ? e * L1 + (l + 1) : -1;
+            bad |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
+        }
+        if (bad) atomicOr(&hdr->status, bad);
+    }
     __syncthreads();
 
     // each warp owns pairs [seg_beg, seg_end), walked 32 at a time
@@ -115,25 +142,15 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     const int seg_beg = min(P, warp * seg);
     const int seg_end = min(P, seg_beg + seg);
     int* my_hist = hist + warp * NB;
-    int bad_bits = 0;
 
     // pass 1: per-warp bucket counts
     for (int base = seg_beg; base < seg_end; base += 32) {
         const int p = base + lane;
-        int b = -1;
-        if (p < seg_end) {
-            const int e = a.topk_ids[p];
-            const int l = a.lora_ids[p / a.k];
-            const bool e_ok = e >= 0 && e < a.E;
-            const bool l_ok = l >= -1 && l < a.L;
-            if (e_ok && l_ok) b = e * L1 + (l + 1);
-            else bad_bits |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
-        }
+        const int b = p < seg_end ? keys[p] : -1;
         const unsigned peers = __match_any_sync(kFull, b);
         if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
         __syncwarp();
     }
-    if (bad_bits) atomicOr(&hdr->status, bad_bits);
     __syncthreads();
 
     // per bucket: exclusive prefix over warps, and the bucket size
@@ -144,34 +161,34 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             hist[w * NB + b] = run;
             run += c;
         }
-        a.bucket_count[b] = run;
+        cnt_t[b] = run;
+        if (a.tabs_in_smem) a.bucket_count[b] = run;
     }
     __syncthreads();
 
     // padded offsets (bucket_offset) and compact offsets, both exclusive scans
     const int bm = a.bm;
-    const int* cnt = a.bucket_count;
+    const int* cnt = cnt_t;
     block_scan_items(
         NB, [&](int b) { const int c = cnt[b]; return make_int2((c + bm - 1) / bm * bm, c); },
-        a.bucket_offset, a.compact_offset, sw);
+        boff_t, coff_t, sw);
     __syncthreads();
+    if (a.tabs_in_smem) {
+        for (int b = threadIdx.x; b <= NB; b += kAlignThreads) {
+            a.bucket_offset[b] = boff_t[b];
+            a.compact_offset[b] = coff_t[b];
+        }
+    }
 
     // pass 2: stable placement
     for (int base = seg_beg; base < seg_end; base += 32) {
         const int p = base + lane;
-        int b = -1;
-        if (p < seg_end) {
-            const int e = a.topk_ids[p];
-            const int l = a.lora_ids[p / a.k];
-            if (e >= 0 && e < a.E && l >= -1 && l < a.L) b = e * L1 + (l + 1);
-        }
+        const int b = p < seg_end ? keys[p] : -1;
         const unsigned peers = __match_any_sync(kFull, b);
         if (b >= 0) {
             const int rank = my_hist[b] + __popc(peers & lanemask_lt());
-            const int pos = a.bucket_offset[b] + rank;
-            const int cpos = a.compact_offset[b] + rank;
-            a.sorted_ids[pos] = p;
-            a.compact_ids[cpos] = p;
+            if (a.full_outputs) a.sorted_ids[boff_t[b] + rank] = p;
+            a.compact_ids[coff_t[b] + rank] = p;
         }
         __syncwarp();
         if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
@@ -179,33 +196,26 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     }
     __syncthreads();
 
-    // padding sentinels
-    for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
-        const int end = a.bucket_offset[b + 1];
-        for (int q = a.bucket_offset[b] + cnt[b]; q < end; q++) a.sorted_ids[q] = P;
-    }
-    // per-tile (expert, adapter): the bucket holding row q*bm
-    const int total_padded = a.bucket_offset[NB];
-    const int n_tiles = total_padded / bm;
-    for (int q = threadIdx.x; q < n_tiles; q += kAlignThreads) {
-        const int row = q * bm;
-        int lo = 0, hi = NB;  // find the last b with bucket_offset[b] <= row < bucket_offset[b+1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (a.bucket_offset[mid] <= row) lo = mid;
-            else hi = mid;
+    if (a.full_outputs) {
+        // padding sentinels, and each bucket's tiles tagged with its (expert, adapter)
+        for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
+            const int beg = boff_t[b], end = boff_t[b + 1];
+            for (int q = beg + cnt[b]; q < end; q++) a.sorted_ids[q] = P;
+            for (int q = beg / bm; q < end / bm; q++) {
+                a.tile_expert[q] = b / L1;
+                a.tile_lora[q] = b % L1 - 1;
+            }
         }
-        a.tile_expert[q] = lo / L1;
-        a.tile_lora[q] = lo % L1 - 1;
     }
+    const int total_padded = boff_t[NB];
     if (threadIdx.x == 0) {
         hdr->num_post_padded = total_padded;
-        hdr->n_valid = a.compact_offset[NB];
+        hdr->n_valid = coff_t[NB];
         if (a.num_post_padded) *a.num_post_padded = total_padded;
     }
     if (a.active_experts) {
         // compact list of experts with pairs, and of (e, l >= 0) buckets with pairs
-        const int* coff = a.compact_offset;
+        const int* coff = coff_t;
         const int E = a.E;
         block_scan_items(
             E, [&](int e) { return make_int2(coff[(e + 1) * L1] > coff[e * L1] ? 1 : 0, 0); },
@@ -252,6 +262,23 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
 
 }  // namespace
 
+// Optional shared-memory parts after the histogram (which must be there too):
+// the bucket tables first, then the pair keys, as long as the total fits.
+int align_tabs_smem_bytes(int E, int L) {
+    const int hist = align_hist_smem_bytes(E, L);
+    const long bytes = (3L * E * (L + 1) + 2) * (long)sizeof(int);
+    return hist && hist + bytes <= kAlignMaxSmem ? (int)bytes : 0;
+}
+
+int align_keys_smem_bytes(int E, int L, long P) {
+    const long bytes = P * (long)sizeof(int);
+    return align_hist_smem_bytes(E, L) + align_tabs_smem_bytes(E, L) + bytes <= kAlignMaxSmem ? (int)bytes : 0;
+}
+
+int align_smem_bytes(int E, int L, long P) {
+    return align_hist_smem_bytes(E, L) + align_tabs_smem_bytes(E, L) + align_keys_smem_bytes(E, L, P);
+}
+
 int align_hist_smem_bytes(int E, int L) {
     const long nb = (long)E * (L + 1);
     const long bytes = nb * kAlignWarps * (long)sizeof(int);
@@ -263,7 +290,7 @@ long align_hist_global_ints(int E, int L) {
 }
 
 cudaError_t init_align_attributes() {
-    return cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmemHist);
+    return cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmem);
 }
 
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream) {

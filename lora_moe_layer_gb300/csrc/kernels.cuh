@@ -11,6 +11,7 @@ namespace moelora {
 
 // ---------------------------------------------------------------- align ----
 constexpr int kAlignMaxSmemHist = 160 * 1024;
+constexpr int kAlignMaxSmem = 200 * 1024;  // histogram + pair keys
 
 struct AlignArgs {
     int T, k, E, L, bm;
@@ -37,10 +38,17 @@ struct AlignArgs {
     // st_G, each group's rows in chunks of at most st_BN, as (group, first row, rows, 0)
     int4* st_tasks;
     int st_G, st_BN;
+    int* keys_global;          // [P] pair keys when they do not fit in shared memory
+    int keys_in_smem;          // 1: keys in shared memory
+    int tabs_in_smem;          // 1: bucket sizes and offsets also in shared memory
+    int full_outputs;          // 1: also sentinels and per-tile expert/adapter (standalone align)
     WsHeader* hdr;
 };
 
 int align_hist_smem_bytes(int E, int L);   // 0 if the histogram must live in global memory
+int align_keys_smem_bytes(int E, int L, long P);  // 0 if the pair keys must live in global memory
+int align_tabs_smem_bytes(int E, int L);           // 0 if the bucket tables stay in global memory only
+int align_smem_bytes(int E, int L, long P);        // dynamic shared memory of the align launch
 long align_hist_global_ints(int E, int L);
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream);
 cudaError_t init_align_attributes();

@@ -71,7 +71,10 @@ struct TcShape {
     static constexpr int kAB = GATE_UP ? 2 * kATile : kATile;  // weight bytes per stage
     static constexpr int kStage = kAB + BN * kBK * 2;          // + pair rows
     static constexpr int kAccCols = GATE_UP ? 2 * BN : BN;      // TMEM columns per accumulator set
-    static constexpr int kTmemCols = 2 * kAccCols <= 32 ? 32 : 2 * kAccCols;
+    // accumulator sets in TMEM: as many as fit, up to 4, so the MMAs can run
+    // ahead of the epilogue on short tasks
+    static constexpr int kNAcc = 4 * kAccCols <= 512 ? 4 : 2;
+    static constexpr int kTmemCols = kNAcc * kAccCols <= 32 ? 32 : kNAcc * kAccCols;
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM allocation");
     static_assert(BN % 16 == 0 && BN <= 256, "MMA N");
 };
@@ -186,33 +189,42 @@ struct EpiRow {
     }
 };
 
-// LoRA expand on the tensor cores: one 64-wide K block per adapter l, whose A
-// tile is that adapter's B rows (a 64-element TMA box over the r-wide rows reads
-// zeros beyond r) and whose B tile is zexp rows, where a pair's z sits in its
-// adapter's 64-wide slot and all other slots are zero.
+// LoRA expand on the tensor cores.  An adapter's share of the expand is a
+// K-major tile pair of width r_pad (r rounded up to 16, 32 or 64; TMA reads
+// zeros beyond r): A = its B rows (128 weight rows x r_pad), B = zexp rows
+// (pairs x r_pad), where zexp holds each pair's z in its adapter's r_pad-wide
+// slot and zeros in every other slot.  The tiles use the swizzle whose span is
+// one row (32, 64 or 128 bytes), and 64 / r_pad adapters share one ring stage
+// as separate sub-tiles, each with its own MMA descriptors.
+__host__ __device__ inline int expand_rpad(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
+__device__ inline uint32_t expand_layout(int rp) { return rp == 16 ? 6u : rp == 32 ? 4u : 2u; }
 
-// The expand blocks of one GEMM task: one per adapter with pairs in the task's
-// chunk, dealt to the task's K-splits by jb mod ksplit so a split-K task
-// spreads its expand work too.  With up to 64 adapters the set comes from the
-// chunk's adapter mask built at kernel start and is walked by its set bits, so
-// the single MMA-issuing thread spends a few instructions per task on it.
-// Beyond that, the pairs of a chunk (sorted by adapter) span the adapters la ..
-// lb of its first and last pair, read from global memory, and every adapter of
-// the span gets a block (zexp zeros make the absent ones add nothing).
+// The expand blocks of one GEMM task: block jb holds the adapters jb*apb ..
+// jb*apb+apb-1 that have pairs in the task's chunk.  Blocks are dealt to the
+// task's K-splits by jb mod ksplit, so a split-K task spreads its expand work
+// too.  With up to 64 adapters the set comes from the chunk's adapter mask
+// built at kernel start and is walked by its set bits (the single MMA-issuing
+// thread spends a few instructions per task on it).  Beyond that, the pairs of
+// a chunk (sorted by adapter) span the adapters la .. lb of its first and last
+// pair, read from global memory, and every adapter of the span is taken (zexp
+// zeros make the absent ones add nothing).
 struct ExpandRange {
-    int la, lb, p0, p1, split, ksplit;
+    int la, lb, p0, p1, split, ksplit, apb, L;
     bool wide;
-    unsigned long long bits;   // blocks of this split (ids < 64)
-    __device__ void from_mask(unsigned long long m, int split_, int ksplit_) {
+    unsigned long long bits;   // adapters of this split's blocks (ids < 64)
+    __device__ void from_mask(const TcArgs& a, unsigned long long m, int split_, int ksplit_) {
         la = 0;
         lb = -1;
         split = split_;
         ksplit = ksplit_;
+        apb = 64 / expand_rpad(a.r);
+        L = a.L;
         wide = false;
         bits = m;
         if (ksplit > 1) {
+            const unsigned long long blk = apb == 64 ? ~0ull : (1ull << apb) - 1;
             unsigned long long mine = 0;
-            for (int jb = split; jb < 64; jb += ksplit) mine |= 1ull << jb;
+            for (int jb = split; jb * apb < 64; jb += ksplit) mine |= blk << (jb * apb);
             bits &= mine;
         }
     }
@@ -226,23 +238,35 @@ struct ExpandRange {
         lb = a.lora_ids[p1 / a.k];
         split = split_;
         ksplit = ksplit_;
+        apb = 64 / expand_rpad(a.r);
+        L = a.L;
         wide = true;
         bits = 0;
     }
-    __device__ void none() { la = 0; lb = -1; split = 0; ksplit = 1; wide = false; bits = 0; }
+    __device__ void none() { la = 0; lb = -1; split = 0; ksplit = 1; apb = 1; L = 0; wide = false; bits = 0; }
     // first block >= jb of this task's split, or -1
     __device__ int next(int jb) const {
         if (!wide) {
-            if (jb >= 64) return -1;
-            const unsigned long long rest = bits & (~0ull << jb);
-            return rest ? __ffsll((long long)rest) - 1 : -1;
+            if (jb * apb >= 64) return -1;
+            const unsigned long long rest = bits & (~0ull << (jb * apb));
+            return rest ? (__ffsll((long long)rest) - 1) / apb : -1;
         }
-        for (jb = max(jb, la); jb <= lb; jb++)
+        for (jb = max(jb, la / apb); jb * apb <= lb; jb++)
             if (jb % ksplit == split) return jb;
         return -1;
     }
+    // adapters of block jb (bit s = adapter jb*apb + s)
+    __device__ uint32_t slots(int jb) const {
+        const uint32_t all = (1u << apb) - 1u;
+        if (!wide) return (uint32_t)(bits >> (jb * apb)) & all;
+        uint32_t sm = 0;
+        for (int s = 0; s < apb; s++) {
+            const int l = jb * apb + s;
+            if (l >= la && l <= lb && l < L) sm |= 1u << s;
+        }
+        return sm;
+    }
     __device__ int count() const {
-        if (!wide) return __popcll(bits);
         int n = 0;
         for (int jb = next(0); jb >= 0; jb = next(jb + 1)) n++;
         return n;
@@ -279,13 +303,14 @@ __device__ __forceinline__ int wait_count(const int* p, int target) {
     return 0;
 }
 
-// Epilogue of shrink item t: each thread is one TMEM lane = (slot, rank
+// Epilogue of shrink item t (in accumulator set b, used `use` times before):
+// each thread is one TMEM lane = (slot, rank
 // index) row and stores z for the pairs of its slot; the two warps of a lane
 // quadrant take alternate 4-column groups.  With a K-split, the split that
 // arrives last sums all partials in split order.  The item then counts
 // itself in zdone.  False on a timeout (warp-uniform).
 template <typename Rdv>
-__device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int it, uint32_t tmem_base,
+__device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int use, uint32_t tmem_base,
                                 uint32_t acc_cols, int qd, int half, int lane, int etid, int* s_cb, int* s_ce,
                                 int* s_misc, uint64_t* tfull, uint64_t* tempty, Rdv& rendezvous) {
     ShItem sh;
@@ -309,11 +334,12 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
     const int clo = s_lo < sh.nb ? s_cb[s_lo] : 0;
     const int chi = s_lo < sh.nb ? s_ce[s_hi] : 0;
     float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
-    // bf16 copy for the tensor-core expand: row q, the 64-wide slot of adapter l
-    const size_t zx_cols = (size_t)a.L * 64;
-    uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + s_sl[my_s] * 64 + j : nullptr;
+    // bf16 copy for the tensor-core expand: row q, the r_pad-wide slot of adapter l
+    const int rp = expand_rpad(r);
+    const size_t zx_cols = (size_t)a.L * rp;
+    uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + s_sl[my_s] * rp + j : nullptr;
 
-    if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) return false;
+    if (!__all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)use & 1u))) return false;
     tc_fence_after();
     const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)b * acc_cols;
     for (int c4 = (clo & ~3) + 4 * half; c4 < chi; c4 += 8) {
@@ -364,7 +390,7 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int i
                     uint2 pk;
                     pk.x = (uint32_t)f32_to_bf16_rne(acc.x) | ((uint32_t)f32_to_bf16_rne(acc.y) << 16);
                     pk.y = (uint32_t)f32_to_bf16_rne(acc.z) | ((uint32_t)f32_to_bf16_rne(acc.w) << 16);
-                    *reinterpret_cast<uint2*>(a.zexp + (size_t)q * zx_cols + l * 64 + kk) = pk;
+                    *reinterpret_cast<uint2*>(a.zexp + (size_t)q * zx_cols + l * rp + kk) = pk;
                 }
             }
         }
@@ -391,9 +417,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     int* s_misc = reinterpret_cast<int*>(s_w + BN);  // [kMisc] shared by the epilogue warps
     uint64_t* full = reinterpret_cast<uint64_t*>(s_misc + kMisc);
     uint64_t* empty = full + NS;
-    uint64_t* tfull = empty + NS;   // [2] accumulator ready for the epilogue
-    uint64_t* tempty = tfull + 2;   // [2] accumulator drained by the epilogue
-    uint64_t* ebar = tempty + 2;    // epilogue rendezvous (kEpiWarps * 32 arrivals)
+    uint64_t* tfull = empty + NS;       // [kNAcc] accumulator ready for the epilogue
+    uint64_t* tempty = tfull + S::kNAcc;  // [kNAcc] accumulator drained by the epilogue
+    uint64_t* ebar = tempty + S::kNAcc;   // epilogue rendezvous (kEpiWarps * 32 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
     TaskTable tt;
     tt.cmask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
@@ -408,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < S::kNAcc; b++) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], kEpiWarps);
         }
@@ -546,7 +572,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 xr.none();
                 int n_x = 0;
                 if (expand && a.chunk_masks) {
-                    xr.from_mask(tt.cmask[tw.chunk], tw.split, ksplit);
+                    xr.from_mask(a, tt.cmask[tw.chunk], tw.split, ksplit);
                     n_x = xr.count();
                 } else if (expand) {
                     xr.begin(a, row0, tw.n_real);
@@ -579,21 +605,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     z_seen = true;
                 }
+                // per adapter: A sub-tile (128 x r_pad) and zexp sub-tile (rows x r_pad)
+                const int xrp = expand_rpad(a.r);
+                const uint32_t xa_bytes = 128u * xrp * 2u, xb_bytes = (uint32_t)(n_box * kRows) * xrp * 2u;
                 for (int jb = n_x > 0 ? xr.next(0) : -1; ok && jb >= 0; jb = xr.next(jb + 1)) {
+                    const uint32_t sm = xr.slots(jb);
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)__popc(sm) * ((GATE_UP ? 2u : 1u) * xa_bytes + xb_bytes));
                     uint8_t* dst = base + (size_t)stage * S::kStage;
-                    const int l0 = jb;
-                    // B rows of adapter l0 (one adapter per block): coordinates
-                    // (k, unit, half, expert, adapter) / (k, row, expert, adapter)
-                    if (GATE_UP) {
-                        tma_load_5d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l0);
-                        tma_load_5d(dst + kATile, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l0);
-                    } else {
-                        tma_load_4d(dst, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l0);
+                    for (int q = 0; q < xr.apb; q++) {
+                        if (!((sm >> q) & 1u)) continue;
+                        const int l = jb * xr.apb + q;
+                        // B rows of adapter l: coordinates (k, unit, half, expert, adapter)
+                        // or (k, row, expert, adapter)
+                        if (GATE_UP) {
+                            tma_load_5d(dst + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l);
+                            tma_load_5d(dst + kATile + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l);
+                        } else {
+                            tma_load_4d(dst + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l);
+                        }
+                        uint8_t* zdst = dst + S::kAB + q * xb_bytes;
+                        for (int g = 0; g < n_box; g++)
+                            tma_load_2d(zdst + g * kRows * xrp * 2, &a.zxmap, &full[stage], l * xrp, row0 + g * kRows);
                     }
-                    for (int g = 0; g < n_box; g++)
-                        tma_load_2d(dst + S::kAB + g * kRows * kBK * 2, &a.zxmap, &full[stage], jb * kBK, row0 + g * kRows);
                     armed |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -607,14 +641,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         // -------------------------------------------------------------- MMA issuer
         // Walks the same item sequence as the producer (shrink items, then GEMM
         // tasks with their expand K-blocks); task data comes from the shared
-        // table, so the per-stage path is MMA issue only.
+        // table.  Descriptors are built by adds from two base descriptors (the
+        // start-address field counts 16-byte units: a stage adds kStage / 16, a
+        // sub-tile its offset / 16, a 16-wide K step 2), since this one thread
+        // issues every MMA of the CTA.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            const int xsteps = (a.r + 15) / 16;  // K steps of an expand block
+            // expand sub-tiles: r_pad-wide K-major rows, swizzle span = one row
+            const int xrp = expand_rpad(a.r);
+            const uint32_t xa16 = 128u * xrp * 2u / 16u;  // one adapter's A sub-tile, in 16-byte units
+            const uint64_t d0 = umma_desc_sw128(smem_u32(base));
+            const uint64_t dx0 = umma_desc_kmajor(smem_u32(base), expand_layout(xrp), 8u * xrp * 2u);
+            constexpr uint64_t kStage16 = S::kStage / 16, kUp16 = kATile / 16, kPair16 = S::kAB / 16;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-                const int b = it & 1;
-                if (!mbar_wait(&tempty[b], ((it >> 1) & 1) ^ 1)) { ok = false; break; }
+                const int b = it % S::kNAcc;
+                if (!mbar_wait(&tempty[b], ((uint32_t)(it / S::kNAcc) & 1u) ^ 1u)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_first = tmem_base + (uint32_t)(b * S::kAccCols);
                 if (t < n_sh) {
@@ -625,11 +667,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                         tc_fence_after();
-                        const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
+                        const uint64_t da = d0 + (uint64_t)stage * kStage16;
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; kk++)
-                            umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32),
-                                      umma_desc_sw128(a_addr + kATile + kk * 32), idesc, (kb != kb0) || (kk != 0));
+                            umma_bf16(d_first, da + 2 * kk, da + kUp16 + 2 * kk, idesc, (kb != kb0) || (kk != 0));
                         umma_commit(&empty[stage]);
                         if (++stage == NS) { stage = 0; phase ^= 1; }
                     }
@@ -644,7 +685,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 ExpandRange xr;
                 xr.none();
                 if (expand && a.chunk_masks) {
-                    xr.from_mask(tt.cmask[tw.chunk], tw.split, ksplit);
+                    xr.from_mask(a, tt.cmask[tw.chunk], tw.split, ksplit);
                 } else if (expand) {
                     // the expand blocks (same rule as the producer), looked up while
                     // the first stage is in flight
@@ -654,29 +695,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
-                    const uint32_t b_addr = a_addr + S::kAB;
+                    const uint64_t da = d0 + (uint64_t)stage * kStage16;
+                    const uint64_t db = da + kPair16;
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++) {
-                        const uint64_t bdesc = umma_desc_sw128(b_addr + kk * 32);
                         const uint32_t acc = (kb != kb0) || (kk != 0);
-                        umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32), bdesc, idesc, acc);
-                        if (GATE_UP)
-                            umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, acc);
+                        umma_bf16(d_first, da + 2 * kk, db + 2 * kk, idesc, acc);
+                        if (GATE_UP) umma_bf16(d_first + BN, da + kUp16 + 2 * kk, db + 2 * kk, idesc, acc);
                     }
                     umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
+                const uint32_t xb16 = (uint32_t)(((tw.n_cols + kRows - 1) / kRows) * kRows) * xrp * 2u / 16u;
                 for (int jb = xr.next(0); jb >= 0 && ok; jb = xr.next(jb + 1)) {
+                    const uint32_t sm = xr.slots(jb);
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(base + (size_t)stage * S::kStage);
-                    const uint32_t b_addr = a_addr + S::kAB;
-                    for (int kk = 0; kk < xsteps; kk++) {
-                        const uint64_t bdesc = umma_desc_sw128(b_addr + kk * 32);
-                        umma_bf16(d_first, umma_desc_sw128(a_addr + kk * 32), bdesc, idesc, 1u);
-                        if (GATE_UP)
-                            umma_bf16(d_first + BN, umma_desc_sw128(a_addr + kATile + kk * 32), bdesc, idesc, 1u);
+                    const uint64_t dxs = dx0 + (uint64_t)stage * kStage16;
+                    for (int q = 0; q < xr.apb; q++) {
+                        if (!((sm >> q) & 1u)) continue;
+                        const uint64_t da = dxs + q * xa16;
+                        const uint64_t db = dxs + kPair16 + q * xb16;
+                        for (int kk = 0; kk < xrp / 16; kk++) {
+                            umma_bf16(d_first, da + 2 * kk, db + 2 * kk, idesc, 1u);
+                            if (GATE_UP) umma_bf16(d_first + BN, da + kUp16 + 2 * kk, db + 2 * kk, idesc, 1u);
+                        }
                     }
                     umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -706,9 +749,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             return r_ok;
         };
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-            const int b = it & 1;
+            const int b = it % S::kNAcc;
+            const int use = it / S::kNAcc;  // how often this accumulator set was used before
             if (t < n_sh) {
-                if (!shrink_epilogue(a, t, n_lora, b, it, tmem_base, S::kAccCols, qd, half, lane, etid, s_pair,
+                if (!shrink_epilogue(a, t, n_lora, b, use, tmem_base, S::kAccCols, qd, half, lane, etid, s_pair,
                                      s_lora, s_misc, tfull, tempty, rendezvous)) { ok = false; break; }
                 continue;
             }
@@ -739,7 +783,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             if (!rendezvous()) { ok = false; break; }
 
             // warp-uniform outcome: the TMEM loads below are warp-collective
-            if (!__all_sync(kFull, mbar_wait(&tfull[b], (it >> 1) & 1))) { ok = false; break; }
+            if (!__all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)use & 1u))) { ok = false; break; }
             tc_fence_after();
             const int w_row = tw.mt * kBM + row;
             const bool row_ok = w_row < N_out;
@@ -854,7 +898,7 @@ int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expan
     const int stage = ab + bn * kBK * 2;
     const int staging = (tc_expand ? 0 : bn * r * 4) + 3 * bn * 4 + kMisc * 4;
     const int table = 8 * mask_chunks + (4 * E + 1) * 4;
-    return 1024 + nstages * stage + staging + (2 * nstages + 5) * 8 + 16 + table;
+    return 1024 + nstages * stage + staging + (2 * nstages + 2 * 4 + 1) * 8 + 16 + table;
 }
 
 int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks) {

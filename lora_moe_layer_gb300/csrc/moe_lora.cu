@@ -33,8 +33,14 @@ namespace {
 constexpr int kDefaultBlockM = 16;
 constexpr long kMaxZexpElems = 1L << 23;  // bf16 elements per zexp buffer (16 MiB)
 
-// zexp columns: one 64-wide slot per adapter (the expand's K block of that adapter)
-long zexp_cols(int L, int /*r*/) { return (long)L * 64; }
+// The expand's per-adapter width: r rounded up to 16, 32 or 64 (TMA reads zeros
+// beyond r), with the swizzle whose span is one such row.
+int expand_rpad_host(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
+CUtensorMapSwizzle expand_swizzle(int rp) {
+    return rp == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : rp == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+}
+// zexp columns: one r_pad-wide slot per adapter
+long zexp_cols(int L, int r) { return (long)L * expand_rpad_host(r); }
 constexpr int kMaxDevices = 64;
 constexpr int kMaxChunkMasks = 2048;  // 16 KiB of shared memory for the expand's chunk masks
 
@@ -46,7 +52,7 @@ struct Layout {
     int s1, s2, st_G, st_bn;
     long st_tasks_max;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
-        compact_ids, active_experts, lora_buckets, scan_tmp, hist, st_tasks, counters, z1, z1f, xc, act, z2,
+        compact_ids, active_experts, lora_buckets, scan_tmp, hist, keys, st_tasks, counters, z1, z1f, xc, act, z2,
         z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
     // LoRA expand on the tensor cores (zexp buffers bounded), else on CUDA cores
     bool tc_expand;
@@ -187,6 +193,7 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
+    L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
     // split arrivals of the two shrinks' tasks, then the two finished-task counts
     L->counters = take(sizeof(int32_t) * (2 * std::max<long>(L->st_tasks_max, 1) + 2));
@@ -260,15 +267,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// bf16 tiled tensor map, 128-byte swizzle, OOB elements read as zero
+// bf16 tiled tensor map (128-byte swizzle unless given), OOB elements read as zero
 bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
-                     const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+                     const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                     CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
     const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
                            strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -297,32 +305,44 @@ bool encode_adapter_map(CUtensorMap* map, const void* A, int L, int E, int r, in
     return encode_bf16_map(map, A, 2, dims, strides, box);
 }
 
-// pair rows [P][K] (x in bucket order, act, or zexp): boxes of 64 (K) x
-// box_rows rows (16 for decode-sized chunks, 64 for wide ones)
+// pair rows [P][K] (x in bucket order, or act): boxes of 64 (K) x box_rows
+// rows (16 for decode-sized chunks, 64 for wide ones)
 bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K, int box_rows) {
     const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)P};
     const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     return encode_bf16_map(map, rows, 2, dims, strides, box);
 }
+
+// zexp [P][L * r_pad]: boxes of r_pad (one adapter's slot) x box_rows rows
+bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, int box_rows) {
+    const int rp = expand_rpad_host(r);
+    const cuuint64_t dims[2] = {(cuuint64_t)L * rp, (cuuint64_t)P};
+    const cuuint64_t strides[1] = {(cuuint64_t)L * rp * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)rp, (cuuint32_t)box_rows};
+    return encode_bf16_map(map, zexp, 2, dims, strides, box, expand_swizzle(rp));
+}
 int pair_box_rows(int bn) { return bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
 
-// B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of 64 (K; zeros beyond r) x 128
-// units of one half, for one adapter (strides increase with the dimension)
+// B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of r_pad (zeros beyond r) x 128
+// units of one half, for one adapter (strides increase with the dimension;
+// the swizzle span is one r_pad-wide row)
 bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r) {
+    const int rp = expand_rpad_host(r);
     const cuuint64_t dims[5] = {(cuuint64_t)r, (cuuint64_t)I, 2, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[4] = {(cuuint64_t)r * 2, (cuuint64_t)I * r * 2, (cuuint64_t)2 * I * r * 2,
                                    (cuuint64_t)E * 2 * I * r * 2};
-    const cuuint32_t box[5] = {64, 128, 1, 1, 1};
-    return encode_bf16_map(map, B1, 5, dims, strides, box);
+    const cuuint32_t box[5] = {(cuuint32_t)rp, 128, 1, 1, 1};
+    return encode_bf16_map(map, B1, 5, dims, strides, box, expand_swizzle(rp));
 }
 
-// B2 [L][E][H][r] as {r, H, E, L}: boxes of 64 (K; zeros beyond r) x 128 rows
+// B2 [L][E][H][r] as {r, H, E, L}: boxes of r_pad (zeros beyond r) x 128 rows
 bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r) {
+    const int rp = expand_rpad_host(r);
     const cuuint64_t dims[4] = {(cuuint64_t)r, (cuuint64_t)H, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[3] = {(cuuint64_t)r * 2, (cuuint64_t)H * r * 2, (cuuint64_t)E * H * r * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
-    return encode_bf16_map(map, B2, 4, dims, strides, box);
+    const cuuint32_t box[4] = {(cuuint32_t)rp, 128, 1, 1};
+    return encode_bf16_map(map, B2, 4, dims, strides, box, expand_swizzle(rp));
 }
 
 template <typename T>
@@ -346,6 +366,10 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.lora_buckets = at<int32_t>(ws, L.lora_buckets);
     a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
+    a.keys_in_smem = align_keys_smem_bytes(d->E, d->L, L.P) ? 1 : 0;
+    a.tabs_in_smem = align_tabs_smem_bytes(d->E, d->L) ? 1 : 0;
+    a.keys_global = a.keys_in_smem ? nullptr : at<int>(ws, L.keys);
+    a.full_outputs = 0;
     a.zero_ints = at<int>(ws, L.counters);
     a.n_zero = d->L > 0 ? (int)(2 * L.st_tasks_max + 2) : 0;
     a.st_tasks = d->L > 0 ? at<int4>(ws, L.st_tasks) : nullptr;
@@ -432,7 +456,8 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
     a.bucket_count = bucket_count;
     a.bucket_offset = bucket_offset;
     a.active_experts = nullptr;  // the standalone entry point skips the forward's work lists
-    const cudaError_t e = launch_align(a, align_hist_smem_bytes(d->E, d->L), (cudaStream_t)stream);
+    a.full_outputs = 1;
+    const cudaError_t e = launch_align(a, align_smem_bytes(d->E, d->L, L.P), (cudaStream_t)stream);
     return e == cudaSuccess ? MOELORA_OK : MOELORA_ECUDA;
 }
 
@@ -479,7 +504,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
     tr.mark(0);
-    if (launch_align(aa, align_hist_smem_bytes(d->E, d->L), s) != cudaSuccess) return MOELORA_ECUDA;
+    if (launch_align(aa, align_smem_bytes(d->E, d->L, L.P), s) != cudaSuccess) return MOELORA_ECUDA;
     if (d->T == 0) {
         for (int i = 1; i < MOELORA_TRACE_EVENTS; i++) tr.mark(i);
         return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
@@ -550,7 +575,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
-                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, (int)zexp_cols(d->L, d->r), rows))))
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
@@ -579,7 +604,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
-                             !encode_rows_map(&tc.zxmap, tc.zexp, L.P, (int)zexp_cols(d->L, d->r), rows))))
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, rows))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));

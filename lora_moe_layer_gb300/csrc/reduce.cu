@@ -24,11 +24,14 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
         const int l = a.lora_ids[t];
         const bool l_ok = l >= -1 && l < a.L;
         float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        // every slot's row is loaded (rows of left-out pairs exist but are not
+        // added), so the k loads go out together
+#pragma unroll 4
         for (int j = 0; j < a.k; j++) {
             const int p = t * a.k + j;
             const int e = a.topk_ids[p];
+            const float4 v = __ldcs(reinterpret_cast<const float4*>(a.pair_out + (size_t)p * a.H) + h4);
             if (l_ok && e >= 0 && e < a.E) {
-                const float4 v = reinterpret_cast<const float4*>(a.pair_out + (size_t)p * a.H)[h4];
                 s.x += v.x;
                 s.y += v.y;
                 s.z += v.z;

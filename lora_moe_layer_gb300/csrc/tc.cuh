@@ -46,6 +46,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// ---- the same descriptor for K-major tiles whose rows are 32 or 64 bytes
+// (32- or 64-byte swizzle, layout codes 6 and 4) or 128 bytes (code 2); the
+// stride-byte offset is the distance between 8-row groups (8 x row bytes).
+__device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t smem_addr, uint32_t layout, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+
 // ---- instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A bf16
 // (7-9 = 1), B bf16 (10-12 = 1), both K-major (bits 15, 16 = 0),
 // N >> 3 (17-22), M >> 4 (24-28).
