@@ -109,12 +109,16 @@ int pick_ksplit(long tiles, int K) {
     return best;
 }
 
-// K-splits of a shrink: enough (task, split) items for one wave of SMs, at
-// least two 64-wide K steps per split.
+// K-splits of a shrink.  Shrink items are dealt round-robin ahead of the GEMM
+// tasks, so when there are many shrink tasks (a quarter of the SMs or more),
+// unsplit items about the size of a GEMM task keep the SMs balanced and skip
+// the partial sums; with few (decode), the items are split so every SM takes a
+// small share instead of a few SMs taking whole items.  At least two 64-wide K
+// steps per split.
 int pick_shrink_split(long est_tasks, int K) {
     constexpr long kSms = 152;
     const int nkb = (K + 63) / 64;
-    if (est_tasks >= kSms) return 1;
+    if (est_tasks * 4 >= kSms) return 1;
     const long want = (kSms + std::max<long>(est_tasks, 1) - 1) / std::max<long>(est_tasks, 1);
     return (int)std::max<long>(1, std::min<long>({want, (long)std::max(1, nkb / 2), 32L}));
 }
