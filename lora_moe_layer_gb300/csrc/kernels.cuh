@@ -60,8 +60,9 @@ struct TcArgs {
     CUtensorMap wmap;            // W1 as [E][2][I][H] (gate_up) or W2 [E][H][I]; box 64 (K) x 128 rows
     CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16 rows
     CUtensorMap amap;            // LoRA A (A1 / A2) as [L*E*r][K]; box 64 (K) x r rows
-    CUtensorMap bmap;            // LoRA B: B1 as {r, I, 2, E, L} / B2 as {r, H, E, L}; box 64 x 128 rows
-    CUtensorMap zxmap;           // zexp [P][L*64] bf16; box 64 x pair rows
+    CUtensorMap bmap;            // LoRA B: B1 as {r, I, 2, E, L} / B2 as {r, H, E, L}; box r_pad x 128 rows x 64/r_pad adapters
+    CUtensorMap bmap1;           // the same LoRA B with a one-adapter box
+    CUtensorMap zxmap;           // zexp [L][P][r_pad] bf16; box r_pad x BN rows x 64/r_pad adapters
     int E, L, k, r, I, H, P;
     const uint16_t* B;           // B1 / B2 (null: no LoRA)
     float* z;                    // shrink output [P][r], written by the shrink items (null: no LoRA)
@@ -74,7 +75,7 @@ struct TcArgs {
     int* sh_counters;            // [tasks] split arrivals, zeroed by align
     int* zdone;                  // shrink tasks finished, zeroed by align
     int tc_expand;               // 1: LoRA expand as extra tensor-core K-blocks; 0: CUDA cores in the epilogue
-    uint16_t* zexp;              // [P][L*64] bf16: a pair's z in its adapter's 64-column slot, zeros elsewhere
+    uint16_t* zexp;              // [L][P][r_pad] bf16: z of each pair under its own adapter, zeros elsewhere
     int chunk_masks;             // 1: per-(expert, pair chunk) adapter masks in shared memory (L <= 64)
     int max_chunks;              // bound on (expert, pair chunk) count, for the mask table
     const int32_t* lora_ids;
@@ -101,9 +102,9 @@ struct GatherArgs {
     const int32_t* compact_ids;
     const WsHeader* hdr;
     uint16_t* out;               // [P][H] rows in bucket order
-    uint16_t* zexp1;             // [P][zx_cols] zeroed here (null: none)
+    uint16_t* zexp1;             // [zx_elems] zeroed here (null: none)
     uint16_t* zexp2;
-    int zx_cols;
+    long zx_elems;
 };
 cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t stream, bool pdl);
 

@@ -191,11 +191,12 @@ struct EpiRow {
 
 // LoRA expand on the tensor cores.  An adapter's share of the expand is a
 // K-major tile pair of width r_pad (r rounded up to 16, 32 or 64; TMA reads
-// zeros beyond r): A = its B rows (128 weight rows x r_pad), B = zexp rows
-// (pairs x r_pad), where zexp holds each pair's z in its adapter's r_pad-wide
-// slot and zeros in every other slot.  The tiles use the swizzle whose span is
-// one row (32, 64 or 128 bytes), and 64 / r_pad adapters share one ring stage
-// as separate sub-tiles, each with its own MMA descriptors.
+// zeros beyond r): A = its B rows (128 weight rows x r_pad), B = its zexp rows
+// (pairs x r_pad).  zexp [L][P][r_pad] holds, per adapter, every pair's z for
+// pairs of that adapter and zeros for all others.  The tiles use the swizzle
+// whose span is one row (32, 64 or 128 bytes).  The 64 / r_pad adapters of one
+// block share a ring stage as consecutive sub-tiles, loaded by one copy each
+// for A (the adapter is the outermost box dimension) and for zexp.
 __host__ __device__ inline int expand_rpad(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 __device__ inline uint32_t expand_layout(int rp) { return rp == 16 ? 6u : rp == 32 ? 4u : 2u; }
 
@@ -334,10 +335,9 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int u
     const int clo = s_lo < sh.nb ? s_cb[s_lo] : 0;
     const int chi = s_lo < sh.nb ? s_ce[s_hi] : 0;
     float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
-    // bf16 copy for the tensor-core expand: row q, the r_pad-wide slot of adapter l
+    // bf16 copy for the tensor-core expand: zexp[l][q][0:r] for the pair in row q
     const int rp = expand_rpad(r);
-    const size_t zx_cols = (size_t)a.L * rp;
-    uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + s_sl[my_s] * rp + j : nullptr;
+    uint16_t* zx = (a.zexp != nullptr && a.sh_ks == 1 && mine) ? a.zexp + (size_t)s_sl[my_s] * a.P * rp + j : nullptr;
 
     if (!__all_sync(kFull, mbar_wait(&tfull[b], (uint32_t)use & 1u))) return false;
     tc_fence_after();
@@ -350,7 +350,7 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int u
             const int cc = c4 + c;
             if (cc >= mcb && cc < mce) {
                 dst[(size_t)(sh.q0c + cc) * r + j] = v[c];
-                if (zx) zx[(size_t)(sh.q0c + cc) * zx_cols] = f32_to_bf16_rne(v[c]);
+                if (zx) zx[(size_t)(sh.q0c + cc) * rp] = f32_to_bf16_rne(v[c]);
             }
         }
     }
@@ -390,7 +390,7 @@ __device__ bool shrink_epilogue(const TcArgs& a, int t, int n_lora, int b, int u
                     uint2 pk;
                     pk.x = (uint32_t)f32_to_bf16_rne(acc.x) | ((uint32_t)f32_to_bf16_rne(acc.y) << 16);
                     pk.y = (uint32_t)f32_to_bf16_rne(acc.z) | ((uint32_t)f32_to_bf16_rne(acc.w) << 16);
-                    *reinterpret_cast<uint2*>(a.zexp + (size_t)q * zx_cols + l * rp + kk) = pk;
+                    *reinterpret_cast<uint2*>(a.zexp + ((size_t)l * a.P + q) * rp + kk) = pk;
                 }
             }
         }
@@ -451,6 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
         if (a.sh_tasks) prefetch_tensormap(&a.amap);
         if (a.tc_expand) {
             prefetch_tensormap(&a.bmap);
+            prefetch_tensormap(&a.bmap1);
             prefetch_tensormap(&a.zxmap);
         }
     }
@@ -605,29 +606,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     z_seen = true;
                 }
-                // per adapter: A sub-tile (128 x r_pad) and zexp sub-tile (rows x r_pad)
-                const int xrp = expand_rpad(a.r);
-                const uint32_t xa_bytes = 128u * xrp * 2u, xb_bytes = (uint32_t)(n_box * kRows) * xrp * 2u;
+                // a block's adapters: A sub-tiles (128 x r_pad each, one copy per
+                // half) and zexp sub-tiles (BN rows x r_pad each, one copy)
+                const uint32_t xa1 = 128u * expand_rpad(a.r) * 2u;  // one adapter's A sub-tile
                 for (int jb = n_x > 0 ? xr.next(0) : -1; ok && jb >= 0; jb = xr.next(jb + 1)) {
+                    // a block with one adapter present loads that adapter's rows only
                     const uint32_t sm = xr.slots(jb);
+                    const bool one = __popc(sm) == 1;
+                    const uint32_t abytes = one ? xa1 : (uint32_t)kATile;
                     if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[stage], (uint32_t)__popc(sm) * ((GATE_UP ? 2u : 1u) * xa_bytes + xb_bytes));
+                    mbar_arrive_expect_tx(&full[stage], (GATE_UP ? 2u : 1u) * abytes + (uint32_t)BN * kBK * 2u);
                     uint8_t* dst = base + (size_t)stage * S::kStage;
-                    for (int q = 0; q < xr.apb; q++) {
-                        if (!((sm >> q) & 1u)) continue;
-                        const int l = jb * xr.apb + q;
-                        // B rows of adapter l: coordinates (k, unit, half, expert, adapter)
-                        // or (k, row, expert, adapter)
-                        if (GATE_UP) {
-                            tma_load_5d(dst + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, 0, e, l);
-                            tma_load_5d(dst + kATile + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, 1, e, l);
-                        } else {
-                            tma_load_4d(dst + q * xa_bytes, &a.bmap, &full[stage], 0, tw.mt * kBM, e, l);
-                        }
-                        uint8_t* zdst = dst + S::kAB + q * xb_bytes;
-                        for (int g = 0; g < n_box; g++)
-                            tma_load_2d(zdst + g * kRows * xrp * 2, &a.zxmap, &full[stage], l * xrp, row0 + g * kRows);
+                    const int l0 = jb * xr.apb;
+                    const int q1 = __ffs(sm) - 1;
+                    const CUtensorMap* bm = one ? &a.bmap1 : &a.bmap;
+                    const int la = one ? l0 + q1 : l0;
+                    const uint32_t ao = one ? q1 * xa1 : 0u;
+                    // coordinates (k, unit, half, expert, adapter) / (k, row, expert, adapter)
+                    if (GATE_UP) {
+                        tma_load_5d(dst + ao, bm, &full[stage], 0, tw.mt * kBM, 0, e, la);
+                        tma_load_5d(dst + kATile + ao, bm, &full[stage], 0, tw.mt * kBM, 1, e, la);
+                    } else {
+                        tma_load_4d(dst + ao, bm, &full[stage], 0, tw.mt * kBM, e, la);
                     }
+                    tma_load_3d(dst + S::kAB, &a.zxmap, &full[stage], 0, row0, l0);
                     armed |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
@@ -706,7 +708,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
-                const uint32_t xb16 = (uint32_t)(((tw.n_cols + kRows - 1) / kRows) * kRows) * xrp * 2u / 16u;
                 for (int jb = xr.next(0); jb >= 0 && ok; jb = xr.next(jb + 1)) {
                     const uint32_t sm = xr.slots(jb);
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
@@ -715,7 +716,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     for (int q = 0; q < xr.apb; q++) {
                         if (!((sm >> q) & 1u)) continue;
                         const uint64_t da = dxs + q * xa16;
-                        const uint64_t db = dxs + kPair16 + q * xb16;
+                        const uint64_t db = dxs + kPair16 + q * (uint32_t)(BN * xrp * 2 / 16);
                         for (int kk = 0; kk < xrp / 16; kk++) {
                             umma_bf16(d_first, da + 2 * kk, db + 2 * kk, idesc, 1u);
                             if (GATE_UP) umma_bf16(d_first + BN, da + kUp16 + 2 * kk, db + 2 * kk, idesc, 1u);
@@ -880,9 +881,9 @@ __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
         const int t = a.compact_ids[q] / a.k;
         *reinterpret_cast<uint4*>(a.out + (size_t)q * a.H + c * 8) = ld_ro16(a.x + (size_t)t * a.H + c * 8);
     }
-    // zexp rows start as zeros; the shrink items fill each pair's own slot
+    // zexp starts as zeros; the shrink items fill each pair's own adapter
     if (a.zexp1) {
-        const long nz = (long)n * a.zx_cols / 8;
+        const long nz = a.zx_elems / 8;
         const uint4 zero = make_uint4(0, 0, 0, 0);
         for (long i = first; i < nz; i += stride) {
             reinterpret_cast<uint4*>(a.zexp1)[i] = zero;

@@ -318,34 +318,36 @@ bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K, int box_
     return encode_bf16_map(map, rows, 2, dims, strides, box);
 }
 
-// zexp [P][L * r_pad]: boxes of r_pad (one adapter's slot) x box_rows rows
-bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, int box_rows) {
+// zexp [L][P][r_pad]: boxes of r_pad x rows pair rows x 64 / r_pad adapters
+// (one ring stage's sub-tiles, adapter outermost)
+bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, int rows) {
     const int rp = expand_rpad_host(r);
-    const cuuint64_t dims[2] = {(cuuint64_t)L * rp, (cuuint64_t)P};
-    const cuuint64_t strides[1] = {(cuuint64_t)L * rp * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)rp, (cuuint32_t)box_rows};
-    return encode_bf16_map(map, zexp, 2, dims, strides, box, expand_swizzle(rp));
+    const cuuint64_t dims[3] = {(cuuint64_t)rp, (cuuint64_t)P, (cuuint64_t)L};
+    const cuuint64_t strides[2] = {(cuuint64_t)rp * 2, (cuuint64_t)P * rp * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)rp, (cuuint32_t)rows, (cuuint32_t)(64 / rp)};
+    return encode_bf16_map(map, zexp, 3, dims, strides, box, expand_swizzle(rp));
 }
 int pair_box_rows(int bn) { return bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
 
 // B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of r_pad (zeros beyond r) x 128
-// units of one half, for one adapter (strides increase with the dimension;
-// the swizzle span is one r_pad-wide row)
-bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r) {
+// units of one half x 64 / r_pad adapters (zeros beyond L); strides increase
+// with the dimension, the swizzle span is one r_pad-wide row, and each
+// adapter's 128 x r_pad tile lands after the previous one
+bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r, bool one_adapter = false) {
     const int rp = expand_rpad_host(r);
     const cuuint64_t dims[5] = {(cuuint64_t)r, (cuuint64_t)I, 2, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[4] = {(cuuint64_t)r * 2, (cuuint64_t)I * r * 2, (cuuint64_t)2 * I * r * 2,
                                    (cuuint64_t)E * 2 * I * r * 2};
-    const cuuint32_t box[5] = {(cuuint32_t)rp, 128, 1, 1, 1};
+    const cuuint32_t box[5] = {(cuuint32_t)rp, 128, 1, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, B1, 5, dims, strides, box, expand_swizzle(rp));
 }
 
-// B2 [L][E][H][r] as {r, H, E, L}: boxes of r_pad (zeros beyond r) x 128 rows
-bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r) {
+// B2 [L][E][H][r] as {r, H, E, L}: boxes of r_pad x 128 rows x 64 / r_pad adapters
+bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r, bool one_adapter = false) {
     const int rp = expand_rpad_host(r);
     const cuuint64_t dims[4] = {(cuuint64_t)r, (cuuint64_t)H, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[3] = {(cuuint64_t)r * 2, (cuuint64_t)H * r * 2, (cuuint64_t)E * H * r * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)rp, 128, 1, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)rp, 128, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, B2, 4, dims, strides, box, expand_swizzle(rp));
 }
 
@@ -527,7 +529,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     if (L.tc_expand) {
         ga.zexp1 = at<uint16_t>(ws, L.zexp1);
         ga.zexp2 = at<uint16_t>(ws, L.zexp2);
-        ga.zx_cols = (int)zexp_cols(d->L, d->r);
+        ga.zx_elems = L.P * zexp_cols(d->L, d->r);
     }
     tr.mark(1);
     {
@@ -579,7 +581,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, rows))))
+                             !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
@@ -608,7 +611,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, rows))))
+                             !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
