@@ -20,7 +20,8 @@
 //     offset[b] + (pairs of b in earlier warps) + (earlier lanes of b in this step).
 // Walking each segment in order and the warps in order keeps ascending p.
 // The padded outputs (sentinels, per-tile expert and adapter) are written only
-// for the standalone entry point; the forward works on the compact order.
+// for the standalone entry point; the forward works on the compact order and
+// places pairs inside a bucket in any order (shared-memory atomics).
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -143,23 +144,42 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     const int seg_end = min(P, seg_beg + seg);
     int* my_hist = hist + warp * NB;
 
-    // pass 1: per-warp bucket counts
-    for (int base = seg_beg; base < seg_end; base += 32) {
-        const int p = base + lane;
-        const int b = p < seg_end ? keys[p] : -1;
-        const unsigned peers = __match_any_sync(kFull, b);
-        if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
-        __syncwarp();
+    // The forward only needs each bucket's pairs together: its per-pair results
+    // do not depend on their order inside a bucket, so it counts and places
+    // with shared-memory atomics (row 0 of the histogram is the block's count,
+    // then its placement cursor).  The standalone entry point keeps ascending p
+    // inside a bucket: per-warp counts with warp match-any in pass 1, ranks in
+    // pass 2.
+    const bool stable = a.full_outputs != 0;
+    if (stable) {
+        // pass 1: per-warp bucket counts
+        for (int base = seg_beg; base < seg_end; base += 32) {
+            const int p = base + lane;
+            const int b = p < seg_end ? keys[p] : -1;
+            const unsigned peers = __match_any_sync(kFull, b);
+            if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
+            __syncwarp();
+        }
+    } else {
+        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
+            const int b = keys[p];
+            if (b >= 0) atomicAdd(&hist[b], 1);
+        }
     }
     __syncthreads();
 
-    // per bucket: exclusive prefix over warps, and the bucket size
+    // per bucket: the bucket size (stable: and the exclusive prefix over warps)
     for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
         int run = 0;
-        for (int w = 0; w < kAlignWarps; w++) {
-            const int c = hist[w * NB + b];
-            hist[w * NB + b] = run;
-            run += c;
+        if (stable) {
+            for (int w = 0; w < kAlignWarps; w++) {
+                const int c = hist[w * NB + b];
+                hist[w * NB + b] = run;
+                run += c;
+            }
+        } else {
+            run = hist[b];
+            hist[b] = 0;
         }
         cnt_t[b] = run;
         if (a.tabs_in_smem) a.bucket_count[b] = run;
@@ -180,19 +200,26 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         }
     }
 
-    // pass 2: stable placement
-    for (int base = seg_beg; base < seg_end; base += 32) {
-        const int p = base + lane;
-        const int b = p < seg_end ? keys[p] : -1;
-        const unsigned peers = __match_any_sync(kFull, b);
-        if (b >= 0) {
-            const int rank = my_hist[b] + __popc(peers & lanemask_lt());
-            if (a.full_outputs) a.sorted_ids[boff_t[b] + rank] = p;
-            a.compact_ids[coff_t[b] + rank] = p;
+    // pass 2: placement
+    if (stable) {
+        for (int base = seg_beg; base < seg_end; base += 32) {
+            const int p = base + lane;
+            const int b = p < seg_end ? keys[p] : -1;
+            const unsigned peers = __match_any_sync(kFull, b);
+            if (b >= 0) {
+                const int rank = my_hist[b] + __popc(peers & lanemask_lt());
+                a.sorted_ids[boff_t[b] + rank] = p;
+                a.compact_ids[coff_t[b] + rank] = p;
+            }
+            __syncwarp();
+            if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
+            __syncwarp();
         }
-        __syncwarp();
-        if (b >= 0 && lane == __ffs(peers) - 1) my_hist[b] += __popc(peers);
-        __syncwarp();
+    } else {
+        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
+            const int b = keys[p];
+            if (b >= 0) a.compact_ids[coff_t[b] + atomicAdd(&hist[b], 1)] = p;
+        }
     }
     __syncthreads();
 

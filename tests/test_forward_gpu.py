@@ -113,6 +113,27 @@ def test_intermediates_config0():
         assert norm_err(pair_out[p], w * ref["d"]) < 1e-2
 
 
+@pytest.mark.parametrize("which", ["config0", "config3"])
+def test_forward_groups_pairs_by_bucket(which):
+    """The forward's own bucketing (compact order in the workspace): bucket b's
+    rows hold exactly the pairs with key e*(L+1)+(l+1), in any order (the
+    standalone align's ascending order is checked bit-exact elsewhere)."""
+    layer = wl.make_config(0) if which == "config0" else wl.make_config(3)
+    dl, st = run(layer)
+    assert st == 0
+    P, L1 = layer.P, layer.L + 1
+    nb = layer.E * L1
+    rows = dl.workspace_view("compact_ids", torch.int32, (P,)).cpu().numpy()
+    off = dl.workspace_view("compact_offset", torch.int32, (nb + 1,)).cpu().numpy()
+    key = layer.topk_ids.reshape(-1).astype(np.int64) * L1 + np.repeat(layer.lora_ids, layer.k) + 1
+    assert off[0] == 0 and off[-1] == P
+    expect = np.bincount(key, minlength=nb)
+    assert np.array_equal(np.diff(off), expect)
+    for b in np.nonzero(expect)[0]:
+        got = np.sort(rows[off[b]:off[b + 1]])
+        assert np.array_equal(got, np.nonzero(key == b)[0])
+
+
 # ------------------------------------------------------------------ invariants
 
 def test_zero_B_bit_identical_to_base_only():
