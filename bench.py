@@ -63,15 +63,16 @@ def algorithmic(layer):
     H, I, r, T, k = layer.H, layer.I, layer.r, layer.T, layer.k
     layer_bytes = 2 * (experts * 3 * H * I + buckets * r * (2 * H + 3 * I) + 2 * T * H) + 8 * T * k + 4 * T
     flops = P * 6 * H * I + int(lora_mask.sum()) * 2 * r * (2 * H + 3 * I)
-    # per-kernel I/O of the two GEMV kernels (inputs + outputs they must move)
-    s_gu = -(-H // 512)
-    s_dn = -(-I // 512)
-    n_lora_pairs = int(lora_mask.sum())
-    gate_up = (experts * 2 * I * H * 2 + buckets * 2 * I * r * 2 + T * H * 2 + P * I * 2
-               + s_gu * n_lora_pairs * r * 4)
-    down = (experts * H * I * 2 + buckets * H * r * 2 + P * I * 2 + P * H * 4 + s_dn * n_lora_pairs * r * 4)
+    # per-kernel bytes the two tcgen05 kernels must move: weights of the touched
+    # experts (W) and adapter buckets (the expand's B and the shrink's A), the
+    # pair rows they read (x in bucket order / act) and what they write
+    gate_up = experts * 2 * I * H * 2 + buckets * (2 * I * r + r * H) * 2 + P * H * 2 + P * I * 2
+    down = experts * H * I * 2 + buckets * (H * r + r * I) * 2 + P * I * 2 + P * H * 4
+    gate_up_flops = P * 2 * H * 2 * I + int(lora_mask.sum()) * 2 * r * (H + 2 * I)
+    down_flops = P * 2 * I * H + int(lora_mask.sum()) * 2 * r * (I + H)
     return dict(bytes=layer_bytes, flops=flops, experts_touched=experts, lora_buckets_touched=buckets,
-                kernel_bytes={"gate_up_gemm": gate_up, "down_gemm": down})
+                kernel_bytes={"gate_up_gemm": gate_up, "down_gemm": down},
+                kernel_flops={"gate_up_gemm": gate_up_flops, "down_gemm": down_flops})
 
 
 class ClockSampler:
@@ -321,10 +322,13 @@ def run_ours(args, rank, world, local_rank):
                   "lora_buckets_touched": alg["lora_buckets_touched"],
                   "achieved_gbs": alg["bytes"] / (ms_step * 1e-3) / 1e9,
                   "hbm_frac": alg["bytes"] / (ms_step * 1e-3) / 1e9 / pk["hbm_gbs"],
-                  "roof_ms": max(alg["bytes"] / (pk["hbm_gbs"] * 1e9), alg["flops"] / (pk["bf16_tflops"] * 1e12)) * 1e3},
+                  "roof_ms": max(alg["bytes"] / (pk["hbm_gbs"] * 1e9), alg["flops"] / (pk["bf16_tflops"] * 1e12)) * 1e3,
+                  "tensor_tflops": alg["flops"] / (ms_step * 1e-3) / 1e12,
+                  "tensor_frac": alg["flops"] / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"]},
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": dom_gbs / pk["hbm_gbs"], "traffic": traffic,
                      "bytes_per_launch": dom_bytes, "launch_us": kern_ms[dom] * 1e3,
+                     "tensor_frac": alg["kernel_flops"][dom] / (kern_ms[dom] * 1e-3) / 1e12 / pk["bf16_tflops"],
                      "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)" if pk["source"] == "measured" else "fallback",
                      "timed": "kernel events recorded between the kernels over K traced forwards on the launch stream",
                      "traffic_source": traffic_src},
