@@ -65,6 +65,7 @@ constexpr int kATile = kBM * kBK * 2;    // 16 KiB
 template <int BN>
 constexpr int kRowsFor = BN >= 128 ? 64 : 16;
 constexpr int kMisc = 20;  // shared verdicts [0..3] and shrink-slot adapters [4..19]
+constexpr int kMaxKsplit = 8;  // K-splits of a GEMM task (the host plans at most this many)
 
 template <bool GATE_UP, int BN>
 struct TcShape {
@@ -824,15 +825,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                         tmem_ld4(t_lane + c4, g4);
                         if (GATE_UP) tmem_ld4(t_lane + BN + c4, u4);
                     } else {
-                        // every split's partial (this one's included), added in split order
+                        // every split's partial added in split order: this split's own
+                        // from TMEM, the others' from global memory, all of a column
+                        // group's loads issued before the first add
+                        float og[4], ou[4];
+                        tmem_ld4(t_lane + c4, og);
+                        if (GATE_UP) tmem_ld4(t_lane + BN + c4, ou);
 #pragma unroll
                         for (int c = 0; c < 4; c++) g4[c] = u4[c] = 0.f;
-                        for (int sp = 0; sp < ksplit; sp++) {
-                            const float* ps = part_tile + (size_t)sp * S::kAccCols * kBM + row;
+                        constexpr int kCols = GATE_UP ? 2 : 4;  // columns per batch of loads
 #pragma unroll
-                            for (int c = 0; c < 4; c++) {
-                                g4[c] += __ldcg(ps + (size_t)(c4 + c) * kBM);
-                                if (GATE_UP) u4[c] += __ldcg(ps + (size_t)(BN + c4 + c) * kBM);
+                        for (int cb = 0; cb < 4; cb += kCols) {
+                            float pg[kMaxKsplit][kCols], pu[kMaxKsplit][kCols];
+#pragma unroll
+                            for (int sp = 0; sp < kMaxKsplit; sp++) {
+                                if (sp < ksplit && sp != tw.split) {
+                                    const float* ps = part_tile + (size_t)sp * S::kAccCols * kBM + row;
+#pragma unroll
+                                    for (int c = 0; c < kCols; c++) {
+                                        pg[sp][c] = __ldcg(ps + (size_t)(c4 + cb + c) * kBM);
+                                        if (GATE_UP) pu[sp][c] = __ldcg(ps + (size_t)(BN + c4 + cb + c) * kBM);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int sp = 0; sp < kMaxKsplit; sp++) {
+                                if (sp < ksplit) {
+#pragma unroll
+                                    for (int c = 0; c < kCols; c++) {
+                                        g4[cb + c] += sp == tw.split ? og[cb + c] : pg[sp][c];
+                                        if (GATE_UP) u4[cb + c] += sp == tw.split ? ou[cb + c] : pu[sp][c];
+                                    }
+                                }
                             }
                         }
                     }
