@@ -285,17 +285,10 @@ def run_ours(args, rank, world, local_rank):
                   "status": status, "checked": "all outputs vs fp64 oracle"}
 
     # max over ranks
-    t_dev = torch.tensor([dev_s], device=dev)
-    t_e2e = torch.tensor([e2e_time], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_dev, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
-    dev_s, e2e_time = float(t_dev.item()), float(t_e2e.item())
+    dev_s, e2e_time, value = aggregate_replicas(dev_s, e2e_time, layer.T * args.steps, world, dev)
     if rank != 0:
         return None
 
-    tokens = layer.T * args.steps * world
-    value = tokens / dev_s
     alg = algorithmic(layer)
     pk = peaks()
     ms_step = dev_s * 1e3 / args.steps
@@ -345,6 +338,17 @@ def run_ours(args, rank, world, local_rank):
     if cpu is not None:
         line["cpu_baseline"] = cpu
     return line
+
+
+def aggregate_replicas(dev_s, e2e_s, tokens_per_rank, world, device):
+    """Whole-job numbers of N independent replicas: the slowest rank's device
+    and end-to-end times, and tokens of all ranks / that device time."""
+    import torch
+    t = torch.tensor([dev_s, e2e_s], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    dev_s, e2e_s = float(t[0].item()), float(t[1].item())
+    return dev_s, e2e_s, tokens_per_rank * world / dev_s
 
 
 def _threads():
