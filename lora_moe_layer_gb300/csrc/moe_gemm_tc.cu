@@ -81,6 +81,9 @@ struct TcShape {
 };
 
 __device__ __forceinline__ float silu_f(float u) { return u / (1.0f + expf(-u)); }
+// the same with the fast exponential and division intrinsics, for the lean
+// epilogue (its result is rounded to bf16)
+__device__ __forceinline__ float silu_fast(float u) { return __fdividef(u, 1.0f + __expf(-u)); }
 
 // Task table built once per CTA in shared memory: for active expert a,
 // expert id, first pair row, pair count, and the exclusive prefix of its task
@@ -814,6 +817,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 if (!rendezvous()) { ok = false; break; }
                 finish = s_misc[1] != 0;
                 if (finish) __threadfence();
+            }
+            if (!has_lora && ksplit == 1) {
+                // lean epilogue (no CUDA-core expand, no K split): 16 columns of
+                // each accumulator per TMEM load, one wait for both
+                for (int c0 = half * 16; c0 < n_real; c0 += 32) {
+                    float g[16], u[16];
+                    if (GATE_UP) tmem_ld16x2(t_lane + c0, t_lane + BN + c0, g, u);
+                    else tmem_ld16(t_lane + c0, g);
+                    if (row_ok) {
+#pragma unroll
+                        for (int c = 0; c < 16; c++) {
+                            const int cc = c0 + c;
+                            if (cc < n_real) {
+                                if (GATE_UP)
+                                    a.act_out[(size_t)(q0c + cc) * a.I + w_row] = f32_to_bf16_rne(silu_fast(g[c]) * u[c]);
+                                else
+                                    a.pair_out[(size_t)s_pair[cc] * a.H + w_row] = s_w[cc] * g[c];
+                            }
+                        }
+                    }
+                }
+                finish = false;
             }
             EpiRow<GATE_UP> er;
             er.init(a, e, w_row, row_ok, rows_per_expert);
