@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
     {
         int bad = 0;
-#pragma unroll 4
+#pragma unroll 8
         for (int p = threadIdx.x; p < P; p += kAlignThreads) {
             const int e = a.topk_ids[p];
             const int l = a.lora_ids[p / a.k];
@@ -241,47 +241,54 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         if (a.num_post_padded) *a.num_post_padded = total_padded;
     }
     if (a.active_experts) {
-        // compact list of experts with pairs, and of (e, l >= 0) buckets with pairs
+        // compact list of experts with pairs, and of (e, l >= 0) buckets with pairs.
+        // The histogram's shared memory is free after pass 2: the scans and the
+        // bucket list are read back from there when the histogram lives there.
+        int* tmp = a.hist_global ? a.scan_tmp : hist;                 // max(E, NB) + 1 ints
+        int* lbs = a.hist_global ? a.lora_buckets : hist + NB + 1;    // copy of the bucket list
         const int* coff = coff_t;
         const int E = a.E;
         block_scan_items(
             E, [&](int e) { return make_int2(coff[(e + 1) * L1] > coff[e * L1] ? 1 : 0, 0); },
-            a.scan_tmp, nullptr, sw);
+            tmp, nullptr, sw);
         __syncthreads();
         for (int e = threadIdx.x; e < E; e += kAlignThreads)
-            if (coff[(e + 1) * L1] > coff[e * L1]) a.active_experts[a.scan_tmp[e]] = e;
-        if (threadIdx.x == 0) hdr->n_active = a.scan_tmp[E];
+            if (coff[(e + 1) * L1] > coff[e * L1]) a.active_experts[tmp[e]] = e;
+        if (threadIdx.x == 0) hdr->n_active = tmp[E];
         __syncthreads();
         block_scan_items(
             NB, [&](int b) { return make_int2((b % L1) != 0 && cnt[b] > 0 ? 1 : 0, 0); },
-            a.scan_tmp, nullptr, sw);
+            tmp, nullptr, sw);
         __syncthreads();
         for (int b = threadIdx.x; b < NB; b += kAlignThreads)
-            if ((b % L1) != 0 && cnt[b] > 0) a.lora_buckets[a.scan_tmp[b]] = b;
-        if (threadIdx.x == 0) hdr->n_lora_buckets = a.scan_tmp[NB];
+            if ((b % L1) != 0 && cnt[b] > 0) {
+                a.lora_buckets[tmp[b]] = b;
+                lbs[tmp[b]] = b;
+            }
+        if (threadIdx.x == 0) hdr->n_lora_buckets = tmp[NB];
         __syncthreads();
         if (a.st_tasks) {
             // shrink tasks: st_G consecutive adapter buckets per group; a group's
             // rows are contiguous in bucket order and split into chunks of st_BN
-            const int n = a.scan_tmp[NB];
+            const int n = tmp[NB];
             __syncthreads();
             const int G = a.st_G, BN = a.st_BN;
             const int ng = (n + G - 1) / G;
-            const int* lb = a.lora_buckets;
+            const int* lb = lbs;
             auto rows = [&](int g) {
                 const int j1 = min(n, g * G + G) - 1;
                 return make_int2(coff[lb[g * G]], coff[lb[j1] + 1]);
             };
             block_scan_items(
                 ng, [&](int g) { const int2 q = rows(g); return make_int2((q.y - q.x + BN - 1) / BN, 0); },
-                a.scan_tmp, nullptr, sw);
+                tmp, nullptr, sw);
             __syncthreads();
             for (int g = threadIdx.x; g < ng; g += kAlignThreads) {
                 const int2 q = rows(g);
-                int at = a.scan_tmp[g];
+                int at = tmp[g];
                 for (int q0 = q.x; q0 < q.y; q0 += BN) a.st_tasks[at++] = make_int4(g, q0, min(BN, q.y - q0), 0);
             }
-            if (threadIdx.x == 0) hdr->n_shrink_tasks = a.scan_tmp[ng];
+            if (threadIdx.x == 0) hdr->n_shrink_tasks = tmp[ng];
         }
     }
     pdl_trigger();
