@@ -166,6 +166,20 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
                                         void *const *kernel_events, int32_t n_events);
 
 /*
+ * Self-test of the device-side wait bounds (the pages have no counterpart).
+ * Launches one small kernel on `stream` whose wait nothing will satisfy --
+ * kind 0: an mbarrier phase that expects an arrival nobody makes; kind 1: a
+ * global counter (in the workspace header) nobody increments.  The wait gives
+ * up under the same bounds as the forward's waits (2^20 rounds or one second
+ * of the GPU's global timer) and records the timeout in the workspace status
+ * word, so a following moe_lora_get_status returns MOELORA_ETIMEOUT; the
+ * context stays usable.  workspace: device pointer to at least 256 bytes, 16-byte aligned,
+ * overwritten (header only).  Returns MOELORA_EINVAL for another kind or a NULL
+ * workspace, MOELORA_ECUDA if the launch fails.  Asynchronous.
+ */
+MOELORA_API int moe_lora_selftest_wait(int32_t kind, void *workspace, void *stream);
+
+/*
  * Waits for `stream`, then returns MOELORA_OK if the last align/forward that
  * used this workspace met no out-of-range id, MOELORA_EDEVICE_ID if it did,
  * MOELORA_ETIMEOUT if one of its kernels abandoned a bounded wait inside its

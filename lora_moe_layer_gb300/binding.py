@@ -27,7 +27,7 @@ MOELORA_ETIMEOUT = -6
 EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_workspace_bytes", "moe_lora_align", "moe_lora_forward",
             "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced",
-            "moe_lora_forward_noalloc")
+            "moe_lora_forward_noalloc", "moe_lora_selftest_wait")
 MOELORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MOELORA_TRACE_EVENTS = 6
 # kernel slots of one forward, in launch order
@@ -88,6 +88,8 @@ def load(path: Optional[str] = None):
     lib.moe_lora_forward_noalloc.argtypes = [D] + [V] * 12
     lib.moe_lora_get_status.restype = I32
     lib.moe_lora_get_status.argtypes = [V, V]
+    lib.moe_lora_selftest_wait.restype = I32
+    lib.moe_lora_selftest_wait.argtypes = [I32, V, V]
     lib.moe_lora_workspace_layout.restype = I32
     lib.moe_lora_workspace_layout.argtypes = [D, ctypes.POINTER(moe_lora_ws_layout)]
     if path is None:
@@ -194,6 +196,10 @@ def moe_lora_forward_noalloc(d: moe_lora_dims, x, topk_ids, topk_weights, token_
     return load().moe_lora_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                            _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
                                            _ptr(A2), _ptr(B2), _ptr(out), _stream(stream))
+
+
+def moe_lora_selftest_wait(kind: int, workspace, stream=None) -> int:
+    return load().moe_lora_selftest_wait(kind, _ptr(workspace), _stream(stream))
 
 
 def moe_lora_get_status(workspace, stream=None) -> int:

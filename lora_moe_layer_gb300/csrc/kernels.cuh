@@ -118,6 +118,10 @@ struct ReduceArgs {
 };
 cudaError_t launch_reduce(const ReduceArgs& args, int grid, cudaStream_t stream, bool pdl);
 
+// ------------------------------------------------------------- self-test ----
+// one kernel whose wait nothing satisfies (kind 0: mbarrier phase, 1: counter)
+cudaError_t launch_selftest_wait(int kind, void* workspace, cudaStream_t stream);
+
 // common launch helper: optional programmatic-dependent-launch attribute
 template <typename Kern, typename Args>
 cudaError_t launch_k(Kern kernel, dim3 grid, dim3 block, int smem, cudaStream_t stream, bool pdl,

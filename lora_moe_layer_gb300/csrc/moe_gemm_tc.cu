@@ -297,17 +297,6 @@ struct ShItem {
     }
 };
 
-// spin (bounded) until *p >= target; 1 on success
-__device__ __forceinline__ int wait_count(const int* p, int target) {
-    for (uint32_t i = 0; i < kWaitRounds; i++) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        if (v >= target) return 1;
-        __nanosleep(64);
-    }
-    return 0;
-}
-
 // Epilogue of shrink item t (in accumulator set b, used `use` times before):
 // each thread is one TMEM lane = (slot, rank
 // index) row and stores z for the pairs of its slot; the two warps of a lane

@@ -722,6 +722,12 @@ MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims* d, const void* x,
                         g_noalloc_ptr[dev], kNoAllocScratchBytes, stream, nullptr, 0);
 }
 
+MOELORA_API int moe_lora_selftest_wait(int32_t kind, void* workspace, void* stream) {
+    if ((kind != 0 && kind != 1) || !workspace) return MOELORA_EINVAL;
+    if (!aligned16(workspace)) return MOELORA_EUNSUPPORTED;
+    return launch_selftest_wait(kind, workspace, (cudaStream_t)stream) == cudaSuccess ? MOELORA_OK : MOELORA_ECUDA;
+}
+
 MOELORA_API int moe_lora_get_status(const void* workspace, void* stream) {
     if (!workspace) return MOELORA_EINVAL;
     int32_t status = 0;

@@ -1,8 +1,10 @@
 // tma.cuh -- mbarrier and TMA (cp.async.bulk.tensor) helpers for sm_103a.
 //
 // Every wait is bounded: a wait that does not complete within kWaitRounds
-// try_wait rounds returns false, and the caller records kStatusTimeout in the
-// workspace status word and leaves its loop instead of spinning forever.
+// rounds or kWaitNs nanoseconds of the global timer (checked every 256 rounds,
+// so a wait that completes never reads it) returns false, and the caller
+// records kStatusTimeout in the workspace status word and leaves its loop
+// instead of spinning forever.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (type only; encoding happens on the host)
@@ -15,6 +17,13 @@ namespace moelora {
 
 constexpr int kStatusTimeout = 4;        // a bounded wait gave up (device status bit)
 constexpr uint32_t kWaitRounds = 1u << 20;
+constexpr uint64_t kWaitNs = 1000000000ull;  // one second
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -52,9 +61,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitRounds; i++)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kWaitRounds; i++) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && global_ns() - t0 > kWaitNs) return false;
+    }
     return false;
+}
+
+// Spin (bounded) until the global counter *p reaches target; 1 on success.
+__device__ __forceinline__ int wait_count(const int* p, int target) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < kWaitRounds; i++) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return 1;
+        if (i == 0) t0 = global_ns();
+        else if ((i & 255u) == 0 && global_ns() - t0 > kWaitNs) return 0;
+        __nanosleep(64);
+    }
+    return 0;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
