@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     // inside a bucket: per-warp counts with warp match-any in pass 1, ranks in
     // pass 2.
     const bool stable = a.full_outputs != 0;
+    const int run = ((P + kAlignThreads - 1) / kAlignThreads) | 1;  // pairs per thread, odd
+    const int run0 = threadIdx.x * run;
     if (stable) {
         // pass 1: per-warp bucket counts
         for (int base = seg_beg; base < seg_end; base += 32) {
@@ -161,8 +163,13 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             __syncwarp();
         }
     } else {
-        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
-            const int b = keys[p];
+        // each thread walks its own run of pairs, so one step's atomics spread
+        // over the whole batch (consecutive pairs mostly share a bucket); an
+        // odd run length keeps the shared-memory key reads free of bank conflicts
+#pragma unroll 4
+        for (int s = 0; s < run; s++) {
+            const int p = run0 + s;
+            const int b = p < P ? keys[p] : -1;
             if (b >= 0) atomicAdd(&hist[b], 1);
         }
     }
@@ -216,8 +223,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             __syncwarp();
         }
     } else {
-        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
-            const int b = keys[p];
+#pragma unroll 4
+        for (int s = 0; s < run; s++) {
+            const int p = run0 + s;
+            const int b = p < P ? keys[p] : -1;
             if (b >= 0) a.compact_ids[coff_t[b] + atomicAdd(&hist[b], 1)] = p;
         }
     }
