@@ -58,7 +58,7 @@ cudaError_t init_align_attributes();
 constexpr int kTcSmemLimit = 227 * 1024 - 1024;
 struct TcArgs {
     CUtensorMap wmap;            // W1 as [E][2][I][H] (gate_up) or W2 [E][H][I]; box 64 (K) x 128 rows
-    CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16 rows
+    CUtensorMap xmap;            // pair rows: x in bucket order [P][H] or act [P][I]; box 64 x 16, 64 or 256 rows
     CUtensorMap amap;            // LoRA A (A1 / A2) as [L*E*r][K]; box 64 (K) x r rows
     CUtensorMap bmap;            // LoRA B: B1 as {r, I, 2, E, L} / B2 as {r, H, E, L}; box r_pad x 128 rows x 64/r_pad adapters
     CUtensorMap bmap1;           // the same LoRA B with a one-adapter box
@@ -85,10 +85,11 @@ struct TcArgs {
     const int32_t* compact_ids;
     WsHeader* hdr;
     uint16_t* act_out;           // gate_up: [P][I] bf16
-    float* pair_out;             // down: [P][H] fp32 by pair id
+    float* pair_out;             // down: [ksplit][P][H] fp32 by pair id, one slab per K-split
+    size_t pair_split;           // down: elements between two K-splits' slabs (P * H)
     int nstages;
     int ksplit;                  // K-splits per weight tile (1: none)
-    float* part;                 // split-K partial tiles [tiles][ksplit][acc columns][128]
+    float* part;                 // gate_up split-K partial tiles [tiles][ksplit][acc columns][128]
     int* tile_counters;          // [tiles] split arrivals, zeroed by align
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
@@ -109,9 +110,12 @@ struct GatherArgs {
 cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t stream, bool pdl);
 
 // --------------------------------------------------------------- reduce ----
+constexpr int kMaxSplitSlabs = 8;  // the host plans at most 8 K-splits per GEMM
 struct ReduceArgs {
     int T, k, H, E, L;
-    const float* pair_out;       // [P][H]
+    const float* pair_out;       // [nsplit][P][H]: the down GEMM's K-split slabs
+    int nsplit;                  // 1 .. kMaxSplitSlabs
+    size_t split_stride;         // elements between slabs
     const int32_t* topk_ids;
     const int32_t* lora_ids;
     uint16_t* out;               // [T][H]

@@ -40,8 +40,9 @@
 //            completion to mbarriers;
 //   warps 2-9 epilogue: each thread owns one weight row (its TMEM lane; two
 //            warps per lane quadrant take alternate 16-column chunks), adds the
-//            LoRA expand B[l][e][row] . z[pair] on CUDA cores, and writes bf16
-//            SiLU(gate)*up or fp32 w * d.  Per task the column metadata (pair,
+//            LoRA expand B[l][e][row] . z[pair] on CUDA cores when the tensor
+//            cores do not take it, and writes bf16 SiLU(gate)*up or fp32 w * d
+//            (down with split K: one slab per split, added by the reduce).  Per task the column metadata (pair,
 //            adapter, weight) and the chunk's z rows are first staged in
 //            shared memory, while the task's MMAs are still running.
 // The two accumulators alternate, so one task's epilogue overlaps the next
@@ -60,10 +61,11 @@ constexpr int kTcThreads = (2 + kEpiWarps) * 32;
 constexpr int kBM = 128;                 // weight rows per task (MMA M)
 constexpr int kBK = 64;                  // K per stage: one 128-byte swizzle row
 constexpr int kATile = kBM * kBK * 2;    // 16 KiB
-// pair rows per TMA box: 16 for decode-sized chunks, 64 when chunks are wide
-// (fewer, larger copies keep the TMA issue rate off the critical path)
+// pair rows per TMA box: 16 for decode-sized chunks, 64 for 128-pair chunks,
+// one 256-row box for 256-pair chunks (fewer, larger copies keep the TMA
+// issue rate off the critical path)
 template <int BN>
-constexpr int kRowsFor = BN >= 128 ? 64 : 16;
+constexpr int kRowsFor = BN >= 256 ? 256 : BN >= 128 ? 64 : 16;
 constexpr int kMisc = 20;  // shared verdicts [0..3] and shrink-slot adapters [4..19]
 constexpr int kMaxKsplit = 8;  // K-splits of a GEMM task (the host plans at most this many)
 
@@ -132,13 +134,15 @@ struct EpiRow {
     int e, w_row, cur_l;
     bool row_ok;
     size_t rows_per_expert;
+    float* pout;         // down: this K-split's [P][H] slab
     uint4 bg[8], bu[8];  // r <= 64 bf16 each
 
-    __device__ void init(const TcArgs& a, int e_, int w_row_, bool row_ok_, size_t rpe) {
+    __device__ void init(const TcArgs& a, int e_, int w_row_, bool row_ok_, size_t rpe, float* pout_) {
         e = e_;
         w_row = w_row_;
         row_ok = row_ok_;
         rows_per_expert = rpe;
+        pout = pout_;
         cur_l = -2;
     }
 
@@ -188,7 +192,7 @@ struct EpiRow {
             if (GATE_UP)
                 a.act_out[(size_t)q * a.I + w_row] = f32_to_bf16_rne(silu_f(vg) * vu);
             else
-                a.pair_out[(size_t)p * a.H + w_row] = w * vg;
+                pout[(size_t)p * a.H + w_row] = w * vg;
         }
     }
 };
@@ -782,11 +786,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             const int w_row = tw.mt * kBM + row;
             const bool row_ok = w_row < N_out;
             const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * S::kAccCols);
-            // split-K: partial tiles go to global memory; the split that arrives
-            // last adds the others' partials (in split order) to its own
+            // split-K of gate_up: partial tiles go to global memory; the split
+            // that arrives last adds the others' partials (in split order) to
+            // its own.  Split-K of down: every split writes w * its partial to
+            // its own slab of pair_out (the reduce kernel adds the slabs in
+            // split order), so no split waits for another.
+            const bool slab = !GATE_UP && ksplit > 1;
+            float* const pout = GATE_UP ? nullptr : a.pair_out + (slab ? (size_t)tw.split * a.pair_split : 0);
             bool finish = true;
             float* part_tile = nullptr;
-            if (ksplit > 1) {
+            if (ksplit > 1 && !slab) {
                 part_tile = a.part + (size_t)tw.tile * ksplit * S::kAccCols * kBM;
                 float* mine = part_tile + (size_t)tw.split * S::kAccCols * kBM;
                 for (int c0 = half * 16; c0 < n_cols; c0 += 32) {
@@ -807,9 +816,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 finish = s_misc[1] != 0;
                 if (finish) __threadfence();
             }
-            if (!has_lora && ksplit == 1) {
-                // lean epilogue (no CUDA-core expand, no K split): 16 columns of
-                // each accumulator per TMEM load, one wait for both
+            if (!has_lora && (ksplit == 1 || slab)) {
+                // lean epilogue (no CUDA-core expand, no split-K finish): 16
+                // columns of each accumulator per TMEM load, one wait for both
                 for (int c0 = half * 16; c0 < n_real; c0 += 32) {
                     float g[16], u[16];
                     if (GATE_UP) tmem_ld16x2(t_lane + c0, t_lane + BN + c0, g, u);
@@ -822,7 +831,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                                 if (GATE_UP)
                                     a.act_out[(size_t)(q0c + cc) * a.I + w_row] = f32_to_bf16_rne(silu_fast(g[c]) * u[c]);
                                 else
-                                    a.pair_out[(size_t)s_pair[cc] * a.H + w_row] = s_w[cc] * g[c];
+                                    pout[(size_t)s_pair[cc] * a.H + w_row] = s_w[cc] * g[c];
                             }
                         }
                     }
@@ -830,12 +839,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 finish = false;
             }
             EpiRow<GATE_UP> er;
-            er.init(a, e, w_row, row_ok, rows_per_expert);
+            er.init(a, e, w_row, row_ok, rows_per_expert, pout);
+            // the CUDA-core expand is added once: by split 0 when splits write slabs
+            const bool add_lora = has_lora && (!slab || tw.split == 0);
             for (int c0 = half * 16; finish && c0 < n_cols; c0 += 32) {
                 // columns in groups of four keep the loop small (instruction cache)
                 for (int c4 = c0; c4 < c0 + 16 && c4 < n_real; c4 += 4) {
                     float g4[4], u4[4];
-                    if (ksplit == 1) {
+                    if (ksplit == 1 || slab) {
                         tmem_ld4(t_lane + c4, g4);
                         if (GATE_UP) tmem_ld4(t_lane + BN + c4, u4);
                     } else {
@@ -879,7 +890,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                         const int cc = c4 + c;
                         if (cc < n_real)
                             er.column(a, q0c + cc, s_pair[cc], s_lora[cc], s_w[cc], zs + cc * r, g4[c],
-                                      GATE_UP ? u4[c] : 0.f, has_lora);
+                                      GATE_UP ? u4[c] : 0.f, add_lora);
                     }
                 }
             }

@@ -217,10 +217,10 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * zexp_cols(d->L, d->r) : 0;
     L->zexp1 = take(zx);
     L->zexp2 = take(zx);
-    L->pair_out = take(sizeof(float) * (size_t)L->P * d->H);
+    // one [P][H] slab per K-split of the down GEMM (summed by the reduce)
+    L->pair_out = take(sizeof(float) * (size_t)std::max(1, L->ks_dn) * L->P * d->H);
     const size_t part_gu = L->ks_gu > 1 ? (size_t)L->tiles_gu * L->ks_gu * 2 * L->bn_gu * 128 : 0;
-    const size_t part_dn = L->ks_dn > 1 ? (size_t)L->tiles_dn * L->ks_dn * L->bn_dn * 128 : 0;
-    L->tc_part = take(sizeof(float) * std::max(part_gu, part_dn));
+    L->tc_part = take(sizeof(float) * part_gu);
     L->tc_counters = take(sizeof(int32_t) * (L->tiles_gu + L->tiles_dn));
     L->total = o;
     return MOELORA_OK;
@@ -327,7 +327,7 @@ bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, i
     const cuuint32_t box[3] = {(cuuint32_t)rp, (cuuint32_t)rows, (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, zexp, 3, dims, strides, box, expand_swizzle(rp));
 }
-int pair_box_rows(int bn) { return bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
+int pair_box_rows(int bn) { return bn >= 256 ? 256 : bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
 
 // B1 [L][E][2I][r] as {r, I, 2, E, L}: boxes of r_pad (zeros beyond r) x 128
 // units of one half x 64 / r_pad adapters (zeros beyond L); strides increase
@@ -602,6 +602,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.sh_counters = sh_counters + L.st_tasks_max;
         tc.zdone = sh_counters + 2 * L.st_tasks_max + 1;
         tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp2) : nullptr;
+        tc.pair_split = (size_t)L.P * d->H;
         tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
         tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
         tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
@@ -623,6 +624,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ReduceArgs ra = {};
     ra.T = d->T; ra.k = d->k; ra.H = d->H; ra.E = d->E; ra.L = d->L;
     ra.pair_out = at<float>(ws, L.pair_out);
+    ra.nsplit = std::max(1, L.ks_dn);
+    ra.split_stride = (size_t)L.P * d->H;
     ra.topk_ids = topk_ids;
     ra.lora_ids = token_lora_ids;
     ra.out = static_cast<uint16_t*>(out);

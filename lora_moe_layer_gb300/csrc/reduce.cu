@@ -1,12 +1,15 @@
-// reduce.cu -- top-k weighted aggregation: out[t] = bf16(sum_j pair_out[t*k + j]).
+// reduce.cu -- top-k weighted aggregation:
+//   out[t] = bf16(sum_j sum_s pair_out[s][t*k + j]).
 //
 // The router's k experts of a token are aggregated ("Efficiently serve dozens
 // of fine-tuned models with vLLM ...", section "Implementing multi-LoRA
 // inference for MoE models in vLLM"); the down kernel has already applied the
-// top-k weights, so this is a fixed-order sum over the token's slots (j = 0
-// .. k-1, deterministic) and one round-to-nearest-even to bf16.  Pairs that
-// carry an out-of-range id were left out upstream and are skipped here.
-// Four hidden elements per thread: 16-byte fp32 loads, 8-byte bf16 stores.
+// top-k weights.  When the down GEMM splits K, each split s wrote its own
+// slab, and the slabs are added here.  Both sums run in a fixed order (slot j
+// = 0 .. k-1, inside it split s = 0 .. nsplit-1: deterministic), then one
+// round-to-nearest-even to bf16.  Pairs that carry an out-of-range id were
+// left out upstream and are skipped here.  Four hidden elements per thread:
+// 16-byte fp32 loads, 8-byte bf16 stores.
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -14,11 +17,20 @@ namespace moelora {
 
 namespace {
 
+__device__ __forceinline__ void add4(float4& s, const float4& v) {
+    s.x += v.x;
+    s.y += v.y;
+    s.z += v.z;
+    s.w += v.w;
+}
+
+template <bool SPLIT>
 __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
     pdl_wait();
     pdl_trigger();
     const int H4 = a.H >> 2;
     const long n = (long)a.T * H4;
+    const size_t split4 = a.split_stride / 4;
     for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (long)gridDim.x * blockDim.x) {
         const int t = (int)(idx / H4), h4 = (int)(idx % H4);
         const int l = a.lora_ids[t];
@@ -30,13 +42,18 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
         for (int j = 0; j < a.k; j++) {
             const int p = t * a.k + j;
             const int e = a.topk_ids[p];
-            const float4 v = __ldcs(reinterpret_cast<const float4*>(a.pair_out + (size_t)p * a.H) + h4);
-            if (l_ok && e >= 0 && e < a.E) {
-                s.x += v.x;
-                s.y += v.y;
-                s.z += v.z;
-                s.w += v.w;
+            const float4* src = reinterpret_cast<const float4*>(a.pair_out + (size_t)p * a.H) + h4;
+            float4 v = __ldcs(src);
+            if (SPLIT) {
+                float4 u[kMaxSplitSlabs - 1];
+#pragma unroll
+                for (int sp = 1; sp < kMaxSplitSlabs; sp++)
+                    if (sp < a.nsplit) u[sp - 1] = __ldcs(src + sp * split4);
+#pragma unroll
+                for (int sp = 1; sp < kMaxSplitSlabs; sp++)
+                    if (sp < a.nsplit) add4(v, u[sp - 1]);
             }
+            if (l_ok && e >= 0 && e < a.E) add4(s, v);
         }
         uint2 o;
         o.x = (uint32_t)f32_to_bf16_rne(s.x) | ((uint32_t)f32_to_bf16_rne(s.y) << 16);
@@ -48,7 +65,9 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
 }  // namespace
 
 cudaError_t launch_reduce(const ReduceArgs& args, int grid, cudaStream_t stream, bool pdl) {
-    return launch_k(k_reduce, dim3(grid), dim3(256), 0, stream, pdl, args);
+    if (args.nsplit < 1 || args.nsplit > kMaxSplitSlabs) return cudaErrorInvalidValue;
+    if (args.nsplit > 1) return launch_k(k_reduce<true>, dim3(grid), dim3(256), 0, stream, pdl, args);
+    return launch_k(k_reduce<false>, dim3(grid), dim3(256), 0, stream, pdl, args);
 }
 
 }  // namespace moelora
