@@ -63,6 +63,7 @@ struct TcArgs {
     CUtensorMap bmap;            // LoRA B: B1 as {r, I, 2, E, L} / B2 as {r, H, E, L}; box r_pad x 128 rows x 64/r_pad adapters
     CUtensorMap bmap1;           // the same LoRA B with a one-adapter box
     CUtensorMap zxmap;           // zexp [L][P][r_pad] bf16; box r_pad x BN rows x 64/r_pad adapters
+    CUtensorMap zxmap1;          // the same zexp with a one-adapter box
     int E, L, k, r, I, H, P;
     const uint16_t* B;           // B1 / B2 (null: no LoRA)
     float* z;                    // shrink output [P][r], written by the shrink items (null: no LoRA)

@@ -208,19 +208,20 @@ struct EpiRow {
 __host__ __device__ inline int expand_rpad(int r) { return r <= 16 ? 16 : r <= 32 ? 32 : 64; }
 __device__ inline uint32_t expand_layout(int rp) { return rp == 16 ? 6u : rp == 32 ? 4u : 2u; }
 
-// The expand blocks of one GEMM task: block jb holds the adapters jb*apb ..
-// jb*apb+apb-1 that have pairs in the task's chunk.  Blocks are dealt to the
-// task's K-splits by jb mod ksplit, so a split-K task spreads its expand work
-// too.  With up to 64 adapters the set comes from the chunk's adapter mask
-// built at kernel start and is walked by its set bits (the single MMA-issuing
-// thread spends a few instructions per task on it).  Beyond that, the pairs of
-// a chunk (sorted by adapter) span the adapters la .. lb of its first and last
-// pair, read from global memory, and every adapter of the span is taken (zexp
-// zeros make the absent ones add nothing).
+// The expand blocks of one GEMM task.  With up to 64 adapters the chunk's
+// adapter set comes from its mask (built at kernel start) and the blocks are
+// packed: block g holds the g-th group of 64 / r_pad adapters present in the
+// chunk, in id order, each loaded into its own sub-tile.  Beyond 64 adapters,
+// the pairs of a chunk (sorted by adapter) span the adapters la .. lb of its
+// first and last pair, read from global memory, and block jb covers the fixed
+// adapter range jb*apb .. jb*apb+apb-1 of the span (zexp zeros make absent
+// adapters add nothing).  Either way, block j goes to the task's K-split
+// j mod ksplit, so a split-K task spreads its expand work too (with one
+// adapter per block, adapter l goes to split l mod ksplit).
 struct ExpandRange {
     int la, lb, p0, p1, split, ksplit, apb, L;
     bool wide;
-    unsigned long long bits;   // adapters of this split's blocks (ids < 64)
+    unsigned long long bits;   // adapters (ids < 64) present in the chunk
     __device__ void from_mask(const TcArgs& a, unsigned long long m, int split_, int ksplit_) {
         la = 0;
         lb = -1;
@@ -230,11 +231,14 @@ struct ExpandRange {
         L = a.L;
         wide = false;
         bits = m;
-        if (ksplit > 1) {
-            const unsigned long long blk = apb == 64 ? ~0ull : (1ull << apb) - 1;
-            unsigned long long mine = 0;
-            for (int jb = split; jb * apb < 64; jb += ksplit) mine |= blk << (jb * apb);
-            bits &= mine;
+        if (apb == 1 && ksplit > 1) {
+            // one adapter per block: deal the blocks by adapter id, so each
+            // split walks only its own adapters
+            unsigned long long own = 0ull;
+            for (int l = split; l < 64; l += ksplit) own |= 1ull << l;
+            bits &= own;
+            split = 0;
+            ksplit = 1;
         }
     }
     // pair ids of the chunk's first and last row (issued early), then their adapters
@@ -253,21 +257,17 @@ struct ExpandRange {
         bits = 0;
     }
     __device__ void none() { la = 0; lb = -1; split = 0; ksplit = 1; apb = 1; L = 0; wide = false; bits = 0; }
-    // first block >= jb of this task's split, or -1
+    // packed blocks: how many the chunk has, and how many adapters block g holds
+    __device__ int groups() const { return (__popcll(bits) + apb - 1) / apb; }
+    __device__ int group_size(int g) const { return min(apb, __popcll(bits) - g * apb); }
+    // fixed blocks (beyond 64 adapters): first block >= jb of this task's split, or -1
     __device__ int next(int jb) const {
-        if (!wide) {
-            if (jb * apb >= 64) return -1;
-            const unsigned long long rest = bits & (~0ull << (jb * apb));
-            return rest ? (__ffsll((long long)rest) - 1) / apb : -1;
-        }
         for (jb = max(jb, la / apb); jb * apb <= lb; jb++)
             if (jb % ksplit == split) return jb;
         return -1;
     }
-    // adapters of block jb (bit s = adapter jb*apb + s)
+    // adapters of fixed block jb (bit s = adapter jb*apb + s)
     __device__ uint32_t slots(int jb) const {
-        const uint32_t all = (1u << apb) - 1u;
-        if (!wide) return (uint32_t)(bits >> (jb * apb)) & all;
         uint32_t sm = 0;
         for (int s = 0; s < apb; s++) {
             const int l = jb * apb + s;
@@ -275,7 +275,12 @@ struct ExpandRange {
         }
         return sm;
     }
+    // this split's expand blocks
     __device__ int count() const {
+        if (!wide) {
+            const int ng = groups();
+            return ng > split ? (ng - 1 - split) / ksplit + 1 : 0;
+        }
         int n = 0;
         for (int jb = next(0); jb >= 0; jb = next(jb + 1)) n++;
         return n;
@@ -450,6 +455,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             prefetch_tensormap(&a.bmap);
             prefetch_tensormap(&a.bmap1);
             prefetch_tensormap(&a.zxmap);
+            prefetch_tensormap(&a.zxmap1);
         }
     }
     tc_fence_before();
@@ -604,9 +610,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     z_seen = true;
                 }
                 // a block's adapters: A sub-tiles (128 x r_pad each, one copy per
-                // half) and zexp sub-tiles (BN rows x r_pad each, one copy)
+                // half) and zexp sub-tiles (BN rows x r_pad each)
                 const uint32_t xa1 = 128u * expand_rpad(a.r) * 2u;  // one adapter's A sub-tile
-                for (int jb = n_x > 0 ? xr.next(0) : -1; ok && jb >= 0; jb = xr.next(jb + 1)) {
+                const uint32_t zx1 = (uint32_t)BN * expand_rpad(a.r) * 2u;  // one adapter's zexp sub-tile
+                if (n_x > 0 && !xr.wide) {
+                    // packed blocks: the next 64 / r_pad present adapters, one
+                    // single-adapter copy each for A (per half) and for zexp
+                    // (other splits' groups are skipped by clearing their bits:
+                    // this one thread issues every copy of the CTA)
+                    unsigned long long rem = xr.bits;
+                    for (int g = 0, mine = xr.split; ok && rem != 0ull; g++) {
+                        if (g != mine) {
+                            for (int q = 0; q < xr.apb; q++) rem &= rem - 1ull;
+                            continue;
+                        }
+                        mine += xr.ksplit;
+                        int ids[4];
+                        int cnt = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (q < xr.apb && rem != 0ull) {
+                                ids[q] = __ffsll((long long)rem) - 1;
+                                rem &= rem - 1ull;
+                                cnt = q + 1;
+                            }
+                        }
+                        if (!mbar_wait(&empty[stage], phase ^ 1)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&full[stage], (uint32_t)cnt * ((GATE_UP ? 2u : 1u) * xa1 + zx1));
+                        uint8_t* dst = base + (size_t)stage * S::kStage;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (q < cnt) {
+                                // coordinates (k, unit, half, expert, adapter) / (k, row, expert, adapter)
+                                if (GATE_UP) {
+                                    tma_load_5d(dst + q * xa1, &a.bmap1, &full[stage], 0, tw.mt * kBM, 0, e, ids[q]);
+                                    tma_load_5d(dst + kATile + q * xa1, &a.bmap1, &full[stage], 0, tw.mt * kBM, 1, e,
+                                                ids[q]);
+                                } else {
+                                    tma_load_4d(dst + q * xa1, &a.bmap1, &full[stage], 0, tw.mt * kBM, e, ids[q]);
+                                }
+                                tma_load_3d(dst + S::kAB + q * zx1, &a.zxmap1, &full[stage], 0, row0, ids[q]);
+                            }
+                        }
+                        armed |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                }
+                for (int jb = (n_x > 0 && xr.wide) ? xr.next(0) : -1; ok && jb >= 0; jb = xr.next(jb + 1)) {
                     // a block with one adapter present loads that adapter's rows only
                     const uint32_t sm = xr.slots(jb);
                     const bool one = __popc(sm) == 1;
@@ -705,7 +756,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                     umma_commit(&empty[stage]);
                     if (++stage == NS) { stage = 0; phase ^= 1; }
                 }
-                for (int jb = xr.next(0); jb >= 0 && ok; jb = xr.next(jb + 1)) {
+                if (!xr.wide) {
+                    // packed blocks of this split: sub-tiles 0 .. cnt-1
+                    const int ng = xr.groups();
+                    for (int g = xr.split; g < ng && ok; g += xr.ksplit) {
+                        const int cnt = xr.group_size(g);
+                        if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint64_t dxs = dx0 + (uint64_t)stage * kStage16;
+                        for (int q = 0; q < cnt; q++) {
+                            const uint64_t da = dxs + q * xa16;
+                            const uint64_t db = dxs + kPair16 + q * (uint32_t)(BN * xrp * 2 / 16);
+                            for (int kk = 0; kk < xrp / 16; kk++) {
+                                umma_bf16(d_first, da + 2 * kk, db + 2 * kk, idesc, 1u);
+                                if (GATE_UP) umma_bf16(d_first + BN, da + kUp16 + 2 * kk, db + 2 * kk, idesc, 1u);
+                            }
+                        }
+                        umma_commit(&empty[stage]);
+                        if (++stage == NS) { stage = 0; phase ^= 1; }
+                    }
+                }
+                for (int jb = xr.wide ? xr.next(0) : -1; jb >= 0 && ok; jb = xr.next(jb + 1)) {
                     const uint32_t sm = xr.slots(jb);
                     if (!mbar_wait(&full[stage], phase)) { ok = false; break; }
                     tc_fence_after();

@@ -320,11 +320,11 @@ bool encode_rows_map(CUtensorMap* map, const void* rows, long P, int K, int box_
 
 // zexp [L][P][r_pad]: boxes of r_pad x rows pair rows x 64 / r_pad adapters
 // (one ring stage's sub-tiles, adapter outermost)
-bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, int rows) {
+bool encode_zexp_map(CUtensorMap* map, const void* zexp, long P, int L, int r, int rows, bool one_adapter = false) {
     const int rp = expand_rpad_host(r);
     const cuuint64_t dims[3] = {(cuuint64_t)rp, (cuuint64_t)P, (cuuint64_t)L};
     const cuuint64_t strides[2] = {(cuuint64_t)rp * 2, (cuuint64_t)P * rp * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)rp, (cuuint32_t)rows, (cuuint32_t)(64 / rp)};
+    const cuuint32_t box[3] = {(cuuint32_t)rp, (cuuint32_t)rows, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, zexp, 3, dims, strides, box, expand_swizzle(rp));
 }
 int pair_box_rows(int bn) { return bn >= 256 ? 256 : bn >= 128 ? 64 : 16; }  // matches the kernels' kRowsFor<BN>
@@ -582,7 +582,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
                              !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn))))
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
@@ -613,7 +614,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
                              !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn))))
+                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));

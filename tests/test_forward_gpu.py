@@ -71,6 +71,9 @@ RAGGED = [
     (600, 128, 136, 2, 2, 5, 32),
     (200, 264, 136, 3, 2, 6, 24),
     (300, 96, 1032, 2, 1, 8, 64),
+    # one expert, K split across CTAs, packed expand blocks (four adapters of
+    # r = 16 per block) dealt to the splits
+    (64, 1024, 2048, 1, 1, 12, 16),
 ]
 
 
