@@ -95,9 +95,59 @@ __device__ void block_scan_items(int n, F item, int* out_a, int* out_b, int2* sw
     }
 }
 
+__device__ __forceinline__ int4 add4(int4 a, int4 b) { return make_int4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w); }
+__device__ __forceinline__ int4 sub4(int4 a, int4 b) { return make_int4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+
+__device__ __forceinline__ int4 warp_incl_scan4(int4 v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int4 u;
+        u.x = __shfl_up_sync(kFull, v.x, o);
+        u.y = __shfl_up_sync(kFull, v.y, o);
+        u.z = __shfl_up_sync(kFull, v.z, o);
+        u.w = __shfl_up_sync(kFull, v.w, o);
+        if (lane >= o) v = add4(v, u);
+    }
+    return v;
+}
+
+// Exclusive scan over n items of four counts each: item(i) gives them, and
+// emit(i, prefix, item) is called once per item in order within each
+// thread's contiguous run.  Every thread gets the totals.  sw needs
+// kAlignWarps + 1 entries.  Contains __syncthreads.
+template <typename F, typename G>
+__device__ int4 block_scan4(int n, F item, G emit, int4* sw) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per = (n + kAlignThreads - 1) / kAlignThreads;
+    const int beg = min(n, (int)threadIdx.x * per);
+    const int end = min(n, beg + per);
+    int4 local = make_int4(0, 0, 0, 0);
+    for (int i = beg; i < end; i++) local = add4(local, item(i));
+    const int4 inc = warp_incl_scan4(local, lane);
+    if (lane == 31) sw[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int4 w = lane < kAlignWarps ? sw[lane] : make_int4(0, 0, 0, 0);
+        const int4 wi = warp_incl_scan4(w, lane);
+        if (lane < kAlignWarps) sw[lane] = sub4(wi, w);
+        if (lane == 31) sw[kAlignWarps] = wi;
+    }
+    __syncthreads();
+    int4 run = add4(sw[warp], sub4(inc, local));
+    const int4 total = sw[kAlignWarps];
+    for (int i = beg; i < end; i++) {
+        const int4 v = item(i);
+        emit(i, run, v);
+        run = add4(run, v);
+    }
+    __syncthreads();
+    return total;
+}
+
 __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     extern __shared__ __align__(16) int smem_hist[];
     __shared__ int2 sw[kAlignWarps + 1];
+    __shared__ int4 sw4[kAlignWarps + 1];
     // The first kernel of a forward is launched without a programmatic
     // dependency, so this wait is a no-op; it stays for standalone use.
     pdl_wait();
@@ -119,8 +169,23 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     int* keys = a.keys_in_smem ? sm : a.keys_global;
     WsHeader* hdr = a.hdr;
 
+    // The forward only needs each bucket's pairs together: its per-pair results
+    // do not depend on their order inside a bucket, so it counts and places
+    // with shared-memory atomics on histogram row 0 (the block's count, then
+    // its placement cursor); rows 1.. then hold the adapter-bucket list and
+    // the last row the experts that have pairs.  The standalone entry point
+    // keeps ascending p inside a bucket: per-warp counts with warp match-any
+    // in pass 1 (all rows), ranks in pass 2.
+    const bool stable = a.full_outputs != 0;
+    const bool lists = a.active_experts != nullptr && !stable;
+    int* e_act = hist + (kAlignWarps - 1) * NB;   // [E] experts with pairs (lists only)
+    int* lbs = hist + NB + 1;                      // copy of the adapter-bucket list (lists only)
+
     if (threadIdx.x == 0) hdr->status = 0;
-    for (int i = threadIdx.x; i < kAlignWarps * NB; i += kAlignThreads) hist[i] = 0;
+    const int n_hist = stable ? kAlignWarps * NB : NB;
+    for (int i = threadIdx.x; i < n_hist; i += kAlignThreads) hist[i] = 0;
+    if (lists)
+        for (int i = threadIdx.x; i < a.E; i += kAlignThreads) e_act[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero; i += kAlignThreads) a.zero_ints[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
     {
@@ -143,14 +208,6 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     const int seg_beg = min(P, warp * seg);
     const int seg_end = min(P, seg_beg + seg);
     int* my_hist = hist + warp * NB;
-
-    // The forward only needs each bucket's pairs together: its per-pair results
-    // do not depend on their order inside a bucket, so it counts and places
-    // with shared-memory atomics (row 0 of the histogram is the block's count,
-    // then its placement cursor).  The standalone entry point keeps ascending p
-    // inside a bucket: per-warp counts with warp match-any in pass 1, ranks in
-    // pass 2.
-    const bool stable = a.full_outputs != 0;
     const int run = ((P + kAlignThreads - 1) / kAlignThreads) | 1;  // pairs per thread, odd
     const int run0 = threadIdx.x * run;
     if (stable) {
@@ -170,7 +227,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         for (int s = 0; s < run; s++) {
             const int p = run0 + s;
             const int b = p < P ? keys[p] : -1;
-            if (b >= 0) atomicAdd(&hist[b], 1);
+            if (b >= 0) {
+                atomicAdd(&hist[b], 1);
+                if (lists) e_act[b / L1] = 1;
+            }
         }
     }
     __syncthreads();
@@ -193,19 +253,49 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     }
     __syncthreads();
 
-    // padded offsets (bucket_offset) and compact offsets, both exclusive scans
+    // one scan over the buckets: padded offsets (bucket_offset), compact
+    // offsets, and for the forward the list of (e, l >= 0) buckets with pairs
+    // and the list of experts with pairs (counted at each expert's first bucket)
     const int bm = a.bm;
     const int* cnt = cnt_t;
-    block_scan_items(
-        NB, [&](int b) { const int c = cnt[b]; return make_int2((c + bm - 1) / bm * bm, c); },
-        boff_t, coff_t, sw);
-    __syncthreads();
-    if (a.tabs_in_smem) {
-        for (int b = threadIdx.x; b <= NB; b += kAlignThreads) {
-            a.bucket_offset[b] = boff_t[b];
-            a.compact_offset[b] = coff_t[b];
+    const int4 tot = block_scan4(
+        NB,
+        [&](int b) {
+            const int c = cnt[b];
+            const int sub = b % L1;
+            return make_int4((c + bm - 1) / bm * bm, c, lists && sub != 0 && c > 0 ? 1 : 0,
+                             lists && sub == 0 && e_act[b / L1] ? 1 : 0);
+        },
+        [&](int b, int4 pre, int4 v) {
+            boff_t[b] = pre.x;
+            coff_t[b] = pre.y;
+            if (a.tabs_in_smem) {
+                a.bucket_offset[b] = pre.x;
+                a.compact_offset[b] = pre.y;
+            }
+            if (v.z) {
+                a.lora_buckets[pre.z] = b;
+                lbs[pre.z] = b;
+            }
+            if (v.w) a.active_experts[pre.w] = b / L1;
+        },
+        sw4);
+    if (threadIdx.x == 0) {
+        boff_t[NB] = tot.x;
+        coff_t[NB] = tot.y;
+        if (a.tabs_in_smem) {
+            a.bucket_offset[NB] = tot.x;
+            a.compact_offset[NB] = tot.y;
+        }
+        hdr->num_post_padded = tot.x;
+        hdr->n_valid = tot.y;
+        if (a.num_post_padded) *a.num_post_padded = tot.x;
+        if (lists) {
+            hdr->n_lora_buckets = tot.z;
+            hdr->n_active = tot.w;
         }
     }
+    __syncthreads();
 
     // pass 2: placement
     if (stable) {
@@ -230,9 +320,9 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             if (b >= 0) a.compact_ids[coff_t[b] + atomicAdd(&hist[b], 1)] = p;
         }
     }
-    __syncthreads();
 
     if (a.full_outputs) {
+        __syncthreads();
         // padding sentinels, and each bucket's tiles tagged with its (expert, adapter)
         for (int b = threadIdx.x; b < NB; b += kAlignThreads) {
             const int beg = boff_t[b], end = boff_t[b + 1];
@@ -243,62 +333,30 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             }
         }
     }
-    const int total_padded = boff_t[NB];
-    if (threadIdx.x == 0) {
-        hdr->num_post_padded = total_padded;
-        hdr->n_valid = coff_t[NB];
-        if (a.num_post_padded) *a.num_post_padded = total_padded;
-    }
-    if (a.active_experts) {
-        // compact list of experts with pairs, and of (e, l >= 0) buckets with pairs.
-        // The histogram's shared memory is free after pass 2: the scans and the
-        // bucket list are read back from there when the histogram lives there.
-        int* tmp = a.hist_global ? a.scan_tmp : hist;                 // max(E, NB) + 1 ints
-        int* lbs = a.hist_global ? a.lora_buckets : hist + NB + 1;    // copy of the bucket list
+    if (lists && a.st_tasks) {
+        // shrink tasks: st_G consecutive adapter buckets per group; a group's
+        // rows are contiguous in bucket order and split into chunks of st_BN.
+        // The scan's output reuses histogram row 0, free after the placement.
+        __syncthreads();
+        int* tmp = hist;
+        const int n = tot.z;
+        const int G = a.st_G, BN = a.st_BN;
+        const int ng = (n + G - 1) / G;
         const int* coff = coff_t;
-        const int E = a.E;
+        auto rows = [&](int g) {
+            const int j1 = min(n, g * G + G) - 1;
+            return make_int2(coff[lbs[g * G]], coff[lbs[j1] + 1]);
+        };
         block_scan_items(
-            E, [&](int e) { return make_int2(coff[(e + 1) * L1] > coff[e * L1] ? 1 : 0, 0); },
+            ng, [&](int g) { const int2 q = rows(g); return make_int2((q.y - q.x + BN - 1) / BN, 0); },
             tmp, nullptr, sw);
         __syncthreads();
-        for (int e = threadIdx.x; e < E; e += kAlignThreads)
-            if (coff[(e + 1) * L1] > coff[e * L1]) a.active_experts[tmp[e]] = e;
-        if (threadIdx.x == 0) hdr->n_active = tmp[E];
-        __syncthreads();
-        block_scan_items(
-            NB, [&](int b) { return make_int2((b % L1) != 0 && cnt[b] > 0 ? 1 : 0, 0); },
-            tmp, nullptr, sw);
-        __syncthreads();
-        for (int b = threadIdx.x; b < NB; b += kAlignThreads)
-            if ((b % L1) != 0 && cnt[b] > 0) {
-                a.lora_buckets[tmp[b]] = b;
-                lbs[tmp[b]] = b;
-            }
-        if (threadIdx.x == 0) hdr->n_lora_buckets = tmp[NB];
-        __syncthreads();
-        if (a.st_tasks) {
-            // shrink tasks: st_G consecutive adapter buckets per group; a group's
-            // rows are contiguous in bucket order and split into chunks of st_BN
-            const int n = tmp[NB];
-            __syncthreads();
-            const int G = a.st_G, BN = a.st_BN;
-            const int ng = (n + G - 1) / G;
-            const int* lb = lbs;
-            auto rows = [&](int g) {
-                const int j1 = min(n, g * G + G) - 1;
-                return make_int2(coff[lb[g * G]], coff[lb[j1] + 1]);
-            };
-            block_scan_items(
-                ng, [&](int g) { const int2 q = rows(g); return make_int2((q.y - q.x + BN - 1) / BN, 0); },
-                tmp, nullptr, sw);
-            __syncthreads();
-            for (int g = threadIdx.x; g < ng; g += kAlignThreads) {
-                const int2 q = rows(g);
-                int at = tmp[g];
-                for (int q0 = q.x; q0 < q.y; q0 += BN) a.st_tasks[at++] = make_int4(g, q0, min(BN, q.y - q0), 0);
-            }
-            if (threadIdx.x == 0) hdr->n_shrink_tasks = tmp[ng];
+        for (int g = threadIdx.x; g < ng; g += kAlignThreads) {
+            const int2 q = rows(g);
+            int at = tmp[g];
+            for (int q0 = q.x; q0 < q.y; q0 += BN) a.st_tasks[at++] = make_int4(g, q0, min(BN, q.y - q0), 0);
         }
+        if (threadIdx.x == 0) hdr->n_shrink_tasks = tmp[ng];
     }
     pdl_trigger();
 }

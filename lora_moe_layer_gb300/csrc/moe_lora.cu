@@ -382,7 +382,7 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.st_G = L.st_G;
     a.st_BN = L.st_bn;
     a.zero_ints2 = at<int>(ws, L.tc_counters);
-    a.n_zero2 = (L.ks_gu > 1 || L.ks_dn > 1) ? (int)(L.tiles_gu + L.tiles_dn) : 0;
+    a.n_zero2 = L.ks_gu > 1 ? (int)L.tiles_gu : 0;  // gate_up split arrivals (down splits write slabs)
     a.hdr = at<WsHeader>(ws, L.hdr);
     return a;
 }
