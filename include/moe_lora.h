@@ -237,8 +237,11 @@ typedef struct moe_lora_ws_layout {
                                 adapter pairs only; other rows are left undefined) */
     size_t act;              /* bf16 [P][I]: SiLU(gate)*up per row */
     size_t z2;               /* float [P][r]: down LoRA shrink A2 act per row (same rows) */
-    size_t pair_out;         /* float [P][H]: w * d per pair id p */
+    size_t pair_out;         /* float [down_splits][P][H]: w * d per pair id p, one slab per
+                                K-split of the down GEMM (their sum is the pair's output) */
     int32_t s1, s2;          /* K-split counts the two shrinks used */
+    int32_t down_splits;     /* K-splits of the down GEMM (>= 1) */
+    int32_t launches;        /* kernels one forward launches for these dims (T > 0) */
     size_t total;            /* == moe_lora_workspace_bytes */
 } moe_lora_ws_layout;
 

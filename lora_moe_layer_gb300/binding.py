@@ -48,7 +48,7 @@ class moe_lora_ws_layout(ctypes.Structure):
     _fields_ = [("compact_ids", ctypes.c_size_t), ("compact_offset", ctypes.c_size_t),
                 ("z1", ctypes.c_size_t), ("act", ctypes.c_size_t), ("z2", ctypes.c_size_t),
                 ("pair_out", ctypes.c_size_t), ("s1", ctypes.c_int32), ("s2", ctypes.c_int32),
-                ("total", ctypes.c_size_t)]
+                ("down_splits", ctypes.c_int32), ("launches", ctypes.c_int32), ("total", ctypes.c_size_t)]
 
 
 _lib = None

@@ -434,6 +434,8 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     out->pair_out = L.pair_out;
     out->s1 = L.s1;
     out->s2 = L.s2;
+    out->down_splits = std::max(1, L.ks_dn);
+    out->launches = 5;  // align, gather, gate_up, down, reduce
     out->total = L.total;
     return MOELORA_OK;
 }

@@ -57,13 +57,24 @@ def test_workspace_bytes_and_layout(lib):
     for s in (lay["s1"], lay["s2"]):
         assert 1 < s <= min(32, (2880 // 64) // 2)
     # regions are disjoint and inside the workspace
+    assert lay["down_splits"] == 1
+    assert lay["launches"] == 5  # align, gather, gate_up, down, reduce
     regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * P * 32),
                       (lay["act"], 2 * P * 2880), (lay["z2"], 4 * P * 32),
-                      (lay["pair_out"], 4 * P * 2880)])
+                      (lay["pair_out"], 4 * P * 2880 * lay["down_splits"])])
     for (a, na), (b, _) in zip(regions, regions[1:]):
         assert a + na <= b
     assert regions[-1][0] + regions[-1][1] <= n
     assert all(off % 256 == 0 for off, _ in regions)
+
+
+def test_layout_of_split_and_expand_workloads(lib):
+    # one expert with few weight tiles: the down GEMM splits K, one pair_out
+    # slab per split
+    d = B.dims(256, 8192, 28672, 1, 1, 32, 64)
+    lay = B.moe_lora_workspace_layout(d)
+    assert 1 < lay["down_splits"] <= 8
+    assert lay["pair_out"] + 4 * 256 * 8192 * lay["down_splits"] <= lay["total"]
 
 
 @pytest.mark.parametrize("bad", [
