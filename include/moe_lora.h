@@ -70,7 +70,15 @@ typedef struct moe_lora_dims {
     int32_t L;       /* adapters, >= 0 (0: no LoRA; A and B pointers may be NULL) */
     int32_t r;       /* LoRA rank: multiple of 8 in [8, 64] if L > 0, ignored if L == 0 */
     int32_t block_m; /* 0 = default 16; otherwise a power of two in [1, 256] */
+    int32_t options; /* 0, or MOELORA_OPT_PAIR_CTA */
 } moe_lora_dims;
+
+/* Experimental: run the two GEMMs of batches with wide expert chunks (more
+ * than 48 pairs per expert on average) on CTA pairs (tcgen05.mma.cta_group::2,
+ * 256 weight rows x up to 256 pairs per task) when the pair kernel covers
+ * the layer; otherwise, and by default, one CTA per weight tile.  Same
+ * results within rounding; measured slower than the default on GB300. */
+#define MOELORA_OPT_PAIR_CTA 1
 
 /* Status codes (return values; moe_lora_strerror gives a message). */
 #define MOELORA_OK 0
@@ -242,6 +250,8 @@ typedef struct moe_lora_ws_layout {
     int32_t s1, s2;          /* K-split counts the two shrinks used */
     int32_t down_splits;     /* K-splits of the down GEMM (>= 1) */
     int32_t launches;        /* kernels one forward launches for these dims (T > 0) */
+    int32_t gemm_ctas;       /* CTAs per GEMM task: 2 when MOELORA_OPT_PAIR_CTA took effect, else 1 */
+    int32_t reserved;
     size_t total;            /* == moe_lora_workspace_bytes */
 } moe_lora_ws_layout;
 

@@ -56,8 +56,11 @@ struct Layout {
         z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
     // LoRA expand on the tensor cores (zexp buffers bounded), else on CUDA cores
     bool tc_expand;
-    // tensor-core GEMM plan (shared by the launch code and the workspace size)
+    // tensor-core GEMM plan (shared by the launch code and the workspace size):
+    // chunk widths, K-splits, and whether wide chunks run on CTA pairs
     int bn_gu, bn_dn, ks_gu, ks_dn;
+    bool pair_cta;   // the GEMMs run as CTA pairs (moe_gemm_2sm.cu)
+    int ranks;       // CTAs per GEMM task: 2 with pair_cta, else 1
     long tiles_gu, tiles_dn;
     long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
 };
@@ -71,6 +74,7 @@ int check_dims(const moe_lora_dims* d) {
     if (!d) return MOELORA_EINVAL;
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->L < 0) return MOELORA_EINVAL;
     if (d->block_m != 0 && (!is_pow2(d->block_m) || d->block_m > 256)) return MOELORA_EINVAL;
+    if (d->options & ~MOELORA_OPT_PAIR_CTA) return MOELORA_EINVAL;
     if (d->L > 0) {
         if (d->r <= 0) return MOELORA_EINVAL;
         if (d->r % 8 != 0 || d->r > 64) return MOELORA_EUNSUPPORTED;
@@ -91,8 +95,7 @@ int check_dims(const moe_lora_dims* d) {
 // smallest split count whose task count fills the SMs' waves to >= 90%,
 // keeping >= 512 K-elements per split.  Sized for a 152-SM GB300; on other
 // parts it only changes the balance, not the result.
-int pick_ksplit(long tiles, int K) {
-    constexpr long kSms = 152;
+int pick_ksplit(long tiles, int K, long kSms = 152) {
     if (tiles >= 2 * kSms) return 1;
     int best = 1;
     double best_eff = 0.0;
@@ -115,8 +118,7 @@ int pick_ksplit(long tiles, int K) {
 // the partial sums; with few (decode), the items are split so every SM takes a
 // small share instead of a few SMs taking whole items.  At least two 64-wide K
 // steps per split.
-int pick_shrink_split(long est_tasks, int K) {
-    constexpr long kSms = 152;
+int pick_shrink_split(long est_tasks, int K, long kSms = 152) {
     const int nkb = (K + 63) / 64;
     if (est_tasks * 4 >= kSms) return 1;
     const long want = (kSms + std::max<long>(est_tasks, 1) - 1) / std::max<long>(est_tasks, 1);
@@ -132,16 +134,18 @@ void plan_shrinks(const moe_lora_dims* d, Layout* L) {
         L->st_tasks_max = 0;
         return;
     }
-    L->st_G = 128 / d->r;
+    // a shrink item stacks 128 / r buckets per CTA of its task
+    L->st_G = L->ranks * (128 / d->r);
     const double nbl = (double)d->E * d->L;
     const double est_buckets = std::max(1.0, nbl * (1.0 - std::exp(-(double)L->P / nbl)));
     const long est_groups = std::max<long>(1, (long)std::ceil(est_buckets / L->st_G));
     const long rows_per_group = (L->P + est_groups - 1) / est_groups;
     // an item's pairs fit one TMEM accumulator buffer of both GEMM kernels
-    L->st_bn = std::min(2 * L->bn_gu, L->bn_dn);
+    L->st_bn = L->pair_cta ? 256 : std::min(2 * L->bn_gu, L->bn_dn);
     const long est_tasks = est_groups * ((rows_per_group + L->st_bn - 1) / L->st_bn);
-    L->s1 = pick_shrink_split(est_tasks, d->H);
-    L->s2 = pick_shrink_split(est_tasks, d->I);
+    const long slots = 152 / L->ranks;
+    L->s1 = pick_shrink_split(est_tasks, d->H, slots);
+    L->s2 = pick_shrink_split(est_tasks, d->I, slots);
     L->st_tasks_max = (L->nbl + L->st_G - 1) / L->st_G + (L->P + L->st_bn - 1) / L->st_bn;
 }
 
@@ -154,10 +158,37 @@ double expected_adapters_per_chunk(const moe_lora_dims* d, long P) {
     return d->L * (1.0 - std::pow(1.0 - 1.0 / d->L, pairs));
 }
 
+// With MOELORA_OPT_PAIR_CTA, wide chunks (more than 48 pairs per expert on
+// average) run on CTA pairs:
+// chunks of 256 pairs, gate_up tiles of 256 units, down tiles of 256 rows, as
+// long as the pair kernel covers the layer (tensor-core expand with chunk
+// masks when there are adapters, no gate_up K split, a ring that fits).
+bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long avg_pairs) {
+    if (d->L > 0 && (!L->tc_expand || d->L > 64)) return false;
+    const long chunks = experts_max + (L->P + 255) / 256;
+    if (d->L > 0 && chunks > kMaxChunkMasks) return false;
+    const long masks = d->L > 0 ? chunks : 0;
+    if (tc2_plan_stages(true, d->E, (int)masks) < 3 || tc2_plan_stages(false, d->E, (int)masks) < 3) return false;
+    const long nt_gu = (d->I + 255) / 256, nt_dn = (d->H + 255) / 256;
+    const long per_expert = (avg_pairs + 255) / 256;
+    if (pick_ksplit(nt_gu * experts_max * per_expert, d->H, 76) != 1) return false;
+    L->pair_cta = true;
+    L->ranks = 2;
+    L->bn_gu = L->bn_dn = 256;
+    L->tiles_gu = nt_gu * chunks;
+    L->tiles_dn = nt_dn * chunks;
+    L->ks_gu = 1;
+    L->ks_dn = pick_ksplit(nt_dn * experts_max * per_expert, d->I, 76);
+    return true;
+}
+
 void plan_gemms(const moe_lora_dims* d, Layout* L) {
     const long experts_max = std::max<long>(1, std::min<long>(d->E, L->P));
     const long avg_pairs = L->P > 0 ? (L->P + experts_max - 1) / experts_max : 0;
     const bool narrow = avg_pairs <= 48;
+    L->pair_cta = false;
+    L->ranks = 1;
+    if (!narrow && (d->options & MOELORA_OPT_PAIR_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return;
     L->bn_gu = narrow ? 64 : 128;
     L->bn_dn = narrow ? 64 : 256;
     const long nt_gu = (d->I + 127) / 128, nt_dn = (d->H + 127) / 128;
@@ -181,6 +212,13 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->tiles = L->cap / L->bm;
     const int r = d->L > 0 ? d->r : 0;
     L->nbl = std::max<long>(std::min<long>((long)d->E * d->L, L->P), 1);
+    // zexp: per pair, one r_pad-wide slot per adapter.  The tensor-core expand
+    // pays one K block per group of a chunk's adapters; it is used when chunks
+    // are expected to mix several adapters (the CUDA-core expand then reloads
+    // B rows per adapter run) and while zexp stays small (it is rewritten
+    // every forward).
+    L->tc_expand = d->L > 0 && L->P * zexp_cols(d->L, d->r) <= kMaxZexpElems &&
+                   expected_adapters_per_chunk(d, L->P) >= 4.0;
     plan_gemms(d, L);
     plan_shrinks(d, L);
     size_t o = 0;
@@ -199,21 +237,15 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
     L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
-    // split arrivals of the two shrinks' tasks, then the two finished-task counts
-    L->counters = take(sizeof(int32_t) * (2 * std::max<long>(L->st_tasks_max, 1) + 2));
+    // split arrivals of the two shrinks' tasks (per CTA of a task), then the
+    // two finished-task counts
+    L->counters = take(sizeof(int32_t) * (2 * L->ranks * std::max<long>(L->st_tasks_max, 1) + 2));
     L->z1 = take(sizeof(float) * (size_t)(L->s1 > 1 ? L->s1 : 0) * L->P * r);
     L->z1f = take(sizeof(float) * (size_t)L->P * r);
     L->xc = take(sizeof(uint16_t) * (size_t)L->P * d->H);
     L->act = take(sizeof(uint16_t) * (size_t)L->P * d->I);
     L->z2 = take(sizeof(float) * (size_t)(L->s2 > 1 ? L->s2 : 0) * L->P * r);
     L->z2f = take(sizeof(float) * (size_t)L->P * r);
-    // zexp: per pair, one 64-wide slot per adapter.  The tensor-core expand
-    // pays one K block per adapter of a chunk; it is used when chunks are
-    // expected to mix several adapters (the CUDA-core expand then reloads B rows
-    // per adapter run) and while zexp stays small (it is rewritten every
-    // forward).
-    L->tc_expand = d->L > 0 && L->P * zexp_cols(d->L, d->r) <= kMaxZexpElems &&
-                   expected_adapters_per_chunk(d, L->P) >= 4.0;
     const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * zexp_cols(d->L, d->r) : 0;
     L->zexp1 = take(zx);
     L->zexp2 = take(zx);
@@ -228,6 +260,7 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
 
 struct DeviceInfo {
     int sms = 0;
+    int pairs_gu = 0, pairs_dn = 0;  // co-resident CTA pairs of the two pair-GEMM kernels
     cudaError_t init_err = cudaSuccess;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -245,6 +278,11 @@ int device_setup(DeviceInfo** out) {
         cudaError_t e = cudaDeviceGetAttribute(&info->sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess) e = init_align_attributes();
         if (e == cudaSuccess) e = init_tc_attributes();
+        if (e == cudaSuccess) e = init_tc2_attributes();
+        if (e == cudaSuccess) {
+            info->pairs_gu = tc2_max_pairs(true);
+            info->pairs_dn = tc2_max_pairs(false);
+        }
         info->init_err = e;
     });
     if (info->init_err != cudaSuccess) return MOELORA_ECUDA;
@@ -286,10 +324,10 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint6
 }
 
 // W1 [E][2I][H] viewed as [E][2][I][H]: boxes of 64 (K) x 128 units of one half
-bool encode_w1_map(CUtensorMap* map, const void* W1, int E, int I, int H) {
+bool encode_w1_map(CUtensorMap* map, const void* W1, int E, int I, int H, int box_rows = 128) {
     const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
     const cuuint64_t strides[3] = {(cuuint64_t)H * 2, (cuuint64_t)I * H * 2, (cuuint64_t)2 * I * H * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
     return encode_bf16_map(map, W1, 4, dims, strides, box);
 }
 
@@ -333,12 +371,13 @@ int pair_box_rows(int bn) { return bn >= 256 ? 256 : bn >= 128 ? 64 : 16; }  // 
 // units of one half x 64 / r_pad adapters (zeros beyond L); strides increase
 // with the dimension, the swizzle span is one r_pad-wide row, and each
 // adapter's 128 x r_pad tile lands after the previous one
-bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r, bool one_adapter = false) {
+bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r, bool one_adapter = false,
+                   int box_rows = 128) {
     const int rp = expand_rpad_host(r);
     const cuuint64_t dims[5] = {(cuuint64_t)r, (cuuint64_t)I, 2, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[4] = {(cuuint64_t)r * 2, (cuuint64_t)I * r * 2, (cuuint64_t)2 * I * r * 2,
                                    (cuuint64_t)E * 2 * I * r * 2};
-    const cuuint32_t box[5] = {(cuuint32_t)rp, 128, 1, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
+    const cuuint32_t box[5] = {(cuuint32_t)rp, (cuuint32_t)box_rows, 1, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, B1, 5, dims, strides, box, expand_swizzle(rp));
 }
 
@@ -377,7 +416,7 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.keys_global = a.keys_in_smem ? nullptr : at<int>(ws, L.keys);
     a.full_outputs = 0;
     a.zero_ints = at<int>(ws, L.counters);
-    a.n_zero = d->L > 0 ? (int)(2 * L.st_tasks_max + 2) : 0;
+    a.n_zero = d->L > 0 ? (int)(2 * L.ranks * L.st_tasks_max + 2) : 0;
     a.st_tasks = d->L > 0 ? at<int4>(ws, L.st_tasks) : nullptr;
     a.st_G = L.st_G;
     a.st_BN = L.st_bn;
@@ -436,6 +475,8 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     out->s2 = L.s2;
     out->down_splits = std::max(1, L.ks_dn);
     out->launches = 5;  // align, gather, gate_up, down, reduce
+    out->gemm_ctas = L.ranks;
+    out->reserved = 0;
     out->total = L.total;
     return MOELORA_OK;
 }
@@ -561,6 +602,9 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.lora_buckets = at<int32_t>(ws, L.lora_buckets);
     }
 
+    // wide chunks: both GEMMs on CTA pairs (moe_gemm_2sm.cu)
+    const bool pc = L.pair_cta;
+
     // gate_up on the tensor cores: W1 tiles x (x rows in bucket order)
     {
         const int bn = L.bn_gu;
@@ -572,25 +616,37 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.zpart = at<float>(ws, L.z1);
         tc.sh_ks = L.s1;
         tc.sh_counters = sh_counters;
-        tc.zdone = sh_counters + 2 * L.st_tasks_max;
+        tc.zdone = sh_counters + 2 * L.ranks * L.st_tasks_max;
         tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp1) : nullptr;
         tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
         tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
-        tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+        if (pc) {
+            if (!tc.chunk_masks) tc.max_chunks = 0;
+            tc.nstages = tc2_plan_stages(true, d->E, tc.max_chunks);
+        } else {
+            tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+        }
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
-        const int rows = pair_box_rows(bn);
+        // a CTA pair loads its pair rows in 64-row boxes
+        const int rows = pc ? 64 : pair_box_rows(bn);
         if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
                              !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
                              !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? 128 : bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
-        const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
         tr.mark(2);
-        if (launch_moe_gemm_tc(tc, true, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        if (pc) {
+            if (dev->pairs_gu < 1) return MOELORA_EUNSUPPORTED;
+            const int grid = 2 * (int)std::max<long>(1, std::min<long>(tasks, dev->pairs_gu));
+            if (launch_moe_gemm_2sm(tc, true, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        } else {
+            const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
+            if (launch_moe_gemm_tc(tc, true, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        }
     }
 
     // down on the tensor cores: W2 tiles x act rows
@@ -602,27 +658,38 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
         tc.zpart = at<float>(ws, L.z2);
         tc.sh_ks = L.s2;
-        tc.sh_counters = sh_counters + L.st_tasks_max;
-        tc.zdone = sh_counters + 2 * L.st_tasks_max + 1;
+        tc.sh_counters = sh_counters + L.ranks * L.st_tasks_max;
+        tc.zdone = sh_counters + 2 * L.ranks * L.st_tasks_max + 1;
         tc.zexp = L.tc_expand ? at<uint16_t>(ws, L.zexp2) : nullptr;
         tc.pair_split = (size_t)L.P * d->H;
         tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
         tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
-        tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+        if (pc) {
+            if (!tc.chunk_masks) tc.max_chunks = 0;
+            tc.nstages = tc2_plan_stages(false, d->E, tc.max_chunks);
+        } else {
+            tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+        }
         if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
-        const int rows = pair_box_rows(bn);
+        const int rows = pc ? 64 : pair_box_rows(bn);
         if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
             !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
             (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
                              !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
                              !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? 128 : bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
-        const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
         tr.mark(3);
-        if (launch_moe_gemm_tc(tc, false, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        if (pc) {
+            if (dev->pairs_dn < 1) return MOELORA_EUNSUPPORTED;
+            const int grid = 2 * (int)std::max<long>(1, std::min<long>(tasks, dev->pairs_dn));
+            if (launch_moe_gemm_2sm(tc, false, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        } else {
+            const int grid = (int)std::max<long>(1, std::min<long>(tasks, sms));
+            if (launch_moe_gemm_tc(tc, false, bn, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
+        }
     }
 
     ReduceArgs ra = {};

@@ -19,10 +19,10 @@ def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
 class DeviceLayer:
     """Weights and one batch of a ``workloads.Layer`` copied to a CUDA device."""
 
-    def __init__(self, layer, device="cuda", block_m: int = 0):
+    def __init__(self, layer, device="cuda", block_m: int = 0, options: int = 0):
         self.layer = layer
         self.device = torch.device(device)
-        self.d = B.dims(layer.T, layer.H, layer.I, layer.E, layer.k, layer.L, layer.r, block_m)
+        self.d = B.dims(layer.T, layer.H, layer.I, layer.E, layer.k, layer.L, layer.r, block_m, options)
         dev = self.device
         self.W1 = _dev_bf16(layer.W1, dev)
         self.W2 = _dev_bf16(layer.W2, dev)

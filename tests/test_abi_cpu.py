@@ -124,3 +124,15 @@ def test_no_device_is_an_error_not_a_fallback(lib):
     st = B.load().moe_lora_forward(ctypes.byref(d), f, f, f, f, f, f, None, None, None, None, f, f,
                                    B.moe_lora_workspace_bytes(d), None)
     assert st == B.MOELORA_ECUDA
+
+
+def test_pair_cta_option_plan(lib):
+    # wide chunks with the option: CTA pairs; without it, or for decode-sized
+    # chunks, one CTA per tile; unknown option bits are rejected
+    wide = B.dims(2048, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_PAIR_CTA)
+    assert B.moe_lora_workspace_layout(wide)["gemm_ctas"] == 2
+    assert B.moe_lora_workspace_layout(B.dims(2048, 2880, 2880, 32, 4, 8, 32))["gemm_ctas"] == 1
+    decode = B.dims(16, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_PAIR_CTA)
+    assert B.moe_lora_workspace_layout(decode)["gemm_ctas"] == 1
+    with pytest.raises(B.MoeLoraError):
+        B.moe_lora_workspace_layout(B.dims(16, 64, 64, 2, 1, 0, 0, 0, 2))

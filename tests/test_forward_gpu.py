@@ -21,15 +21,15 @@ from gpu_helpers import TOL, norm_err
 pytestmark = pytest.mark.gpu
 
 
-def run(layer, block_m=0):
-    dl = DeviceLayer(layer, "cuda", block_m=block_m)
+def run(layer, block_m=0, options=0):
+    dl = DeviceLayer(layer, "cuda", block_m=block_m, options=options)
     B.check(dl.forward(), "moe_lora_forward")
     st = dl.status()
     return dl, st
 
 
-def check_layer(layer, tokens=None, block_m=0, tol=TOL):
-    dl, st = run(layer, block_m)
+def check_layer(layer, tokens=None, block_m=0, tol=TOL, options=0):
+    dl, st = run(layer, block_m, options)
     assert st == 0
     got = dl.out_f64()
     ref, inv = oracle.forward(layer, tokens=tokens)
@@ -74,6 +74,11 @@ RAGGED = [
     # one expert, K split across CTAs, packed expand blocks (four adapters of
     # r = 16 per block) dealt to the splits
     (64, 1024, 2048, 1, 1, 12, 16),
+    # wide chunks on CTA pairs: no adapters, two chunks per expert
+    (300, 256, 520, 2, 2, 0, 0),
+    # CTA pairs with the down GEMM's K split into slabs, both shrinks split, and
+    # shrink items whose buckets all sit in the first CTA of the pair
+    (256, 512, 1024, 1, 1, 4, 16),
 ]
 
 
@@ -81,6 +86,38 @@ RAGGED = [
 def test_ragged_shapes(shape):
     layer = wl.make_random(*shape, seed=7)
     check_layer(layer)
+
+
+# wide chunks, the LoRA mixes the pair kernel covers (tensor-core expand with
+# r_pad 16 / 32 / 64, shrink items in one or both CTAs, shrink and down K
+# splits), ragged tiles of both GEMMs, and a mix it does not cover (CUDA-core
+# expand: the option falls back to one CTA per tile)
+PAIR_SHAPES = [
+    (300, 256, 520, 2, 2, 0, 0),
+    (256, 512, 1024, 1, 1, 4, 16),
+    (600, 128, 136, 2, 2, 5, 32),
+    (200, 264, 136, 3, 2, 6, 24),
+    (300, 96, 1032, 2, 1, 8, 64),
+    (160, 128, 96, 2, 2, 11, 8),
+    (130, 200, 48, 1, 1, 3, 32),
+]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_pair_cta_option(shape):
+    layer = wl.make_random(*shape, seed=7)
+    dl, err = check_layer(layer, options=B.MOELORA_OPT_PAIR_CTA)
+    pair = B.moe_lora_workspace_layout(dl.d)["gemm_ctas"] == 2
+    assert pair == (shape != PAIR_SHAPES[-1])
+    # same results as one CTA per tile, within rounding
+    base = check_layer(layer)[0].out_f64()
+    assert norm_err(dl.out_f64(), base) <= TOL
+
+
+@pytest.mark.slow
+def test_pair_cta_option_prefill():
+    layer = wl.make_config(2)
+    check_layer(layer, tokens=list(range(0, layer.T, 64)), options=B.MOELORA_OPT_PAIR_CTA)
 
 
 def test_config0():
