@@ -28,7 +28,6 @@ struct AlignArgs {
     int32_t* compact_ids;      // [P] pair of each compact row
     int32_t* active_experts;   // [E] or null (then the two lists below are skipped)
     int32_t* lora_buckets;     // [min(NB, P)]
-    int32_t* scan_tmp;         // [max(E, NB) + 1]
     int* hist_global;          // [16 * NB] when the histogram does not fit in shared memory, else null
     int* zero_ints;            // [n_zero] cleared for the kernels that follow (shrink counters), or null
     int n_zero;

@@ -52,7 +52,7 @@ struct Layout {
     int s1, s2, st_G, st_bn;
     long st_tasks_max;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
-        compact_ids, active_experts, lora_buckets, scan_tmp, hist, keys, st_tasks, counters, z1, z1f, xc, act, z2,
+        compact_ids, active_experts, lora_buckets, hist, keys, st_tasks, counters, z1, z1f, xc, act, z2,
         z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
     // LoRA expand on the tensor cores (zexp buffers bounded), else on CUDA cores
     bool tc_expand;
@@ -233,7 +233,6 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->compact_ids = take(sizeof(int32_t) * std::max<long>(L->P, 1));
     L->active_experts = take(sizeof(int32_t) * d->E);
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
-    L->scan_tmp = take(sizeof(int32_t) * (std::max<long>(d->E, L->NB) + 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
     L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
@@ -409,7 +408,6 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.compact_ids = at<int32_t>(ws, L.compact_ids);
     a.active_experts = at<int32_t>(ws, L.active_experts);
     a.lora_buckets = at<int32_t>(ws, L.lora_buckets);
-    a.scan_tmp = at<int32_t>(ws, L.scan_tmp);
     a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
     a.keys_in_smem = align_keys_smem_bytes(d->E, d->L, L.P) ? 1 : 0;
     a.tabs_in_smem = align_tabs_smem_bytes(d->E, d->L) ? 1 : 0;

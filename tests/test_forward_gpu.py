@@ -74,6 +74,9 @@ RAGGED = [
     # one expert, K split across CTAs, packed expand blocks (four adapters of
     # r = 16 per block) dealt to the splits
     (64, 1024, 2048, 1, 1, 12, 16),
+    # many (expert, adapter) buckets: the forward's align keeps its histogram
+    # and work lists in the workspace instead of shared memory
+    (300, 64, 64, 256, 4, 63, 8),
     # wide chunks on CTA pairs: no adapters, two chunks per expert
     (300, 256, 520, 2, 2, 0, 0),
     # CTA pairs with the down GEMM's K split into slabs, both shrinks split, and
