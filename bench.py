@@ -141,6 +141,9 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "window": window}
 
 
+HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the roofline's denominator)
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -228,6 +231,16 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         dev_s = sum(step_ms) / 1e3
+
+        # ---- beside it: the same forward with L2 left warm (no flush between steps)
+        warm = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        fwd()
+        warm[0].record(stream)
+        for _ in range(args.steps):
+            fwd()
+        warm[1].record(stream)
+        torch.cuda.synchronize()
+        warm_ms = warm[0].elapsed_time(warm[1]) / args.steps
 
         # ---- per-kernel durations: K traced forwards (events between the kernels, same stream)
         n_ev = B.MOELORA_TRACE_EVENTS
@@ -318,7 +331,9 @@ def run_ours(args, rank, world, local_rank):
                   "hbm_frac": alg["bytes"] / (ms_step * 1e-3) / 1e9 / pk["hbm_gbs"],
                   "roof_ms": max(alg["bytes"] / (pk["hbm_gbs"] * 1e9), alg["flops"] / (pk["bf16_tflops"] * 1e12)) * 1e3,
                   "tensor_tflops": alg["flops"] / (ms_step * 1e-3) / 1e12,
-                  "tensor_frac": alg["flops"] / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"]},
+                  "tensor_frac": alg["flops"] / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
+                  "hbm_frac_nominal": alg["bytes"] / (ms_step * 1e-3) / 1e9 / HBM_NOMINAL_GBS,
+                  "warm_l2_ms_per_step": warm_ms},
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": dom_gbs / pk["hbm_gbs"], "traffic": traffic,
                      "bytes_per_launch": dom_bytes, "launch_us": kern_ms[dom] * 1e3,

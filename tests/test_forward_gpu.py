@@ -358,3 +358,34 @@ def test_config4_dense(T):
     layer = wl.make_config(4, T=T)
     tokens = None if T <= 16 else list(range(0, T, 32))
     check_layer(layer, tokens=tokens)
+
+
+def _silu_probe_layer(u):
+    """One expert whose first gate unit copies feature 0 of x, whose first up
+    unit copies the constant feature 1, and whose first output copies act unit
+    0: out[t][0] = bf16(SiLU(u_t)) with every product and sum exact."""
+    T, H, I = len(u), 64, 64
+    x = np.zeros((T, H), np.float32)
+    x[:, 0] = u
+    x[:, 1] = 1.0
+    W1 = np.zeros((1, 2 * I, H), np.float32)
+    W1[0, 0, 0] = 1.0          # gate unit 0 <- x[:, 0]
+    W1[0, I, 1] = 1.0          # up unit 0 <- 1
+    W2 = np.zeros((1, H, I), np.float32)
+    W2[0, 0, 0] = 1.0          # out[:, 0] <- act unit 0
+    b = wl.bf16_bits
+    return wl.Layer("silu_probe", T, H, I, 1, 1, 0, 0, b(x), b(W1), b(W2), None, None, None, None,
+                    np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), np.full(T, -1, np.int32))
+
+
+def test_silu_sweep_against_fp64():
+    # u over [-20, 20] (bf16 values): the GPU's SiLU(u) = u / (1 + exp(-u)),
+    # rounded once to bf16, against the fp64 definition; one bf16 ulp allowed
+    u = wl.bf16_to_f32(wl.bf16_bits(np.linspace(-20.0, 20.0, 1024).astype(np.float32))).astype(np.float64)
+    dl, st = run(_silu_probe_layer(u.astype(np.float32)))
+    assert st == 0
+    got = dl.out_f64()[:, 0]
+    ref = u / (1.0 + np.exp(-u))
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+    # every other output column is exactly zero (no other unit leaks in)
+    assert np.all(dl.out_f64()[:, 1:] == 0.0)
