@@ -3,8 +3,9 @@
 // tcgen05.mma.cta_group::2 with M = 256 weight rows, the pair's two CTAs
 // holding 128 rows each, and N up to 256 pairs, each CTA holding half of the
 // pair rows.  Per unit of work a CTA stages half the pair rows of the
-// single-CTA kernel and every weight tile streams once per 256 pairs, so the
-// ring holds twice the work per byte of shared memory.
+// single-CTA kernel and every weight tile streams once per 256 pairs.  It is
+// selected by MOELORA_OPT_PAIR_CTA only: on GB300 its stages still take about
+// twice their MMA time, as in the single-CTA kernel, and it measured slower.
 //
 // Layer math ("Efficiently serve dozens of fine-tuned models with vLLM on
 // Amazon SageMaker AI and Amazon Bedrock", section "Implementing multi-LoRA
