@@ -1,11 +1,12 @@
 // moe_gemm_2sm.cu -- the grouped expert GEMMs for wide pair chunks (prefill
 // and other many-pairs-per-expert batches) on a CTA pair: one
 // tcgen05.mma.cta_group::2 with M = 256 weight rows, the pair's two CTAs
-// holding 128 rows each, and N up to 256 pairs, each CTA holding half of the
-// pair rows.  Per unit of work a CTA stages half the pair rows of the
-// single-CTA kernel and every weight tile streams once per 256 pairs.  It is
-// selected by MOELORA_OPT_PAIR_CTA only: on GB300 its stages still take about
-// twice their MMA time, as in the single-CTA kernel, and it measured slower.
+// holding 128 rows each, and N up to 128 (gate_up) or 256 (down) pairs, each
+// CTA holding half of the pair rows.  Per unit of work a CTA stages half the
+// pair rows of the single-CTA kernel.  It is selected by MOELORA_OPT_PAIR_CTA
+// only: on the prefill workload it measured no faster than the single-CTA
+// kernel (its stages move about as many shared-memory bytes per MMA, and its
+// 256-unit gate_up tiles waste more of a ragged intermediate size).
 //
 // Layer math ("Efficiently serve dozens of fine-tuned models with vLLM on
 // Amazon SageMaker AI and Amazon Bedrock", section "Implementing multi-LoRA
@@ -13,13 +14,15 @@
 //   gate_up:  g = W1[e] x + B1[l][e] z1,  act = SiLU(g[0:I]) * g[I:2I]
 //   down:     d = W2[e] act + B2[l][e] z2, pair_out = w * d
 //
-// A task is (active expert, weight tile, chunk of at most 256 pairs).  The
-// gate_up tile is 256 intermediate units: the CTA of rank q holds the gate
-// rows and the up rows of units 128q .. 128q+127 and the pair issues two MMAs
-// per K step, one into a gate and one into an up accumulator (the gate and up
-// values of a unit land in the same TMEM lane, 256 columns apart; the two
-// fill the SM's 512 columns, so there is one accumulator set).  The down tile
-// is 256 rows of W2, 128 per CTA, with two accumulator sets.  LoRA shrink items stack the A
+// A task is (active expert, weight tile, pair chunk): gate_up chunks of at
+// most 128 pairs, down chunks of at most 256.  The gate_up tile is 256
+// intermediate units: the CTA of rank q holds the gate rows and the up rows
+// of units 128q .. 128q+127 and the pair issues two MMAs per K step, one into
+// a gate and one into an up accumulator (independent chains, so one's MMA
+// latency overlaps the other's; the gate and up values of a unit land in the
+// same TMEM lane, 128 columns apart).  The down tile is 256 rows of W2, 128
+// per CTA.  Both GEMMs keep two accumulator sets of 256 columns, so one
+// task's epilogue overlaps the next task's MMAs.  LoRA shrink items stack the A
 // matrices of up to 2 * 128 / r adapter buckets on M (128 / r per CTA), and
 // the expand blocks are extra K-blocks (B rows of the chunk's adapters x
 // zexp rows), as in the single-CTA kernel.
@@ -44,19 +47,23 @@ namespace moelora {
 
 namespace {
 
-constexpr int kPairBN = 256;                     // pairs per chunk: the MMA's N
-constexpr int kHalfRows = kPairBN / 2;           // pair rows per CTA
+constexpr int kPairBN = 256;                     // most pairs in a chunk or shrink item (column staging)
 constexpr int kTmem2 = 512;                      // the whole TMEM of the SM
 constexpr int kMaxNAcc2 = 2;
+constexpr int kSub = 64 * kBK * 2;               // one 64-row box of pair rows (8 KiB)
 
 template <bool GATE_UP>
 struct Pair {
+    // pairs per chunk: gate_up 128 (its gate and up accumulators of N <= 128
+    // fill 256 columns, so two accumulator sets fit), down 256
+    static constexpr int kBN = GATE_UP ? 128 : 256;
     // weight bytes per stage: gate_up the CTA's 128 gate rows and their 128
-    // up rows, down its 128 W2 rows; then half of the pair rows
+    // up rows, down its 128 W2 rows; then this CTA's half of the pair rows
+    // in 64-row boxes
     static constexpr int kW = GATE_UP ? 2 * kATile : kATile;
-    static constexpr int kStage = kW + kHalfRows * kBK * 2;
-    static constexpr int kAccCols = GATE_UP ? 2 * kPairBN : kPairBN;  // TMEM columns per accumulator set
-    static constexpr int kNAcc = kTmem2 / kAccCols;                    // 1 (gate_up) or 2 (down)
+    static constexpr int kStage = kW + (kBN / 128) * kSub;
+    static constexpr int kAccCols = 256;             // TMEM columns per accumulator set
+    static constexpr int kNAcc = kTmem2 / kAccCols;  // 2: one task's epilogue overlaps the next task's MMAs
 };
 
 // MMA N of a chunk: pairs rounded up to 32, so each CTA holds a multiple of 16 rows
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     const int ntiles = (N_out + 255) / 256;
     const int nkb = (K + kBK - 1) / kBK;
     const int n_active = a.hdr->n_active;
-    build_task_table<kPairBN>(a, tt, n_active, ntiles);
+    build_task_table<PT::kBN>(a, tt, n_active, ntiles);
     const int ksplit = a.ksplit;
     const bool shrink = a.sh_tasks != nullptr && a.r > 0;
     const bool expand = a.tc_expand != 0 && a.r > 0;
@@ -277,7 +284,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     const int total = n_sh + tt.cum[n_active] * ksplit;
     const int t_first = (int)cluster_index(), t_step = (int)cluster_count();
     const int rp = expand_rpad(a.r);
-    const uint32_t xa1 = 128u * rp * 2u;  // one adapter's sub-tile (weight rows or pair rows)
+    const uint32_t xa1 = 128u * rp * 2u;  // one adapter's weight-row sub-tile (and down's zexp sub-tile)
+    // one adapter's zexp sub-tile (this CTA's half of the chunk's pairs)
+    const uint32_t zx1 = (uint32_t)(PT::kBN / 2) * rp * 2u;
     bool ok = true;
 
     if (warp == 0) {
@@ -329,13 +338,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                     }
                     continue;
                 }
-                Task<kPairBN> tw;
+                Task<PT::kBN> tw;
                 tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+                // this CTA's half of the chunk's pair rows (N = pairs rounded up
+                // to 32), in 64-row boxes
                 const int e = tw.e, half = n32(tw.n_real) / 2, n_box = (half + 63) / 64;
                 const int brow0 = tw.q0c + (int)rank * half;
                 // first of this CTA's 128 units (gate_up) or W2 rows (down)
                 const int wrow0 = tw.mt * 256 + (int)rank * 128;
-                const uint32_t bytes_pair = 2u * ((uint32_t)PT::kW + (uint32_t)n_box * 64 * kBK * 2);
+                const uint32_t bytes_pair = 2u * ((uint32_t)PT::kW + (uint32_t)n_box * kSub);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 ExpandRange xr;
                 xr.none();
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                     } else {
                         tma2_3d(dst, &a.wmap, bar, k0, wrow0, e);
                     }
-                    for (int g = 0; g < n_box; g++) tma2_2d(dst + PT::kW + g * 64 * kBK * 2, &a.xmap, bar, k0, brow0 + g * 64);
+                    for (int g = 0; g < n_box; g++) tma2_2d(dst + PT::kW + g * kSub, &a.xmap, bar, k0, brow0 + g * 64);
                     advance();
                 }
                 if (ok && n_x > 0 && !z_seen) {
@@ -385,7 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                         }
                     }
                     // per adapter and CTA: B rows (gate_up: gate and up sub-tiles) and zexp rows
-                    if (!acquire((uint32_t)cnt * 2u * (GATE_UP ? 3u : 2u) * xa1)) { ok = false; break; }
+                    if (!acquire((uint32_t)cnt * 2u * ((GATE_UP ? 2u : 1u) * xa1 + zx1))) { ok = false; break; }
                     uint8_t* dst = m.ring + (size_t)stage * PT::kStage;
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
 #pragma unroll
@@ -398,7 +409,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                             } else {
                                 tma2_4d(dst + q * xa1, &a.bmap1, bar, 0, wrow0, e, ids[q]);
                             }
-                            tma2_3d(dst + PT::kW + q * xa1, &a.zxmap1, bar, 0, brow0, ids[q]);
+                            tma2_3d(dst + PT::kW + q * zx1, &a.zxmap1, bar, 0, brow0, ids[q]);
                         }
                     }
                     advance();
@@ -420,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             // barriers of both CTAs.
             int stage = 0;
             uint32_t phase = 0;
-            const uint32_t xa16 = xa1 / 16;
+            const uint32_t xa16 = xa1 / 16, zx16 = zx1 / 16;
             const uint64_t d0 = umma_desc_sw128(smem_u32(m.ring));
             const uint64_t dx0 = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
             constexpr uint64_t kStage16 = PT::kStage / 16, kA16 = kATile / 16, kW16 = PT::kW / 16;
@@ -455,8 +466,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                     umma2_commit_both(&m.tfull[b]);
                     continue;
                 }
-                Task<kPairBN> tw;
+                Task<PT::kBN> tw;
                 tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+                // gate_up: a gate and an up chain per K step (independent
+                // accumulators, so one's MMA latency overlaps the other's)
                 const uint32_t idesc = umma_idesc_bf16_f32(256, n32(tw.n_real));
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
@@ -466,7 +479,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                     for (int kk = 0; kk < kBK / 16; kk++) {
                         const uint32_t acc = (kb != kb0) || (kk != 0);
                         umma2_bf16(d, da + 2 * kk, da + kW16 + 2 * kk, idesc, acc);
-                        if (GATE_UP) umma2_bf16(d + kPairBN, da + kA16 + 2 * kk, da + kW16 + 2 * kk, idesc, acc);
+                        if (GATE_UP) umma2_bf16(d + PT::kBN, da + kA16 + 2 * kk, da + kW16 + 2 * kk, idesc, acc);
                     }
                     release();
                 }
@@ -479,10 +492,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                         if (!take()) { ok = false; break; }
                         const uint64_t dxs = dx0 + (uint64_t)stage * kStage16;
                         for (int q = 0; q < cnt; q++) {
-                            const uint64_t da = dxs + q * xa16, db = dxs + kW16 + q * xa16;
+                            const uint64_t da = dxs + q * xa16, db = dxs + kW16 + q * zx16;
                             for (int kk = 0; kk < rp / 16; kk++) {
                                 umma2_bf16(d, da + 2 * kk, db + 2 * kk, idesc, 1u);
-                                if (GATE_UP) umma2_bf16(d + kPairBN, da + kA16 + 2 * kk, db + 2 * kk, idesc, 1u);
+                                if (GATE_UP) umma2_bf16(d + PT::kBN, da + kA16 + 2 * kk, db + 2 * kk, idesc, 1u);
                             }
                         }
                         release();
@@ -522,7 +535,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                 }
                 continue;
             }
-            Task<kPairBN> tw;
+            Task<PT::kBN> tw;
             tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
             const int q0c = tw.q0c, n_real = tw.n_real;
             // stage the column data while the task's MMAs run (after everyone is
@@ -541,11 +554,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             bool step_ok = got;
             if (GATE_UP) {
                 // lane = one of this CTA's 128 units; its gate values in columns
-                // 0..255 and its up values 256 columns further
+                // 0..127 and its up values 128 columns further
                 const int w_unit = tw.mt * 256 + (int)rank * 128 + qd * 32 + lane;
                 for (int c0 = half * 16; got && c0 < n_real; c0 += 32) {
                     float g[16], u[16];
-                    tmem_ld16x2(t_lane + c0, t_lane + kPairBN + c0, g, u);
+                    tmem_ld16x2(t_lane + c0, t_lane + PT::kBN + c0, g, u);
                     if (w_unit < a.I) {
 #pragma unroll
                         for (int c = 0; c < 16; c++) {

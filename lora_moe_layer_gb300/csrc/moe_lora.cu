@@ -165,20 +165,21 @@ double expected_adapters_per_chunk(const moe_lora_dims* d, long P) {
 // masks when there are adapters, no gate_up K split, a ring that fits).
 bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long avg_pairs) {
     if (d->L > 0 && (!L->tc_expand || d->L > 64)) return false;
-    const long chunks = experts_max + (L->P + 255) / 256;
-    if (d->L > 0 && chunks > kMaxChunkMasks) return false;
-    const long masks = d->L > 0 ? chunks : 0;
-    if (tc2_plan_stages(true, d->E, (int)masks) < 3 || tc2_plan_stages(false, d->E, (int)masks) < 3) return false;
+    // pair chunks: gate_up 128 pairs, down 256 (the kernel's Pair<>::kBN)
+    const long chunks_gu = experts_max + (L->P + 127) / 128, chunks_dn = experts_max + (L->P + 255) / 256;
+    if (d->L > 0 && chunks_gu > kMaxChunkMasks) return false;
+    const int masks_gu = d->L > 0 ? (int)chunks_gu : 0, masks_dn = d->L > 0 ? (int)chunks_dn : 0;
+    if (tc2_plan_stages(true, d->E, masks_gu) < 3 || tc2_plan_stages(false, d->E, masks_dn) < 3) return false;
     const long nt_gu = (d->I + 255) / 256, nt_dn = (d->H + 255) / 256;
-    const long per_expert = (avg_pairs + 255) / 256;
-    if (pick_ksplit(nt_gu * experts_max * per_expert, d->H, 76) != 1) return false;
+    if (pick_ksplit(nt_gu * experts_max * ((avg_pairs + 127) / 128), d->H, 76) != 1) return false;
     L->pair_cta = true;
     L->ranks = 2;
-    L->bn_gu = L->bn_dn = 256;
-    L->tiles_gu = nt_gu * chunks;
-    L->tiles_dn = nt_dn * chunks;
+    L->bn_gu = 128;
+    L->bn_dn = 256;
+    L->tiles_gu = nt_gu * chunks_gu;
+    L->tiles_dn = nt_dn * chunks_dn;
     L->ks_gu = 1;
-    L->ks_dn = pick_ksplit(nt_dn * experts_max * per_expert, d->I, 76);
+    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, 76);
     return true;
 }
 
@@ -633,7 +634,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
                              !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
                              !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? 128 : bn, true))))
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? bn / 2 : bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         tr.mark(2);
@@ -676,7 +677,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
                              !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
                              !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? 128 : bn, true))))
+                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? bn / 2 : bn, true))))
             return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         tr.mark(3);
