@@ -167,7 +167,7 @@ def recorded_traffic(kernel: str, workload_tag: str):
     try:
         if not files or kernel_source_hash(files) != vals.get("kernel_source_sha256"):
             return None, "kernel changed since the counters were taken"
-        return float(vals["dram_bytes_per_launch"]), path
+        return float(vals["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
     except Exception:
         return None, None
 
