@@ -91,6 +91,8 @@ struct TcArgs {
     int ksplit;                  // K-splits per weight tile (1: none)
     float* part;                 // gate_up split-K partial tiles [tiles][ksplit][acc columns][128]
     int* tile_counters;          // [tiles] split arrivals, zeroed by align
+    int* task_counter;           // next task to take (each CTA takes its next one when it is ready for
+                                 // it), zeroed by align; null: tasks dealt round-robin over the CTAs
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
 int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks);

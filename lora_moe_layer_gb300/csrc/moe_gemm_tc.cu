@@ -54,6 +54,10 @@ namespace moelora {
 
 namespace {
 
+// depth of the queue that hands the producer's task indices to the MMA and
+// epilogue roles
+constexpr int kTaskQ = 8;
+
 template <bool GATE_UP, int BN>
 struct TcShape {
     static constexpr int kAB = GATE_UP ? 2 * kATile : kATile;  // weight bytes per stage
@@ -157,8 +161,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     uint64_t* tempty = tfull + S::kNAcc;  // [kNAcc] accumulator drained by the epilogue
     uint64_t* ebar = tempty + S::kNAcc;   // epilogue rendezvous (kEpiWarps * 32 arrivals)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ebar + 1);
+    uint64_t* tq_full = reinterpret_cast<uint64_t*>(tmem_slot + 4);  // [kTaskQ] task index written
+    uint64_t* tq_empty = tq_full + kTaskQ;                            // [kTaskQ] read by the MMA thread and every epilogue warp
+    int* tq = reinterpret_cast<int*>(tq_empty + kTaskQ);              // [kTaskQ] task indices
     TaskTable tt;
-    tt.cmask = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
+    tt.cmask = reinterpret_cast<unsigned long long*>(tq + kTaskQ);
     tt.e = reinterpret_cast<int*>(tt.cmask + (a.chunk_masks ? a.max_chunks : 0));
     tt.q0 = tt.e + a.E;
     tt.m = tt.q0 + a.E;
@@ -175,6 +182,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(ebar, kEpiWarps * 32);
+        for (int q = 0; q < kTaskQ; q++) {
+            mbar_init(&tq_full[q], 1);
+            mbar_init(&tq_empty[q], 1 + kEpiWarps);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -216,10 +227,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
     const int n_lora = shrink ? a.hdr->n_lora_buckets : 0;
     const int L1 = a.L + 1;
     const int total = n_sh + tt.cum[n_active] * ksplit;
-    // tasks are dealt round-robin, so the pair chunks of one weight tile (and
-    // the tiles of one expert) stream on neighbouring CTAs at the same time and
-    // share their operands through L2
+    // Tasks are taken in order: with a task counter each CTA's producer takes
+    // the next index when it is ready for a new task (so CTAs that drew cheap
+    // tasks take more) and passes it to the MMA thread and the epilogue
+    // through the tq queue; without one they are dealt round-robin.  Either
+    // way the pair chunks of one weight tile (and the tiles of one expert)
+    // stream on neighbouring CTAs at about the same time and share their
+    // operands through L2, and every shrink item is taken before any GEMM task.
     const int t_first = blockIdx.x, t_step = gridDim.x;
+    const bool dyn = a.task_counter != nullptr;
+    // the consumers' view of task it: from the queue, or from the deal
+    auto take_task = [&](int it, bool& good) -> int {
+        if (!dyn) return t_first + it * t_step;
+        const int q = it % kTaskQ;
+        good = __all_sync(__activemask(), mbar_wait(&tq_full[q], (uint32_t)(it / kTaskQ) & 1u));
+        const int t = good ? tq[q] : total;
+        __syncwarp(__activemask());
+        // one arrival from the MMA thread and one per epilogue warp
+        if (good && (warp == 1 || lane == 0)) mbar_arrive(&tq_empty[q]);
+        return t;
+    };
     bool ok = true;
 
     if (warp == 0) {
@@ -229,7 +256,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             uint32_t phase = 0, armed = 0, last_par = 0;
             bool z_seen = false;
             int arow[kMaxSlots];
-            for (int t = t_first; t < total && ok; t += t_step) {
+            int t = t_first;
+            for (int it = 0; ok; it++) {
+                if (dyn) {
+                    const int q = it % kTaskQ;
+                    if (!mbar_wait(&tq_empty[q], ((uint32_t)(it / kTaskQ) & 1u) ^ 1u)) { ok = false; break; }
+                    t = atomicAdd(a.task_counter, 1);
+                    tq[q] = t;
+                    mbar_arrive(&tq_full[q]);  // also for the end marker t >= total
+                } else if (it > 0) {
+                    t += t_step;
+                }
+                if (t >= total) break;
                 if (t < n_sh) {
                     // shrink item: one r-row box per slot, then the pair rows
                     ShItem sh;
@@ -396,7 +434,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             const uint64_t d0 = umma_desc_sw128(smem_u32(base));
             const uint64_t dx0 = umma_desc_kmajor(smem_u32(base), expand_layout(xrp), 8u * xrp * 2u);
             constexpr uint64_t kStage16 = S::kStage / 16, kUp16 = kATile / 16, kPair16 = S::kAB / 16;
-            for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+            for (int it = 0; ok; it++) {
+                bool good = true;
+                const int t = take_task(it, good);
+                if (!good) { ok = false; break; }
+                if (t >= total) break;
                 const int b = it % S::kNAcc;
                 if (!mbar_wait(&tempty[b], ((uint32_t)(it / S::kNAcc) & 1u) ^ 1u)) { ok = false; break; }
                 tc_fence_after();
@@ -509,7 +551,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             epar ^= 1;
             return r_ok;
         };
-        for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+        for (int it = 0; ok; it++) {
+            bool good = true;
+            const int t = take_task(it, good);
+            if (!good) { ok = false; break; }
+            if (t >= total) break;
             const int b = it % S::kNAcc;
             const int use = it / S::kNAcc;  // how often this accumulator set was used before
             if (t < n_sh) {
@@ -714,7 +760,8 @@ int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expan
     const int table = 8 * mask_chunks + (4 * E + 1) * 4;
     // at least half an SM's shared memory: one CTA per SM, so a TMEM
     // allocation never waits for another CTA
-    return std::max(1024 + nstages * stage + staging + (2 * nstages + 2 * 4 + 1) * 8 + 16 + table,
+    const int queue = kTaskQ * (2 * 8 + 4);
+    return std::max(1024 + nstages * stage + staging + (2 * nstages + 2 * 4 + 1) * 8 + 16 + queue + table,
                     kTcSmemLimit / 2 + 1024);
 }
 

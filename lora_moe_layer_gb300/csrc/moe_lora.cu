@@ -237,9 +237,9 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
     L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
-    // split arrivals of the two shrinks' tasks (per CTA of a task), then the
-    // two finished-task counts
-    L->counters = take(sizeof(int32_t) * (2 * L->ranks * std::max<long>(L->st_tasks_max, 1) + 2));
+    // the two GEMMs' task counters, the split arrivals of the two shrinks'
+    // tasks (per CTA of a task), then the two finished-task counts
+    L->counters = take(sizeof(int32_t) * (2 + 2 * L->ranks * std::max<long>(L->st_tasks_max, 1) + 2));
     L->z1 = take(sizeof(float) * (size_t)(L->s1 > 1 ? L->s1 : 0) * L->P * r);
     L->z1f = take(sizeof(float) * (size_t)L->P * r);
     L->xc = take(sizeof(uint16_t) * (size_t)L->P * d->H);
@@ -415,7 +415,7 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.keys_global = a.keys_in_smem ? nullptr : at<int>(ws, L.keys);
     a.full_outputs = 0;
     a.zero_ints = at<int>(ws, L.counters);
-    a.n_zero = d->L > 0 ? (int)(2 * L.ranks * L.st_tasks_max + 2) : 0;
+    a.n_zero = 2 + (d->L > 0 ? (int)(2 * L.ranks * L.st_tasks_max + 2) : 0);
     a.st_tasks = d->L > 0 ? at<int4>(ws, L.st_tasks) : nullptr;
     a.st_G = L.st_G;
     a.st_BN = L.st_bn;
@@ -592,7 +592,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tc.hdr = hdr;
     tc.act_out = at<uint16_t>(ws, L.act);
     tc.pair_out = at<float>(ws, L.pair_out);
-    int* sh_counters = at<int>(ws, L.counters);
+    int* task_counters = at<int>(ws, L.counters);  // gate_up, down; then the shrink counters
+    int* sh_counters = task_counters + 2;
     tc.tc_expand = L.tc_expand ? 1 : 0;
     const long experts_bound = std::max<long>(1, std::min<long>(d->E, L.P));
     if (has_lora) {
@@ -608,6 +609,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     {
         const int bn = L.bn_gu;
         tc.ksplit = L.ks_gu;
+        tc.task_counter = pc ? nullptr : task_counters;
         tc.part = at<float>(ws, L.tc_part);
         tc.tile_counters = at<int>(ws, L.tc_counters);
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
@@ -652,6 +654,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     {
         const int bn = L.bn_dn;
         tc.ksplit = L.ks_dn;
+        tc.task_counter = pc ? nullptr : task_counters + 1;
         tc.tile_counters = at<int>(ws, L.tc_counters) + L.tiles_gu;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
