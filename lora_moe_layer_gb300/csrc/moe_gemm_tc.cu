@@ -23,12 +23,13 @@
 // bucket order -- on N, and each pair keeps its own slot's r rows (the cross
 // terms cost tensor time only).  K is split across items when the buckets are
 // few; the split that arrives last adds the partials in split order
-// (deterministic).  Every CTA runs its shrink items before its GEMM tasks, and
-// a GEMM epilogue reads z only after a device counter shows every shrink task
+// (deterministic).  Every shrink item is taken before any GEMM task, and a
+// GEMM epilogue reads z only after a device counter shows every shrink task
 // finished, so the shrink hides under the weight streaming instead of being a
 // launch of its own.
 //
-// Warp roles (one CTA per SM, persistent; items dealt round-robin):
+// Warp roles (one CTA per SM, persistent; items taken in order from a device
+// counter by the producer, which passes each index to the other roles):
 //   warp 0   TMA producer: per 64-wide K step, the weight tile (gate_up: the
 //            128 gate rows and the 128 matching up rows) and the pairs' rows
 //            (x or act in bucket order, 16-row boxes), all 128-byte swizzled,

@@ -112,8 +112,8 @@ int pick_ksplit(long tiles, int K, long kSms = 152) {
     return best;
 }
 
-// K-splits of a shrink.  Shrink items are dealt round-robin ahead of the GEMM
-// tasks, so when there are many shrink tasks (a quarter of the SMs or more),
+// K-splits of a shrink.  Shrink items are taken ahead of the GEMM tasks, so
+// when there are many shrink tasks (a quarter of the SMs or more),
 // unsplit items about the size of a GEMM task keep the SMs balanced and skip
 // the partial sums; with few (decode), the items are split so every SM takes a
 // small share instead of a few SMs taking whole items.  At least two 64-wide K
