@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             Task<BN> tw;
             tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
             const int e = tw.e, q0c = tw.q0c, n_real = tw.n_real, n_cols = tw.n_cols;
-            // z is complete once every shrink task has finished (they run first on every CTA)
+            // z is complete once every shrink task has finished (all are taken before any GEMM task)
             if (!z_ready && etid == 0) s_misc[0] = wait_count(a.zdone, n_sh_tasks);
             // stage this task's column data while its MMAs run (after everyone
             // is done with the previous task's)
