@@ -77,8 +77,8 @@ typedef struct moe_lora_dims {
  * than 48 pairs per expert on average) on CTA pairs (tcgen05.mma.cta_group::2,
  * 256 weight rows per task x up to 128 pairs for gate_up, 256 for down) when
  * the pair kernel covers the layer; otherwise, and by default, one CTA per
- * weight tile.  Same results within rounding; on GB300 about 1% slower than
- * the default on the GPT-OSS-20B-shaped prefill and 2% faster on the dense
+ * weight tile.  Same results within rounding; on GB300 about 5% slower than
+ * the default on the GPT-OSS-20B-shaped prefill and 1% faster on the dense
  * Llama-3.3-70B-shaped T=256 MLP. */
 #define MOELORA_OPT_PAIR_CTA 1
 
