@@ -134,5 +134,11 @@ def test_pair_cta_option_plan(lib):
     assert B.moe_lora_workspace_layout(B.dims(2048, 2880, 2880, 32, 4, 8, 32))["gemm_ctas"] == 1
     decode = B.dims(16, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_PAIR_CTA)
     assert B.moe_lora_workspace_layout(decode)["gemm_ctas"] == 1
+    # the dense T=256 MLP: 224 gate_up pair tasks (112 tiles x two 128-pair chunks) need no K split
+    dense = B.dims(256, 8192, 28672, 1, 1, 32, 64, 0, B.MOELORA_OPT_PAIR_CTA)
+    assert B.moe_lora_workspace_layout(dense)["gemm_ctas"] == 2
+    # more adapters than a chunk mask holds: the pair kernel does not cover it
+    many = B.dims(2048, 2880, 2880, 32, 4, 80, 32, 0, B.MOELORA_OPT_PAIR_CTA)
+    assert B.moe_lora_workspace_layout(many)["gemm_ctas"] == 1
     with pytest.raises(B.MoeLoraError):
         B.moe_lora_workspace_layout(B.dims(16, 64, 64, 2, 1, 0, 0, 0, 2))
