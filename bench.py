@@ -5,8 +5,9 @@
 A step is one full layer forward (align, both LoRA shrinks, gate_up with the
 fused expand and SiLU*up, down with the fused expand and top-k weight, top-k
 reduce) over one batch of the seeded synthetic workload; by default the
-GPT-OSS-20B-shaped decode layer (T=16, H=I=2880, E=32, top-4, 8 adapters of
-rank 32).  Rank 0 prints one JSON line.
+GPT-OSS-20B-shaped prefill chunk (T=2048 tokens from 16 sequences of 128,
+H=I=2880, E=32, top-4, 8 adapters of rank 32), the largest of the workloads;
+--config 1 selects the decode layer (T=16).  Rank 0 prints one JSON line.
 
 --impl ours       time the CUDA library (inputs resident in HBM), plus the
                   end-to-end call from pinned host buffers, the roofline of the
@@ -308,13 +309,23 @@ def run_ours(args, rank, world, local_rank):
     ms_step = dev_s * 1e3 / args.steps
     dom = max(("gate_up_gemm", "down_gemm"), key=lambda k: kern_ms[k])
     dom_bytes = alg["kernel_bytes"][dom]
-    dom_gbs = dom_bytes / (kern_ms[dom] * 1e-3) / 1e9
+    dom_flops = alg["kernel_flops"][dom]
+    dom_s = kern_ms[dom] * 1e-3
+    dom_gbs = dom_bytes / dom_s / 1e9
+    dom_tflops = dom_flops / dom_s / 1e12
+    # The bound: tensor when the kernel's algorithmic intensity is at least half
+    # the machine balance (measured bf16 burst peak / measured copy bandwidth,
+    # ~287 flop/B), i.e. when its flops alone take at least half as long as its
+    # bytes at peak (the prefill and dense T=256 GEMMs, gated on the tensor
+    # pipe); else HBM (decode-sized batches).  Both fractions are reported.
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tensor_bound = dom_flops / dom_bytes >= 0.5 * ridge
     tag = f"config{args.config}" + (f"_T{layer.T}" if args.config == 4 else "")
     traffic, traffic_src = recorded_traffic(dom, tag)
 
     cpu = None
     if world == 1 and not args.skip_oracle:
-        cpu = cpu_baseline(layer, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(layer, budget_s=args.cpu_seconds, warmed=parity is not None)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -334,13 +345,22 @@ def run_ours(args, rank, world, local_rank):
                   "tensor_frac": alg["flops"] / (ms_step * 1e-3) / 1e12 / pk["bf16_tflops"],
                   "hbm_frac_nominal": alg["bytes"] / (ms_step * 1e-3) / 1e9 / HBM_NOMINAL_GBS,
                   "warm_l2_ms_per_step": warm_ms},
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                     "frac": dom_gbs / pk["hbm_gbs"], "traffic": traffic,
-                     "bytes_per_launch": dom_bytes, "launch_us": kern_ms[dom] * 1e3,
-                     "tensor_frac": alg["kernel_flops"][dom] / (kern_ms[dom] * 1e-3) / 1e12 / pk["bf16_tflops"],
-                     "peak_source": pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)" if pk["source"] == "measured" else "fallback",
-                     "timed": "kernel events recorded between the kernels over K traced forwards on the launch stream",
-                     "traffic_source": traffic_src},
+        "roofline": dict(
+            {"kernel": dom, "bound": "tensor", "achieved": dom_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+             "frac": dom_tflops / pk["bf16_tflops"],
+             "peak_source": (pk["source"] + " (MEASURED_PEAKS.json bf16_tflops, cuBLAS bf16 burst)")
+             if pk["source"] == "measured" else "fallback"}
+            if tensor_bound else
+            {"kernel": dom, "bound": "hbm", "achieved": dom_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+             "frac": dom_gbs / pk["hbm_gbs"],
+             "peak_source": (pk["source"] + " (MEASURED_PEAKS.json hbm_gbs, copy)")
+             if pk["source"] == "measured" else "fallback"},
+            traffic=traffic, bytes_per_launch=dom_bytes, flops_per_launch=dom_flops, launch_us=kern_ms[dom] * 1e3,
+            hbm_gbs=dom_gbs, hbm_frac=dom_gbs / pk["hbm_gbs"], tensor_tflops=dom_tflops,
+            tensor_frac=dom_tflops / pk["bf16_tflops"], intensity_flop_per_byte=dom_flops / dom_bytes,
+            ridge_flop_per_byte=ridge,
+            timed="kernel events recorded between the kernels over K traced forwards on the launch stream",
+            traffic_source=traffic_src),
         "kernels_us": {k: v * 1e3 for k, v in kern_ms.items()},
         "traced_ms_per_step": traced_step_ms,
         "e2e": {"value": layer.T * e2e_steps / e2e_time, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -374,11 +394,13 @@ def _threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(layer, budget_s: float = 12.0):
-    """The oracle as it stands on the host cores: whole batches until ~budget_s of CPU work."""
+def cpu_baseline(layer, budget_s: float = 12.0, warmed: bool = False):
+    """The oracle as it stands on the host cores: whole batches until ~budget_s
+    of CPU work (at least one; a prefill batch takes several seconds)."""
     import oracle
     nt = _threads()
-    oracle.forward(layer, n_threads=nt)  # warm (page in weights)
+    if not warmed:
+        oracle.forward(layer, n_threads=nt)  # warm (page in weights)
     t0 = time.perf_counter()
     n = 0
     while True:
@@ -457,7 +479,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--config", type=int, default=1, help="workload index (default 1: the decode layer)")
+    ap.add_argument("--config", type=int, default=2,
+                    help="workload index (default 2: the prefill chunk; 1: the decode layer)")
     ap.add_argument("--T", type=int, default=None, help="token count for the dense workload (config 4)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)

@@ -71,6 +71,12 @@ typedef struct moe_lora_dims {
     int32_t r;       /* LoRA rank: multiple of 8 in [8, 64] if L > 0, ignored if L == 0 */
     int32_t block_m; /* 0 = default 16; otherwise a power of two in [1, 256] */
     int32_t options; /* 0, or MOELORA_OPT_PAIR_CTA */
+    int32_t sm_count; /* SMs the work is planned for (K-split and shrink-split choice, and
+                         with them the workspace size): 0 = the current device's
+                         multiprocessor count (152 on GB300; 152 when no device is
+                         visible), else a count in [1, 4096].  A workspace sized for one
+                         count serves any forward planned with the same count; the
+                         results do not depend on it. */
 } moe_lora_dims;
 
 /* Experimental: run the two GEMMs of batches with wide expert chunks (more
@@ -104,7 +110,9 @@ MOELORA_API int moe_lora_version(void);
 MOELORA_API int64_t moe_lora_align_capacity(const moe_lora_dims *d);
 
 /* Bytes of device workspace that moe_lora_forward and moe_lora_align need
- * for these dims (0 if the dims are invalid).  Host only, pure. */
+ * for these dims (0 if the dims are invalid).  Host only; with
+ * d->sm_count == 0 it reads the current device's multiprocessor count (no
+ * launch, no allocation), else it is pure. */
 MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims *d);
 
 /*
@@ -222,9 +230,12 @@ MOELORA_API int moe_lora_get_status(const void *workspace, void *stream);
  *     (two streams, or two host threads, of the same device) race on it:
  *     order them on one stream or serialise them.  No part of the buffer has
  *     to start at zero; every call rewrites what it reads.
- *   - Out-of-range expert or adapter ids are still left out of the result, but
- *     their status word lives in the shared buffer and is not reported; use
- *     moe_lora_forward with a workspace where that status matters.
+ *   - The status word lives in the shared buffer and is not reported:
+ *     out-of-range expert or adapter ids are still left out of the result, and
+ *     a kernel that gives up a bounded wait (MOELORA_ETIMEOUT with a
+ *     workspace) still leaves an incomplete output, but this call returns
+ *     MOELORA_OK for both.  Use moe_lora_forward with a workspace where that
+ *     status matters.
  */
 #define MOELORA_NOALLOC_SCRATCH_BYTES (16u << 20)
 MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims *d, const void *x,
@@ -253,11 +264,14 @@ typedef struct moe_lora_ws_layout {
     int32_t down_splits;     /* K-splits of the down GEMM (>= 1) */
     int32_t launches;        /* kernels one forward launches for these dims (T > 0) */
     int32_t gemm_ctas;       /* CTAs per GEMM task: 2 when MOELORA_OPT_PAIR_CTA took effect, else 1 */
-    int32_t reserved;
+    int32_t tc_expand;       /* 1: the LoRA expand runs as tensor-core K blocks of the base GEMMs;
+                                0: on CUDA cores in the epilogue (or no adapters) */
     size_t total;            /* == moe_lora_workspace_bytes */
 } moe_lora_ws_layout;
 
-/* Fills *out for dims d; returns a status. Host only, pure. */
+/* Fills *out for dims d; returns a status.  Host only (reads the current
+ * device's multiprocessor count when d->sm_count == 0, like
+ * moe_lora_workspace_bytes). */
 MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims *d, moe_lora_ws_layout *out);
 
 #ifdef __cplusplus

@@ -41,7 +41,8 @@ class MoeLoraError(RuntimeError):
 
 
 class moe_lora_dims(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "L", "r", "block_m", "options")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "E", "k", "L", "r", "block_m", "options",
+                                                     "sm_count")]
 
 
 class moe_lora_ws_layout(ctypes.Structure):
@@ -49,7 +50,7 @@ class moe_lora_ws_layout(ctypes.Structure):
                 ("z1", ctypes.c_size_t), ("act", ctypes.c_size_t), ("z2", ctypes.c_size_t),
                 ("pair_out", ctypes.c_size_t), ("s1", ctypes.c_int32), ("s2", ctypes.c_int32),
                 ("down_splits", ctypes.c_int32), ("launches", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("total", ctypes.c_size_t)]
+                ("tc_expand", ctypes.c_int32), ("total", ctypes.c_size_t)]
 
 
 _lib = None
@@ -104,8 +105,8 @@ MOELORA_OPT_PAIR_CTA = 1
 
 
 def dims(T: int, H: int, I: int, E: int, k: int, L: int, r: int, block_m: int = 0,
-         options: int = 0) -> moe_lora_dims:
-    return moe_lora_dims(T, H, I, E, k, L, r if L > 0 else 0, block_m, options)
+         options: int = 0, sm_count: int = 0) -> moe_lora_dims:
+    return moe_lora_dims(T, H, I, E, k, L, r if L > 0 else 0, block_m, options, sm_count)
 
 
 def _ptr(t) -> Optional[int]:

@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -41,11 +42,11 @@ CUtensorMapSwizzle expand_swizzle(int rp) {
 }
 // zexp columns: one r_pad-wide slot per adapter
 long zexp_cols(int L, int r) { return (long)L * expand_rpad_host(r); }
-constexpr int kMaxDevices = 64;
 constexpr int kMaxChunkMasks = 2048;  // 16 KiB of shared memory for the expand's chunk masks
 
 struct Layout {
     int bm;
+    int sms;  // SMs the split choices are planned for
     long P, NB, cap, tiles;
     // LoRA shrink plan: K-splits of the two shrinks, adapter buckets per task,
     // pairs per task, and the task-list bound
@@ -69,12 +70,35 @@ size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 bool is_pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
 
+constexpr int kMaxDevices = 64;
+constexpr int kFallbackSms = 152;  // GB300, when no device is visible (planning on a host without GPU)
+
+// Multiprocessor count of the current device, looked up once per device (an
+// attribute query: no context work, no allocation); kFallbackSms without one.
+int current_device_sms() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return kFallbackSms;
+    }
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+        cudaGetLastError();
+        return kFallbackSms;
+    }
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
 // host-checkable validation; returns a status
 int check_dims(const moe_lora_dims* d) {
     if (!d) return MOELORA_EINVAL;
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->L < 0) return MOELORA_EINVAL;
     if (d->block_m != 0 && (!is_pow2(d->block_m) || d->block_m > 256)) return MOELORA_EINVAL;
     if (d->options & ~MOELORA_OPT_PAIR_CTA) return MOELORA_EINVAL;
+    if (d->sm_count < 0 || d->sm_count > 4096) return MOELORA_EINVAL;
     if (d->L > 0) {
         if (d->r <= 0) return MOELORA_EINVAL;
         if (d->r % 8 != 0 || d->r > 64) return MOELORA_EUNSUPPORTED;
@@ -92,10 +116,10 @@ int check_dims(const moe_lora_dims* d) {
 }
 
 // K-splits for a GEMM whose weight tiles alone would leave SMs idle: the
-// smallest split count whose task count fills the SMs' waves to >= 90%,
-// keeping >= 512 K-elements per split.  Sized for a 152-SM GB300; on other
-// parts it only changes the balance, not the result.
-int pick_ksplit(long tiles, int K, long kSms = 152) {
+// smallest split count whose task count fills the kSms SMs' waves to >= 90%,
+// keeping >= 512 K-elements per split.  The count only changes the balance,
+// not the result.
+int pick_ksplit(long tiles, int K, long kSms) {
     if (tiles >= 2 * kSms) return 1;
     int best = 1;
     double best_eff = 0.0;
@@ -118,7 +142,7 @@ int pick_ksplit(long tiles, int K, long kSms = 152) {
 // the partial sums; with few (decode), the items are split so every SM takes a
 // small share instead of a few SMs taking whole items.  At least two 64-wide K
 // steps per split.
-int pick_shrink_split(long est_tasks, int K, long kSms = 152) {
+int pick_shrink_split(long est_tasks, int K, long kSms) {
     const int nkb = (K + 63) / 64;
     if (est_tasks * 4 >= kSms) return 1;
     const long want = (kSms + std::max<long>(est_tasks, 1) - 1) / std::max<long>(est_tasks, 1);
@@ -143,7 +167,7 @@ void plan_shrinks(const moe_lora_dims* d, Layout* L) {
     // an item's pairs fit one TMEM accumulator buffer of both GEMM kernels
     L->st_bn = L->pair_cta ? 256 : std::min(2 * L->bn_gu, L->bn_dn);
     const long est_tasks = est_groups * ((rows_per_group + L->st_bn - 1) / L->st_bn);
-    const long slots = 152 / L->ranks;
+    const long slots = std::max(1, L->sms / L->ranks);
     L->s1 = pick_shrink_split(est_tasks, d->H, slots);
     L->s2 = pick_shrink_split(est_tasks, d->I, slots);
     L->st_tasks_max = (L->nbl + L->st_G - 1) / L->st_G + (L->P + L->st_bn - 1) / L->st_bn;
@@ -171,7 +195,8 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     const int masks_gu = d->L > 0 ? (int)chunks_gu : 0, masks_dn = d->L > 0 ? (int)chunks_dn : 0;
     if (tc2_plan_stages(true, d->E, masks_gu) < 3 || tc2_plan_stages(false, d->E, masks_dn) < 3) return false;
     const long nt_gu = (d->I + 255) / 256, nt_dn = (d->H + 255) / 256;
-    if (pick_ksplit(nt_gu * experts_max * ((avg_pairs + 127) / 128), d->H, 76) != 1) return false;
+    const long pairs = std::max(1, L->sms / 2);
+    if (pick_ksplit(nt_gu * experts_max * ((avg_pairs + 127) / 128), d->H, pairs) != 1) return false;
     L->pair_cta = true;
     L->ranks = 2;
     L->bn_gu = 128;
@@ -179,7 +204,7 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     L->tiles_gu = nt_gu * chunks_gu;
     L->tiles_dn = nt_dn * chunks_dn;
     L->ks_gu = 1;
-    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, 76);
+    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, pairs);
     return true;
 }
 
@@ -199,14 +224,15 @@ void plan_gemms(const moe_lora_dims* d, Layout* L) {
     // expected counts with the pairs spread evenly, for the split choice
     const long est_gu = nt_gu * experts_max * ((avg_pairs + L->bn_gu - 1) / L->bn_gu);
     const long est_dn = nt_dn * experts_max * ((avg_pairs + L->bn_dn - 1) / L->bn_dn);
-    L->ks_gu = pick_ksplit(est_gu, d->H);
-    L->ks_dn = pick_ksplit(est_dn, d->I);
+    L->ks_gu = pick_ksplit(est_gu, d->H, L->sms);
+    L->ks_dn = pick_ksplit(est_dn, d->I, L->sms);
 }
 
 int make_layout(const moe_lora_dims* d, Layout* L) {
     const int st = check_dims(d);
     if (st != MOELORA_OK) return st;
     L->bm = d->block_m ? d->block_m : kDefaultBlockM;
+    L->sms = d->sm_count > 0 ? d->sm_count : current_device_sms();
     L->P = (long)d->T * d->k;
     L->NB = (long)d->E * (d->L + 1);
     L->cap = L->P + std::min(L->NB, L->P) * (L->bm - 1);
@@ -475,7 +501,7 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     out->down_splits = std::max(1, L.ks_dn);
     out->launches = 5;  // align, gather, gate_up, down, reduce
     out->gemm_ctas = L.ranks;
-    out->reserved = 0;
+    out->tc_expand = L.tc_expand ? 1 : 0;
     out->total = L.total;
     return MOELORA_OK;
 }

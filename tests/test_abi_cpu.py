@@ -77,6 +77,34 @@ def test_layout_of_split_and_expand_workloads(lib):
     assert lay["pair_out"] + 4 * 256 * 8192 * lay["down_splits"] <= lay["total"]
 
 
+def test_split_plan_follows_the_sm_count(lib):
+    """K-split and shrink-split choices are planned for dims.sm_count SMs (0:
+    the current device's count; 152, a GB300, with no device visible): fewer
+    SMs need fewer splits to fill their waves, more need more.  Each count's
+    workspace holds its own plan's regions."""
+    def lay(sms, *shape):
+        d = B.dims(*shape, sm_count=sms)
+        out = B.moe_lora_workspace_layout(d)
+        assert out["total"] == B.moe_lora_workspace_bytes(d)
+        return out
+
+    decode = (16, 2880, 2880, 32, 4, 8, 32)
+    dense = (256, 8192, 28672, 1, 1, 32, 64)
+    s = {n: lay(n, *decode) for n in (1, 38, 76, 152, 304)}
+    assert s[1]["s1"] == s[1]["s2"] == 1
+    assert s[1]["s1"] <= s[38]["s1"] <= s[76]["s1"] <= s[152]["s1"] <= s[304]["s1"]
+    assert s[76]["s1"] < s[152]["s1"] < s[304]["s1"]
+    dn = {n: lay(n, *dense)["down_splits"] for n in (1, 38, 152)}
+    assert dn[1] == 1 and 1 < dn[38] < dn[152] <= 8
+    for n in (1, 38, 76, 152, 304):
+        L = lay(n, *dense)
+        assert L["pair_out"] + 4 * 256 * 8192 * L["down_splits"] <= L["total"]
+        L = lay(n, *decode)
+        assert L["pair_out"] + 4 * 64 * 2880 * L["down_splits"] <= L["total"]
+    assert B.moe_lora_workspace_bytes(B.dims(*decode, sm_count=-1)) == 0
+    assert B.moe_lora_workspace_bytes(B.dims(*decode, sm_count=5000)) == 0
+
+
 @pytest.mark.parametrize("bad", [
     dict(H=0), dict(E=0), dict(k=0), dict(T=-1), dict(L=-1), dict(block_m=3), dict(block_m=512),
 ])
@@ -142,3 +170,19 @@ def test_pair_cta_option_plan(lib):
     assert B.moe_lora_workspace_layout(many)["gemm_ctas"] == 1
     with pytest.raises(B.MoeLoraError):
         B.moe_lora_workspace_layout(B.dims(16, 64, 64, 2, 1, 0, 0, 0, 2))
+
+
+def test_noalloc_refuses_oversized_problems_on_the_host(lib):
+    """moe_lora_forward_noalloc checks the problem against its built-in scratch
+    size before touching the GPU: a workspace one token over the limit is
+    refused with ENOSPC, also on a host without a device."""
+    shape = (520, 200, 5, 3, 3, 24)
+    lim = B.MOELORA_NOALLOC_SCRATCH_BYTES
+    T = 1
+    while B.moe_lora_workspace_bytes(B.dims(T * 2, *shape)) <= lim:
+        T *= 2
+    while B.moe_lora_workspace_bytes(B.dims(T + 1, *shape)) <= lim:
+        T += 1
+    f = 1 << 20  # never dereferenced; stream 0 (no torch stream on a host without a device)
+    st = B.moe_lora_forward_noalloc(B.dims(T + 1, *shape), f, f, f, f, f, f, f, f, f, f, f, stream=0)
+    assert st == B.MOELORA_ENOSPC

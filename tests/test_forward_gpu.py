@@ -119,8 +119,8 @@ def test_pair_cta_option(shape):
 
 @pytest.mark.slow
 def test_pair_cta_option_prefill():
-    layer = wl.make_config(2)
-    check_layer(layer, tokens=list(range(0, layer.T, 64)), options=B.MOELORA_OPT_PAIR_CTA)
+    # every output of the prefill chunk (wide chunks, K-split slabs, expand blocks)
+    check_layer(wl.make_config(2), options=B.MOELORA_OPT_PAIR_CTA)
 
 
 def test_config0():
@@ -280,6 +280,34 @@ def test_all_pairs_on_one_expert_and_all_base_only():
     check_layer(dataclasses.replace(layer, lora_ids=np.full(50, -1, np.int32)))
 
 
+@pytest.mark.parametrize("adapters", [False, True])
+def test_duplicate_experts_in_one_tokens_top_k(adapters):
+    """A token may name the same expert in several of its top-k slots (a
+    router cannot produce it, but the input format allows it): each slot is a
+    pair of its own, computed and weighted separately.  Mixed duplicates
+    (two and three slots), all-duplicate tokens, with and without adapters
+    (the same (expert, adapter) bucket then holds several pairs of one token)."""
+    layer = wl.make_random(48, 264, 136, 6, 4, 3 if adapters else 0, 16 if adapters else 0, seed=31)
+    tk = layer.topk_ids.copy()
+    tk[0] = [2, 2, 2, 2]
+    tk[1] = [5, 1, 5, 1]
+    tk[7] = [3, 3, 0, 4]
+    tk[20:30, 1] = tk[20:30, 0]
+    tk[40:, :] = 1
+    lo = layer.lora_ids.copy()
+    if not adapters:
+        lo[:] = -1
+    dup = dataclasses.replace(layer, topk_ids=tk, lora_ids=lo)
+    dl, err = check_layer(dup)
+    # a token whose k slots name one expert equals that expert's FFN scaled by
+    # the sum of its weights: check it against the oracle on one slot of weight 1
+    one = dataclasses.replace(dup, T=1, k=1, x=dup.x[:1], topk_ids=np.array([[2]], np.int32),
+                              topk_weights=np.array([[float(dup.topk_weights[0].sum())]], np.float32),
+                              lora_ids=dup.lora_ids[:1])
+    ref_one, _ = oracle.forward(one)
+    assert norm_err(dl.out_f64()[:1], ref_one) <= TOL
+
+
 def test_no_adapters_null_pointers():
     layer = wl.make_random(12, 64, 64, 4, 2, 0, 0, seed=2)
     assert layer.A1 is None
@@ -338,11 +366,10 @@ def test_intermediates_config1(config1):
 
 
 @pytest.mark.slow
-def test_config2_prefill_sampled():
-    layer = wl.make_config(2)
-    # two tokens of every 128-token sequence, first and last
-    tokens = sorted({s * 128 + o for s in range(16) for o in (0, 127)})
-    check_layer(layer, tokens=tokens)
+def test_config2_prefill_full():
+    # all 2048 x 2880 outputs: 128- and 256-pair chunks, each expert's last
+    # partial chunk, the tensor-core expand blocks of every adapter mix
+    check_layer(wl.make_config(2))
 
 
 @pytest.mark.slow
@@ -355,15 +382,17 @@ def test_config3_mixed_full():
 @pytest.mark.slow
 @pytest.mark.parametrize("T", [1, 16, 256])
 def test_config4_dense(T):
-    layer = wl.make_config(4, T=T)
-    tokens = None if T <= 16 else list(range(0, T, 32))
-    check_layer(layer, tokens=tokens)
+    check_layer(wl.make_config(4, T=T))
 
 
-def _silu_probe_layer(u):
+def _silu_probe_layer(u, adapters: bool):
     """One expert whose first gate unit copies feature 0 of x, whose first up
     unit copies the constant feature 1, and whose first output copies act unit
-    0: out[t][0] = bf16(SiLU(u_t)) with every product and sum exact."""
+    0: out[t][0] = bf16(SiLU(u_t)) with every product and sum exact.  With
+    `adapters`, every token carries adapter 0 of a rank-8 LoRA whose A and B
+    are zero: its delta adds exact zeros, and with one adapter per expert
+    chunk the expand runs on CUDA cores, so the activation goes through that
+    epilogue instead of the lean one."""
     T, H, I = len(u), 64, 64
     x = np.zeros((T, H), np.float32)
     x[:, 0] = u
@@ -374,18 +403,40 @@ def _silu_probe_layer(u):
     W2 = np.zeros((1, H, I), np.float32)
     W2[0, 0, 0] = 1.0          # out[:, 0] <- act unit 0
     b = wl.bf16_bits
-    return wl.Layer("silu_probe", T, H, I, 1, 1, 0, 0, b(x), b(W1), b(W2), None, None, None, None,
-                    np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), np.full(T, -1, np.int32))
+    L, r = (1, 8) if adapters else (0, 0)
+    A1 = B1 = A2 = B2 = None
+    if adapters:
+        A1 = np.zeros((L, 1, r, H), np.uint16)
+        B1 = np.zeros((L, 1, 2 * I, r), np.uint16)
+        A2 = np.zeros((L, 1, r, I), np.uint16)
+        B2 = np.zeros((L, 1, H, r), np.uint16)
+    lora = np.zeros(T, np.int32) if adapters else np.full(T, -1, np.int32)
+    return wl.Layer("silu_probe", T, H, I, 1, 1, L, r, b(x), b(W1), b(W2), A1, B1, A2, B2,
+                    np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), lora)
 
 
-def test_silu_sweep_against_fp64():
-    # u over [-20, 20] (bf16 values): the GPU's SiLU(u) = u / (1 + exp(-u)),
-    # rounded once to bf16, against the fp64 definition; one bf16 ulp allowed
-    u = wl.bf16_to_f32(wl.bf16_bits(np.linspace(-20.0, 20.0, 1024).astype(np.float32))).astype(np.float64)
-    dl, st = run(_silu_probe_layer(u.astype(np.float32)))
+@pytest.mark.parametrize("epilogue", ["lean", "cuda_core_expand"])
+def test_silu_sweep_against_fp64(epilogue):
+    """The GPU's SiLU(u) = u / (1 + exp(-u)), rounded once to bf16, against the
+    fp64 definition over every bf16 value of u in [-120, 120] on a grid, in
+    both epilogues that compute it: the lean one (no CUDA-core expand, fast
+    exponential and division) and the one that adds the LoRA expand on CUDA
+    cores.  Past |u| ~ 88 the exponential of -u leaves the fp32 range
+    (overflow to infinity for u < 0, underflow to zero for u > 0): SiLU must
+    then give 0 (at most 1e-30 away from the true, tiny value) or u itself.
+    One bf16 ulp (2^-8 relative) is allowed elsewhere."""
+    grid = np.concatenate([np.linspace(-120.0, 120.0, 3001), [-88.7, -88.0, -87.3, 87.3, 88.0, 88.7]])
+    u = np.unique(wl.bf16_to_f32(wl.bf16_bits(grid.astype(np.float32))).astype(np.float64))
+    dl, st = run(_silu_probe_layer(u.astype(np.float32), adapters=epilogue != "lean"))
     assert st == 0
+    lay = B.moe_lora_workspace_layout(dl.d)
+    assert lay["tc_expand"] == 0
     got = dl.out_f64()[:, 0]
     ref = u / (1.0 + np.exp(-u))
+    assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+    # saturated ends: exactly u for large positive u, zero for large negative u
+    assert np.all(got[u >= 90.0] == u[u >= 90.0])
+    assert np.all(got[u <= -104.0] == 0.0)
     # every other output column is exactly zero (no other unit leaks in)
     assert np.all(dl.out_f64()[:, 1:] == 0.0)

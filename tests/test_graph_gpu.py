@@ -1,10 +1,16 @@
 """The forward is asynchronous on its stream and capturable in a CUDA graph:
 captured once, replayed on new inputs written into the same buffers, it gives
 bit-for-bit the output of eager calls (the kernels read every size and count
-from the device, so one capture serves any routing of the same shape)."""
+from the device, so one capture serves any routing of the same shape), and
+each replayed output matches the fp64 oracle of the routing it was given."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
+
+import oracle
+from gpu_helpers import TOL, norm_err
 
 from lora_moe_layer_gb300 import binding as B
 from lora_moe_layer_gb300 import workloads as wl
@@ -45,6 +51,8 @@ def test_graph_replay_matches_eager(which):
     torch.cuda.synchronize()
     assert dl.status() == 0
     assert torch.equal(dl.out.view(torch.int16), ref1.view(torch.int16))
+    want1, inv = oracle.forward(layer)
+    assert inv == 0 and norm_err(dl.out_f64(), want1) <= TOL
 
     # new tokens and routing copied into the same buffers: the replay follows them
     dev = dl.x.device
@@ -57,4 +65,9 @@ def test_graph_replay_matches_eager(which):
     dl.out.zero_()
     graph.replay()
     torch.cuda.synchronize()
+    assert dl.status() == 0
     assert torch.equal(dl.out.view(torch.int16), ref2.view(torch.int16))
+    # the second routing with the first layer's weights (only x and the routing were copied in)
+    want2, inv = oracle.forward(dataclasses.replace(layer, x=other.x, topk_ids=other.topk_ids,
+                                                    topk_weights=other.topk_weights, lora_ids=other.lora_ids))
+    assert inv == 0 and norm_err(dl.out_f64(), want2) <= TOL

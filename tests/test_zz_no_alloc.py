@@ -45,6 +45,44 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row():
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 
 
+def _largest_fitting_T(shape):
+    """The largest token count whose workspace still fits the built-in scratch
+    (host-only size queries: the layout grows with T)."""
+    lim = B.MOELORA_NOALLOC_SCRATCH_BYTES
+    lo, hi = 1, 1 << 17
+    assert B.moe_lora_workspace_bytes(B.dims(lo, *shape)) <= lim < B.moe_lora_workspace_bytes(B.dims(hi, *shape))
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if B.moe_lora_workspace_bytes(B.dims(mid, *shape)) <= lim:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def test_noalloc_at_the_edge_of_its_scratch():
+    """A problem whose workspace takes all but a few KiB of the scratch buffer,
+    so its last regions (split-K partials and counters) sit at the end of it,
+    matches moe_lora_forward bit for bit; one more token does not fit and is
+    refused before any launch."""
+    shape = (520, 200, 5, 3, 3, 24)
+    T = _largest_fitting_T(shape)
+    need = B.moe_lora_workspace_bytes(B.dims(T, *shape))
+    assert need > B.MOELORA_NOALLOC_SCRATCH_BYTES - (64 << 10)
+    layer = wl.make_random(T, *shape, seed=12)
+    dl = DeviceLayer(layer, "cuda")
+    B.check(dl.forward(), "moe_lora_forward")
+    ref = dl.out.clone()
+    out = torch.full_like(dl.out, float("nan"))
+    for _ in range(2):
+        B.check(_noalloc(dl, out), "moe_lora_forward_noalloc")
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    d = B.dims(T + 1, *shape)
+    f = 1 << 20  # never dereferenced: the call returns before any launch
+    assert B.moe_lora_forward_noalloc(d, f, f, f, f, f, f, f, f, f, f, f) == B.MOELORA_ENOSPC
+
+
 def test_noalloc_refuses_problems_larger_than_its_scratch():
     d = B.dims(2048, 2880, 2880, 32, 4, 8, 32)
     assert B.moe_lora_workspace_bytes(d) > B.MOELORA_NOALLOC_SCRATCH_BYTES
