@@ -70,7 +70,7 @@ typedef struct moe_lora_dims {
     int32_t L;       /* adapters, >= 0 (0: no LoRA; A and B pointers may be NULL) */
     int32_t r;       /* LoRA rank: multiple of 8 in [8, 64] if L > 0, ignored if L == 0 */
     int32_t block_m; /* 0 = default 16; otherwise a power of two in [1, 256] */
-    int32_t options; /* 0, or MOELORA_OPT_PAIR_CTA */
+    int32_t options; /* 0, or MOELORA_OPT_SINGLE_CTA */
     int32_t sm_count; /* SMs the work is planned for (K-split and shrink-split choice, and
                          with them the workspace size): 0 = the current device's
                          multiprocessor count (152 on GB300; 152 when no device is
@@ -79,14 +79,15 @@ typedef struct moe_lora_dims {
                          results do not depend on it. */
 } moe_lora_dims;
 
-/* Experimental: run the two GEMMs of batches with wide expert chunks (more
- * than 48 pairs per expert on average) on CTA pairs (tcgen05.mma.cta_group::2,
- * 256 weight rows per task x up to 128 pairs for gate_up, 256 for down) when
- * the pair kernel covers the layer; otherwise, and by default, one CTA per
- * weight tile.  Same results within rounding; on GB300 about 5% slower than
- * the default on the GPT-OSS-20B-shaped prefill and 1% faster on the dense
- * Llama-3.3-70B-shaped T=256 MLP. */
-#define MOELORA_OPT_PAIR_CTA 1
+/* Batches with wide expert chunks (more than 48 pairs per expert on average)
+ * run their two GEMMs on CTA pairs by default: tcgen05.mma.cta_group::2 with
+ * 256 pair rows on M (128 per CTA) and two chains of up to 256 weight rows on
+ * N, when that kernel covers the layer (at most 64 adapters, the tensor-core
+ * LoRA expand, its per-chunk adapter masks and zexp buffers within bounds).
+ * MOELORA_OPT_SINGLE_CTA keeps them on the one-CTA kernel (one tile of 128
+ * weight rows per task), the path every other batch takes: same results
+ * within rounding, for comparison and testing. */
+#define MOELORA_OPT_SINGLE_CTA 1
 
 /* Status codes (return values; moe_lora_strerror gives a message). */
 #define MOELORA_OK 0
@@ -263,7 +264,7 @@ typedef struct moe_lora_ws_layout {
     int32_t s1, s2;          /* K-split counts the two shrinks used */
     int32_t down_splits;     /* K-splits of the down GEMM (>= 1) */
     int32_t launches;        /* kernels one forward launches for these dims (T > 0) */
-    int32_t gemm_ctas;       /* CTAs per GEMM task: 2 when MOELORA_OPT_PAIR_CTA took effect, else 1 */
+    int32_t gemm_ctas;       /* CTAs per GEMM task: 2 on the CTA-pair kernel (wide chunks), else 1 */
     int32_t tc_expand;       /* 1: the LoRA expand runs as tensor-core K blocks of the base GEMMs;
                                 0: on CUDA cores in the epilogue (or no adapters) */
     size_t total;            /* == moe_lora_workspace_bytes */

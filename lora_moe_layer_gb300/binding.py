@@ -101,7 +101,7 @@ def load(path: Optional[str] = None):
 
 # ---------------------------------------------------------------- marshalling
 
-MOELORA_OPT_PAIR_CTA = 1
+MOELORA_OPT_SINGLE_CTA = 1
 
 
 def dims(T: int, H: int, I: int, E: int, k: int, L: int, r: int, block_m: int = 0,

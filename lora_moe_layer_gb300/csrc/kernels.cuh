@@ -93,16 +93,17 @@ struct TcArgs {
     int* tile_counters;          // [tiles] split arrivals, zeroed by align
     int* task_counter;           // next task to take (each CTA takes its next one when it is ready for
                                  // it), zeroed by align; null: tasks dealt round-robin over the CTAs
+    int nu;                      // CTA-pair kernel: weight rows per MMA chain (multiple of 16, <= 256)
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
 int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks);
 cudaError_t init_tc_attributes();
 cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int grid, cudaStream_t stream, bool pdl);
 // The same GEMMs for wide pair chunks on CTA pairs (moe_gemm_2sm.cu): M = 256
-// weight rows over the pair, chunks of up to 256 pairs, tensor-core expand
-// only, chunk masks required, gate_up without K split.
-int tc2_smem_bytes(bool gate_up, int E, int nstages, int max_chunks);
-int tc2_plan_stages(bool gate_up, int E, int max_chunks);
+// pair rows over the pair (chunks of up to 256 pairs), two chains of nu weight
+// rows, tensor-core expand only, chunk masks required, gate_up without K split.
+int tc2_smem_bytes(int E, int nstages, int max_chunks);
+int tc2_plan_stages(int E, int max_chunks);
 cudaError_t init_tc2_attributes();
 int tc2_max_pairs(bool gate_up);  // co-resident pairs (0: none or query failed)
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl);

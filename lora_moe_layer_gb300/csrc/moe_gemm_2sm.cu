@@ -1,12 +1,9 @@
 // moe_gemm_2sm.cu -- the grouped expert GEMMs for wide pair chunks (prefill
-// and other many-pairs-per-expert batches) on a CTA pair: one
-// tcgen05.mma.cta_group::2 with M = 256 weight rows, the pair's two CTAs
-// holding 128 rows each, and N up to 128 (gate_up) or 256 (down) pairs, each
-// CTA holding half of the pair rows.  Per unit of work a CTA stages half the
-// pair rows of the single-CTA kernel.  It is selected by MOELORA_OPT_PAIR_CTA
-// only: on the prefill workload it measured no faster than the single-CTA
-// kernel (its stages move about as many shared-memory bytes per MMA, and its
-// 256-unit gate_up tiles waste more of a ragged intermediate size).
+// and other batches with many pairs per expert) on CTA pairs, with the pairs
+// on the MMA's M side: one tcgen05.mma.cta_group::2 multiplies 256 pair rows
+// (128 in each CTA of the pair) by up to 256 weight rows (half of them in each
+// CTA's shared memory), and every CTA's tensor memory receives its own 128
+// pairs x all of the weight rows.
 //
 // Layer math ("Efficiently serve dozens of fine-tuned models with vLLM on
 // Amazon SageMaker AI and Amazon Bedrock", section "Implementing multi-LoRA
@@ -14,60 +11,66 @@
 //   gate_up:  g = W1[e] x + B1[l][e] z1,  act = SiLU(g[0:I]) * g[I:2I]
 //   down:     d = W2[e] act + B2[l][e] z2, pair_out = w * d
 //
-// A task is (active expert, weight tile, pair chunk): gate_up chunks of at
-// most 128 pairs, down chunks of at most 256.  The gate_up tile is 256
-// intermediate units: the CTA of rank q holds the gate rows and the up rows
-// of units 128q .. 128q+127 and the pair issues two MMAs per K step, one into
-// a gate and one into an up accumulator (independent chains, so one's MMA
-// latency overlaps the other's; the gate and up values of a unit land in the
-// same TMEM lane, 128 columns apart).  The down tile is 256 rows of W2, 128
-// per CTA.  Both GEMMs keep two accumulator sets of 256 columns, so one
-// task's epilogue overlaps the next task's MMAs.  LoRA shrink items stack the A
-// matrices of up to 2 * 128 / r adapter buckets on M (128 / r per CTA), and
-// the expand blocks are extra K-blocks (B rows of the chunk's adapters x
-// zexp rows), as in the single-CTA kernel.
+// Why this orientation.  On GB300 a ring stage of TMA copies costs about the
+// same few hundred cycles whatever its size up to 64 KiB, so a wide-chunk
+// GEMM is bound by its copies per MAC, not by the tensor pipe.  Here a task is
+// (active expert, tile of weight rows, chunk of up to 256 pairs) and each K
+// step issues two independent MMA chains of N = nu weight rows each: gate_up
+// chain 0 the gate rows and chain 1 the up rows of nu intermediate units,
+// down chain 0 and chain 1 two consecutive ranges of nu W2 rows.  Per K step
+// a CTA copies its 128 pair rows and nu/2 rows of each chain (three boxes,
+// at most 48 KiB) for 2 x 128 x nu x 64 MACs: twice the MACs per copied byte
+// of a one-CTA tile of 128 weight rows.  Two independent chains keep the
+// tensor pipe at its rate (one chain alone leaves gaps between dependent
+// MMAs).  The two chains fill the 512 columns of tensor memory, so a task's
+// epilogue does not overlap the next task's MMAs; it is short because each
+// epilogue thread owns one pair and writes whole runs of its output row.
 //
-// Roles, in each CTA of the pair (one pair per two SMs, persistent, tasks
-// dealt round-robin over the pairs):
-//   warp 0   TMA producer for this CTA's halves of every stage; the copies
-//            of both CTAs count on the leader's (rank 0) full barrier
-//            (.cta_group::2 copies), which the leader arms with both byte
-//            counts;
-//   warp 1   allocates TMEM (collectively with the peer); in the leader one
-//            thread issues every MMA of the pair and commits stage releases
-//            and accumulator completion to both CTAs' mbarriers;
-//   warps 2-9 epilogue of this CTA's 128 TMEM lanes; the peer's epilogue
-//            warps free an accumulator set on the leader's mbarrier.
-// Every wait is bounded; on a timeout the CTA records kStatusTimeout, keeps
-// walking its loops without waiting (so its peer is never left waiting on
-// it), drains its copies, frees TMEM and exits.
+// gate_up puts a unit's gate value and its up value in the same thread (the
+// same pair's TMEM lane, 256 columns apart), so SiLU(gate) * up is local.
+//
+// LoRA, in the same orientation:
+//   shrink items (the blog's shrink, section "Kernel optimizations"): the A
+//     matrices of 256 / r consecutive (expert, adapter) buckets stacked on N
+//     (r rows each, half of the buckets in each CTA) against the pair rows of
+//     those buckets on M; each pair keeps the r columns of its own bucket.
+//     Items are taken before every GEMM task; split over K when they are few
+//     (the split that arrives last adds the partials in split order).
+//   expand (the blog's fused LoRA add): extra K blocks of the base GEMM into
+//     the same accumulators, A = zexp rows (each pair's z under its own
+//     adapter's slot, zeros under the others) and B = the adapters' B rows of
+//     the task's weight tile; a block holds 64 / r_pad consecutive adapters,
+//     and only blocks with an adapter present in the chunk are issued.
+//
+// Roles in each CTA of the pair (one pair per two SMs, persistent, tasks
+// dealt round-robin over the pairs, shrink items first):
+//   warp 0   TMA producer of this CTA's halves of every stage; the copies of
+//            both CTAs count on the leader's (rank 0) full barrier, which the
+//            leader arms with both byte counts;
+//   warp 1   allocates the 512 TMEM columns (collectively with the peer); in
+//            the leader one thread issues every MMA of the pair and commits
+//            stage releases and accumulator completion to both CTAs;
+//   warps 2-9 epilogue of this CTA's 128 TMEM lanes (= pairs); the peer's
+//            warps free the accumulator on the leader's barrier.
+// Every wait is bounded; on a timeout the CTA records kStatusTimeout, stops
+// waiting, drains its copies, frees TMEM and exits at the final pair barrier.
 #include "gemm_tasks.cuh"
 
 namespace moelora {
 
 namespace {
 
-constexpr int kPairBN = 256;                     // most pairs in a chunk or shrink item (column staging)
-constexpr int kTmem2 = 512;                      // the whole TMEM of the SM
-constexpr int kMaxNAcc2 = 2;
-constexpr int kSub = 64 * kBK * 2;               // one 64-row box of pair rows (8 KiB)
-
-template <bool GATE_UP>
-struct Pair {
-    // pairs per chunk: gate_up 128 (its gate and up accumulators of N <= 128
-    // fill 256 columns, so two accumulator sets fit), down 256
-    static constexpr int kBN = GATE_UP ? 128 : 256;
-    // weight bytes per stage: gate_up the CTA's 128 gate rows and their 128
-    // up rows, down its 128 W2 rows; then this CTA's half of the pair rows
-    // in 64-row boxes
-    static constexpr int kW = GATE_UP ? 2 * kATile : kATile;
-    static constexpr int kStage = kW + (kBN / 128) * kSub;
-    static constexpr int kAccCols = 256;             // TMEM columns per accumulator set
-    static constexpr int kNAcc = kTmem2 / kAccCols;  // 2: one task's epilogue overlaps the next task's MMAs
-};
-
-// MMA N of a chunk: pairs rounded up to 32, so each CTA holds a multiple of 16 rows
-__device__ __forceinline__ int n32(int n_real) { return (n_real + 31) & ~31; }
+constexpr int kPairRows = 256;                  // pairs per chunk (M of one MMA over the pair)
+constexpr int kTmem2 = 512;                     // the whole TMEM of the SM: one accumulator set
+constexpr int kChain1Col = 256;                 // first TMEM column of chain 1
+constexpr int kSlot = 128 * kBK * 2;            // 16 KiB: 128 rows of one 64-wide K step
+constexpr int kStage2 = 3 * kSlot;              // pair rows, chain-0 rows, chain-1 rows
+constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
+// down epilogue: each warp turns its 32 pairs x 16 columns into whole
+// 64-byte runs of 8 rows per store through a padded tile (row stride of 20
+// floats: the 8 rows of a quarter-warp hit distinct banks)
+constexpr int kTrStride = 20;
+constexpr int kTrFloats = 32 * kTrStride;
 
 // ---------------------------------------------------------------- CTA pair
 __device__ __forceinline__ uint32_t cta_rank() {
@@ -181,44 +184,179 @@ __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
         : "memory");
 }
 
-// Shared memory after the stage ring: column staging, verdicts, barriers,
-// the TMEM base and the task table.
+// 8 consecutive 32-bit columns of this thread's TMEM lane (warp-wide)
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// two fp32 -> two bf16 (round to nearest even) packed low, high: one cvt
+// instruction (its first source goes to the upper half)
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Shared memory after the stage ring: barriers, the TMEM base, shrink-slot
+// tables and the task table.
 struct Smem2 {
     uint8_t* ring;
-    int* s_pair;      // [kPairBN] pair id of each column (shrink items: slot column ranges)
-    int* s_lora;      // [kPairBN]
-    float* s_w;       // [kPairBN] top-k weight of each column
-    int* s_misc;      // [kMisc]
     uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed
     uint64_t* empty;  // [NS] the pair's MMAs are done with stage s
-    uint64_t* tfull;  // [kNAcc] accumulator set ready for the epilogue
-    uint64_t* tempty; // [kNAcc] leader: accumulator set drained by both CTAs' epilogues
+    uint64_t* tfull;  // accumulator ready for the epilogue
+    uint64_t* tempty; // leader: accumulator drained by both CTAs' epilogues
     uint64_t* ebar;   // epilogue rendezvous
     uint32_t* tmem_slot;
+    int* s_cb;        // [kMaxShrinkSlots] first row (relative to the item) of each slot's bucket
+    int* s_ce;        // [kMaxShrinkSlots] one past its last row
+    int* s_sl;        // [kMaxShrinkSlots] adapter of each slot
+    int* s_misc;      // [4] shared verdicts
+    float* tr;        // [kEpiWarps][kTrFloats] down epilogue transpose tiles
     TaskTable tt;
 };
 
-__device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS, int stage_bytes) {
+__device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     Smem2 m;
     m.ring = base;
-    uint8_t* p = base + (size_t)NS * stage_bytes;
-    m.s_pair = reinterpret_cast<int*>(p);
-    m.s_lora = m.s_pair + kPairBN;
-    m.s_w = reinterpret_cast<float*>(m.s_lora + kPairBN);
-    m.s_misc = reinterpret_cast<int*>(m.s_w + kPairBN);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(m.s_misc + kMisc + (kMisc & 1));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * kStage2);
     m.full = bars;
     m.empty = m.full + NS;
     m.tfull = m.empty + NS;
-    m.tempty = m.tfull + kMaxNAcc2;
-    m.ebar = m.tempty + kMaxNAcc2;
+    m.tempty = m.tfull + 1;
+    m.ebar = m.tempty + 1;
     m.tmem_slot = reinterpret_cast<uint32_t*>(m.ebar + 1);
-    m.tt.cmask = reinterpret_cast<unsigned long long*>(m.tmem_slot + 4);
+    m.s_cb = reinterpret_cast<int*>(m.tmem_slot + 4);
+    m.s_ce = m.s_cb + kMaxShrinkSlots;
+    m.s_sl = m.s_ce + kMaxShrinkSlots;
+    m.s_misc = m.s_sl + kMaxShrinkSlots;
+    m.tt.cmask = reinterpret_cast<unsigned long long*>(m.s_misc + 4);
     m.tt.e = reinterpret_cast<int*>(m.tt.cmask + a.max_chunks);
     m.tt.q0 = m.tt.e + a.E;
     m.tt.m = m.tt.q0 + a.E;
     m.tt.cum = m.tt.m + a.E;
+    m.tr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(m.tt.cum + a.E + 1) + 15) & ~uintptr_t(15));
     return m;
+}
+
+// Epilogue of shrink item t (accumulator used `use` times before), pairs on
+// the lanes: this CTA's TMEM lane L holds item row rank * 128 + L, and r
+// columns per slot s hold that row times the A matrix of slot s (slots
+// 0 .. 128/r - 1 from column 0, the peer CTA's slots from column 128).
+// A row keeps the columns of the slot whose bucket it belongs to (rows of
+// base-only buckets between the item's buckets keep nothing).  Without a K
+// split it writes z (fp32) and, for the tensor-core expand, zexp (bf16, the
+// pair's own adapter slot); with one, its partial, and the split of this
+// CTA's half that arrives last adds all partials in split order and writes
+// z and zexp.  Each CTA then counts itself once in zdone.  False on a
+// timeout (warp-uniform).
+template <typename Rdv, typename Rel>
+__device__ bool shrink_epilogue_m(const TcArgs& a, int t, int n_lora, int use, uint32_t tmem_base, int qd, int half,
+                                  int lane, int etid, const Smem2& m, Rdv& rendezvous, Rel& release, int rank) {
+    ShItem sh;
+    sh.load(a, t, n_lora);
+    const int r = a.r;
+    // slot row ranges (after everyone is done with the previous item's)
+    if (!rendezvous()) return false;
+    if (etid < sh.nb) {
+        const int bk = a.lora_buckets[sh.j0 + etid];
+        m.s_cb[etid] = min(max(a.compact_offset[bk] - sh.q0c, 0), sh.n_real);
+        m.s_ce[etid] = min(max(a.compact_offset[bk + 1] - sh.q0c, 0), sh.n_real);
+        m.s_sl[etid] = bk % (a.L + 1) - 1;
+    }
+    if (!rendezvous()) return false;
+    const int row = rank * 128 + qd * 32 + lane;      // row of the item held by this lane
+    int my_s = -1;
+    for (int s = 0; s < sh.nb; s++)
+        if (row >= m.s_cb[s] && row < m.s_ce[s]) my_s = s;
+    // the slots this warp's 32 rows touch (rows are in slot order)
+    const int w_lo = rank * 128 + qd * 32, w_hi = w_lo + 31;
+    int s_lo = sh.nb, s_hi = -1;
+    for (int s = 0; s < sh.nb; s++) {
+        if (m.s_ce[s] > w_lo && m.s_cb[s] <= w_hi) {
+            s_lo = min(s_lo, s);
+            s_hi = max(s_hi, s);
+        }
+    }
+    const size_t q = (size_t)sh.q0c + row;
+    float* dst = a.sh_ks > 1 ? a.zpart + (size_t)sh.sp * a.P * r : a.z;
+    const int rp = expand_rpad(r);
+    const bool zx = a.zexp != nullptr && a.sh_ks == 1;
+
+    if (!__all_sync(kFull, mbar_wait(m.tfull, (uint32_t)use & 1u))) return false;
+    tc_fence_after();
+    const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16);
+    // the two warps of a lane quadrant take alternate slots; slot s is column
+    // range g * 128 + (s - g * g_cta) * r of the CTA g = s / g_cta that holds
+    // its A rows (the N half of that CTA starts at column 128 g)
+    const int g_cta = 128 / r;
+    for (int s = s_lo + half; s <= s_hi; s += 2) {
+        const int col = (s / g_cta) * 128 + (s % g_cta) * r;
+        for (int j0 = 0; j0 < r; j0 += 8) {
+            float v[8];
+            tmem_ld8(t_lane + (uint32_t)(col + j0), v);
+            if (my_s == s) {
+                float4* zo = reinterpret_cast<float4*>(dst + q * r + j0);
+                zo[0] = make_float4(v[0], v[1], v[2], v[3]);
+                zo[1] = make_float4(v[4], v[5], v[6], v[7]);
+                if (zx) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(v[0], v[1]);
+                    pk.y = pack_bf16x2(v[2], v[3]);
+                    pk.z = pack_bf16x2(v[4], v[5]);
+                    pk.w = pack_bf16x2(v[6], v[7]);
+                    *reinterpret_cast<uint4*>(a.zexp + ((size_t)m.s_sl[s] * a.P + q) * rp + j0) = pk;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) release();
+    __threadfence();
+    if (!rendezvous()) return false;
+    if (a.sh_ks > 1) {
+        if (etid == 0) m.s_misc[1] = atomicAdd(&a.sh_counters[sh.i * 2 + rank], 1) == a.sh_ks - 1;
+        if (!rendezvous()) return false;
+        if (!m.s_misc[1]) return true;  // the last split of this CTA's half counts it
+        __threadfence();
+        // this CTA's rows, r / 4 float4 per row, summed in split order
+        const int lo = min(rank * 128, sh.n_real), hi = min(rank * 128 + 128, sh.n_real);
+        const int r4 = r / 4;
+        const size_t split4 = (size_t)a.P * r / 4;
+        const float4* src = reinterpret_cast<const float4*>(a.zpart);
+        float4* zout = reinterpret_cast<float4*>(a.z);
+        for (int i = etid; i < (hi - lo) * r4; i += kEpiWarps * 32) {
+            const int rr = lo + i / r4, j4 = i % r4;
+            const size_t at = ((size_t)sh.q0c + rr) * r4 + j4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < a.sh_ks; sp++) {
+                const float4 v = __ldcg(src + sp * split4 + at);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            zout[at] = acc;
+            if (a.zexp != nullptr) {
+                int l = -1;
+                for (int s = 0; s < sh.nb; s++)
+                    if (rr >= m.s_cb[s] && rr < m.s_ce[s]) l = m.s_sl[s];
+                if (l >= 0) {
+                    uint2 pk;
+                    pk.x = pack_bf16x2(acc.x, acc.y);
+                    pk.y = pack_bf16x2(acc.z, acc.w);
+                    *reinterpret_cast<uint2*>(a.zexp + ((size_t)l * a.P + sh.q0c + rr) * rp + j4 * 4) = pk;
+                }
+            }
+        }
+        __threadfence();
+        if (!rendezvous()) return false;
+    }
+    if (etid == 0) atomicAdd(a.zdone, 1);
+    return true;
 }
 
 template <bool GATE_UP>
@@ -226,8 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
-    using PT = Pair<GATE_UP>;
-    Smem2 m = carve2(base, a, NS, PT::kStage);
+    Smem2 m = carve2(base, a, NS);
     const TaskTable& tt = m.tt;
     const uint32_t rank = cta_rank();
     const bool leader = rank == 0;
@@ -238,10 +375,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             mbar_init(&m.full[s], 1);
             mbar_init(&m.empty[s], 1);
         }
-        for (int b = 0; b < PT::kNAcc; b++) {
-            mbar_init(&m.tfull[b], 1);
-            mbar_init(&m.tempty[b], 2 * kEpiWarps);
-        }
+        mbar_init(m.tfull, 1);
+        mbar_init(m.tempty, 2 * kEpiWarps);
         mbar_init(m.ebar, kEpiWarps * 32);
         fence_barrier_init();
     }
@@ -251,8 +386,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
         prefetch_tensormap(&a.xmap);
         if (a.sh_tasks) prefetch_tensormap(&a.amap);
         if (a.tc_expand) {
-            prefetch_tensormap(&a.bmap1);
-            prefetch_tensormap(&a.zxmap1);
+            prefetch_tensormap(&a.bmap);
+            prefetch_tensormap(&a.zxmap);
         }
     }
     tc_fence_before();
@@ -265,13 +400,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     pdl_wait();
     pdl_trigger();
 
-    // weight tiles: 256 units (gate_up) or W2 rows (down), 128 per CTA
+    // a task covers nu units (gate_up: the gate and the up rows of each) or
+    // 2 * nu W2 rows (down); each CTA copies nu / 2 rows of each chain
+    const int nu = a.nu, nu2 = nu / 2;
     const int N_out = GATE_UP ? a.I : a.H;
     const int K = GATE_UP ? a.H : a.I;
-    const int ntiles = (N_out + 255) / 256;
+    const int tile_rows = GATE_UP ? nu : 2 * nu;
+    const int ntiles = (N_out + tile_rows - 1) / tile_rows;
     const int nkb = (K + kBK - 1) / kBK;
     const int n_active = a.hdr->n_active;
-    build_task_table<PT::kBN>(a, tt, n_active, ntiles);
+    build_task_table<kPairRows>(a, tt, n_active, ntiles);
     const int ksplit = a.ksplit;
     const bool shrink = a.sh_tasks != nullptr && a.r > 0;
     const bool expand = a.tc_expand != 0 && a.r > 0;
@@ -280,26 +418,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     const int n_sh = n_sh_tasks * sh_ks;
     const int n_lora = shrink ? a.hdr->n_lora_buckets : 0;
     const int L1 = a.L + 1;
-    const int g_cta = a.r > 0 ? 128 / a.r : 0;  // shrink slots per CTA
+    const int g2 = a.r > 0 ? 128 / a.r : 0;  // shrink slots per CTA
     const int total = n_sh + tt.cum[n_active] * ksplit;
     const int t_first = (int)cluster_index(), t_step = (int)cluster_count();
     const int rp = expand_rpad(a.r);
-    const uint32_t xa1 = 128u * rp * 2u;  // one adapter's weight-row sub-tile (and down's zexp sub-tile)
-    // one adapter's zexp sub-tile (this CTA's half of the chunk's pairs)
-    const uint32_t zx1 = (uint32_t)(PT::kBN / 2) * rp * 2u;
+    const int apb = 64 / rp;  // adapters per expand block
+    const int n_groups = a.L > 0 ? (a.L + apb - 1) / apb : 0;
+    // chain row of this CTA's half for chain c of weight tile mt
+    auto chain_row = [&](int mt, int c) {
+        return GATE_UP ? mt * nu + (int)rank * nu2 : mt * 2 * nu + c * nu + (int)rank * nu2;
+    };
+    // expand block j of a chunk's mask: the j-th adapter group with an adapter present
+    auto group_present = [&](unsigned long long mask, int g) {
+        const unsigned long long gm = apb >= 64 ? ~0ull : ((1ull << apb) - 1ull);
+        return ((mask >> (g * apb)) & gm) != 0ull;
+    };
     bool ok = true;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        // This CTA's halves of every stage: its 128 weight (or adapter) rows and
-        // its half of the chunk's pair rows, in 64-row boxes.  The copies count
-        // on the leader's full barrier; the leader arms it with both CTAs' bytes.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0, armed = 0, last_par = 0;
             bool z_seen = false;
             const uint32_t full0 = cluster_addr(m.full, 0);  // the leader's full[0]
-            // wait until the pair's MMAs are done with the slot; the leader arms it
             auto acquire = [&](uint32_t bytes_pair) {
                 if (!mbar_wait_cluster(&m.empty[stage], phase ^ 1)) return false;
                 if (leader) mbar_arrive_expect_tx(&m.full[stage], bytes_pair);
@@ -312,112 +454,89 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             };
             for (int t = t_first; t < total && ok; t += t_step) {
                 if (t < n_sh) {
-                    // shrink item: this CTA's slots' A boxes, then its half of the pair rows
+                    // shrink item: this CTA's 128 pair rows, then the A boxes of its slots
                     ShItem sh;
                     sh.load(a, t, n_lora);
-                    const int ns0 = max(0, min(sh.nb, g_cta)), ns1 = max(0, min(sh.nb - g_cta, g_cta));
-                    const int g0 = (int)rank * g_cta, ns_mine = rank ? ns1 : ns0;
-                    int arow[kMaxSlots];
-                    for (int q = 0; q < ns_mine; q++) {
+                    const int ns0 = min(sh.nb, g2), ns1 = max(0, min(sh.nb - g2, g2));
+                    const int mine = rank ? ns1 : ns0, g0 = (int)rank * g2;
+                    int arow[kMaxShrinkSlots / 2];
+                    for (int q = 0; q < mine; q++) {
                         const int b = a.lora_buckets[sh.j0 + g0 + q];
                         arow[q] = ((b % L1 - 1) * a.E + b / L1) * a.r;  // first row of A[l][e]
                     }
-                    const int half = n32(sh.n_real) / 2, n_box = (half + 63) / 64;
-                    const int brow0 = sh.q0c + (int)rank * half;
-                    const uint32_t bytes_pair = (uint32_t)((ns0 + ns1) * a.r + 2 * n_box * 64) * kBK * 2;
+                    const uint32_t bytes_pair = 2u * kSlot + (uint32_t)((ns0 + ns1) * a.r) * kBK * 2u;
+                    const int rows0 = sh.q0c + (int)rank * 128;
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!acquire(bytes_pair)) { ok = false; break; }
-                        uint8_t* dst = m.ring + (size_t)stage * PT::kStage;
+                        uint8_t* dst = m.ring + (size_t)stage * kStage2;
                         const uint32_t bar = full0 + (uint32_t)stage * 8u;
                         const int k0 = kb * kBK;
-                        for (int q = 0; q < ns_mine; q++) tma2_2d(dst + q * a.r * kBK * 2, &a.amap, bar, k0, arow[q]);
-                        for (int g = 0; g < n_box; g++)
-                            tma2_2d(dst + kATile + g * 64 * kBK * 2, &a.xmap, bar, k0, brow0 + g * 64);
+                        tma2_2d(dst, &a.xmap, bar, k0, rows0);
+                        for (int q = 0; q < mine; q++)
+                            tma2_2d(dst + kSlot + q * a.r * kBK * 2, &a.amap, bar, k0, arow[q]);
                         advance();
                     }
                     continue;
                 }
-                Task<PT::kBN> tw;
+                Task<kPairRows> tw;
                 tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-                // this CTA's half of the chunk's pair rows (N = pairs rounded up
-                // to 32), in 64-row boxes
-                const int e = tw.e, half = n32(tw.n_real) / 2, n_box = (half + 63) / 64;
-                const int brow0 = tw.q0c + (int)rank * half;
-                // first of this CTA's 128 units (gate_up) or W2 rows (down)
-                const int wrow0 = tw.mt * 256 + (int)rank * 128;
-                const uint32_t bytes_pair = 2u * ((uint32_t)PT::kW + (uint32_t)n_box * kSub);
+                const int e = tw.e;
+                const int rows0 = tw.q0c + (int)rank * 128;
+                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
+                // per CTA: 128 pair rows + nu / 2 rows of each chain (also for expand blocks)
+                const uint32_t bytes_pair = 2u * ((uint32_t)kSlot + 2u * (uint32_t)nu2 * kBK * 2u);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                ExpandRange xr;
-                xr.none();
-                int n_x = 0;
-                if (expand) {
-                    xr.from_mask(a, tt.cmask[tw.chunk], tw.split, ksplit);
-                    n_x = xr.count();
-                }
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!acquire(bytes_pair)) { ok = false; break; }
-                    uint8_t* dst = m.ring + (size_t)stage * PT::kStage;
+                    uint8_t* dst = m.ring + (size_t)stage * kStage2;
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
                     const int k0 = kb * kBK;
+                    tma2_2d(dst, &a.xmap, bar, k0, rows0);
                     if (GATE_UP) {
-                        // the gate rows of the CTA's 128 units, then their up rows
-                        tma2_4d(dst, &a.wmap, bar, k0, wrow0, 0, e);
-                        tma2_4d(dst + kATile, &a.wmap, bar, k0, wrow0, 1, e);
+                        // the gate rows, then the up rows, of this CTA's nu / 2 units
+                        tma2_4d(dst + kSlot, &a.wmap, bar, k0, c0row, 0, e);
+                        tma2_4d(dst + 2 * kSlot, &a.wmap, bar, k0, c0row, 1, e);
                     } else {
-                        tma2_3d(dst, &a.wmap, bar, k0, wrow0, e);
+                        tma2_3d(dst + kSlot, &a.wmap, bar, k0, c0row, e);
+                        tma2_3d(dst + 2 * kSlot, &a.wmap, bar, k0, c1row, e);
                     }
-                    for (int g = 0; g < n_box; g++) tma2_2d(dst + PT::kW + g * kSub, &a.xmap, bar, k0, brow0 + g * 64);
                     advance();
                 }
-                if (ok && n_x > 0 && !z_seen) {
+                if (!ok || !expand) continue;
+                const unsigned long long mask = tt.cmask[tw.chunk];
+                if (mask == 0ull) continue;
+                if (!z_seen) {
                     // the expand reads zexp: every shrink item, in both CTAs of its pair, is done
-                    if (!wait_count(a.zdone, 2 * n_sh_tasks)) ok = false;
+                    if (!wait_count(a.zdone, 2 * n_sh_tasks)) { ok = false; break; }
+                    // the shrink items' generic stores before the TMA (async proxy) reads
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     z_seen = true;
                 }
-                // packed expand blocks: the next 64 / r_pad adapters present in the
-                // chunk; per adapter this CTA's 128 B rows and its zexp rows
-                unsigned long long rem = n_x > 0 ? xr.bits : 0ull;
-                for (int g = 0, mine = xr.split; ok && rem != 0ull; g++) {
-                    if (g != mine) {
-                        for (int q = 0; q < xr.apb; q++) rem &= rem - 1ull;
-                        continue;
-                    }
-                    mine += xr.ksplit;
-                    int ids[4];
-                    int cnt = 0;
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (q < xr.apb && rem != 0ull) {
-                            ids[q] = __ffsll((long long)rem) - 1;
-                            rem &= rem - 1ull;
-                            cnt = q + 1;
-                        }
-                    }
-                    // per adapter and CTA: B rows (gate_up: gate and up sub-tiles) and zexp rows
-                    if (!acquire((uint32_t)cnt * 2u * ((GATE_UP ? 2u : 1u) * xa1 + zx1))) { ok = false; break; }
-                    uint8_t* dst = m.ring + (size_t)stage * PT::kStage;
+                // expand blocks with an adapter present, dealt over the K splits
+                for (int g = 0, j = 0; g < n_groups && ok; g++) {
+                    if (!group_present(mask, g)) continue;
+                    if (j++ % ksplit != tw.split) continue;
+                    if (!acquire(bytes_pair)) { ok = false; break; }
+                    uint8_t* dst = m.ring + (size_t)stage * kStage2;
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        if (q < cnt) {
-                            if (GATE_UP) {
-                                // coordinates (k, unit, half, expert, adapter)
-                                tma2_5d(dst + q * xa1, &a.bmap1, bar, 0, wrow0, 0, e, ids[q]);
-                                tma2_5d(dst + kATile + q * xa1, &a.bmap1, bar, 0, wrow0, 1, e, ids[q]);
-                            } else {
-                                tma2_4d(dst + q * xa1, &a.bmap1, bar, 0, wrow0, e, ids[q]);
-                            }
-                            tma2_3d(dst + PT::kW + q * zx1, &a.zxmap1, bar, 0, brow0, ids[q]);
-                        }
+                    const int l0 = g * apb;
+                    // zexp rows of this CTA's pairs (apb adapter sub-tiles), then the
+                    // adapters' B rows of each chain
+                    tma2_3d(dst, &a.zxmap, bar, 0, rows0, l0);
+                    if (GATE_UP) {
+                        tma2_5d(dst + kSlot, &a.bmap, bar, 0, c0row, 0, e, l0);
+                        tma2_5d(dst + 2 * kSlot, &a.bmap, bar, 0, c0row, 1, e, l0);
+                    } else {
+                        tma2_4d(dst + kSlot, &a.bmap, bar, 0, c0row, e, l0);
+                        tma2_4d(dst + 2 * kSlot, &a.bmap, bar, 0, c1row, e, l0);
                     }
                     advance();
                 }
             }
             // every issued copy of both CTAs lands before either CTA may exit (the
             // leader's full barriers count both; the peer waits at the final
-            // cluster barrier)
+            // pair barrier)
             if (leader)
                 for (int s = 0; s < NS; s++)
                     if ((armed >> s) & 1u) mbar_wait(&m.full[s], (last_par >> s) & 1u);
@@ -425,16 +544,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     } else if (warp == 1) {
         if (leader && lane == 0) {
             // ------------------------------------------------- MMA issuer (leader)
-            // Walks the same items as the producers; a stage is used once both
-            // CTAs' copies landed (the leader's full barrier counts both); its
-            // release and each accumulator's completion are committed to the
-            // barriers of both CTAs.
             int stage = 0;
             uint32_t phase = 0;
-            const uint32_t xa16 = xa1 / 16, zx16 = zx1 / 16;
             const uint64_t d0 = umma_desc_sw128(smem_u32(m.ring));
             const uint64_t dx0 = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
-            constexpr uint64_t kStage16 = PT::kStage / 16, kA16 = kATile / 16, kW16 = PT::kW / 16;
+            constexpr uint64_t kStage16 = kStage2 / 16, kSlot16 = kSlot / 16;
+            const uint64_t zsub16 = 128u * rp * 2u / 16u, bsub16 = (uint64_t)nu2 * rp * 2u / 16u;
             auto take = [&]() {
                 if (!mbar_wait_cluster(&m.full[stage], phase)) return false;
                 tc_fence_after();
@@ -444,33 +559,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                 umma2_commit_both(&m.empty[stage]);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
             };
+            const uint32_t d_c0 = tmem_base, d_c1 = tmem_base + kChain1Col;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-                const int b = it % PT::kNAcc;
-                if (!mbar_wait_cluster(&m.tempty[b], ((uint32_t)(it / PT::kNAcc) & 1u) ^ 1u)) { ok = false; break; }
+                // the accumulator is free once both CTAs' epilogues drained the previous task
+                if (!mbar_wait_cluster(m.tempty, ((uint32_t)it & 1u) ^ 1u)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d = tmem_base + (uint32_t)(b * PT::kAccCols);
                 if (t < n_sh) {
                     ShItem sh;
                     sh.load(a, t, n_lora);
-                    const uint32_t idesc = umma_idesc_bf16_f32(256, n32(sh.n_real));
+                    const uint32_t idesc = umma_idesc_bf16_f32(256, 256);
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!take()) { ok = false; break; }
                         const uint64_t da = d0 + (uint64_t)stage * kStage16;
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; kk++)
-                            umma2_bf16(d, da + 2 * kk, da + kA16 + 2 * kk, idesc, (kb != kb0) || (kk != 0));
+                            umma2_bf16(d_c0, da + 2 * kk, da + kSlot16 + 2 * kk, idesc, (kb != kb0) || (kk != 0));
                         release();
                     }
                     if (!ok) break;
-                    umma2_commit_both(&m.tfull[b]);
+                    umma2_commit_both(m.tfull);
                     continue;
                 }
-                Task<PT::kBN> tw;
+                Task<kPairRows> tw;
                 tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-                // gate_up: a gate and an up chain per K step (independent
-                // accumulators, so one's MMA latency overlaps the other's)
-                const uint32_t idesc = umma_idesc_bf16_f32(256, n32(tw.n_real));
+                const uint32_t idesc = umma_idesc_bf16_f32(256, nu);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!take()) { ok = false; break; }
@@ -478,38 +591,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++) {
                         const uint32_t acc = (kb != kb0) || (kk != 0);
-                        umma2_bf16(d, da + 2 * kk, da + kW16 + 2 * kk, idesc, acc);
-                        if (GATE_UP) umma2_bf16(d + PT::kBN, da + kA16 + 2 * kk, da + kW16 + 2 * kk, idesc, acc);
+                        umma2_bf16(d_c0, da + 2 * kk, da + kSlot16 + 2 * kk, idesc, acc);
+                        umma2_bf16(d_c1, da + 2 * kk, da + 2 * kSlot16 + 2 * kk, idesc, acc);
                     }
                     release();
                 }
-                if (ok && expand) {
-                    ExpandRange xr;
-                    xr.from_mask(a, tt.cmask[tw.chunk], tw.split, ksplit);
-                    const int ng = xr.groups();
-                    for (int g = xr.split; g < ng && ok; g += xr.ksplit) {
-                        const int cnt = xr.group_size(g);
-                        if (!take()) { ok = false; break; }
-                        const uint64_t dxs = dx0 + (uint64_t)stage * kStage16;
-                        for (int q = 0; q < cnt; q++) {
-                            const uint64_t da = dxs + q * xa16, db = dxs + kW16 + q * zx16;
-                            for (int kk = 0; kk < rp / 16; kk++) {
-                                umma2_bf16(d, da + 2 * kk, db + 2 * kk, idesc, 1u);
-                                if (GATE_UP) umma2_bf16(d + PT::kBN, da + kA16 + 2 * kk, db + 2 * kk, idesc, 1u);
-                            }
+                const unsigned long long mask = expand ? tt.cmask[tw.chunk] : 0ull;
+                for (int g = 0, j = 0; ok && mask != 0ull && g < n_groups; g++) {
+                    if (!group_present(mask, g)) continue;
+                    if (j++ % ksplit != tw.split) continue;
+                    if (!take()) { ok = false; break; }
+                    const uint64_t dx = dx0 + (uint64_t)stage * kStage16;
+                    for (int q = 0; q < apb; q++) {
+                        const uint64_t za = dx + q * zsub16;
+                        const uint64_t b0 = dx + kSlot16 + q * bsub16, b1 = dx + 2 * kSlot16 + q * bsub16;
+                        for (int kk = 0; kk < rp / 16; kk++) {
+                            umma2_bf16(d_c0, za + 2 * kk, b0 + 2 * kk, idesc, 1u);
+                            umma2_bf16(d_c1, za + 2 * kk, b1 + 2 * kk, idesc, 1u);
                         }
-                        release();
                     }
+                    release();
                 }
                 if (!ok) break;
-                umma2_commit_both(&m.tfull[b]);
+                umma2_commit_both(m.tfull);
             }
         }
     } else {
         // -------------------------------------------------------------- epilogue
         const int ew = warp - 2;         // 0 .. kEpiWarps-1
         const int qd = warp & 3;         // TMEM lane quadrant of this warp
-        const int half = ew >> 2;        // which alternate 16-column chunks
+        const int half = ew >> 2;        // which alternate 16-column groups
         const int etid = ew * 32 + lane;
         uint32_t epar = 0;
         auto rendezvous = [&]() {
@@ -518,76 +629,102 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             epar ^= 1;
             return r_ok;
         };
-        // an accumulator set is free once both CTAs' epilogue warps released it
+        // the accumulator is free once both CTAs' epilogue warps released it
         const uint32_t lead_tempty = cluster_addr(m.tempty, 0);
-        auto release = [&](int bb) {
-            if (leader) mbar_arrive(&m.tempty[bb]);
-            else mbar_arrive_cluster(lead_tempty + (uint32_t)bb * 8u);
+        auto release = [&]() {
+            if (leader) mbar_arrive(m.tempty);
+            else mbar_arrive_cluster(lead_tempty);
         };
+        const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16);
+        const int ngroups = nu / 16;
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
-            const int b = it % PT::kNAcc;
-            const int use = it / PT::kNAcc;
             if (t < n_sh) {
-                if (!shrink_epilogue(a, t, n_lora, b, use, tmem_base, PT::kAccCols, qd, half, lane, etid, m.s_pair,
-                                     m.s_lora, m.s_misc, m.tfull, rendezvous, release, (int)rank, 2)) {
+                if (!shrink_epilogue_m(a, t, n_lora, it, tmem_base, qd, half, lane, etid, m, rendezvous, release,
+                                       (int)rank)) {
                     ok = false;
                     break;
                 }
                 continue;
             }
-            Task<PT::kBN> tw;
+            Task<kPairRows> tw;
             tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-            const int q0c = tw.q0c, n_real = tw.n_real;
-            // stage the column data while the task's MMAs run (after everyone is
-            // done with the previous task's)
-            if (!rendezvous()) { ok = false; break; }
-            for (int c = etid; c < n_real; c += kEpiWarps * 32) {
-                const int p = a.compact_ids[q0c + c];
-                m.s_pair[c] = p;
-                m.s_w[c] = a.topk_weights[p];
+            // this lane's pair row of the chunk
+            const int row = (int)rank * 128 + qd * 32 + lane;
+            const bool valid = row < tw.n_real;
+            const size_t q = (size_t)tw.q0c + row;
+            int p = 0;
+            float w = 0.f;
+            if (!GATE_UP && valid) {
+                p = a.compact_ids[q];
+                w = a.topk_weights[p];
             }
-            if (!rendezvous()) { ok = false; break; }
             // warp-uniform: the TMEM loads below are warp-collective
-            const bool got = __all_sync(kFull, mbar_wait(&m.tfull[b], (uint32_t)use & 1u));
+            if (!__all_sync(kFull, mbar_wait(m.tfull, (uint32_t)it & 1u))) { ok = false; break; }
             tc_fence_after();
-            const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16) + (uint32_t)(b * PT::kAccCols);
-            bool step_ok = got;
             if (GATE_UP) {
-                // lane = one of this CTA's 128 units; its gate values in columns
-                // 0..127 and its up values 128 columns further
-                const int w_unit = tw.mt * 256 + (int)rank * 128 + qd * 32 + lane;
-                for (int c0 = half * 16; got && c0 < n_real; c0 += 32) {
-                    float g[16], u[16];
-                    tmem_ld16x2(t_lane + c0, t_lane + PT::kBN + c0, g, u);
-                    if (w_unit < a.I) {
-#pragma unroll
-                        for (int c = 0; c < 16; c++) {
-                            const int cc = c0 + c;
-                            if (cc < n_real)
-                                a.act_out[(size_t)(q0c + cc) * a.I + w_unit] = f32_to_bf16_rne(silu_fast(g[c]) * u[c]);
-                        }
+                // units u0 + 16 g .. u0 + 16 g + 15: gate in columns 16 g.., up 256 further
+                const int u0 = tw.mt * nu;
+                uint16_t* arow = a.act_out + q * a.I;
+                for (int g = half; g < ngroups; g += 2) {
+                    float gv[16], uv[16];
+                    tmem_ld16x2(t_lane + g * 16, t_lane + kChain1Col + g * 16, gv, uv);
+                    const int u = u0 + g * 16;
+                    if (valid) {
+                        uint4 lo, hi;
+                        lo.x = pack_bf16x2(silu_fast(gv[0]) * uv[0], silu_fast(gv[1]) * uv[1]);
+                        lo.y = pack_bf16x2(silu_fast(gv[2]) * uv[2], silu_fast(gv[3]) * uv[3]);
+                        lo.z = pack_bf16x2(silu_fast(gv[4]) * uv[4], silu_fast(gv[5]) * uv[5]);
+                        lo.w = pack_bf16x2(silu_fast(gv[6]) * uv[6], silu_fast(gv[7]) * uv[7]);
+                        hi.x = pack_bf16x2(silu_fast(gv[8]) * uv[8], silu_fast(gv[9]) * uv[9]);
+                        hi.y = pack_bf16x2(silu_fast(gv[10]) * uv[10], silu_fast(gv[11]) * uv[11]);
+                        hi.z = pack_bf16x2(silu_fast(gv[12]) * uv[12], silu_fast(gv[13]) * uv[13]);
+                        hi.w = pack_bf16x2(silu_fast(gv[14]) * uv[14], silu_fast(gv[15]) * uv[15]);
+                        if (u + 8 <= a.I) *reinterpret_cast<uint4*>(arow + u) = lo;
+                        if (u + 16 <= a.I) *reinterpret_cast<uint4*>(arow + u + 8) = hi;
                     }
                 }
             } else {
-                // this CTA's 128 W2 rows; with split K every split writes its own slab
-                const int w_row = tw.mt * 256 + (int)rank * 128 + qd * 32 + lane;
-                float* const pout = a.pair_out + (ksplit > 1 ? (size_t)tw.split * a.pair_split : 0);
-                for (int c0 = half * 16; got && c0 < n_real; c0 += 32) {
-                    float g[16];
-                    tmem_ld16(t_lane + c0, g);
-                    if (w_row < a.H) {
+                // W2 rows h0 + c * nu + 16 g ..: w * d into this split's slab of
+                // pair_out.  A group's 32 rows x 16 columns go through the
+                // warp's tile: each store then writes 64 contiguous bytes of 8
+                // rows (lane / 4 + 8 i, quarter lane % 4) instead of 16 bytes of
+                // 32 rows.
+                float* const slab = a.pair_out + (ksplit > 1 ? (size_t)tw.split * a.pair_split : 0);
+                float* const tr = m.tr + ew * kTrFloats;
+                const int c4 = lane & 3;
+                int rp_row[4];
+                bool rv[4];
 #pragma unroll
-                        for (int c = 0; c < 16; c++) {
-                            const int cc = c0 + c;
-                            if (cc < n_real) pout[(size_t)m.s_pair[cc] * a.H + w_row] = m.s_w[cc] * g[c];
+                for (int i = 0; i < 4; i++) {
+                    const int src = (lane >> 2) + 8 * i;
+                    rp_row[i] = __shfl_sync(kFull, p, src);
+                    rv[i] = __shfl_sync(kFull, valid ? 1 : 0, src) != 0;
+                }
+                for (int c = 0; c < 2; c++) {
+                    const int h0 = tw.mt * 2 * nu + c * nu;
+                    for (int g = half; g < ngroups; g += 2) {
+                        float v[16];
+                        tmem_ld16(t_lane + c * kChain1Col + g * 16, v);
+                        float4* mine = reinterpret_cast<float4*>(tr + lane * kTrStride);
+#pragma unroll
+                        for (int j = 0; j < 4; j++)
+                            mine[j] = make_float4(w * v[4 * j], w * v[4 * j + 1], w * v[4 * j + 2], w * v[4 * j + 3]);
+                        __syncwarp();
+                        const int h = h0 + g * 16 + 4 * c4;
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int row = (lane >> 2) + 8 * i;
+                            const float4 val = *reinterpret_cast<const float4*>(tr + row * kTrStride + 4 * c4);
+                            if (rv[i] && h + 4 <= a.H)
+                                *reinterpret_cast<float4*>(slab + (size_t)rp_row[i] * a.H + h) = val;
                         }
+                        __syncwarp();
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) release(b);
-            if (!step_ok) { ok = false; break; }
+            if (lane == 0) release();
         }
     }
 
@@ -609,17 +746,17 @@ cudaError_t set_attr2() {
 
 // at least half an SM's shared memory: one CTA per SM, so the whole TMEM
 // allocation never waits for another CTA
-int tc2_smem_bytes(bool gate_up, int E, int nstages, int max_chunks) {
-    const int stage = gate_up ? Pair<true>::kStage : Pair<false>::kStage;
-    const int staging = 3 * kPairBN * 4 + (kMisc + (kMisc & 1)) * 4;
-    const int bars = (2 * nstages + 2 * kMaxNAcc2 + 1) * 8 + 16;
+int tc2_smem_bytes(int E, int nstages, int max_chunks) {
+    const int bars = (2 * nstages + 3) * 8 + 16;
+    const int slots = (3 * kMaxShrinkSlots + 4) * 4;
     const int table = 8 * max_chunks + (4 * E + 1) * 4;
-    return std::max(1024 + nstages * stage + staging + bars + table, kTcSmemLimit / 2 + 1024);
+    const int tr = 16 + kEpiWarps * kTrFloats * 4;
+    return std::max(1024 + nstages * kStage2 + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
 }
 
-int tc2_plan_stages(bool gate_up, int E, int max_chunks) {
+int tc2_plan_stages(int E, int max_chunks) {
     for (int ns = 8; ns >= 3; ns--)
-        if (tc2_smem_bytes(gate_up, E, ns, max_chunks) <= kTcSmemLimit) return ns;
+        if (tc2_smem_bytes(E, ns, max_chunks) <= kTcSmemLimit) return ns;
     return 0;
 }
 
@@ -630,7 +767,7 @@ cudaError_t init_tc2_attributes() {
 }
 
 // Pairs of this kernel that fit on the device at once (with the largest
-// shared-memory request): the persistent grid must not exceed it, since items
+// shared-memory request): the persistent grid must not exceed it, since tasks
 // wait on each other's progress (shrink before expand).
 int tc2_max_pairs(bool gate_up) {
     cudaLaunchConfig_t cfg = {};
@@ -657,7 +794,9 @@ int tc2_max_pairs(bool gate_up) {
 // grid: an even number of CTAs (pairs of SMs); clusters of two, with the
 // programmatic-dependent-launch attribute when asked
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl) {
-    const int smem = tc2_smem_bytes(gate_up, args.E, args.nstages, args.max_chunks);
+    if (args.nu < 16 || args.nu > 256 || args.nu % 16 != 0) return cudaErrorInvalidValue;
+    if (args.r > 0 && (128 / args.r) * 2 > kMaxShrinkSlots) return cudaErrorInvalidValue;
+    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kTcThreads);

@@ -62,6 +62,7 @@ struct Layout {
     int bn_gu, bn_dn, ks_gu, ks_dn;
     bool pair_cta;   // the GEMMs run as CTA pairs (moe_gemm_2sm.cu)
     int ranks;       // CTAs per GEMM task: 2 with pair_cta, else 1
+    int nu_gu, nu_dn;  // CTA pairs: weight rows per MMA chain of the two GEMMs
     long tiles_gu, tiles_dn;
     long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
 };
@@ -97,7 +98,7 @@ int check_dims(const moe_lora_dims* d) {
     if (!d) return MOELORA_EINVAL;
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->L < 0) return MOELORA_EINVAL;
     if (d->block_m != 0 && (!is_pow2(d->block_m) || d->block_m > 256)) return MOELORA_EINVAL;
-    if (d->options & ~MOELORA_OPT_PAIR_CTA) return MOELORA_EINVAL;
+    if (d->options & ~MOELORA_OPT_SINGLE_CTA) return MOELORA_EINVAL;
     if (d->sm_count < 0 || d->sm_count > 4096) return MOELORA_EINVAL;
     if (d->L > 0) {
         if (d->r <= 0) return MOELORA_EINVAL;
@@ -160,11 +161,12 @@ void plan_shrinks(const moe_lora_dims* d, Layout* L) {
     }
     // a shrink item stacks 128 / r buckets per CTA of its task
     L->st_G = L->ranks * (128 / d->r);
+    // an item's pairs: one TMEM accumulator buffer of both one-CTA GEMM
+    // kernels, or the 256 pair rows of a CTA pair
     const double nbl = (double)d->E * d->L;
     const double est_buckets = std::max(1.0, nbl * (1.0 - std::exp(-(double)L->P / nbl)));
     const long est_groups = std::max<long>(1, (long)std::ceil(est_buckets / L->st_G));
     const long rows_per_group = (L->P + est_groups - 1) / est_groups;
-    // an item's pairs fit one TMEM accumulator buffer of both GEMM kernels
     L->st_bn = L->pair_cta ? 256 : std::min(2 * L->bn_gu, L->bn_dn);
     const long est_tasks = est_groups * ((rows_per_group + L->st_bn - 1) / L->st_bn);
     const long slots = std::max(1, L->sms / L->ranks);
@@ -182,29 +184,34 @@ double expected_adapters_per_chunk(const moe_lora_dims* d, long P) {
     return d->L * (1.0 - std::pow(1.0 - 1.0 / d->L, pairs));
 }
 
-// With MOELORA_OPT_PAIR_CTA, wide chunks (more than 48 pairs per expert on
-// average) run on CTA pairs:
-// chunks of 256 pairs, gate_up tiles of 256 units, down tiles of 256 rows, as
-// long as the pair kernel covers the layer (tensor-core expand with chunk
-// masks when there are adapters, no gate_up K split, a ring that fits).
+// Weight rows per MMA chain of the CTA-pair kernel: `rows` split into the
+// fewest chains of at most 256, each a multiple of 16 (2880 -> 12 x 240).
+int chain_rows(long rows) {
+    const long n = (rows + 255) / 256;
+    return (int)(((rows + n - 1) / n + 15) / 16 * 16);
+}
+
+// Wide chunks (more than 48 pairs per expert on average) run on CTA pairs:
+// chunks of 256 pairs, gate_up tasks of nu units (chains: their gate and
+// their up rows), down tasks of 2 nu W2 rows, as long as the pair kernel
+// covers the layer (at most 64 adapters with the tensor-core expand, its
+// chunk masks and zexp buffers within bounds, a ring that fits).
 bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long avg_pairs) {
-    if (d->L > 0 && (!L->tc_expand || d->L > 64)) return false;
-    // pair chunks: gate_up 128 pairs, down 256 (the kernel's Pair<>::kBN)
-    const long chunks_gu = experts_max + (L->P + 127) / 128, chunks_dn = experts_max + (L->P + 255) / 256;
-    if (d->L > 0 && chunks_gu > kMaxChunkMasks) return false;
-    const int masks_gu = d->L > 0 ? (int)chunks_gu : 0, masks_dn = d->L > 0 ? (int)chunks_dn : 0;
-    if (tc2_plan_stages(true, d->E, masks_gu) < 3 || tc2_plan_stages(false, d->E, masks_dn) < 3) return false;
-    const long nt_gu = (d->I + 255) / 256, nt_dn = (d->H + 255) / 256;
-    const long pairs = std::max(1, L->sms / 2);
-    if (pick_ksplit(nt_gu * experts_max * ((avg_pairs + 127) / 128), d->H, pairs) != 1) return false;
+    if (d->L > 0 && (d->L > 64 || L->P * zexp_cols(d->L, d->r) > kMaxZexpElems)) return false;
+    const long chunks = experts_max + (L->P + 255) / 256;
+    if (d->L > 0 && chunks > kMaxChunkMasks) return false;
+    if (tc2_plan_stages(d->E, d->L > 0 ? (int)chunks : 0) < 3) return false;
     L->pair_cta = true;
     L->ranks = 2;
-    L->bn_gu = 128;
-    L->bn_dn = 256;
-    L->tiles_gu = nt_gu * chunks_gu;
-    L->tiles_dn = nt_dn * chunks_dn;
+    L->tc_expand = d->L > 0;
+    L->bn_gu = L->bn_dn = 256;
+    L->nu_gu = chain_rows(d->I);
+    L->nu_dn = chain_rows((d->H + 1) / 2);
+    const long nt_gu = (d->I + L->nu_gu - 1) / L->nu_gu, nt_dn = (d->H + 2 * L->nu_dn - 1) / (2 * L->nu_dn);
+    L->tiles_gu = nt_gu * chunks;
+    L->tiles_dn = nt_dn * chunks;
     L->ks_gu = 1;
-    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, pairs);
+    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, std::max(1, L->sms / 2));
     return true;
 }
 
@@ -214,7 +221,8 @@ void plan_gemms(const moe_lora_dims* d, Layout* L) {
     const bool narrow = avg_pairs <= 48;
     L->pair_cta = false;
     L->ranks = 1;
-    if (!narrow && (d->options & MOELORA_OPT_PAIR_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return;
+    L->nu_gu = L->nu_dn = 0;
+    if (!narrow && !(d->options & MOELORA_OPT_SINGLE_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return;
     L->bn_gu = narrow ? 64 : 128;
     L->bn_dn = narrow ? 64 : 256;
     const long nt_gu = (d->I + 127) / 128, nt_dn = (d->H + 127) / 128;
@@ -357,11 +365,11 @@ bool encode_w1_map(CUtensorMap* map, const void* W1, int E, int I, int H, int bo
     return encode_bf16_map(map, W1, 4, dims, strides, box);
 }
 
-// W2 [E][H][I]: boxes of 64 (K) x 128 rows
-bool encode_w2_map(CUtensorMap* map, const void* W2, int E, int I, int H) {
+// W2 [E][H][I]: boxes of 64 (K) x 128 rows (CTA pairs: half a chain)
+bool encode_w2_map(CUtensorMap* map, const void* W2, int E, int I, int H, int box_rows = 128) {
     const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
     const cuuint64_t strides[2] = {(cuuint64_t)I * 2, (cuuint64_t)H * I * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     return encode_bf16_map(map, W2, 3, dims, strides, box);
 }
 
@@ -407,12 +415,14 @@ bool encode_b1_map(CUtensorMap* map, const void* B1, int L, int E, int I, int r,
     return encode_bf16_map(map, B1, 5, dims, strides, box, expand_swizzle(rp));
 }
 
-// B2 [L][E][H][r] as {r, H, E, L}: boxes of r_pad x 128 rows x 64 / r_pad adapters
-bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r, bool one_adapter = false) {
+// B2 [L][E][H][r] as {r, H, E, L}: boxes of r_pad x 128 rows (CTA pairs: half a
+// chain) x 64 / r_pad adapters
+bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r, bool one_adapter = false,
+                   int box_rows = 128) {
     const int rp = expand_rpad_host(r);
     const cuuint64_t dims[4] = {(cuuint64_t)r, (cuuint64_t)H, (cuuint64_t)E, (cuuint64_t)L};
     const cuuint64_t strides[3] = {(cuuint64_t)r * 2, (cuuint64_t)H * r * 2, (cuuint64_t)E * H * r * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)rp, 128, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
+    const cuuint32_t box[4] = {(cuuint32_t)rp, (cuuint32_t)box_rows, 1, one_adapter ? 1u : (cuuint32_t)(64 / rp)};
     return encode_bf16_map(map, B2, 4, dims, strides, box, expand_swizzle(rp));
 }
 
@@ -648,22 +658,31 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
         tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
         if (pc) {
+            // CTA pairs: 128 pair rows per CTA, chains of nu units (each CTA half of them)
             if (!tc.chunk_masks) tc.max_chunks = 0;
-            tc.nstages = tc2_plan_stages(true, d->E, tc.max_chunks);
+            tc.nu = L.nu_gu;
+            tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
+            if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
+            const int half = L.nu_gu / 2;
+            if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H, half) ||
+                !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, 128) ||
+                (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
+                (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r, false, half) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128))))
+                return MOELORA_ECUDA;
         } else {
             tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+            if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+            const int rows = pair_box_rows(bn);
+            if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
+                !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
+                (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
+                (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
+                                 !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
+                                 !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
+                return MOELORA_ECUDA;
         }
-        if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
-        // a CTA pair loads its pair rows in 64-row boxes
-        const int rows = pc ? 64 : pair_box_rows(bn);
-        if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, rows) ||
-            (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
-            (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r) ||
-                             !encode_b1_map(&tc.bmap1, B1, d->L, d->E, d->I, d->r, true) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? bn / 2 : bn, true))))
-            return MOELORA_ECUDA;
         const long tasks = L.tiles_gu * L.ks_gu + L.st_tasks_max * L.s1;
         tr.mark(2);
         if (pc) {
@@ -693,21 +712,31 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
         tc.max_chunks = (int)(experts_bound + (L.P + bn - 1) / bn);
         tc.chunk_masks = L.tc_expand && d->L <= 64 && tc.max_chunks <= kMaxChunkMasks;
         if (pc) {
+            // CTA pairs: 128 act rows per CTA, two chains of nu W2 rows (each CTA half of each)
             if (!tc.chunk_masks) tc.max_chunks = 0;
-            tc.nstages = tc2_plan_stages(false, d->E, tc.max_chunks);
+            tc.nu = L.nu_dn;
+            tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
+            if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
+            const int half = L.nu_dn / 2;
+            if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H, half) ||
+                !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, 128) ||
+                (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
+                (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r, false, half) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128))))
+                return MOELORA_ECUDA;
         } else {
             tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
+            if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+            const int rows = pair_box_rows(bn);
+            if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
+                !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
+                (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
+                (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
+                                 !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
+                                 !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, bn, true))))
+                return MOELORA_ECUDA;
         }
-        if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
-        const int rows = pc ? 64 : pair_box_rows(bn);
-        if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H) ||
-            !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, rows) ||
-            (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
-            (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r) ||
-                             !encode_b2_map(&tc.bmap1, B2, d->L, d->E, d->H, d->r, true) ||
-                             !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, bn) ||
-                             !encode_zexp_map(&tc.zxmap1, tc.zexp, L.P, d->L, d->r, pc ? bn / 2 : bn, true))))
-            return MOELORA_ECUDA;
         const long tasks = L.tiles_dn * L.ks_dn + L.st_tasks_max * L.s2;
         tr.mark(3);
         if (pc) {

@@ -89,7 +89,7 @@ def test_split_plan_follows_the_sm_count(lib):
         return out
 
     decode = (16, 2880, 2880, 32, 4, 8, 32)
-    dense = (256, 8192, 28672, 1, 1, 32, 64)
+    dense = (256, 8192, 28672, 1, 1, 32, 64, 0, B.MOELORA_OPT_SINGLE_CTA)  # one-CTA GEMM plan
     s = {n: lay(n, *decode) for n in (1, 38, 76, 152, 304)}
     assert s[1]["s1"] == s[1]["s2"] == 1
     assert s[1]["s1"] <= s[38]["s1"] <= s[76]["s1"] <= s[152]["s1"] <= s[304]["s1"]
@@ -154,19 +154,28 @@ def test_no_device_is_an_error_not_a_fallback(lib):
     assert st == B.MOELORA_ECUDA
 
 
-def test_pair_cta_option_plan(lib):
-    # wide chunks with the option: CTA pairs; without it, or for decode-sized
-    # chunks, one CTA per tile; unknown option bits are rejected
-    wide = B.dims(2048, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_PAIR_CTA)
-    assert B.moe_lora_workspace_layout(wide)["gemm_ctas"] == 2
-    assert B.moe_lora_workspace_layout(B.dims(2048, 2880, 2880, 32, 4, 8, 32))["gemm_ctas"] == 1
-    decode = B.dims(16, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_PAIR_CTA)
-    assert B.moe_lora_workspace_layout(decode)["gemm_ctas"] == 1
-    # the dense T=256 MLP: 224 gate_up pair tasks (112 tiles x two 128-pair chunks) need no K split
-    dense = B.dims(256, 8192, 28672, 1, 1, 32, 64, 0, B.MOELORA_OPT_PAIR_CTA)
-    assert B.moe_lora_workspace_layout(dense)["gemm_ctas"] == 2
+def test_gemm_plan_cta_pairs_for_wide_chunks(lib):
+    """Wide chunks (more than 48 pairs per expert) run on CTA pairs by default,
+    with chains of at most 256 weight rows (a multiple of 16, as few chains as
+    possible); MOELORA_OPT_SINGLE_CTA, decode-sized chunks and more adapters
+    than a chunk mask holds keep one CTA per task; unknown option bits are
+    rejected."""
+    wide = B.dims(2048, 2880, 2880, 32, 4, 8, 32)
+    lay = B.moe_lora_workspace_layout(wide)
+    assert lay["gemm_ctas"] == 2 and lay["tc_expand"] == 1
+    single = B.dims(2048, 2880, 2880, 32, 4, 8, 32, 0, B.MOELORA_OPT_SINGLE_CTA)
+    assert B.moe_lora_workspace_layout(single)["gemm_ctas"] == 1
+    assert B.moe_lora_workspace_layout(B.dims(16, 2880, 2880, 32, 4, 8, 32))["gemm_ctas"] == 1
+    # the dense T=256 MLP: one 256-pair chunk; the down GEMM splits K into slabs
+    dense = B.moe_lora_workspace_layout(B.dims(256, 8192, 28672, 1, 1, 32, 64))
+    assert dense["gemm_ctas"] == 2 and dense["down_splits"] > 1
+    # a layer without adapters, and one with few adapters (the pair kernel
+    # takes the tensor-core expand whatever the adapter mix)
+    assert B.moe_lora_workspace_layout(B.dims(2048, 2880, 2880, 32, 4, 0, 0))["gemm_ctas"] == 2
+    few = B.moe_lora_workspace_layout(B.dims(600, 128, 136, 2, 2, 1, 8))
+    assert few["gemm_ctas"] == 2 and few["tc_expand"] == 1
     # more adapters than a chunk mask holds: the pair kernel does not cover it
-    many = B.dims(2048, 2880, 2880, 32, 4, 80, 32, 0, B.MOELORA_OPT_PAIR_CTA)
+    many = B.dims(2048, 2880, 2880, 32, 4, 80, 32)
     assert B.moe_lora_workspace_layout(many)["gemm_ctas"] == 1
     with pytest.raises(B.MoeLoraError):
         B.moe_lora_workspace_layout(B.dims(16, 64, 64, 2, 1, 0, 0, 0, 2))

@@ -91,10 +91,13 @@ def test_ragged_shapes(shape):
     check_layer(layer)
 
 
-# wide chunks, the LoRA mixes the pair kernel covers (tensor-core expand with
-# r_pad 16 / 32 / 64, shrink items in one or both CTAs, shrink and down K
-# splits), ragged tiles of both GEMMs, and a mix it does not cover (CUDA-core
-# expand: the option falls back to one CTA per tile)
+# wide chunks on CTA pairs (the default for more than 48 pairs per expert):
+# ragged intermediate and hidden sizes (chains of 16-multiples beyond I or H),
+# r_pad 16 / 32 / 64 with one, two or four adapters per expand block, shrink
+# items in one or both CTAs of a pair and split over K, the down GEMM split
+# over K into slabs, chunks with a tail of a few pairs, a layer without
+# adapters, and one with a single adapter (the tensor-core expand on a
+# one-adapter mix)
 PAIR_SHAPES = [
     (300, 256, 520, 2, 2, 0, 0),
     (256, 512, 1024, 1, 1, 4, 16),
@@ -103,24 +106,28 @@ PAIR_SHAPES = [
     (300, 96, 1032, 2, 1, 8, 64),
     (160, 128, 96, 2, 2, 11, 8),
     (130, 200, 48, 1, 1, 3, 32),
+    (600, 128, 136, 2, 2, 1, 8),
+    (520, 264, 200, 2, 1, 9, 16),
+    (100, 2048, 512, 1, 1, 7, 24),
 ]
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES)
-def test_pair_cta_option(shape):
+def test_cta_pair_kernel(shape):
     layer = wl.make_random(*shape, seed=7)
-    dl, err = check_layer(layer, options=B.MOELORA_OPT_PAIR_CTA)
-    pair = B.moe_lora_workspace_layout(dl.d)["gemm_ctas"] == 2
-    assert pair == (shape != PAIR_SHAPES[-1])
-    # same results as one CTA per tile, within rounding
-    base = check_layer(layer)[0].out_f64()
-    assert norm_err(dl.out_f64(), base) <= TOL
+    dl, err = check_layer(layer)
+    assert B.moe_lora_workspace_layout(dl.d)["gemm_ctas"] == 2
+    # the one-CTA kernels on the same layer agree within rounding
+    one, _ = check_layer(layer, options=B.MOELORA_OPT_SINGLE_CTA)
+    assert B.moe_lora_workspace_layout(one.d)["gemm_ctas"] == 1
+    assert norm_err(dl.out_f64(), one.out_f64()) <= TOL
 
 
 @pytest.mark.slow
-def test_pair_cta_option_prefill():
-    # every output of the prefill chunk (wide chunks, K-split slabs, expand blocks)
-    check_layer(wl.make_config(2), options=B.MOELORA_OPT_PAIR_CTA)
+def test_single_cta_option_prefill():
+    # every output of the prefill chunk on the one-CTA kernels (128- and
+    # 256-pair chunks, K-split slabs, expand blocks)
+    check_layer(wl.make_config(2), options=B.MOELORA_OPT_SINGLE_CTA)
 
 
 def test_config0():
@@ -385,52 +392,67 @@ def test_config4_dense(T):
     check_layer(wl.make_config(4, T=T))
 
 
-def _silu_probe_layer(u, adapters: bool):
-    """One expert whose first gate unit copies feature 0 of x, whose first up
-    unit copies the constant feature 1, and whose first output copies act unit
-    0: out[t][0] = bf16(SiLU(u_t)) with every product and sum exact.  With
-    `adapters`, every token carries adapter 0 of a rank-8 LoRA whose A and B
-    are zero: its delta adds exact zeros, and with one adapter per expert
-    chunk the expand runs on CUDA cores, so the activation goes through that
-    epilogue instead of the lean one."""
-    T, H, I = len(u), 64, 64
+def _silu_probe_layer(u, adapters: bool, experts: int):
+    """Experts (all alike) whose first gate unit copies feature 0 of x, whose
+    first up unit copies the constant feature 1, and whose first output
+    copies act unit 0: out[t][0] = bf16(SiLU(u_t)) with every product and sum
+    exact.  Token t goes to expert t mod `experts`: many experts keep the
+    chunks decode-sized (one-CTA kernels), one expert makes them wide (CTA
+    pairs).  With `adapters`, every token carries adapter 0 of a rank-8 LoRA
+    whose A and B are zero: its delta adds exact zeros, and the activation
+    goes through the epilogue that follows a LoRA expand."""
+    T, H, I, E = len(u), 64, 64, experts
     x = np.zeros((T, H), np.float32)
     x[:, 0] = u
     x[:, 1] = 1.0
-    W1 = np.zeros((1, 2 * I, H), np.float32)
-    W1[0, 0, 0] = 1.0          # gate unit 0 <- x[:, 0]
-    W1[0, I, 1] = 1.0          # up unit 0 <- 1
-    W2 = np.zeros((1, H, I), np.float32)
-    W2[0, 0, 0] = 1.0          # out[:, 0] <- act unit 0
+    W1 = np.zeros((E, 2 * I, H), np.float32)
+    W1[:, 0, 0] = 1.0          # gate unit 0 <- x[:, 0]
+    W1[:, I, 1] = 1.0          # up unit 0 <- 1
+    W2 = np.zeros((E, H, I), np.float32)
+    W2[:, 0, 0] = 1.0          # out[:, 0] <- act unit 0
     b = wl.bf16_bits
     L, r = (1, 8) if adapters else (0, 0)
     A1 = B1 = A2 = B2 = None
     if adapters:
-        A1 = np.zeros((L, 1, r, H), np.uint16)
-        B1 = np.zeros((L, 1, 2 * I, r), np.uint16)
-        A2 = np.zeros((L, 1, r, I), np.uint16)
-        B2 = np.zeros((L, 1, H, r), np.uint16)
+        A1 = np.zeros((L, E, r, H), np.uint16)
+        B1 = np.zeros((L, E, 2 * I, r), np.uint16)
+        A2 = np.zeros((L, E, r, I), np.uint16)
+        B2 = np.zeros((L, E, H, r), np.uint16)
     lora = np.zeros(T, np.int32) if adapters else np.full(T, -1, np.int32)
-    return wl.Layer("silu_probe", T, H, I, 1, 1, L, r, b(x), b(W1), b(W2), A1, B1, A2, B2,
-                    np.zeros((T, 1), np.int32), np.ones((T, 1), np.float32), lora)
+    ids = (np.arange(T, dtype=np.int32) % E).reshape(T, 1)
+    return wl.Layer("silu_probe", T, H, I, E, 1, L, r, b(x), b(W1), b(W2), A1, B1, A2, B2,
+                    ids, np.ones((T, 1), np.float32), lora)
 
 
-@pytest.mark.parametrize("epilogue", ["lean", "cuda_core_expand"])
-def test_silu_sweep_against_fp64(epilogue):
+# (adapters, wide chunks) -> the epilogue that computes SiLU(gate) * up
+SILU_PATHS = {
+    "one_cta_lean": (False, False),
+    "one_cta_cuda_core_expand": (True, False),
+    "cta_pair": (False, True),
+    "cta_pair_tc_expand": (True, True),
+}
+
+
+@pytest.mark.parametrize("path", list(SILU_PATHS))
+def test_silu_sweep_against_fp64(path):
     """The GPU's SiLU(u) = u / (1 + exp(-u)), rounded once to bf16, against the
     fp64 definition over every bf16 value of u in [-120, 120] on a grid, in
-    both epilogues that compute it: the lean one (no CUDA-core expand, fast
-    exponential and division) and the one that adds the LoRA expand on CUDA
-    cores.  Past |u| ~ 88 the exponential of -u leaves the fp32 range
-    (overflow to infinity for u < 0, underflow to zero for u > 0): SiLU must
-    then give 0 (at most 1e-30 away from the true, tiny value) or u itself.
-    One bf16 ulp (2^-8 relative) is allowed elsewhere."""
+    every epilogue that computes it: the one-CTA kernel's lean epilogue and
+    its CUDA-core LoRA expand epilogue, and the CTA-pair kernel's (without
+    and after the tensor-core expand).  Past |u| ~ 88 the exponential of -u
+    leaves the fp32 range (overflow to infinity for u < 0, underflow to zero
+    for u > 0): SiLU must then give 0 (at most 1e-30 away from the true,
+    tiny value) or u itself.  One bf16 ulp (2^-8 relative) is allowed
+    elsewhere."""
+    adapters, wide = SILU_PATHS[path]
     grid = np.concatenate([np.linspace(-120.0, 120.0, 3001), [-88.7, -88.0, -87.3, 87.3, 88.0, 88.7]])
     u = np.unique(wl.bf16_to_f32(wl.bf16_bits(grid.astype(np.float32))).astype(np.float64))
-    dl, st = run(_silu_probe_layer(u.astype(np.float32), adapters=epilogue != "lean"))
+    experts = 1 if wide else (len(u) + 39) // 40
+    dl, st = run(_silu_probe_layer(u.astype(np.float32), adapters, experts))
     assert st == 0
     lay = B.moe_lora_workspace_layout(dl.d)
-    assert lay["tc_expand"] == 0
+    assert lay["gemm_ctas"] == (2 if wide else 1)
+    assert lay["tc_expand"] == (1 if (adapters and wide) else 0)
     got = dl.out_f64()[:, 0]
     ref = u / (1.0 + np.exp(-u))
     assert np.all(np.isfinite(got))
