@@ -114,6 +114,7 @@ struct GatherArgs {
     const int32_t* compact_ids;
     const WsHeader* hdr;
     uint16_t* out;               // [P][H] rows in bucket order
+    int wpr;                     // warps per row (1 .. 8)
     uint16_t* zexp1;             // [zx_elems] zeroed here (null: none)
     uint16_t* zexp2;
     long zx_elems;

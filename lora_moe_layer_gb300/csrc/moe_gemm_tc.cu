@@ -726,26 +726,31 @@ cudaError_t set_attr() {
 }
 
 // ---------------------------------------------------------------- gather
-// rows of x in bucket (compact) order, the B operand of the gate_up GEMM
+// rows of x in bucket (compact) order, the B operand of the gate_up GEMM:
+// `wpr` warps per row (few rows: several warps share one), each row's token
+// id read once per warp, lanes over the row's 16-byte chunks
 __global__ void __launch_bounds__(256) k_gather_rows(GatherArgs a) {
     pdl_wait();
     pdl_trigger();
     const int n = a.hdr->n_valid;
     const int c8 = a.H >> 3;
-    const long total = (long)n * c8;
-    const long stride = (long)gridDim.x * blockDim.x;
-    const long first = (long)blockIdx.x * blockDim.x + threadIdx.x;
-#pragma unroll 4
-    for (long idx = first; idx < total; idx += stride) {
-        const int q = (int)(idx / c8), c = (int)(idx % c8);
+    const int lane = threadIdx.x & 31;
+    const int wpr = a.wpr;
+    const long warps = (long)gridDim.x * (blockDim.x >> 5);
+    for (long w = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < (long)n * wpr; w += warps) {
+        const int q = (int)(w / wpr), part = (int)(w % wpr);
         const int t = a.compact_ids[q] / a.k;
-        *reinterpret_cast<uint4*>(a.out + (size_t)q * a.H + c * 8) = ld_ro16(a.x + (size_t)t * a.H + c * 8);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)t * a.H);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + (size_t)q * a.H);
+#pragma unroll 4
+        for (int c = part * 32 + lane; c < c8; c += 32 * wpr) dst[c] = ld_ro16(src + c);
     }
     // zexp starts as zeros; the shrink items fill each pair's own adapter
     if (a.zexp1) {
         const long nz = a.zx_elems / 8;
+        const long stride = (long)gridDim.x * blockDim.x;
         const uint4 zero = make_uint4(0, 0, 0, 0);
-        for (long i = first; i < nz; i += stride) {
+        for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < nz; i += stride) {
             reinterpret_cast<uint4*>(a.zexp1)[i] = zero;
             reinterpret_cast<uint4*>(a.zexp2)[i] = zero;
         }

@@ -611,8 +611,9 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     }
     tr.mark(1);
     {
-        const long n = L.P * (d->H / 8);
-        const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
+        // warps per row: enough warps for 64 per SM, at most 8 per row
+        ga.wpr = (int)std::max<long>(1, std::min<long>(8, (long)sms * 64 / std::max<long>(L.P, 1)));
+        const int grid = (int)std::max<long>(1, std::min<long>((L.P * ga.wpr + 7) / 8, (long)sms * 8));
         if (launch_gather_rows(ga, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }
 

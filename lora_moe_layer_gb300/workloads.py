@@ -119,6 +119,8 @@ class Layer:
     topk_weights: np.ndarray
     lora_ids: np.ndarray
     meta: dict = dataclasses.field(default_factory=dict)
+    # FP8 base expert weights (see quantize_e4m3), or None
+    w8: Optional["W8Weights"] = None
 
     @property
     def P(self) -> int:
@@ -276,3 +278,38 @@ def make_random(T: int, H: int, I: int, E: int, k: int, L: int, r: int, seed: in
         lora[rng.random(T) < p_base] = -1
     return make_layer(f"random_T{T}_H{H}_I{I}_E{E}_k{k}_L{L}_r{r}", T, H, I, E, k, L, r, lora,
                       seed=seed, with_lora=L > 0)
+
+
+# ---------------------------------------------------------------------------- FP8 weights
+
+@dataclasses.dataclass
+class W8Weights:
+    """E4M3 codes of the base expert weights with one fp32 scale per output
+    row: W1q [E][2I][H] uint8, W1s [E][2I] float32, W2q [E][H][I], W2s [E][H];
+    weight = scale * value(code)."""
+    W1q: np.ndarray
+    W1s: np.ndarray
+    W2q: np.ndarray
+    W2s: np.ndarray
+
+
+def _e4m3_rows(bits: np.ndarray):
+    """Per-row symmetric quantisation of bf16 rows (last axis) to E4M3: scale =
+    max |row| / 448 (the largest finite E4M3 value), codes = the row / scale
+    rounded to nearest by torch's float8_e4m3fn conversion."""
+    import torch
+    w = bf16_to_f32(bits).astype(np.float32)
+    amax = np.max(np.abs(w), axis=-1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = torch.from_numpy(np.ascontiguousarray(w / scale[..., None])).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8).numpy().copy(), scale
+
+
+def quantize_e4m3(layer: Layer) -> Layer:
+    """The layer with its base expert weights W1, W2 replaced by E4M3 codes and
+    per-output-row scales (the LoRA matrices stay bf16).  The bf16 W1 and W2
+    are kept for reference; the FP8 forward reads only layer.w8."""
+    W1q, W1s = _e4m3_rows(layer.W1)
+    W2q, W2s = _e4m3_rows(layer.W2)
+    return dataclasses.replace(layer, name=layer.name + "_e4m3", w8=W8Weights(W1q, W1s, W2q, W2s))
+

@@ -29,6 +29,10 @@ def load_library(path: str):
     P = ctypes.c_void_p
     lib.oracle_forward.restype = ctypes.c_long
     lib.oracle_forward.argtypes = [ctypes.POINTER(_Dims)] + [P] * 10 + [P, ctypes.c_int, P, ctypes.c_int]
+    lib.oracle_forward_w8.restype = ctypes.c_long
+    lib.oracle_forward_w8.argtypes = [ctypes.POINTER(_Dims)] + [P] * 12 + [P, ctypes.c_int, P, ctypes.c_int]
+    lib.oracle_e4m3.restype = ctypes.c_double
+    lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_pair.restype = ctypes.c_int
     lib.oracle_pair.argtypes = [ctypes.POINTER(_Dims)] + [P] * 9 + [ctypes.c_long] + [P] * 5
     lib.oracle_align.restype = ctypes.c_long
@@ -91,6 +95,39 @@ def forward(layer, tokens=None, n_threads: int | None = None, lib=None):
     if inv < 0:
         raise ValueError("oracle_forward: bad arguments")
     return out, int(inv)
+
+
+def forward_w8(layer, tokens=None, n_threads: int | None = None, lib=None):
+    """fp64 layer output with FP8 base expert weights (layer.w8: E4M3 codes and
+    per-output-row scales, weight = scale * value(code)); the LoRA matrices
+    are the layer's bf16 ones.  Returns (out, n_invalid_pairs)."""
+    lib = lib or _load()
+    q = layer.w8
+    if q is None:
+        raise ValueError("forward_w8: the layer has no FP8 weights")
+    d, a = _args(layer)
+    if tokens is None:
+        tok = None
+        n = layer.T
+    else:
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        n = tok.size
+    W1q, W2q = _c(q.W1q, np.uint8), _c(q.W2q, np.uint8)
+    W1s, W2s = _c(q.W1s, np.float32), _c(q.W2s, np.float32)
+    out = np.zeros((n, layer.H), dtype=np.float64)
+    nt = n_threads or default_threads()
+    inv = lib.oracle_forward_w8(ctypes.byref(d), _ptr(a["x"]), _ptr(a["topk_ids"]), _ptr(a["topk_weights"]),
+                                _ptr(a["lora_ids"]), _ptr(W1q), _ptr(W1s), _ptr(W2q), _ptr(W2s),
+                                _ptr(a["A1"]), _ptr(a["B1"]), _ptr(a["A2"]), _ptr(a["B2"]), _ptr(tok), n,
+                                _ptr(out), nt)
+    if inv < 0:
+        raise ValueError("oracle_forward_w8: bad arguments")
+    return out, int(inv)
+
+
+def e4m3(code: int, lib=None) -> float:
+    """Value of one E4M3 code by the oracle's decoder."""
+    return float((lib or _load()).oracle_e4m3(int(code)))
 
 
 def pair(layer, p: int, lib=None):

@@ -34,6 +34,11 @@
  *
  * Pairs with an expert id outside [0, E) or a token adapter id outside
  * [-1, L) contribute nothing and are counted in the return value.
+ *
+ * oracle_forward_w8 is the same layer with FP8 base expert weights (the
+ * fused-MoE news item's second optimisation moves MoE weights to FP8): E4M3
+ * codes with one fp32 scale per output row, each weight scale * value(code)
+ * in fp64, decoded from the format's definition (oracle_e4m3).
  */
 #include <math.h>
 #include <stdint.h>
@@ -44,12 +49,51 @@ typedef struct {
     int T, H, I, E, k, L, r;
 } oracle_dims;
 
+/*
+ * FP8 base expert weights (the fused-MoE news item's second optimisation,
+ * FP8 MoE weights): W1q [E][2I][H] and W2q [E][H][I] hold 8-bit E4M3 codes,
+ * W1s [E][2I] and W2s [E][H] one fp32 scale per output row; the weight is
+ * scale * value(code).  The LoRA A and B stay bfloat16.
+ */
+typedef struct {
+    const uint8_t *W1q, *W2q;
+    const float *W1s, *W2s;
+} oracle_w8;
+
 static double bf(uint16_t b)
 {
     uint32_t u = (uint32_t)b << 16;
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/*
+ * Value of an E4M3 code (OCP 8-bit floating point, the finite "fn" variant):
+ * sign bit s, 4-bit exponent field f with bias 7, 3-bit mantissa m.  f = 0:
+ * subnormal (-1)^s * (m / 8) * 2^-6; f = 15 with m = 7: not a number (the
+ * format has no infinities); otherwise (-1)^s * (1 + m / 8) * 2^(f - 7).
+ */
+double oracle_e4m3(uint8_t c)
+{
+    const int s = c >> 7, f = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (f == 15 && m == 7)
+        return NAN;
+    if (f == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, f - 7);
+    return s ? -v : v;
+}
+
+/* dot(row of E4M3 codes times the row's scale, vector of double), in index order */
+static double dot_w8(const uint8_t *row, float scale, const double *v, long n)
+{
+    double s = 0.0;
+    for (long i = 0; i < n; i++)
+        s += ((double)scale * oracle_e4m3(row[i])) * v[i];
+    return s;
 }
 
 /* SiLU(u) = u * sigmoid(u) = u / (1 + e^{-u}) */
@@ -76,7 +120,8 @@ static double dot_bf(const uint16_t *row, const double *v, long n)
  * work must hold 2I + I + H + 2r doubles.
  */
 static void pair_ffn(const oracle_dims *d, const double *xd, int e, int l,
-                     const uint16_t *W1, const uint16_t *W2, const uint16_t *A1,
+                     const uint16_t *W1, const uint16_t *W2, const oracle_w8 *q,
+                     const uint16_t *A1,
                      const uint16_t *B1, const uint16_t *A2, const uint16_t *B2,
                      double *work, double *z1_out, double *g_out, double *act_out,
                      double *z2_out, double *d_out)
@@ -89,9 +134,14 @@ static void pair_ffn(const oracle_dims *d, const double *xd, int e, int l,
     double *z2 = z1 + r;         /* r  */
     const int lora = (l >= 0) && A1 && B1 && A2 && B2 && r > 0;
 
-    /* gate_up base: g = W1[e] x */
-    for (long o = 0; o < 2 * I; o++)
-        g[o] = dot_bf(W1 + ((long)e * 2 * I + o) * H, xd, H);
+    /* gate_up base: g = W1[e] x (bf16 weights, or FP8 codes times their row's scale) */
+    if (!q) {
+        for (long o = 0; o < 2 * I; o++)
+            g[o] = dot_bf(W1 + ((long)e * 2 * I + o) * H, xd, H);
+    } else {
+        for (long o = 0; o < 2 * I; o++)
+            g[o] = dot_w8(q->W1q + ((long)e * 2 * I + o) * H, q->W1s[(long)e * 2 * I + o], xd, H);
+    }
     /* gate_up LoRA: shrink z1 = A1[l][e] x, expand g += B1[l][e] z1 */
     if (lora) {
         for (long q = 0; q < r; q++)
@@ -106,8 +156,13 @@ static void pair_ffn(const oracle_dims *d, const double *xd, int e, int l,
     for (long i = 0; i < I; i++)
         act[i] = silu(g[i]) * g[I + i];
     /* down base: dv = W2[e] act */
-    for (long h = 0; h < H; h++)
-        dv[h] = dot_bf(W2 + ((long)e * H + h) * I, act, I);
+    if (!q) {
+        for (long h = 0; h < H; h++)
+            dv[h] = dot_bf(W2 + ((long)e * H + h) * I, act, I);
+    } else {
+        for (long h = 0; h < H; h++)
+            dv[h] = dot_w8(q->W2q + ((long)e * H + h) * I, q->W2s[(long)e * H + h], act, I);
+    }
     /* down LoRA: shrink z2 = A2[l][e] act, expand dv += B2[l][e] z2 */
     if (lora) {
         for (long q = 0; q < r; q++)
@@ -136,13 +191,16 @@ static int dims_ok(const oracle_dims *d)
  * out[n][H] receives the unrounded fp64 result of token tokens[n].
  * Returns the number of invalid pairs met, or -1 on bad arguments.
  */
-long oracle_forward(const oracle_dims *d, const uint16_t *x, const int32_t *topk_ids,
-                    const float *topk_weights, const int32_t *lora_ids,
-                    const uint16_t *W1, const uint16_t *W2, const uint16_t *A1,
-                    const uint16_t *B1, const uint16_t *A2, const uint16_t *B2,
-                    const int32_t *tokens, int n_tokens, double *out, int n_threads)
+static long forward_impl(const oracle_dims *d, const uint16_t *x, const int32_t *topk_ids,
+                         const float *topk_weights, const int32_t *lora_ids,
+                         const uint16_t *W1, const uint16_t *W2, const oracle_w8 *q,
+                         const uint16_t *A1, const uint16_t *B1, const uint16_t *A2,
+                         const uint16_t *B2, const int32_t *tokens, int n_tokens, double *out,
+                         int n_threads)
 {
-    if (!dims_ok(d) || !x || !topk_ids || !topk_weights || !lora_ids || !W1 || !W2 || !out)
+    if (!dims_ok(d) || !x || !topk_ids || !topk_weights || !lora_ids || !out)
+        return -1;
+    if (q ? !(q->W1q && q->W2q && q->W1s && q->W2s) : !(W1 && W2))
         return -1;
     if (!tokens)
         n_tokens = d->T;
@@ -175,7 +233,7 @@ long oracle_forward(const oracle_dims *d, const uint16_t *x, const int32_t *topk
                     continue;
                 }
                 const double w = (double)topk_weights[(long)t * d->k + j];
-                pair_ffn(d, xd, e, l, W1, W2, A1, B1, A2, B2, work, NULL, NULL, NULL, NULL, dv);
+                pair_ffn(d, xd, e, l, W1, W2, q, A1, B1, A2, B2, work, NULL, NULL, NULL, NULL, dv);
                 /* weighted aggregation over the token's k experts, in slot order */
                 for (long h = 0; h < H; h++)
                     acc[h] += w * dv[h];
@@ -186,6 +244,33 @@ long oracle_forward(const oracle_dims *d, const uint16_t *x, const int32_t *topk
         free(dv);
     }
     return invalid;
+}
+
+long oracle_forward(const oracle_dims *d, const uint16_t *x, const int32_t *topk_ids,
+                    const float *topk_weights, const int32_t *lora_ids,
+                    const uint16_t *W1, const uint16_t *W2, const uint16_t *A1,
+                    const uint16_t *B1, const uint16_t *A2, const uint16_t *B2,
+                    const int32_t *tokens, int n_tokens, double *out, int n_threads)
+{
+    return forward_impl(d, x, topk_ids, topk_weights, lora_ids, W1, W2, NULL, A1, B1, A2, B2,
+                        tokens, n_tokens, out, n_threads);
+}
+
+/*
+ * The same forward with FP8 base expert weights: W1q [E][2I][H], W2q [E][H][I]
+ * E4M3 codes, W1s [E][2I], W2s [E][H] fp32 row scales (weight = scale *
+ * value(code)); the LoRA matrices stay bf16.
+ */
+long oracle_forward_w8(const oracle_dims *d, const uint16_t *x, const int32_t *topk_ids,
+                       const float *topk_weights, const int32_t *lora_ids,
+                       const uint8_t *W1q, const float *W1s, const uint8_t *W2q,
+                       const float *W2s, const uint16_t *A1, const uint16_t *B1,
+                       const uint16_t *A2, const uint16_t *B2, const int32_t *tokens,
+                       int n_tokens, double *out, int n_threads)
+{
+    const oracle_w8 q = {W1q, W2q, W1s, W2s};
+    return forward_impl(d, x, topk_ids, topk_weights, lora_ids, NULL, NULL, &q, A1, B1, A2, B2,
+                        tokens, n_tokens, out, n_threads);
 }
 
 /*
@@ -218,7 +303,7 @@ int oracle_pair(const oracle_dims *d, const uint16_t *x, const int32_t *topk_ids
     double *xd = (double *)malloc(sizeof(double) * (size_t)H);
     for (long h = 0; h < H; h++)
         xd[h] = bf(x[t * H + h]);
-    pair_ffn(d, xd, e, l, W1, W2, A1, B1, A2, B2, work, z1, g, act, z2, dvec);
+    pair_ffn(d, xd, e, l, W1, W2, NULL, A1, B1, A2, B2, work, z1, g, act, z2, dvec);
     free(work);
     free(xd);
     return 0;
