@@ -110,8 +110,8 @@ MOELORA_API int moe_lora_version(void);
  * Host only, pure. */
 MOELORA_API int64_t moe_lora_align_capacity(const moe_lora_dims *d);
 
-/* Bytes of device workspace that moe_lora_forward and moe_lora_align need
- * for these dims (0 if the dims are invalid).  Host only; with
+/* Bytes of device workspace that moe_lora_forward, moe_lora_forward_w8 and
+ * moe_lora_align need for these dims (0 if the dims are invalid).  Host only; with
  * d->sm_count == 0 it reads the current device's multiprocessor count (no
  * launch, no allocation), else it is pure. */
 MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims *d);
@@ -161,6 +161,32 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
                                  const void *W2, const void *A1, const void *B1,
                                  const void *A2, const void *B2, void *out,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The forward with FP8 base expert weights and bf16 LoRA (the fused-MoE news
+ * item's second optimisation: FP8 MoE weights, dequantised inside the fused
+ * GEMM).  Instead of W1 and W2:
+ *   W1q [E][2I][H], W2q [E][H][I]: 8-bit E4M3 codes (the finite "fn" form:
+ *     sign, 4-bit exponent with bias 7, 3-bit mantissa; largest value 448);
+ *   W1s [E][2I], W2s [E][H]: one fp32 scale per output row; the weight is
+ *     scale * value(code).
+ * Every other argument, the workspace and the result are those of
+ * moe_lora_forward.  The GEMMs run on the CTA-pair kernels for every batch
+ * size: the codes stream from HBM by TMA, and each code is turned into
+ * bf16(scale * value) in shared memory right before the bf16 MMAs read it
+ * (one rounding of the scaled weight to bf16; activations stay bf16, fp32
+ * accumulation).  H and I must be multiples of 16 and the layer within the
+ * CTA-pair kernels' bounds (at most 64 adapters, zexp within bounds), else
+ * MOELORA_EUNSUPPORTED.  Pointers 16-byte aligned.  Asynchronous on
+ * `stream`; same status codes as moe_lora_forward.
+ */
+MOELORA_API int moe_lora_forward_w8(const moe_lora_dims *d, const void *x,
+                                    const int32_t *topk_ids, const float *topk_weights,
+                                    const int32_t *token_lora_ids, const void *W1q,
+                                    const float *W1s, const void *W2q, const float *W2s,
+                                    const void *A1, const void *B1, const void *A2,
+                                    const void *B2, void *out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
 
 /*
  * moe_lora_forward with timing marks, for profiling the kernels one by one on

@@ -94,6 +94,12 @@ struct TcArgs {
     int* task_counter;           // next task to take (each CTA takes its next one when it is ready for
                                  // it), zeroed by align; null: tasks dealt round-robin over the CTAs
     int nu;                      // CTA-pair kernel: weight rows per MMA chain (multiple of 16, <= 256)
+    // CTA-pair kernel with FP8 base weights: E4M3 codes of W1 as {H, I, 2, E} /
+    // W2 as {I, H, E}, box 64 codes x nu/2 rows; one fp32 scale per output row
+    // (W1s [E][2I] / W2s [E][H]); n8 stages of the code staging ring
+    CUtensorMap w8map;
+    const float* wscale;
+    int w8, n8;
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
 int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks);
@@ -102,8 +108,10 @@ cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int gri
 // The same GEMMs for wide pair chunks on CTA pairs (moe_gemm_2sm.cu): M = 256
 // pair rows over the pair (chunks of up to 256 pairs), two chains of nu weight
 // rows, tensor-core expand only, chunk masks required, gate_up without K split.
-int tc2_smem_bytes(int E, int nstages, int max_chunks);
+int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8 = 0);
 int tc2_plan_stages(int E, int max_chunks);
+// FP8 base weights: the main ring and the code staging ring (stages of each), 0 if none fit
+int tc2_plan_stages_w8(int E, int max_chunks, int* n8);
 cudaError_t init_tc2_attributes();
 int tc2_max_pairs(bool gate_up);  // co-resident pairs (0: none or query failed)
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl);

@@ -54,6 +54,8 @@
 //            warps free the accumulator on the leader's barrier.
 // Every wait is bounded; on a timeout the CTA records kStatusTimeout, stops
 // waiting, drains its copies, frees TMEM and exits at the final pair barrier.
+#include <cuda_fp16.h>
+
 #include "gemm_tasks.cuh"
 
 namespace moelora {
@@ -65,6 +67,8 @@ constexpr int kTmem2 = 512;                     // the whole TMEM of the SM: one
 constexpr int kChain1Col = 256;                 // first TMEM column of chain 1
 constexpr int kSlot = 128 * kBK * 2;            // 16 KiB: 128 rows of one 64-wide K step
 constexpr int kStage2 = 3 * kSlot;              // pair rows, chain-0 rows, chain-1 rows
+constexpr int kF8Slot = 2 * 128 * kBK;          // FP8 codes of one K step: nu / 2 rows of each chain
+constexpr int kThreadsW8 = kTcThreads + 32;     // FP8 weights: one more warp, the code producer
 constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
 // down epilogue: each warp turns its 32 pairs x 16 columns into whole
 // 64-byte runs of 8 rows per store through a padded tile (row stride of 20
@@ -207,12 +211,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // tables and the task table.
 struct Smem2 {
     uint8_t* ring;
-    uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed
+    uint8_t* f8;      // [n8][kF8Slot] FP8 weights: staged codes
+    uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed (FP8 weights: and converted)
     uint64_t* empty;  // [NS] the pair's MMAs are done with stage s
     uint64_t* tfull;  // accumulator ready for the epilogue
     uint64_t* tempty; // leader: accumulator drained by both CTAs' epilogues
     uint64_t* ebar;   // epilogue rendezvous
     uint32_t* tmem_slot;
+    uint64_t* w8full;   // [n8] FP8 weights: this CTA's codes of a staging slot landed
+    uint64_t* w8empty;  // [n8] FP8 weights: this CTA's converters are done with a staging slot
     int* s_cb;        // [kMaxShrinkSlots] first row (relative to the item) of each slot's bucket
     int* s_ce;        // [kMaxShrinkSlots] one past its last row
     int* s_sl;        // [kMaxShrinkSlots] adapter of each slot
@@ -224,14 +231,18 @@ struct Smem2 {
 __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     Smem2 m;
     m.ring = base;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * kStage2);
+    m.f8 = base + (size_t)NS * kStage2;
+    const int n8 = a.w8 ? a.n8 : 0;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(m.f8 + (size_t)n8 * kF8Slot);
     m.full = bars;
     m.empty = m.full + NS;
     m.tfull = m.empty + NS;
     m.tempty = m.tfull + 1;
     m.ebar = m.tempty + 1;
     m.tmem_slot = reinterpret_cast<uint32_t*>(m.ebar + 1);
-    m.s_cb = reinterpret_cast<int*>(m.tmem_slot + 4);
+    m.w8full = reinterpret_cast<uint64_t*>(m.tmem_slot + 4);
+    m.w8empty = m.w8full + n8;
+    m.s_cb = reinterpret_cast<int*>(m.w8empty + n8);
     m.s_ce = m.s_cb + kMaxShrinkSlots;
     m.s_sl = m.s_ce + kMaxShrinkSlots;
     m.s_misc = m.s_sl + kMaxShrinkSlots;
@@ -359,8 +370,30 @@ __device__ bool shrink_epilogue_m(const TcArgs& a, int t, int n_lora, int use, u
     return true;
 }
 
-template <bool GATE_UP>
-__global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_constant__ TcArgs a) {
+// E4M3 codes -> bf16 of (scale * value): 16 codes (one 16-byte chunk of a
+// staged row) into the two 16-byte chunks at `dst0` and `dst1`.  The code is
+// widened exactly to f16 by the hardware conversion, then to fp32, scaled and
+// rounded once to bf16.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, float scale, uint4* dst0, uint4* dst1) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const uint16_t pair2 = (uint16_t)(w[i] >> (16 * hh));
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair2));
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+            o[2 * i + hh] = pack_bf16x2(f.x * scale, f.y * scale);
+        }
+    }
+    *dst0 = make_uint4(o[0], o[1], o[2], o[3]);
+    *dst1 = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <bool GATE_UP, bool W8>
+__global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2sm(const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
@@ -370,10 +403,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     const bool leader = rank == 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    const int N8 = W8 ? a.n8 : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
-            mbar_init(&m.full[s], 1);
+            // FP8 weights: the converters of both CTAs arrive too, once per stage
+            mbar_init(&m.full[s], W8 ? 1 + 2 * kEpiWarps : 1);
             mbar_init(&m.empty[s], 1);
+        }
+        for (int j = 0; j < N8; j++) {
+            mbar_init(&m.w8full[j], 1);
+            mbar_init(&m.w8empty[j], kEpiWarps);
         }
         mbar_init(m.tfull, 1);
         mbar_init(m.tempty, 2 * kEpiWarps);
@@ -382,13 +421,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     }
     if (warp == 1) tmem_alloc2(m.tmem_slot, kTmem2);
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&a.wmap);
+        if (!W8) prefetch_tensormap(&a.wmap);
         prefetch_tensormap(&a.xmap);
         if (a.sh_tasks) prefetch_tensormap(&a.amap);
         if (a.tc_expand) {
             prefetch_tensormap(&a.bmap);
             prefetch_tensormap(&a.zxmap);
         }
+        if (W8) prefetch_tensormap(&a.w8map);
     }
     tc_fence_before();
     __syncthreads();
@@ -484,16 +524,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                 const int e = tw.e;
                 const int rows0 = tw.q0c + (int)rank * 128;
                 const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
-                // per CTA: 128 pair rows + nu / 2 rows of each chain (also for expand blocks)
+                // per CTA: 128 pair rows + nu / 2 rows of each chain (also for
+                // expand blocks); with FP8 weights the converters fill the
+                // chain rows of the base K steps
                 const uint32_t bytes_pair = 2u * ((uint32_t)kSlot + 2u * (uint32_t)nu2 * kBK * 2u);
+                const uint32_t bytes_base = W8 ? 2u * (uint32_t)kSlot : bytes_pair;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!acquire(bytes_pair)) { ok = false; break; }
+                    if (!acquire(bytes_base)) { ok = false; break; }
                     uint8_t* dst = m.ring + (size_t)stage * kStage2;
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
                     const int k0 = kb * kBK;
                     tma2_2d(dst, &a.xmap, bar, k0, rows0);
-                    if (GATE_UP) {
+                    if (W8) {
+                        // chain rows come from the converters
+                    } else if (GATE_UP) {
                         // the gate rows, then the up rows, of this CTA's nu / 2 units
                         tma2_4d(dst + kSlot, &a.wmap, bar, k0, c0row, 0, e);
                         tma2_4d(dst + 2 * kSlot, &a.wmap, bar, k0, c0row, 1, e);
@@ -616,6 +661,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
                 umma2_commit_both(m.tfull);
             }
         }
+    } else if (W8 && warp == kEpiWarps + 2) {
+        // --------------------------------------------- FP8 code producer (TMA)
+        // This CTA's codes of both chains for every base K step, into the
+        // staging ring, ahead of the converters by up to n8 steps.
+        if (lane == 0) {
+            int j = 0;
+            uint32_t ph = 0, armed = 0, last_par = 0;
+            const uint32_t bytes = 2u * (uint32_t)nu2 * kBK;
+            for (int t = t_first; t < total && ok; t += t_step) {
+                if (t < n_sh) continue;
+                Task<kPairRows> tw;
+                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+                const int e = tw.e;
+                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
+                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                for (int kb = kb0; kb < kb1; kb++) {
+                    if (!mbar_wait(&m.w8empty[j], ph ^ 1)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&m.w8full[j], bytes);
+                    uint8_t* dst = m.f8 + (size_t)j * kF8Slot;
+                    const int k0 = kb * kBK;
+                    if (GATE_UP) {
+                        tma_load_4d(dst, &a.w8map, &m.w8full[j], k0, c0row, 0, e);
+                        tma_load_4d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c0row, 1, e);
+                    } else {
+                        tma_load_3d(dst, &a.w8map, &m.w8full[j], k0, c0row, e);
+                        tma_load_3d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c1row, e);
+                    }
+                    armed |= 1u << j;
+                    last_par = (last_par & ~(1u << j)) | (ph << j);
+                    if (++j == N8) { j = 0; ph ^= 1; }
+                }
+            }
+            // every issued copy lands before the CTA may exit
+            for (int q = 0; q < N8; q++)
+                if ((armed >> q) & 1u) mbar_wait(&m.w8full[q], (last_par >> q) & 1u);
+        }
     } else {
         // -------------------------------------------------------------- epilogue
         const int ew = warp - 2;         // 0 .. kEpiWarps-1
@@ -637,8 +718,34 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
         };
         const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16);
         const int ngroups = nu / 16;
+        // FP8 weights: these warps also fill the chain rows of every base K step
+        // (main ring position cst / cph, staging ring position cj / cjph) and
+        // arrive on the leader's full barrier for every stage of the ring
+        int cst = 0, cj = 0;
+        uint32_t cph = 0, cjph = 0;
+        const uint32_t lead_full = cluster_addr(m.full, 0);
+        auto stage_done = [&]() {
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(&m.full[cst]);
+                else mbar_arrive_cluster(lead_full + (uint32_t)cst * 8u);
+            }
+            if (++cst == NS) { cst = 0; cph ^= 1; }
+        };
+        // a slot of the main ring is free once the pair's MMAs are done with it
+        auto slot_free = [&]() { return __all_sync(kFull, mbar_wait(&m.empty[cst], cph ^ 1)); };
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
             if (t < n_sh) {
+                if (W8) {
+                    ShItem sh;
+                    sh.load(a, t, n_lora);
+                    const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
+                    for (int kb = kb0; kb < kb1 && ok; kb++) {
+                        if (!slot_free()) { ok = false; break; }
+                        stage_done();
+                    }
+                    if (!ok) break;
+                }
                 if (!shrink_epilogue_m(a, t, n_lora, it, tmem_base, qd, half, lane, etid, m, rendezvous, release,
                                        (int)rank)) {
                     ok = false;
@@ -648,6 +755,63 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
             }
             Task<kPairRows> tw;
             tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+            if (W8) {
+                // bf16 of (scale * code) into this CTA's chain rows of each base
+                // K step: thread etid converts 16-code chunks i = etid + 256 n of
+                // the 2 x nu/2 staged rows (chain c, row r, chunk kc); the rows
+                // and hence the scales of a thread stay the same over the task
+                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
+                const int n_chunks = 8 * nu2;
+                float sc[4];
+#pragma unroll
+                for (int n = 0; n < 4; n++) {
+                    const int i = etid + 256 * n;
+                    sc[n] = 0.f;
+                    if (i < n_chunks) {
+                        const int c = i / (4 * nu2), r = (i % (4 * nu2)) >> 2;
+                        if (GATE_UP) {
+                            const int u = c0row + r;
+                            if (u < a.I) sc[n] = a.wscale[(size_t)tw.e * 2 * a.I + (size_t)c * a.I + u];
+                        } else {
+                            const int h = (c ? c1row : c0row) + r;
+                            if (h < a.H) sc[n] = a.wscale[(size_t)tw.e * a.H + h];
+                        }
+                    }
+                }
+                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+                for (int kb = kb0; kb < kb1 && ok; kb++) {
+                    if (!slot_free()) { ok = false; break; }
+                    if (!__all_sync(kFull, mbar_wait(&m.w8full[cj], cjph))) { ok = false; break; }
+                    const uint8_t* src = m.f8 + (size_t)cj * kF8Slot;
+                    uint8_t* dst = m.ring + (size_t)cst * kStage2 + kSlot;
+#pragma unroll
+                    for (int n = 0; n < 4; n++) {
+                        const int i = etid + 256 * n;
+                        if (i < n_chunks) {
+                            const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
+                            const uint4 code = *reinterpret_cast<const uint4*>(src + (size_t)c * nu2 * kBK + r * kBK + kc * 16);
+                            uint8_t* row = dst + (size_t)c * kSlot + r * 128;
+                            e4m3x16_to_bf16(code, sc[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
+                                            reinterpret_cast<uint4*>(row + (((2 * kc + 1) ^ (r & 7)) << 4)));
+                        }
+                    }
+                    // the generic stores before the tensor cores (async proxy) read them
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&m.w8empty[cj]);
+                    if (++cj == N8) { cj = 0; cjph ^= 1; }
+                    stage_done();
+                }
+                // the expand blocks of the task (bf16 rows by TMA): only the arrival
+                const unsigned long long mask = expand ? tt.cmask[tw.chunk] : 0ull;
+                for (int g = 0, jj = 0; ok && mask != 0ull && g < n_groups; g++) {
+                    if (!group_present(mask, g)) continue;
+                    if (jj++ % ksplit != tw.split) continue;
+                    if (!slot_free()) { ok = false; break; }
+                    stage_done();
+                }
+                if (!ok) break;
+            }
             // this lane's pair row of the chunk
             const int row = (int)rank * 128 + qd * 32 + lane;
             const bool valid = row < tw.n_real;
@@ -737,42 +901,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_2sm(const __grid_con
     if (warp == 1) tmem_dealloc2(tmem_base, kTmem2);
 }
 
-template <bool G>
+template <bool G, bool W8>
 cudaError_t set_attr2() {
-    return cudaFuncSetAttribute(k_moe_gemm_2sm<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
+    return cudaFuncSetAttribute(k_moe_gemm_2sm<G, W8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLimit);
 }
 
-}  // namespace
-
-// at least half an SM's shared memory: one CTA per SM, so the whole TMEM
-// allocation never waits for another CTA
-int tc2_smem_bytes(int E, int nstages, int max_chunks) {
-    const int bars = (2 * nstages + 3) * 8 + 16;
-    const int slots = (3 * kMaxShrinkSlots + 4) * 4;
-    const int table = 8 * max_chunks + (4 * E + 1) * 4;
-    const int tr = 16 + kEpiWarps * kTrFloats * 4;
-    return std::max(1024 + nstages * kStage2 + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
-}
-
-int tc2_plan_stages(int E, int max_chunks) {
-    for (int ns = 8; ns >= 3; ns--)
-        if (tc2_smem_bytes(E, ns, max_chunks) <= kTcSmemLimit) return ns;
-    return 0;
-}
-
-cudaError_t init_tc2_attributes() {
-    cudaError_t e;
-    if ((e = set_attr2<true>()) != cudaSuccess) return e;
-    return set_attr2<false>();
-}
-
-// Pairs of this kernel that fit on the device at once (with the largest
-// shared-memory request): the persistent grid must not exceed it, since tasks
-// wait on each other's progress (shrink before expand).
-int tc2_max_pairs(bool gate_up) {
+template <bool G, bool W8>
+int max_pairs_of() {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(W8 ? kThreadsW8 : kTcThreads);
     cfg.dynamicSmemBytes = kTcSmemLimit;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -782,13 +920,61 @@ int tc2_max_pairs(bool gate_up) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const cudaError_t e = gate_up ? cudaOccupancyMaxActiveClusters(&n, k_moe_gemm_2sm<true>, &cfg)
-                                  : cudaOccupancyMaxActiveClusters(&n, k_moe_gemm_2sm<false>, &cfg);
-    if (e != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, k_moe_gemm_2sm<G, W8>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     return n;
+}
+
+}  // namespace
+
+// at least half an SM's shared memory: one CTA per SM, so the whole TMEM
+// allocation never waits for another CTA
+int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8) {
+    const int bars = (2 * nstages + 3 + 2 * n8) * 8 + 16;
+    const int slots = (3 * kMaxShrinkSlots + 4) * 4;
+    const int table = 8 * max_chunks + (4 * E + 1) * 4;
+    const int tr = 16 + kEpiWarps * kTrFloats * 4;
+    return std::max(1024 + nstages * kStage2 + n8 * kF8Slot + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
+}
+
+int tc2_plan_stages(int E, int max_chunks) {
+    for (int ns = 8; ns >= 3; ns--)
+        if (tc2_smem_bytes(E, ns, max_chunks) <= kTcSmemLimit) return ns;
+    return 0;
+}
+
+// FP8 weights: two main stages (one converted while the other feeds the
+// MMAs) and as deep a code staging ring as fits (at least four steps): the
+// codes are what streams from HBM
+int tc2_plan_stages_w8(int E, int max_chunks, int* n8) {
+    for (int k = 8; k >= 4; k--) {
+        if (tc2_smem_bytes(E, 2, max_chunks, k) <= kTcSmemLimit) {
+            *n8 = k;
+            return 2;
+        }
+    }
+    *n8 = 0;
+    return 0;
+}
+
+cudaError_t init_tc2_attributes() {
+    cudaError_t e;
+    if ((e = set_attr2<true, false>()) != cudaSuccess) return e;
+    if ((e = set_attr2<false, false>()) != cudaSuccess) return e;
+    if ((e = set_attr2<true, true>()) != cudaSuccess) return e;
+    return set_attr2<false, true>();
+}
+
+// Pairs of this kernel that fit on the device at once (with the largest
+// shared-memory request; the FP8 kernels have one more warp): the persistent
+// grid must not exceed it, since tasks wait on each other's progress (shrink
+// before expand).
+int tc2_max_pairs(bool gate_up) {
+    const int a = gate_up ? max_pairs_of<true, false>() : max_pairs_of<false, false>();
+    const int b = gate_up ? max_pairs_of<true, true>() : max_pairs_of<false, true>();
+    return std::min(a, b);
 }
 
 // grid: an even number of CTAs (pairs of SMs); clusters of two, with the
@@ -796,10 +982,11 @@ int tc2_max_pairs(bool gate_up) {
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl) {
     if (args.nu < 16 || args.nu > 256 || args.nu % 16 != 0) return cudaErrorInvalidValue;
     if (args.r > 0 && (128 / args.r) * 2 > kMaxShrinkSlots) return cudaErrorInvalidValue;
-    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks);
+    if (args.w8 && (args.n8 < 1 || args.nstages < 2 || args.wscale == nullptr)) return cudaErrorInvalidValue;
+    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks, args.w8 ? args.n8 : 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(args.w8 ? kThreadsW8 : kTcThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -815,8 +1002,12 @@ cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cuda
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    if (gate_up) return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<true>, args);
-    return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<false>, args);
+    if (args.w8) {
+        if (gate_up) return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<true, true>, args);
+        return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<false, true>, args);
+    }
+    if (gate_up) return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<true, false>, args);
+    return cudaLaunchKernelEx(&cfg, k_moe_gemm_2sm<false, false>, args);
 }
 
 }  // namespace moelora

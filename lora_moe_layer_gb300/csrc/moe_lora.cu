@@ -63,6 +63,7 @@ struct Layout {
     bool pair_cta;   // the GEMMs run as CTA pairs (moe_gemm_2sm.cu)
     int ranks;       // CTAs per GEMM task: 2 with pair_cta, else 1
     int nu_gu, nu_dn;  // CTA pairs: weight rows per MMA chain of the two GEMMs
+    bool w8;           // FP8 (E4M3) base weights: always the CTA-pair kernels
     long tiles_gu, tiles_dn;
     long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
 };
@@ -215,14 +216,17 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     return true;
 }
 
-void plan_gemms(const moe_lora_dims* d, Layout* L) {
+// false: FP8 weights asked for a layer the CTA-pair kernels do not cover
+bool plan_gemms(const moe_lora_dims* d, Layout* L) {
     const long experts_max = std::max<long>(1, std::min<long>(d->E, L->P));
     const long avg_pairs = L->P > 0 ? (L->P + experts_max - 1) / experts_max : 0;
     const bool narrow = avg_pairs <= 48;
     L->pair_cta = false;
     L->ranks = 1;
     L->nu_gu = L->nu_dn = 0;
-    if (!narrow && !(d->options & MOELORA_OPT_SINGLE_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return;
+    // FP8 weights are dequantised in the CTA-pair kernels only, whatever the batch
+    if (L->w8) return plan_pair_gemms(d, L, experts_max, std::max<long>(avg_pairs, 1));
+    if (!narrow && !(d->options & MOELORA_OPT_SINGLE_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return true;
     L->bn_gu = narrow ? 64 : 128;
     L->bn_dn = narrow ? 64 : 256;
     const long nt_gu = (d->I + 127) / 128, nt_dn = (d->H + 127) / 128;
@@ -234,11 +238,16 @@ void plan_gemms(const moe_lora_dims* d, Layout* L) {
     const long est_dn = nt_dn * experts_max * ((avg_pairs + L->bn_dn - 1) / L->bn_dn);
     L->ks_gu = pick_ksplit(est_gu, d->H, L->sms);
     L->ks_dn = pick_ksplit(est_dn, d->I, L->sms);
+    return true;
 }
 
-int make_layout(const moe_lora_dims* d, Layout* L) {
+int make_layout(const moe_lora_dims* d, Layout* L, bool w8 = false) {
     const int st = check_dims(d);
     if (st != MOELORA_OK) return st;
+    // FP8 codes are TMA-copied with byte strides: rows of H and I codes must be
+    // multiples of 16 bytes
+    if (w8 && (d->H % 16 != 0 || d->I % 16 != 0)) return MOELORA_EUNSUPPORTED;
+    L->w8 = w8;
     L->bm = d->block_m ? d->block_m : kDefaultBlockM;
     L->sms = d->sm_count > 0 ? d->sm_count : current_device_sms();
     L->P = (long)d->T * d->k;
@@ -254,7 +263,7 @@ int make_layout(const moe_lora_dims* d, Layout* L) {
     // every forward).
     L->tc_expand = d->L > 0 && L->P * zexp_cols(d->L, d->r) <= kMaxZexpElems &&
                    expected_adapters_per_chunk(d, L->P) >= 4.0;
-    plan_gemms(d, L);
+    if (!plan_gemms(d, L)) return MOELORA_EUNSUPPORTED;
     plan_shrinks(d, L);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = up256(o + bytes); return at; };
@@ -357,6 +366,33 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int rank, const cuuint6
     return r == CUDA_SUCCESS;
 }
 
+// FP8 codes (one byte each), no swizzle (the converters read plain rows)
+bool encode_u8_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                           strides_bytes, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+// E4M3 codes of W1 [E][2I][H] as {H, I, 2, E} / W2 [E][H][I] as {I, H, E}:
+// boxes of 64 codes (one K step) x rows
+bool encode_w1q_map(CUtensorMap* map, const void* W1q, int E, int I, int H, int rows) {
+    const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
+    const cuuint64_t strides[3] = {(cuuint64_t)H, (cuuint64_t)I * H, (cuuint64_t)2 * I * H};
+    const cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+    return encode_u8_map(map, W1q, 4, dims, strides, box);
+}
+bool encode_w2q_map(CUtensorMap* map, const void* W2q, int E, int I, int H, int rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)I, (cuuint64_t)H, (cuuint64_t)E};
+    const cuuint64_t strides[2] = {(cuuint64_t)I, (cuuint64_t)H * I};
+    const cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    return encode_u8_map(map, W2q, 3, dims, strides, box);
+}
+
 // W1 [E][2I][H] viewed as [E][2][I][H]: boxes of 64 (K) x 128 units of one half
 bool encode_w1_map(CUtensorMap* map, const void* W1, int E, int I, int H, int box_rows = 128) {
     const cuuint64_t dims[4] = {(cuuint64_t)H, (cuuint64_t)I, 2, (cuuint64_t)E};
@@ -429,6 +465,17 @@ bool encode_b2_map(CUtensorMap* map, const void* B2, int L, int E, int H, int r,
 template <typename T>
 T* at(void* ws, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(ws) + off); }
 
+// Workspace bytes that serve both forwards of these dims: the bf16 plan and,
+// where the layer supports it, the FP8-weight plan (0 if the dims are invalid).
+size_t workspace_need(const moe_lora_dims* d) {
+    Layout L;
+    if (make_layout(d, &L) != MOELORA_OK) return 0;
+    size_t n = L.total;
+    Layout L8;
+    if (make_layout(d, &L8, true) == MOELORA_OK) n = std::max(n, L8.total);
+    return n;
+}
+
 AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t* topk_ids,
                           const int32_t* lora_ids, void* ws) {
     AlignArgs a = {};
@@ -489,10 +536,7 @@ MOELORA_API int64_t moe_lora_align_capacity(const moe_lora_dims* d) {
     return st == MOELORA_OK ? (int64_t)L.cap : (int64_t)st;
 }
 
-MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* d) {
-    Layout L;
-    return make_layout(d, &L) == MOELORA_OK ? L.total : 0;
-}
+MOELORA_API size_t moe_lora_workspace_bytes(const moe_lora_dims* d) { return workspace_need(d); }
 
 MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_layout* out) {
     if (!out) return MOELORA_EINVAL;
@@ -512,7 +556,7 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     out->launches = 5;  // align, gather, gate_up, down, reduce
     out->gemm_ctas = L.ranks;
     out->tc_expand = L.tc_expand ? 1 : 0;
-    out->total = L.total;
+    out->total = workspace_need(d);
     return MOELORA_OK;
 }
 
@@ -528,7 +572,7 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
         !bucket_offset || !workspace)
         return MOELORA_EINVAL;
     if (d->T > 0 && (!topk_ids || !token_lora_ids)) return MOELORA_EINVAL;
-    if (workspace_bytes < L.total) return MOELORA_ENOSPC;
+    if (workspace_bytes < L.total || workspace_bytes < workspace_need(d)) return MOELORA_ENOSPC;
     if (!aligned16(workspace)) return MOELORA_EUNSUPPORTED;
     DeviceInfo* dev = nullptr;
     if ((st = device_setup(&dev)) != MOELORA_OK) return st;
@@ -561,19 +605,33 @@ struct Tracer {
     }
 };
 
+// FP8 base weights of a forward: E4M3 codes and per-output-row fp32 scales
+struct W8Ptrs {
+    const void* W1q;
+    const float* W1s;
+    const void* W2q;
+    const float* W2s;
+};
+
 int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
                  const float* topk_weights, const int32_t* token_lora_ids, const void* W1,
                  const void* W2, const void* A1, const void* B1, const void* A2, const void* B2,
                  void* out, void* workspace, size_t workspace_bytes, void* stream,
-                 void* const* events, int n_events) {
+                 void* const* events, int n_events, const W8Ptrs* w8 = nullptr) {
     Layout L;
-    int st = make_layout(d, &L);
+    int st = make_layout(d, &L, w8 != nullptr);
     if (st != MOELORA_OK) return st;
-    if (!workspace || !W1 || !W2) return MOELORA_EINVAL;
+    if (!workspace) return MOELORA_EINVAL;
+    if (w8 ? !(w8->W1q && w8->W1s && w8->W2q && w8->W2s) : !(W1 && W2)) return MOELORA_EINVAL;
+    if (w8) {
+        const void* p8[] = {w8->W1q, w8->W2q, w8->W1s, w8->W2s};
+        for (const void* p : p8)
+            if (!aligned16(p)) return MOELORA_EUNSUPPORTED;
+    }
     if (d->T > 0 && (!x || !topk_ids || !topk_weights || !token_lora_ids || !out)) return MOELORA_EINVAL;
     const bool has_lora = d->L > 0;
     if (has_lora && (!A1 || !B1 || !A2 || !B2)) return MOELORA_EINVAL;
-    if (workspace_bytes < L.total) return MOELORA_ENOSPC;
+    if (workspace_bytes < L.total || workspace_bytes < workspace_need(d)) return MOELORA_ENOSPC;
     const void* ptrs[] = {x, W1, W2, A1, B1, A2, B2, out, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return MOELORA_EUNSUPPORTED;
@@ -662,10 +720,18 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             // CTA pairs: 128 pair rows per CTA, chains of nu units (each CTA half of them)
             if (!tc.chunk_masks) tc.max_chunks = 0;
             tc.nu = L.nu_gu;
-            tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
-            if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
             const int half = L.nu_gu / 2;
-            if (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H, half) ||
+            if (w8) {
+                tc.w8 = 1;
+                tc.wscale = w8->W1s;
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8);
+                if (tc.nstages < 2 || !encode_w1q_map(&tc.w8map, w8->W1q, d->E, d->I, d->H, half))
+                    return tc.nstages < 2 ? MOELORA_EUNSUPPORTED : MOELORA_ECUDA;
+            } else {
+                tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
+                if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
+            }
+            if ((!w8 && !encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H, half)) ||
                 !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, 128) ||
                 (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
                 (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r, false, half) ||
@@ -716,10 +782,18 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             // CTA pairs: 128 act rows per CTA, two chains of nu W2 rows (each CTA half of each)
             if (!tc.chunk_masks) tc.max_chunks = 0;
             tc.nu = L.nu_dn;
-            tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
-            if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
             const int half = L.nu_dn / 2;
-            if (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H, half) ||
+            if (w8) {
+                tc.w8 = 1;
+                tc.wscale = w8->W2s;
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8);
+                if (tc.nstages < 2 || !encode_w2q_map(&tc.w8map, w8->W2q, d->E, d->I, d->H, half))
+                    return tc.nstages < 2 ? MOELORA_EUNSUPPORTED : MOELORA_ECUDA;
+            } else {
+                tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
+                if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
+            }
+            if ((!w8 && !encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H, half)) ||
                 !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, 128) ||
                 (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
                 (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r, false, half) ||
@@ -781,6 +855,16 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims* d, const void* x, const in
                         workspace, workspace_bytes, stream, nullptr, 0);
 }
 
+MOELORA_API int moe_lora_forward_w8(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
+                                    const float* topk_weights, const int32_t* token_lora_ids,
+                                    const void* W1q, const float* W1s, const void* W2q, const float* W2s,
+                                    const void* A1, const void* B1, const void* A2, const void* B2, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+    const W8Ptrs w8 = {W1q, W1s, W2q, W2s};
+    return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, nullptr, nullptr, A1, B1, A2, B2, out,
+                        workspace, workspace_bytes, stream, nullptr, 0, &w8);
+}
+
 MOELORA_API int moe_lora_forward_traced(const moe_lora_dims* d, const void* x,
                                         const int32_t* topk_ids, const float* topk_weights,
                                         const int32_t* token_lora_ids, const void* W1,
@@ -835,7 +919,7 @@ MOELORA_API int moe_lora_forward_noalloc(const moe_lora_dims* d, const void* x,
     if (!W1 || !W2) return MOELORA_EINVAL;
     if (d->T > 0 && (!x || !topk_ids || !topk_weights || !token_lora_ids || !out)) return MOELORA_EINVAL;
     if (d->L > 0 && (!A1 || !B1 || !A2 || !B2)) return MOELORA_EINVAL;
-    if (L.total > kNoAllocScratchBytes) return MOELORA_ENOSPC;  // needs more than the built-in scratch
+    if (workspace_need(d) > kNoAllocScratchBytes) return MOELORA_ENOSPC;  // needs more than the built-in scratch
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {

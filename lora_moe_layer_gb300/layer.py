@@ -31,6 +31,13 @@ class DeviceLayer:
         self.B1 = _dev_bf16(layer.B1, dev) if has else None
         self.A2 = _dev_bf16(layer.A2, dev) if has else None
         self.B2 = _dev_bf16(layer.B2, dev) if has else None
+        # FP8 base weights (E4M3 codes and per-row scales), when the layer has them
+        q = getattr(layer, "w8", None)
+        if q is not None:
+            self.W1q = torch.from_numpy(np.ascontiguousarray(q.W1q, dtype=np.uint8)).to(dev)
+            self.W2q = torch.from_numpy(np.ascontiguousarray(q.W2q, dtype=np.uint8)).to(dev)
+            self.W1s = torch.from_numpy(np.ascontiguousarray(q.W1s, dtype=np.float32)).to(dev)
+            self.W2s = torch.from_numpy(np.ascontiguousarray(q.W2s, dtype=np.float32)).to(dev)
         self.set_batch(layer.x, layer.topk_ids, layer.topk_weights, layer.lora_ids)
         self.ws_bytes = B.moe_lora_workspace_bytes(self.d)
         if self.ws_bytes == 0:
@@ -51,6 +58,13 @@ class DeviceLayer:
         return B.moe_lora_forward(self.d, self.x, self.topk_ids, self.topk_weights, self.lora_ids,
                                   self.W1, self.W2, self.A1, self.B1, self.A2, self.B2, o,
                                   self.workspace, stream)
+
+    def forward_w8(self, stream=None, out: Optional[torch.Tensor] = None) -> int:
+        """Launch moe_lora_forward_w8 with the layer's FP8 base weights."""
+        o = self.out if out is None else out
+        return B.moe_lora_forward_w8(self.d, self.x, self.topk_ids, self.topk_weights, self.lora_ids,
+                                     self.W1q, self.W1s, self.W2q, self.W2s, self.A1, self.B1, self.A2, self.B2,
+                                     o, self.workspace, stream)
 
     def status(self, stream=None) -> int:
         return B.moe_lora_get_status(self.workspace, stream)
