@@ -54,8 +54,6 @@
 //            warps free the accumulator on the leader's barrier.
 // Every wait is bounded; on a timeout the CTA records kStatusTimeout, stops
 // waiting, drains its copies, frees TMEM and exits at the final pair barrier.
-#include <cuda_fp16.h>
-
 #include "gemm_tasks.cuh"
 
 namespace moelora {
@@ -68,7 +66,12 @@ constexpr int kChain1Col = 256;                 // first TMEM column of chain 1
 constexpr int kSlot = 128 * kBK * 2;            // 16 KiB: 128 rows of one 64-wide K step
 constexpr int kStage2 = 3 * kSlot;              // pair rows, chain-0 rows, chain-1 rows
 constexpr int kF8Slot = 2 * 128 * kBK;          // FP8 codes of one K step: nu / 2 rows of each chain
-constexpr int kThreadsW8 = kTcThreads + 32;     // FP8 weights: one more warp, the code producer
+// FP8 weights: one more warp streams the codes and kConvWarps warps convert
+// them; the pair rows and the converted chain rows get rings of their own
+constexpr int kConvWarps = 8;
+constexpr int kConvWarp0 = 2 + kEpiWarps + 1;   // first converter warp
+constexpr int kThreadsW8 = (kConvWarp0 + kConvWarps) * 32;
+constexpr int kNW = 2;                          // converted chain-row stages (2 x 16 KiB each)
 constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
 // down epilogue: each warp turns its 32 pairs x 16 columns into whole
 // 64-byte runs of 8 rows per store through a padded tile (row stride of 20
@@ -210,9 +213,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Shared memory after the stage ring: barriers, the TMEM base, shrink-slot
 // tables and the task table.
 struct Smem2 {
-    uint8_t* ring;
+    uint8_t* ring;    // [NS][kStage2]; FP8 weights: [NS][kSlot] pair rows only
+    uint8_t* wring;   // FP8 weights: [kNW][2 kSlot] chain rows (converted, or TMA-copied LoRA rows)
     uint8_t* f8;      // [n8][kF8Slot] FP8 weights: staged codes
-    uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed (FP8 weights: and converted)
+    uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed
+    uint64_t* wready; // FP8 weights: [kNW] leader: both CTAs' converters are done with a chain-row stage
+    uint64_t* wempty; // FP8 weights: [kNW] the pair's MMAs are done with a chain-row stage
     uint64_t* empty;  // [NS] the pair's MMAs are done with stage s
     uint64_t* tfull;  // accumulator ready for the epilogue
     uint64_t* tempty; // leader: accumulator drained by both CTAs' epilogues
@@ -231,12 +237,16 @@ struct Smem2 {
 __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     Smem2 m;
     m.ring = base;
-    m.f8 = base + (size_t)NS * kStage2;
     const int n8 = a.w8 ? a.n8 : 0;
+    const int nw = a.w8 ? kNW : 0;
+    m.wring = base + (size_t)NS * (a.w8 ? kSlot : kStage2);
+    m.f8 = m.wring + (size_t)nw * 2 * kSlot;
     uint64_t* bars = reinterpret_cast<uint64_t*>(m.f8 + (size_t)n8 * kF8Slot);
     m.full = bars;
     m.empty = m.full + NS;
-    m.tfull = m.empty + NS;
+    m.wready = m.empty + NS;
+    m.wempty = m.wready + nw;
+    m.tfull = m.wempty + nw;
     m.tempty = m.tfull + 1;
     m.ebar = m.tempty + 1;
     m.tmem_slot = reinterpret_cast<uint32_t*>(m.ebar + 1);
@@ -371,21 +381,42 @@ __device__ bool shrink_epilogue_m(const TcArgs& a, int t, int n_lora, int use, u
 }
 
 // E4M3 codes -> bf16 of (scale * value): 16 codes (one 16-byte chunk of a
-// staged row) into the two 16-byte chunks at `dst0` and `dst1`.  The code is
-// widened exactly to f16 by the hardware conversion, then to fp32, scaled and
-// rounded once to bf16.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, float scale, uint4* dst0, uint4* dst1) {
+// staged row) into the two 16-byte chunks at `dst0` and `dst1`.
+//
+// A code b (sign bit, 4-bit exponent field f with bias 7, 3-bit mantissa m)
+// placed in an fp32 word as sign -> bit 31 and its other seven bits -> bits
+// 26..20 reads as an fp32 of exponent field f and mantissa m / 8: exactly
+// value(b) * 2^-120, subnormal codes (f = 0) included, since both formats
+// then scale m / 8 by their smallest exponent.  Two packed fp32 multiplies
+// apply the scale and 2^120 (powers of two are exact; the product is
+// rounded once), and one conversion packs two results to bf16 (round to
+// nearest even).  The scale factor is s_hi * s_lo: scale * 2^120 and 1 when
+// that is finite in fp32 (one multiply), else scale * 2^64 and 2^56.
+__device__ __forceinline__ uint32_t e4m3_bits_f32(uint32_t b) { return ((b & 0x80u) << 24) | ((b & 0x7fu) << 20); }
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, float s_hi, float s_lo, uint4* dst0, uint4* dst1) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    const uint64_t sc = ((uint64_t)__float_as_uint(s_hi) << 32) | __float_as_uint(s_hi);
+    const uint64_t k56 = ((uint64_t)__float_as_uint(s_lo) << 32) | __float_as_uint(s_lo);
+    const bool two = s_lo != 1.0f;
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
-            const uint16_t pair2 = (uint16_t)(w[i] >> (16 * hh));
-            uint32_t h2;
-            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair2));
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-            o[2 * i + hh] = pack_bf16x2(f.x * scale, f.y * scale);
+            const uint32_t lo = e4m3_bits_f32((w[i] >> (16 * hh)) & 0xffu);
+            const uint32_t hi = e4m3_bits_f32((w[i] >> (16 * hh + 8)) & 0xffu);
+            uint64_t v = mul_f32x2(((uint64_t)hi << 32) | lo, sc);
+            if (two) v = mul_f32x2(v, k56);
+            uint32_t d;
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(v >> 32)), "r"((uint32_t)v));
+            o[2 * i + hh] = d;
         }
     }
     *dst0 = make_uint4(o[0], o[1], o[2], o[3]);
@@ -406,13 +437,18 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     const int N8 = W8 ? a.n8 : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
-            // FP8 weights: the converters of both CTAs arrive too, once per stage
-            mbar_init(&m.full[s], W8 ? 1 + 2 * kEpiWarps : 1);
+            mbar_init(&m.full[s], 1);
             mbar_init(&m.empty[s], 1);
+        }
+        if (W8) {
+            for (int s = 0; s < kNW; s++) {
+                mbar_init(&m.wready[s], 2 * kConvWarps);  // the converter warps of both CTAs
+                mbar_init(&m.wempty[s], 1);
+            }
         }
         for (int j = 0; j < N8; j++) {
             mbar_init(&m.w8full[j], 1);
-            mbar_init(&m.w8empty[j], kEpiWarps);
+            mbar_init(&m.w8empty[j], kConvWarps);
         }
         mbar_init(m.tfull, 1);
         mbar_init(m.tempty, 2 * kEpiWarps);
@@ -482,8 +518,13 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             uint32_t phase = 0, armed = 0, last_par = 0;
             bool z_seen = false;
             const uint32_t full0 = cluster_addr(m.full, 0);  // the leader's full[0]
-            auto acquire = [&](uint32_t bytes_pair) {
+            // FP8 weights: the chain rows of a stage live in their own ring (wst);
+            // this thread writes them only for shrink items and expand blocks
+            int wst = 0;
+            uint32_t wph = 0;
+            auto acquire = [&](uint32_t bytes_pair, bool chains) {
                 if (!mbar_wait_cluster(&m.empty[stage], phase ^ 1)) return false;
+                if (W8 && chains && !mbar_wait_cluster(&m.wempty[wst], wph ^ 1)) return false;
                 if (leader) mbar_arrive_expect_tx(&m.full[stage], bytes_pair);
                 return true;
             };
@@ -491,6 +532,12 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 armed |= 1u << stage;
                 last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
+                if (W8 && ++wst == kNW) { wst = 0; wph ^= 1; }
+            };
+            // this stage's pair rows and its chain-c rows
+            auto xdst = [&]() { return m.ring + (size_t)stage * (W8 ? kSlot : kStage2); };
+            auto cdst = [&](int c) {
+                return W8 ? m.wring + (size_t)wst * 2 * kSlot + c * kSlot : m.ring + (size_t)stage * kStage2 + (1 + c) * kSlot;
             };
             for (int t = t_first; t < total && ok; t += t_step) {
                 if (t < n_sh) {
@@ -508,13 +555,12 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     const int rows0 = sh.q0c + (int)rank * 128;
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
-                        if (!acquire(bytes_pair)) { ok = false; break; }
-                        uint8_t* dst = m.ring + (size_t)stage * kStage2;
+                        if (!acquire(bytes_pair, true)) { ok = false; break; }
                         const uint32_t bar = full0 + (uint32_t)stage * 8u;
                         const int k0 = kb * kBK;
-                        tma2_2d(dst, &a.xmap, bar, k0, rows0);
+                        tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
                         for (int q = 0; q < mine; q++)
-                            tma2_2d(dst + kSlot + q * a.r * kBK * 2, &a.amap, bar, k0, arow[q]);
+                            tma2_2d(cdst(0) + q * a.r * kBK * 2, &a.amap, bar, k0, arow[q]);
                         advance();
                     }
                     continue;
@@ -531,20 +577,19 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 const uint32_t bytes_base = W8 ? 2u * (uint32_t)kSlot : bytes_pair;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
-                    if (!acquire(bytes_base)) { ok = false; break; }
-                    uint8_t* dst = m.ring + (size_t)stage * kStage2;
+                    if (!acquire(bytes_base, false)) { ok = false; break; }
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
                     const int k0 = kb * kBK;
-                    tma2_2d(dst, &a.xmap, bar, k0, rows0);
+                    tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
                     if (W8) {
                         // chain rows come from the converters
                     } else if (GATE_UP) {
                         // the gate rows, then the up rows, of this CTA's nu / 2 units
-                        tma2_4d(dst + kSlot, &a.wmap, bar, k0, c0row, 0, e);
-                        tma2_4d(dst + 2 * kSlot, &a.wmap, bar, k0, c0row, 1, e);
+                        tma2_4d(cdst(0), &a.wmap, bar, k0, c0row, 0, e);
+                        tma2_4d(cdst(1), &a.wmap, bar, k0, c0row, 1, e);
                     } else {
-                        tma2_3d(dst + kSlot, &a.wmap, bar, k0, c0row, e);
-                        tma2_3d(dst + 2 * kSlot, &a.wmap, bar, k0, c1row, e);
+                        tma2_3d(cdst(0), &a.wmap, bar, k0, c0row, e);
+                        tma2_3d(cdst(1), &a.wmap, bar, k0, c1row, e);
                     }
                     advance();
                 }
@@ -562,19 +607,18 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 for (int g = 0, j = 0; g < n_groups && ok; g++) {
                     if (!group_present(mask, g)) continue;
                     if (j++ % ksplit != tw.split) continue;
-                    if (!acquire(bytes_pair)) { ok = false; break; }
-                    uint8_t* dst = m.ring + (size_t)stage * kStage2;
+                    if (!acquire(bytes_pair, true)) { ok = false; break; }
                     const uint32_t bar = full0 + (uint32_t)stage * 8u;
                     const int l0 = g * apb;
                     // zexp rows of this CTA's pairs (apb adapter sub-tiles), then the
                     // adapters' B rows of each chain
-                    tma2_3d(dst, &a.zxmap, bar, 0, rows0, l0);
+                    tma2_3d(xdst(), &a.zxmap, bar, 0, rows0, l0);
                     if (GATE_UP) {
-                        tma2_5d(dst + kSlot, &a.bmap, bar, 0, c0row, 0, e, l0);
-                        tma2_5d(dst + 2 * kSlot, &a.bmap, bar, 0, c0row, 1, e, l0);
+                        tma2_5d(cdst(0), &a.bmap, bar, 0, c0row, 0, e, l0);
+                        tma2_5d(cdst(1), &a.bmap, bar, 0, c0row, 1, e, l0);
                     } else {
-                        tma2_4d(dst + kSlot, &a.bmap, bar, 0, c0row, e, l0);
-                        tma2_4d(dst + 2 * kSlot, &a.bmap, bar, 0, c1row, e, l0);
+                        tma2_4d(cdst(0), &a.bmap, bar, 0, c0row, e, l0);
+                        tma2_4d(cdst(1), &a.bmap, bar, 0, c1row, e, l0);
                     }
                     advance();
                 }
@@ -589,20 +633,33 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     } else if (warp == 1) {
         if (leader && lane == 0) {
             // ------------------------------------------------- MMA issuer (leader)
-            int stage = 0;
-            uint32_t phase = 0;
-            const uint64_t d0 = umma_desc_sw128(smem_u32(m.ring));
-            const uint64_t dx0 = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
-            constexpr uint64_t kStage16 = kStage2 / 16, kSlot16 = kSlot / 16;
+            int stage = 0, wst = 0;
+            uint32_t phase = 0, wph = 0;
+            // descriptor bases of the pair rows and of the chain rows (FP8
+            // weights: two rings); a stage adds its offset in 16-byte units
+            const uint64_t dxr = umma_desc_sw128(smem_u32(m.ring));
+            const uint64_t dcr = umma_desc_sw128(smem_u32(W8 ? m.wring : m.ring + kSlot));
+            const uint64_t exr = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
+            const uint64_t ecr = umma_desc_kmajor(smem_u32(W8 ? m.wring : m.ring + kSlot), expand_layout(rp), 8u * rp * 2u);
+            constexpr uint64_t kSlot16 = kSlot / 16;
+            constexpr uint64_t kX16 = (W8 ? kSlot : kStage2) / 16;      // pair-row stage stride
+            constexpr uint64_t kC16 = (W8 ? 2 * kSlot : kStage2) / 16;  // chain-row stage stride
             const uint64_t zsub16 = 128u * rp * 2u / 16u, bsub16 = (uint64_t)nu2 * rp * 2u / 16u;
+            auto xoff = [&]() { return (uint64_t)stage * kX16; };
+            auto coff = [&]() { return (uint64_t)(W8 ? wst : stage) * kC16; };
             auto take = [&]() {
                 if (!mbar_wait_cluster(&m.full[stage], phase)) return false;
+                if (W8 && !mbar_wait_cluster(&m.wready[wst], wph)) return false;
                 tc_fence_after();
                 return true;
             };
             auto release = [&]() {
                 umma2_commit_both(&m.empty[stage]);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
+                if (W8) {
+                    umma2_commit_both(&m.wempty[wst]);
+                    if (++wst == kNW) { wst = 0; wph ^= 1; }
+                }
             };
             const uint32_t d_c0 = tmem_base, d_c1 = tmem_base + kChain1Col;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
@@ -616,10 +673,10 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!take()) { ok = false; break; }
-                        const uint64_t da = d0 + (uint64_t)stage * kStage16;
+                        const uint64_t da = dxr + xoff(), db = dcr + coff();
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; kk++)
-                            umma2_bf16(d_c0, da + 2 * kk, da + kSlot16 + 2 * kk, idesc, (kb != kb0) || (kk != 0));
+                            umma2_bf16(d_c0, da + 2 * kk, db + 2 * kk, idesc, (kb != kb0) || (kk != 0));
                         release();
                     }
                     if (!ok) break;
@@ -632,12 +689,12 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!take()) { ok = false; break; }
-                    const uint64_t da = d0 + (uint64_t)stage * kStage16;
+                    const uint64_t da = dxr + xoff(), db = dcr + coff();
 #pragma unroll
                     for (int kk = 0; kk < kBK / 16; kk++) {
                         const uint32_t acc = (kb != kb0) || (kk != 0);
-                        umma2_bf16(d_c0, da + 2 * kk, da + kSlot16 + 2 * kk, idesc, acc);
-                        umma2_bf16(d_c1, da + 2 * kk, da + 2 * kSlot16 + 2 * kk, idesc, acc);
+                        umma2_bf16(d_c0, da + 2 * kk, db + 2 * kk, idesc, acc);
+                        umma2_bf16(d_c1, da + 2 * kk, db + kSlot16 + 2 * kk, idesc, acc);
                     }
                     release();
                 }
@@ -646,10 +703,10 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     if (!group_present(mask, g)) continue;
                     if (j++ % ksplit != tw.split) continue;
                     if (!take()) { ok = false; break; }
-                    const uint64_t dx = dx0 + (uint64_t)stage * kStage16;
+                    const uint64_t ex = exr + xoff(), ec = ecr + coff();
                     for (int q = 0; q < apb; q++) {
-                        const uint64_t za = dx + q * zsub16;
-                        const uint64_t b0 = dx + kSlot16 + q * bsub16, b1 = dx + 2 * kSlot16 + q * bsub16;
+                        const uint64_t za = ex + q * zsub16;
+                        const uint64_t b0 = ec + q * bsub16, b1 = ec + kSlot16 + q * bsub16;
                         for (int kk = 0; kk < rp / 16; kk++) {
                             umma2_bf16(d_c0, za + 2 * kk, b0 + 2 * kk, idesc, 1u);
                             umma2_bf16(d_c1, za + 2 * kk, b1 + 2 * kk, idesc, 1u);
@@ -697,6 +754,98 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             for (int q = 0; q < N8; q++)
                 if ((armed >> q) & 1u) mbar_wait(&m.w8full[q], (last_par >> q) & 1u);
         }
+    } else if (W8 && warp >= kConvWarp0) {
+        // ------------------------------------------------ FP8 code converters
+        // For every stage of the chain-row ring, in the order the MMAs use
+        // them: once the pair's MMAs are done with the slot, the base K steps
+        // get bf16(scale * value) of this CTA's staged codes (thread ct
+        // converts 16-code chunks i = ct + 256 n: chain c, row r, chunk kc);
+        // stages whose chain rows TMA brings (shrink items, expand blocks)
+        // only get the arrival.  Each warp then arrives on the leader's
+        // wready barrier.
+        const int ct = (warp - kConvWarp0) * 32 + lane;
+        const int n_chunks = 8 * nu2;
+        int wst = 0, cj = 0;
+        uint32_t wph = 0, cjph = 0;
+        const uint32_t lead_wready = cluster_addr(m.wready, 0);
+        auto slot_free = [&]() { return __all_sync(kFull, mbar_wait_cluster(&m.wempty[wst], wph ^ 1)); };
+        auto stage_done = [&]() {
+            __syncwarp();
+            if (lane == 0) {
+                if (leader) mbar_arrive(&m.wready[wst]);
+                else mbar_arrive_cluster(lead_wready + (uint32_t)wst * 8u);
+            }
+            if (++wst == kNW) { wst = 0; wph ^= 1; }
+        };
+        for (int t = t_first; t < total && ok; t += t_step) {
+            if (t < n_sh) {
+                ShItem sh;
+                sh.load(a, t, n_lora);
+                const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
+                for (int kb = kb0; kb < kb1 && ok; kb++) {
+                    if (!slot_free()) { ok = false; break; }
+                    stage_done();
+                }
+                continue;
+            }
+            Task<kPairRows> tw;
+            tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+            const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
+            // the scale of each of this thread's rows, as s_hi * s_lo with
+            // s_hi * s_lo = scale * 2^120 (one multiply while that is finite)
+            float sh_[4], sl_[4];
+#pragma unroll
+            for (int n = 0; n < 4; n++) {
+                const int i = ct + 256 * n;
+                float sc = 0.f;
+                if (i < n_chunks) {
+                    const int c = i / (4 * nu2), r = (i % (4 * nu2)) >> 2;
+                    if (GATE_UP) {
+                        const int u = c0row + r;
+                        if (u < a.I) sc = a.wscale[(size_t)tw.e * 2 * a.I + (size_t)c * a.I + u];
+                    } else {
+                        const int h = (c ? c1row : c0row) + r;
+                        if (h < a.H) sc = a.wscale[(size_t)tw.e * a.H + h];
+                    }
+                }
+                const float s120 = sc * 0x1p120f;
+                const bool fits = fabsf(s120) <= 3.0e38f;
+                sh_[n] = fits ? s120 : sc * 0x1p64f;
+                sl_[n] = fits ? 1.0f : 0x1p56f;
+            }
+            const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
+            for (int kb = kb0; kb < kb1 && ok; kb++) {
+                if (!slot_free()) { ok = false; break; }
+                if (!__all_sync(kFull, mbar_wait(&m.w8full[cj], cjph))) { ok = false; break; }
+                const uint8_t* src = m.f8 + (size_t)cj * kF8Slot;
+                uint8_t* dst = m.wring + (size_t)wst * 2 * kSlot;
+#pragma unroll
+                for (int n = 0; n < 4; n++) {
+                    const int i = ct + 256 * n;
+                    if (i < n_chunks) {
+                        const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
+                        const uint4 code = *reinterpret_cast<const uint4*>(src + (size_t)c * nu2 * kBK + r * kBK + kc * 16);
+                        uint8_t* row = dst + (size_t)c * kSlot + r * 128;
+                        e4m3x16_to_bf16(code, sh_[n], sl_[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
+                                        reinterpret_cast<uint4*>(row + (((2 * kc + 1) ^ (r & 7)) << 4)));
+                    }
+                }
+                // the generic stores before the tensor cores (async proxy) read them
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&m.w8empty[cj]);
+                if (++cj == N8) { cj = 0; cjph ^= 1; }
+                stage_done();
+            }
+            // the expand blocks of the task (bf16 rows by TMA): only the arrival
+            const unsigned long long mask = expand ? tt.cmask[tw.chunk] : 0ull;
+            for (int g = 0, jj = 0; ok && mask != 0ull && g < n_groups; g++) {
+                if (!group_present(mask, g)) continue;
+                if (jj++ % ksplit != tw.split) continue;
+                if (!slot_free()) { ok = false; break; }
+                stage_done();
+            }
+        }
     } else {
         // -------------------------------------------------------------- epilogue
         const int ew = warp - 2;         // 0 .. kEpiWarps-1
@@ -718,34 +867,8 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
         };
         const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16);
         const int ngroups = nu / 16;
-        // FP8 weights: these warps also fill the chain rows of every base K step
-        // (main ring position cst / cph, staging ring position cj / cjph) and
-        // arrive on the leader's full barrier for every stage of the ring
-        int cst = 0, cj = 0;
-        uint32_t cph = 0, cjph = 0;
-        const uint32_t lead_full = cluster_addr(m.full, 0);
-        auto stage_done = [&]() {
-            __syncwarp();
-            if (lane == 0) {
-                if (leader) mbar_arrive(&m.full[cst]);
-                else mbar_arrive_cluster(lead_full + (uint32_t)cst * 8u);
-            }
-            if (++cst == NS) { cst = 0; cph ^= 1; }
-        };
-        // a slot of the main ring is free once the pair's MMAs are done with it
-        auto slot_free = [&]() { return __all_sync(kFull, mbar_wait(&m.empty[cst], cph ^ 1)); };
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
             if (t < n_sh) {
-                if (W8) {
-                    ShItem sh;
-                    sh.load(a, t, n_lora);
-                    const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
-                    for (int kb = kb0; kb < kb1 && ok; kb++) {
-                        if (!slot_free()) { ok = false; break; }
-                        stage_done();
-                    }
-                    if (!ok) break;
-                }
                 if (!shrink_epilogue_m(a, t, n_lora, it, tmem_base, qd, half, lane, etid, m, rendezvous, release,
                                        (int)rank)) {
                     ok = false;
@@ -755,63 +878,6 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             }
             Task<kPairRows> tw;
             tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-            if (W8) {
-                // bf16 of (scale * code) into this CTA's chain rows of each base
-                // K step: thread etid converts 16-code chunks i = etid + 256 n of
-                // the 2 x nu/2 staged rows (chain c, row r, chunk kc); the rows
-                // and hence the scales of a thread stay the same over the task
-                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
-                const int n_chunks = 8 * nu2;
-                float sc[4];
-#pragma unroll
-                for (int n = 0; n < 4; n++) {
-                    const int i = etid + 256 * n;
-                    sc[n] = 0.f;
-                    if (i < n_chunks) {
-                        const int c = i / (4 * nu2), r = (i % (4 * nu2)) >> 2;
-                        if (GATE_UP) {
-                            const int u = c0row + r;
-                            if (u < a.I) sc[n] = a.wscale[(size_t)tw.e * 2 * a.I + (size_t)c * a.I + u];
-                        } else {
-                            const int h = (c ? c1row : c0row) + r;
-                            if (h < a.H) sc[n] = a.wscale[(size_t)tw.e * a.H + h];
-                        }
-                    }
-                }
-                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                for (int kb = kb0; kb < kb1 && ok; kb++) {
-                    if (!slot_free()) { ok = false; break; }
-                    if (!__all_sync(kFull, mbar_wait(&m.w8full[cj], cjph))) { ok = false; break; }
-                    const uint8_t* src = m.f8 + (size_t)cj * kF8Slot;
-                    uint8_t* dst = m.ring + (size_t)cst * kStage2 + kSlot;
-#pragma unroll
-                    for (int n = 0; n < 4; n++) {
-                        const int i = etid + 256 * n;
-                        if (i < n_chunks) {
-                            const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
-                            const uint4 code = *reinterpret_cast<const uint4*>(src + (size_t)c * nu2 * kBK + r * kBK + kc * 16);
-                            uint8_t* row = dst + (size_t)c * kSlot + r * 128;
-                            e4m3x16_to_bf16(code, sc[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
-                                            reinterpret_cast<uint4*>(row + (((2 * kc + 1) ^ (r & 7)) << 4)));
-                        }
-                    }
-                    // the generic stores before the tensor cores (async proxy) read them
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&m.w8empty[cj]);
-                    if (++cj == N8) { cj = 0; cjph ^= 1; }
-                    stage_done();
-                }
-                // the expand blocks of the task (bf16 rows by TMA): only the arrival
-                const unsigned long long mask = expand ? tt.cmask[tw.chunk] : 0ull;
-                for (int g = 0, jj = 0; ok && mask != 0ull && g < n_groups; g++) {
-                    if (!group_present(mask, g)) continue;
-                    if (jj++ % ksplit != tw.split) continue;
-                    if (!slot_free()) { ok = false; break; }
-                    stage_done();
-                }
-                if (!ok) break;
-            }
             // this lane's pair row of the chunk
             const int row = (int)rank * 128 + qd * 32 + lane;
             const bool valid = row < tw.n_real;
@@ -931,12 +997,16 @@ int max_pairs_of() {
 
 // at least half an SM's shared memory: one CTA per SM, so the whole TMEM
 // allocation never waits for another CTA
+// n8 > 0 (FP8 weights): nstages pair-row stages, kNW chain-row stages and
+// n8 code staging slots; else nstages full stages
 int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8) {
-    const int bars = (2 * nstages + 3 + 2 * n8) * 8 + 16;
+    const int nw = n8 > 0 ? kNW : 0;
+    const int rings = n8 > 0 ? nstages * kSlot + nw * 2 * kSlot + n8 * kF8Slot : nstages * kStage2;
+    const int bars = (2 * nstages + 2 * nw + 3 + 2 * n8) * 8 + 16;
     const int slots = (3 * kMaxShrinkSlots + 4) * 4;
     const int table = 8 * max_chunks + (4 * E + 1) * 4;
     const int tr = 16 + kEpiWarps * kTrFloats * 4;
-    return std::max(1024 + nstages * kStage2 + n8 * kF8Slot + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
+    return std::max(1024 + rings + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
 }
 
 int tc2_plan_stages(int E, int max_chunks) {
@@ -945,14 +1015,16 @@ int tc2_plan_stages(int E, int max_chunks) {
     return 0;
 }
 
-// FP8 weights: two main stages (one converted while the other feeds the
-// MMAs) and as deep a code staging ring as fits (at least four steps): the
-// codes are what streams from HBM
+// FP8 weights: the deepest code staging ring that fits (the codes are what
+// streams from HBM), then as many pair-row stages as fit (at least two; they
+// come from L2)
 int tc2_plan_stages_w8(int E, int max_chunks, int* n8) {
     for (int k = 8; k >= 4; k--) {
-        if (tc2_smem_bytes(E, 2, max_chunks, k) <= kTcSmemLimit) {
-            *n8 = k;
-            return 2;
+        for (int nx = 4; nx >= 2; nx--) {
+            if (tc2_smem_bytes(E, nx, max_chunks, k) <= kTcSmemLimit) {
+                *n8 = k;
+                return nx;
+            }
         }
     }
     *n8 = 0;
