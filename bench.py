@@ -1,13 +1,15 @@
 """Benchmark of the multi-LoRA fused MoE layer forward on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C] [--T T]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C] [--T T] [--w8]
 
 A step is one full layer forward (align, both LoRA shrinks, gate_up with the
 fused expand and SiLU*up, down with the fused expand and top-k weight, top-k
 reduce) over one batch of the seeded synthetic workload; by default the
 GPT-OSS-20B-shaped prefill chunk (T=2048 tokens from 16 sequences of 128,
 H=I=2880, E=32, top-4, 8 adapters of rank 32), the largest of the workloads;
---config 1 selects the decode layer (T=16).  Rank 0 prints one JSON line.
+--config 1 selects the decode layer (T=16); --w8 runs the same layer with FP8
+(E4M3) base expert weights (moe_lora_forward_w8, parity against the oracle's
+FP8 forward).  Rank 0 prints one JSON line.
 
 --impl ours       time the CUDA library (inputs resident in HBM), plus the
                   end-to-end call from pinned host buffers, the roofline of the
@@ -52,8 +54,10 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def algorithmic(layer):
-    """Layer-level algorithmic bytes and flops from the actual routing (weights bf16)."""
+def algorithmic(layer, w8: bool = False):
+    """Layer-level algorithmic bytes and flops from the actual routing (weights
+    bf16; with w8, the base expert weights as one-byte codes plus an fp32
+    scale per output row)."""
     import numpy as np
     P = layer.P
     e_of = layer.topk_ids.reshape(-1)
@@ -62,13 +66,19 @@ def algorithmic(layer):
     lora_mask = l_of >= 0
     buckets = len({(int(e), int(l)) for e, l in zip(e_of[lora_mask], l_of[lora_mask])})
     H, I, r, T, k = layer.H, layer.I, layer.r, layer.T, layer.k
-    layer_bytes = 2 * (experts * 3 * H * I + buckets * r * (2 * H + 3 * I) + 2 * T * H) + 8 * T * k + 4 * T
+    wb = 1 if w8 else 2                                  # bytes per base weight
+    scales = experts * 4 * (2 * I + H) if w8 else 0      # fp32 row scales of W1, W2
+    layer_bytes = (wb * experts * 3 * H * I + scales + 2 * (buckets * r * (2 * H + 3 * I) + 2 * T * H)
+                   + 8 * T * k + 4 * T)
     flops = P * 6 * H * I + int(lora_mask.sum()) * 2 * r * (2 * H + 3 * I)
     # per-kernel bytes the two tcgen05 kernels must move: weights of the touched
     # experts (W) and adapter buckets (the expand's B and the shrink's A), the
     # pair rows they read (x in bucket order / act) and what they write
-    gate_up = experts * 2 * I * H * 2 + buckets * (2 * I * r + r * H) * 2 + P * H * 2 + P * I * 2
-    down = experts * H * I * 2 + buckets * (H * r + r * I) * 2 + P * I * 2 + P * H * 4
+    gate_up = experts * 2 * I * H * wb + buckets * (2 * I * r + r * H) * 2 + P * H * 2 + P * I * 2
+    down = experts * H * I * wb + buckets * (H * r + r * I) * 2 + P * I * 2 + P * H * 4
+    if w8:
+        gate_up += experts * 2 * I * 4
+        down += experts * H * 4
     gate_up_flops = P * 2 * H * 2 * I + int(lora_mask.sum()) * 2 * r * (H + 2 * I)
     down_flops = P * 2 * I * H + int(lora_mask.sum()) * 2 * r * (I + H)
     return dict(bytes=layer_bytes, flops=flops, experts_touched=experts, lora_buckets_touched=buckets,
@@ -193,6 +203,9 @@ def run_ours(args, rank, world, local_rank):
 
     layer = wl.make_config(args.config, T=args.T)
     workload = wl.CONFIG_NAMES[args.config] + (f" T={layer.T}" if args.config == 4 else "")
+    if args.w8:
+        layer = wl.quantize_e4m3(layer)
+        workload += ", FP8 (E4M3) base expert weights with per-row scales, bf16 LoRA"
     dl = DeviceLayer(layer, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -200,9 +213,9 @@ def run_ours(args, rank, world, local_rank):
     kernels_per_forward = B.moe_lora_workspace_layout(dl.d)["launches"]
 
     def fwd():
-        st = dl.forward(stream=stream)
+        st = dl.forward_w8(stream=stream) if args.w8 else dl.forward(stream=stream)
         if st != 0:
-            raise B.MoeLoraError(st, "moe_lora_forward")
+            raise B.MoeLoraError(st, "moe_lora_forward_w8" if args.w8 else "moe_lora_forward")
 
     clocks = ClockSampler(local_rank)
     clocks.start()
@@ -248,9 +261,7 @@ def run_ours(args, rank, world, local_rank):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
         for i in range(args.steps):
             flush.zero_()
-            st = B.moe_lora_forward_traced(dl.d, dl.x, dl.topk_ids, dl.topk_weights, dl.lora_ids, dl.W1, dl.W2,
-                                           dl.A1, dl.B1, dl.A2, dl.B2, dl.out, dl.workspace, evs[i], stream)
-            B.check(st, "moe_lora_forward_traced")
+            B.check(dl.forward_traced(evs[i], stream, w8=args.w8), "traced forward")
         torch.cuda.synchronize()
         kern_ms = {name: 0.0 for name in B.KERNEL_SLOTS}
         traced_step_ms = 0.0
@@ -294,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
     status = dl.status(stream)
     if rank == 0 and not args.skip_oracle:
         import oracle
-        ref, _ = oracle.forward(layer)
+        ref, _ = oracle.forward_w8(layer) if args.w8 else oracle.forward(layer)
         got = dl.out_f64()
         parity = {"norm_err": float(np.max(np.abs(got - ref)) / np.max(np.abs(ref))), "tol": TOL,
                   "status": status, "checked": "all outputs vs fp64 oracle"}
@@ -304,7 +315,7 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
 
-    alg = algorithmic(layer)
+    alg = algorithmic(layer, w8=args.w8)
     pk = peaks()
     ms_step = dev_s * 1e3 / args.steps
     dom = max(("gate_up_gemm", "down_gemm"), key=lambda k: kern_ms[k])
@@ -320,12 +331,12 @@ def run_ours(args, rank, world, local_rank):
     # pipe); else HBM (decode-sized batches).  Both fractions are reported.
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     tensor_bound = dom_flops / dom_bytes >= 0.5 * ridge
-    tag = f"config{args.config}" + (f"_T{layer.T}" if args.config == 4 else "")
+    tag = f"config{args.config}" + (f"_T{layer.T}" if args.config == 4 else "") + ("_w8" if args.w8 else "")
     traffic, traffic_src = recorded_traffic(dom, tag)
 
     cpu = None
     if world == 1 and not args.skip_oracle:
-        cpu = cpu_baseline(layer, budget_s=args.cpu_seconds, warmed=parity is not None)
+        cpu = cpu_baseline(layer, budget_s=args.cpu_seconds, warmed=parity is not None, w8=args.w8)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -394,17 +405,18 @@ def _threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(layer, budget_s: float = 12.0, warmed: bool = False):
+def cpu_baseline(layer, budget_s: float = 12.0, warmed: bool = False, w8: bool = False):
     """The oracle as it stands on the host cores: whole batches until ~budget_s
     of CPU work (at least one; a prefill batch takes several seconds)."""
     import oracle
     nt = _threads()
+    run = oracle.forward_w8 if w8 else oracle.forward
     if not warmed:
-        oracle.forward(layer, n_threads=nt)  # warm (page in weights)
+        run(layer, n_threads=nt)  # warm (page in weights)
     t0 = time.perf_counter()
     n = 0
     while True:
-        oracle.forward(layer, n_threads=nt)
+        run(layer, n_threads=nt)
         n += 1
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -485,6 +497,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=90.0)
     ap.add_argument("--skip-oracle", action="store_true", help="no parity check or CPU baseline (profiling runs)")
+    ap.add_argument("--w8", action="store_true",
+                    help="FP8 (E4M3) base expert weights with per-row scales (moe_lora_forward_w8)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -172,10 +172,11 @@ MOELORA_API int moe_lora_forward(const moe_lora_dims *d, const void *x,
  *     scale * value(code).
  * Every other argument, the workspace and the result are those of
  * moe_lora_forward.  The GEMMs run on the CTA-pair kernels for every batch
- * size: the codes stream from HBM by TMA, and each code is turned into
- * bf16(scale * value) in shared memory right before the bf16 MMAs read it
- * (one rounding of the scaled weight to bf16; activations stay bf16, fp32
- * accumulation).  H and I must be multiples of 16 and the layer within the
+ * size: the codes stream from HBM by TMA, and each code is turned into a
+ * bf16 weight in shared memory right before the bf16 MMAs read it: the
+ * row's scale is rounded to bf16 precision once (8 significant bits), and
+ * each weight is value(code) times that, rounded to bf16 (activations stay
+ * bf16, fp32 accumulation).  H and I must be multiples of 16 and the layer within the
  * CTA-pair kernels' bounds (at most 64 adapters, zexp within bounds), else
  * MOELORA_EUNSUPPORTED.  Pointers 16-byte aligned.  Asynchronous on
  * `stream`; same status codes as moe_lora_forward.
@@ -209,6 +210,19 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims *d, const void *x,
                                         const void *A2, const void *B2, void *out,
                                         void *workspace, size_t workspace_bytes, void *stream,
                                         void *const *kernel_events, int32_t n_events);
+
+/*
+ * moe_lora_forward_w8 with the timing marks of moe_lora_forward_traced (same
+ * events, kernel slots and extra status codes).
+ */
+MOELORA_API int moe_lora_forward_w8_traced(const moe_lora_dims *d, const void *x,
+                                           const int32_t *topk_ids, const float *topk_weights,
+                                           const int32_t *token_lora_ids, const void *W1q,
+                                           const float *W1s, const void *W2q, const float *W2s,
+                                           const void *A1, const void *B1, const void *A2,
+                                           const void *B2, void *out, void *workspace,
+                                           size_t workspace_bytes, void *stream,
+                                           void *const *kernel_events, int32_t n_events);
 
 /*
  * Self-test of the device-side wait bounds (the pages have no counterpart).

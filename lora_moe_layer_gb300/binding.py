@@ -27,7 +27,8 @@ MOELORA_ETIMEOUT = -6
 EXPORTED = ("moe_lora_strerror", "moe_lora_version", "moe_lora_align_capacity",
             "moe_lora_workspace_bytes", "moe_lora_align", "moe_lora_forward",
             "moe_lora_get_status", "moe_lora_workspace_layout", "moe_lora_forward_traced",
-            "moe_lora_forward_noalloc", "moe_lora_selftest_wait", "moe_lora_forward_w8")
+            "moe_lora_forward_noalloc", "moe_lora_selftest_wait", "moe_lora_forward_w8",
+            "moe_lora_forward_w8_traced")
 MOELORA_NOALLOC_SCRATCH_BYTES = 16 << 20
 MOELORA_TRACE_EVENTS = 6
 # kernel slots of one forward, in launch order
@@ -88,6 +89,8 @@ def load(path: Optional[str] = None):
     lib.moe_lora_forward_traced.argtypes = [D] + [V] * 12 + [SZ, V, ctypes.POINTER(V), ctypes.c_int32]
     lib.moe_lora_forward_w8.restype = I32
     lib.moe_lora_forward_w8.argtypes = [D] + [V] * 14 + [SZ, V]
+    lib.moe_lora_forward_w8_traced.restype = I32
+    lib.moe_lora_forward_w8_traced.argtypes = [D] + [V] * 14 + [SZ, V, ctypes.POINTER(V), ctypes.c_int32]
     lib.moe_lora_forward_noalloc.restype = I32
     lib.moe_lora_forward_noalloc.argtypes = [D] + [V] * 12
     lib.moe_lora_get_status.restype = I32
@@ -177,11 +180,8 @@ def moe_lora_forward(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids
                                    _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb, _stream(stream))
 
 
-def moe_lora_forward_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2,
-                            B2, out, workspace, events, stream=None,
-                            workspace_bytes: Optional[int] = None) -> int:
-    """events: MOELORA_TRACE_EVENTS torch.cuda.Event objects (or raw cudaEvent_t ints)."""
-    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+def _event_handles(events):
+    """cudaEvent_t handles of torch.cuda.Event objects (or raw ints), as a C array."""
     handles = []
     for ev in events:
         if isinstance(ev, int):
@@ -190,11 +190,19 @@ def moe_lora_forward_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_l
             if ev.cuda_event == 0:  # torch creates the event lazily
                 ev.record()
             handles.append(ev.cuda_event)
-    arr = (ctypes.c_void_p * len(handles))(*handles)
+    return (ctypes.c_void_p * len(handles))(*handles), len(handles)
+
+
+def moe_lora_forward_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2,
+                            B2, out, workspace, events, stream=None,
+                            workspace_bytes: Optional[int] = None) -> int:
+    """events: MOELORA_TRACE_EVENTS torch.cuda.Event objects (or raw cudaEvent_t ints)."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    arr, n = _event_handles(events)
     return load().moe_lora_forward_traced(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
                                           _ptr(token_lora_ids), _ptr(W1), _ptr(W2), _ptr(A1), _ptr(B1),
                                           _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb,
-                                          _stream(stream), arr, len(handles))
+                                          _stream(stream), arr, n)
 
 
 def moe_lora_forward_w8(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1q, W1s, W2q, W2s, A1, B1,
@@ -205,6 +213,18 @@ def moe_lora_forward_w8(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_
                                       _ptr(token_lora_ids), _ptr(W1q), _ptr(W1s), _ptr(W2q), _ptr(W2s), _ptr(A1),
                                       _ptr(B1), _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb,
                                       _stream(stream))
+
+
+def moe_lora_forward_w8_traced(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1q, W1s, W2q, W2s,
+                               A1, B1, A2, B2, out, workspace, events, stream=None,
+                               workspace_bytes: Optional[int] = None) -> int:
+    """moe_lora_forward_w8 with the timing marks of moe_lora_forward_traced."""
+    wb = _nbytes(workspace) if workspace_bytes is None else workspace_bytes
+    arr, n = _event_handles(events)
+    return load().moe_lora_forward_w8_traced(ctypes.byref(d), _ptr(x), _ptr(topk_ids), _ptr(topk_weights),
+                                             _ptr(token_lora_ids), _ptr(W1q), _ptr(W1s), _ptr(W2q), _ptr(W2s),
+                                             _ptr(A1), _ptr(B1), _ptr(A2), _ptr(B2), _ptr(out), _ptr(workspace), wb,
+                                             _stream(stream), arr, n)
 
 
 def moe_lora_forward_noalloc(d: moe_lora_dims, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2,

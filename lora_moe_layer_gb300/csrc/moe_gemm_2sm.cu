@@ -65,19 +65,39 @@ constexpr int kTmem2 = 512;                     // the whole TMEM of the SM: one
 constexpr int kChain1Col = 256;                 // first TMEM column of chain 1
 constexpr int kSlot = 128 * kBK * 2;            // 16 KiB: 128 rows of one 64-wide K step
 constexpr int kStage2 = 3 * kSlot;              // pair rows, chain-0 rows, chain-1 rows
-constexpr int kF8Slot = 2 * 128 * kBK;          // FP8 codes of one K step: nu / 2 rows of each chain
+// FP8 weights: a converted chain-row stage holds the bf16 rows of both chains
+// (at most 128 rows each per CTA; chain c from byte c * kWSlot8 / 2), a
+// staging slot their codes
+constexpr int kWSlot8 = 2 * kSlot;
+constexpr int kF8Slot = 2 * 128 * kBK;
+constexpr int kMaxNW8 = 8;                      // converted chain-row stages at most
+// Chunks of an expert in mode 1 hold up to 256 + 128 pairs: the last 128 (64
+// per CTA) on an M = 128 MMA that reads the same weight stage.  Its tensor
+// memory is 64 lanes x nu/2 columns per chain, so chains of nu_t <= 160 rows
+// fit beside the main accumulators (2 nu_t + 2 nu_t / 2 <= 512).  The tail
+// pair rows (and zexp rows) follow the main 128 in the stage; in mode 1 the
+// chain rows start after them.
+constexpr int kTailRows = 128;
+constexpr int kChunkT = kPairRows + kTailRows;
+constexpr int kXTail = kSlot;                   // tail pair rows in a stage (8 KiB)
+constexpr int kC0T = kSlot + kSlot / 2;         // mode 1: chain-0 rows in a bf16 stage
+constexpr int kXSlot8 = kSlot + kSlot / 2;      // FP8 weights: pair-row stage (main + tail rows)
 // FP8 weights: one more warp streams the codes and kConvWarps warps convert
 // them; the pair rows and the converted chain rows get rings of their own
 constexpr int kConvWarps = 8;
 constexpr int kConvWarp0 = 2 + kEpiWarps + 1;   // first converter warp
 constexpr int kThreadsW8 = (kConvWarp0 + kConvWarps) * 32;
-constexpr int kNW = 2;                          // converted chain-row stages (2 x 16 KiB each)
 constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
 // down epilogue: each warp turns its 32 pairs x 16 columns into whole
 // 64-byte runs of 8 rows per store through a padded tile (row stride of 20
 // floats: the 8 rows of a quarter-warp hit distinct banks)
 constexpr int kTrStride = 20;
 constexpr int kTrFloats = 32 * kTrStride;
+
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
+};
 
 // ---------------------------------------------------------------- CTA pair
 __device__ __forceinline__ uint32_t cta_rank() {
@@ -210,15 +230,125 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return d;
 }
 
+// Task table (shared memory; every thread of the CTA builds it): per active
+// expert its first pair row, pair count, chunk mode and the prefix sums of
+// its tasks (weight tiles x chunks) and of its chunks.  Mode 0: chunks of 256
+// pairs, chains of nu rows.  Mode 1: chunks of 256 + 128 pairs, chains of
+// nu_t rows.  An expert takes mode 1 when it copies fewer rows that way: the
+// stages of these GEMMs cost about their copied rows, and a copied weight
+// row is shared by every pair of the chunk, so an expert with 257 - 384 pairs
+// copies its weights once in mode 1 and twice in mode 0.
+struct PairTable {
+    unsigned long long* cmask;  // [chunks] adapters (< 64) with pairs in each (expert, chunk)
+    int* e;     // [n_active]
+    int* q0;    // [n_active]
+    int* m;     // [n_active]
+    int* md;    // [n_active] chunk mode
+    int* cum;   // [n_active + 1] tasks before each expert
+    int* ccum;  // [n_active + 1] chunks before each expert
+};
+
+struct PairTask {
+    int e, mt, q0c, n_real, n_main, n_tail, chunk, split, mode, nu;
+    __device__ void lookup(const PairTable& tt, int n_active, int ksplit, int nu0, int nu1, int t) {
+        const int tile = t / ksplit;
+        split = t % ksplit;
+        int lo = 0, hi = n_active;  // last expert a with cum[a] <= tile
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tt.cum[mid] <= tile) lo = mid;
+            else hi = mid;
+        }
+        mode = tt.md[lo];
+        const int cap = mode ? kChunkT : kPairRows;
+        const int m = tt.m[lo];
+        const int nch = (m + cap - 1) / cap;
+        const int loc = tile - tt.cum[lo];
+        mt = loc / nch;
+        const int ch = loc % nch;
+        chunk = tt.ccum[lo] + ch;
+        e = tt.e[lo];
+        q0c = tt.q0[lo] + ch * cap;
+        n_real = min(cap, m - ch * cap);
+        n_main = min(n_real, kPairRows);
+        n_tail = n_real - n_main;
+        nu = mode ? nu1 : nu0;
+    }
+};
+
+// nt0 / nt1: weight tiles of an expert in mode 0 / 1; nu1 = 0: mode 0 only
+__device__ void build_pair_table(const TcArgs& a, const PairTable& tt, int n_active, int nt0, int nt1, int nu0,
+                                 int nu1) {
+    for (int ai = threadIdx.x; ai < n_active; ai += blockDim.x) {
+        const int L1 = a.L + 1;
+        const int e = a.active_experts[ai];
+        const int q0 = a.compact_offset[e * L1];
+        const int m = a.compact_offset[(e + 1) * L1] - q0;
+        // rows a CTA copies per K step over all of the expert's tasks
+        const int nch0 = (m + kPairRows - 1) / kPairRows;
+        const long rows0 = (long)nch0 * nt0 * (128 + nu0);
+        int mode = 0;
+        if (nu1 > 0) {
+            const int nch1 = (m + kChunkT - 1) / kChunkT;
+            const int tails = m / kChunkT + (m % kChunkT > kPairRows ? 1 : 0);
+            const long rows1 = (long)nt1 * ((long)nch1 * (128 + nu1) + (long)tails * (kTailRows / 2));
+            mode = rows1 < rows0 ? 1 : 0;
+        }
+        const int nch = mode ? (m + kChunkT - 1) / kChunkT : nch0;
+        tt.e[ai] = e;
+        tt.q0[ai] = q0;
+        tt.m[ai] = m;
+        tt.md[ai] = mode;
+        tt.cum[ai + 1] = (mode ? nt1 : nt0) * nch;
+        tt.ccum[ai + 1] = nch;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < 2) {
+        // warp 0 scans the task counts, warp 1 the chunk counts
+        int* const arr = warp == 0 ? tt.cum : tt.ccum;
+        int carry = 0;
+        for (int base = 0; base < n_active; base += 32) {
+            const int i = base + lane;
+            int v = i < n_active ? arr[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, v, o);
+                if (lane >= o) v += y;
+            }
+            if (i < n_active) arr[i + 1] = carry + v;
+            carry += __shfl_sync(kFull, v, 31);
+        }
+        if (lane == 0) arr[0] = 0;
+    }
+    __syncthreads();
+    if (a.chunk_masks) {
+        // adapters with pairs in each (expert, chunk): one item per (expert,
+        // adapter) bucket, OR-ed into the chunks the bucket's rows fall in
+        const int n_chunks = tt.ccum[n_active];
+        for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) tt.cmask[c] = 0ull;
+        __syncthreads();
+        for (int w = threadIdx.x; w < n_active * a.L; w += blockDim.x) {
+            const int ai = w / a.L, l = w % a.L;
+            const int b = tt.e[ai] * (a.L + 1) + l + 1;
+            const int lo = a.compact_offset[b] - tt.q0[ai], hi = a.compact_offset[b + 1] - tt.q0[ai];
+            const int cap = tt.md[ai] ? kChunkT : kPairRows;
+            const int c0 = tt.ccum[ai];
+            for (int ch = lo / cap; hi > lo && ch <= (hi - 1) / cap; ch++) atomicOr(&tt.cmask[c0 + ch], 1ull << l);
+        }
+        __syncthreads();
+    }
+}
+
 // Shared memory after the stage ring: barriers, the TMEM base, shrink-slot
 // tables and the task table.
 struct Smem2 {
-    uint8_t* ring;    // [NS][kStage2]; FP8 weights: [NS][kSlot] pair rows only
-    uint8_t* wring;   // FP8 weights: [kNW][2 kSlot] chain rows (converted, or TMA-copied LoRA rows)
+    uint8_t* ring;    // [NS][kStage2]; FP8 weights: [NS][kXSlot8] pair rows only
+    uint8_t* wring;   // FP8 weights: [nw][kWSlot8] chain rows (converted, or TMA-copied LoRA rows)
     uint8_t* f8;      // [n8][kF8Slot] FP8 weights: staged codes
     uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed
-    uint64_t* wready; // FP8 weights: [kNW] leader: both CTAs' converters are done with a chain-row stage
-    uint64_t* wempty; // FP8 weights: [kNW] the pair's MMAs are done with a chain-row stage
+    uint64_t* wready; // FP8 weights: [nw] leader: both CTAs' converters are done with a chain-row stage
+    uint64_t* wempty; // FP8 weights: [nw] the pair's MMAs are done with a chain-row stage
     uint64_t* empty;  // [NS] the pair's MMAs are done with stage s
     uint64_t* tfull;  // accumulator ready for the epilogue
     uint64_t* tempty; // leader: accumulator drained by both CTAs' epilogues
@@ -231,16 +361,16 @@ struct Smem2 {
     int* s_sl;        // [kMaxShrinkSlots] adapter of each slot
     int* s_misc;      // [4] shared verdicts
     float* tr;        // [kEpiWarps][kTrFloats] down epilogue transpose tiles
-    TaskTable tt;
+    PairTable tt;
 };
 
 __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     Smem2 m;
     m.ring = base;
     const int n8 = a.w8 ? a.n8 : 0;
-    const int nw = a.w8 ? kNW : 0;
-    m.wring = base + (size_t)NS * (a.w8 ? kSlot : kStage2);
-    m.f8 = m.wring + (size_t)nw * 2 * kSlot;
+    const int nw = a.w8 ? a.nw : 0;
+    m.wring = base + (size_t)NS * (a.w8 ? kXSlot8 : kStage2);
+    m.f8 = m.wring + (size_t)nw * kWSlot8;
     uint64_t* bars = reinterpret_cast<uint64_t*>(m.f8 + (size_t)n8 * kF8Slot);
     m.full = bars;
     m.empty = m.full + NS;
@@ -260,8 +390,10 @@ __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     m.tt.e = reinterpret_cast<int*>(m.tt.cmask + a.max_chunks);
     m.tt.q0 = m.tt.e + a.E;
     m.tt.m = m.tt.q0 + a.E;
-    m.tt.cum = m.tt.m + a.E;
-    m.tr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(m.tt.cum + a.E + 1) + 15) & ~uintptr_t(15));
+    m.tt.md = m.tt.m + a.E;
+    m.tt.cum = m.tt.md + a.E;
+    m.tt.ccum = m.tt.cum + a.E + 1;
+    m.tr = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(m.tt.ccum + a.E + 1) + 15) & ~uintptr_t(15));
     return m;
 }
 
@@ -384,40 +516,42 @@ __device__ bool shrink_epilogue_m(const TcArgs& a, int t, int n_lora, int use, u
 // staged row) into the two 16-byte chunks at `dst0` and `dst1`.
 //
 // A code b (sign bit, 4-bit exponent field f with bias 7, 3-bit mantissa m)
-// placed in an fp32 word as sign -> bit 31 and its other seven bits -> bits
-// 26..20 reads as an fp32 of exponent field f and mantissa m / 8: exactly
+// placed in a bf16 as sign -> bit 15 and its other seven bits -> bits 10..4
+// reads as a bf16 of exponent field f and mantissa m / 8: exactly
 // value(b) * 2^-120, subnormal codes (f = 0) included, since both formats
-// then scale m / 8 by their smallest exponent.  Two packed fp32 multiplies
-// apply the scale and 2^120 (powers of two are exact; the product is
-// rounded once), and one conversion packs two results to bf16 (round to
-// nearest even).  The scale factor is s_hi * s_lo: scale * 2^120 and 1 when
-// that is finite in fp32 (one multiply), else scale * 2^64 and 2^56.
-__device__ __forceinline__ uint32_t e4m3_bits_f32(uint32_t b) { return ((b & 0x80u) << 24) | ((b & 0x7fu) << 20); }
-
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+// then scale m / 8 by their smallest exponent.  Two codes at a time: one
+// byte permute puts them in the upper bytes of the two halves of a word, a
+// shift and two logic ops move the bits, and one packed bf16 multiply by
+// the row's factor gives the weights.  The factor is scale * 2^120 rounded
+// once to bf16 (per row), so each weight is bf16(value * that), rounded
+// once; when scale * 2^120 is beyond bf16's range the factor is
+// scale * 2^64 and an exact second multiply by 2^56 follows.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, float s_hi, float s_lo, uint4* dst0, uint4* dst1) {
+// the two codes of w that `sel` picks, as bf16 bits of value * 2^-120 (low, high half)
+__device__ __forceinline__ uint32_t e4m3x2_bits(uint32_t w, uint32_t sel) {
+    const uint32_t t = __byte_perm(w, 0u, sel);
+    return ((t >> 4) & 0x07F007F0u) | (t & 0x80008000u);
+}
+
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, uint32_t f_hi, uint32_t f_lo, bool two, uint4* dst0,
+                                                uint4* dst1) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    const uint64_t sc = ((uint64_t)__float_as_uint(s_hi) << 32) | __float_as_uint(s_hi);
-    const uint64_t k56 = ((uint64_t)__float_as_uint(s_lo) << 32) | __float_as_uint(s_lo);
-    const bool two = s_lo != 1.0f;
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-#pragma unroll
-        for (int hh = 0; hh < 2; hh++) {
-            const uint32_t lo = e4m3_bits_f32((w[i] >> (16 * hh)) & 0xffu);
-            const uint32_t hi = e4m3_bits_f32((w[i] >> (16 * hh + 8)) & 0xffu);
-            uint64_t v = mul_f32x2(((uint64_t)hi << 32) | lo, sc);
-            if (two) v = mul_f32x2(v, k56);
-            uint32_t d;
-            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "r"((uint32_t)(v >> 32)), "r"((uint32_t)v));
-            o[2 * i + hh] = d;
+        uint32_t lo = mul_bf16x2(e4m3x2_bits(w[i], 0x1404u), f_hi);  // codes 4i, 4i + 1
+        uint32_t hi = mul_bf16x2(e4m3x2_bits(w[i], 0x3424u), f_hi);  // codes 4i + 2, 4i + 3
+        if (two) {
+            lo = mul_bf16x2(lo, f_lo);
+            hi = mul_bf16x2(hi, f_lo);
         }
+        o[2 * i] = lo;
+        o[2 * i + 1] = hi;
     }
     *dst0 = make_uint4(o[0], o[1], o[2], o[3]);
     *dst1 = make_uint4(o[4], o[5], o[6], o[7]);
@@ -429,19 +563,20 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int NS = a.nstages;
     Smem2 m = carve2(base, a, NS);
-    const TaskTable& tt = m.tt;
+    const PairTable& tt = m.tt;
     const uint32_t rank = cta_rank();
     const bool leader = rank == 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int N8 = W8 ? a.n8 : 0;
+    const int NW = W8 ? a.nw : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
             mbar_init(&m.full[s], 1);
             mbar_init(&m.empty[s], 1);
         }
         if (W8) {
-            for (int s = 0; s < kNW; s++) {
+            for (int s = 0; s < a.nw; s++) {
                 mbar_init(&m.wready[s], 2 * kConvWarps);  // the converter warps of both CTAs
                 mbar_init(&m.wempty[s], 1);
             }
@@ -459,6 +594,15 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     if (warp == 0 && lane == 0) {
         if (!W8) prefetch_tensormap(&a.wmap);
         prefetch_tensormap(&a.xmap);
+        if (a.nu_t) {
+            if (!W8) prefetch_tensormap(&a.wmap_t);
+            prefetch_tensormap(&a.xmap_t);
+            if (a.tc_expand) {
+                prefetch_tensormap(&a.bmap_t);
+                prefetch_tensormap(&a.zxmap_t);
+            }
+            if (W8) prefetch_tensormap(&a.w8map_t);
+        }
         if (a.sh_tasks) prefetch_tensormap(&a.amap);
         if (a.tc_expand) {
             prefetch_tensormap(&a.bmap);
@@ -477,15 +621,17 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     pdl_trigger();
 
     // a task covers nu units (gate_up: the gate and the up rows of each) or
-    // 2 * nu W2 rows (down); each CTA copies nu / 2 rows of each chain
-    const int nu = a.nu, nu2 = nu / 2;
+    // 2 * nu W2 rows (down), nu = a.nu for mode-0 chunks and a.nu_t for mode-1
+    // chunks; each CTA copies nu / 2 rows of each chain
+    const int nu0 = a.nu, nu1 = a.nu_t;
     const int N_out = GATE_UP ? a.I : a.H;
     const int K = GATE_UP ? a.H : a.I;
-    const int tile_rows = GATE_UP ? nu : 2 * nu;
-    const int ntiles = (N_out + tile_rows - 1) / tile_rows;
+    const int tr0 = GATE_UP ? nu0 : 2 * nu0, tr1 = GATE_UP ? nu1 : 2 * nu1;
+    const int nt0 = (N_out + tr0 - 1) / tr0;
+    const int nt1 = nu1 > 0 ? (N_out + tr1 - 1) / tr1 : 0;
     const int nkb = (K + kBK - 1) / kBK;
     const int n_active = a.hdr->n_active;
-    build_task_table<kPairRows>(a, tt, n_active, ntiles);
+    build_pair_table(a, tt, n_active, nt0, nt1, nu0, nu1);
     const int ksplit = a.ksplit;
     const bool shrink = a.sh_tasks != nullptr && a.r > 0;
     const bool expand = a.tc_expand != 0 && a.r > 0;
@@ -500,10 +646,13 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     const int rp = expand_rpad(a.r);
     const int apb = 64 / rp;  // adapters per expand block
     const int n_groups = a.L > 0 ? (a.L + apb - 1) / apb : 0;
-    // chain row of this CTA's half for chain c of weight tile mt
-    auto chain_row = [&](int mt, int c) {
-        return GATE_UP ? mt * nu + (int)rank * nu2 : mt * 2 * nu + c * nu + (int)rank * nu2;
+    // chain row of this CTA's half for chain c of weight tile mt (chains of nu rows)
+    auto chain_row = [&](int mt, int c, int nu) {
+        return GATE_UP ? mt * nu + (int)rank * (nu / 2) : mt * 2 * nu + c * nu + (int)rank * (nu / 2);
     };
+    // bf16 stage: byte offsets of the chain-0 rows and from them to the chain-1 rows
+    auto c0_off = [&](int mode) { return mode ? kC0T : kSlot; };
+    auto c1_rel = [&](int mode, int nu) { return mode ? (nu / 2) * kBK * 2 : kSlot; };
     // expand block j of a chunk's mask: the j-th adapter group with an adapter present
     auto group_present = [&](unsigned long long mask, int g) {
         const unsigned long long gm = apb >= 64 ? ~0ull : ((1ull << apb) - 1ull);
@@ -532,12 +681,13 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 armed |= 1u << stage;
                 last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
-                if (W8 && ++wst == kNW) { wst = 0; wph ^= 1; }
+                if (W8 && ++wst == NW) { wst = 0; wph ^= 1; }
             };
-            // this stage's pair rows and its chain-c rows
-            auto xdst = [&]() { return m.ring + (size_t)stage * (W8 ? kSlot : kStage2); };
-            auto cdst = [&](int c) {
-                return W8 ? m.wring + (size_t)wst * 2 * kSlot + c * kSlot : m.ring + (size_t)stage * kStage2 + (1 + c) * kSlot;
+            // this stage's pair rows and its chain-c rows (shrink items: mode 0)
+            auto xdst = [&]() { return m.ring + (size_t)stage * (W8 ? kXSlot8 : kStage2); };
+            auto cdst = [&](int c, int mode = 0, int nu = 0) {
+                return W8 ? m.wring + (size_t)wst * kWSlot8 + c * (kWSlot8 / 2)
+                          : m.ring + (size_t)stage * kStage2 + c0_off(mode) + c * c1_rel(mode, nu);
             };
             for (int t = t_first; t < total && ok; t += t_step) {
                 if (t < n_sh) {
@@ -565,63 +715,80 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     }
                     continue;
                 }
-                Task<kPairRows> tw;
-                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-                const int e = tw.e;
+                PairTask tw;
+                tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
+                const int e = tw.e, nu = tw.nu, nu2 = nu / 2;
                 const int rows0 = tw.q0c + (int)rank * 128;
-                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
-                // per CTA: 128 pair rows + nu / 2 rows of each chain (also for
-                // expand blocks); with FP8 weights the converters fill the
-                // chain rows of the base K steps
-                const uint32_t bytes_pair = 2u * ((uint32_t)kSlot + 2u * (uint32_t)nu2 * kBK * 2u);
-                const uint32_t bytes_base = W8 ? 2u * (uint32_t)kSlot : bytes_pair;
+                const int rows_t = tw.q0c + kPairRows + (int)rank * (kTailRows / 2);  // this CTA's tail rows
+                const int c0row = chain_row(tw.mt, 0, nu), c1row = chain_row(tw.mt, 1, nu);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                for (int kb = kb0; kb < kb1; kb++) {
-                    if (!acquire(bytes_base, false)) { ok = false; break; }
-                    const uint32_t bar = full0 + (uint32_t)stage * 8u;
-                    const int k0 = kb * kBK;
-                    tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
-                    if (W8) {
-                        // chain rows come from the converters
-                    } else if (GATE_UP) {
-                        // the gate rows, then the up rows, of this CTA's nu / 2 units
-                        tma2_4d(cdst(0), &a.wmap, bar, k0, c0row, 0, e);
-                        tma2_4d(cdst(1), &a.wmap, bar, k0, c0row, 1, e);
-                    } else {
-                        tma2_3d(cdst(0), &a.wmap, bar, k0, c0row, e);
-                        tma2_3d(cdst(1), &a.wmap, bar, k0, c1row, e);
+                // The task's copies, with the chunk mode and the tail fixed at
+                // compile time (this thread issues every copy of its CTA; each
+                // mode's maps are named directly, so the copies take the
+                // parameters' own addresses).  Per CTA and stage: 128 pair rows
+                // (+ 64 tail rows) + nu / 2 rows of each chain (also for expand
+                // blocks); with FP8 weights the converters fill the chain rows
+                // of the base K steps.
+                auto produce = [&](auto M1, auto TL) {
+                    constexpr bool m1 = decltype(M1)::value, tl = decltype(TL)::value;
+                    const CUtensorMap* wmap = m1 ? &a.wmap_t : &a.wmap;
+                    const CUtensorMap* bmap = m1 ? &a.bmap_t : &a.bmap;
+                    constexpr uint32_t xbytes = (uint32_t)kSlot + (tl ? (uint32_t)kSlot / 2u : 0u);
+                    const uint32_t bytes_pair = 2u * (xbytes + 2u * (uint32_t)nu2 * kBK * 2u);
+                    const uint32_t bytes_base = W8 ? 2u * xbytes : bytes_pair;
+                    for (int kb = kb0; kb < kb1; kb++) {
+                        if (!acquire(bytes_base, false)) { ok = false; return; }
+                        const uint32_t bar = full0 + (uint32_t)stage * 8u;
+                        const int k0 = kb * kBK;
+                        tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
+                        if constexpr (tl) tma2_2d(xdst() + kXTail, &a.xmap_t, bar, k0, rows_t);
+                        if constexpr (W8) {
+                            // chain rows come from the converters
+                        } else if constexpr (GATE_UP) {
+                            // the gate rows, then the up rows, of this CTA's nu / 2 units
+                            tma2_4d(cdst(0, m1, nu), wmap, bar, k0, c0row, 0, e);
+                            tma2_4d(cdst(1, m1, nu), wmap, bar, k0, c0row, 1, e);
+                        } else {
+                            tma2_3d(cdst(0, m1, nu), wmap, bar, k0, c0row, e);
+                            tma2_3d(cdst(1, m1, nu), wmap, bar, k0, c1row, e);
+                        }
+                        advance();
                     }
-                    advance();
-                }
-                if (!ok || !expand) continue;
-                const unsigned long long mask = tt.cmask[tw.chunk];
-                if (mask == 0ull) continue;
-                if (!z_seen) {
-                    // the expand reads zexp: every shrink item, in both CTAs of its pair, is done
-                    if (!wait_count(a.zdone, 2 * n_sh_tasks)) { ok = false; break; }
-                    // the shrink items' generic stores before the TMA (async proxy) reads
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    z_seen = true;
-                }
-                // expand blocks with an adapter present, dealt over the K splits
-                for (int g = 0, j = 0; g < n_groups && ok; g++) {
-                    if (!group_present(mask, g)) continue;
-                    if (j++ % ksplit != tw.split) continue;
-                    if (!acquire(bytes_pair, true)) { ok = false; break; }
-                    const uint32_t bar = full0 + (uint32_t)stage * 8u;
-                    const int l0 = g * apb;
-                    // zexp rows of this CTA's pairs (apb adapter sub-tiles), then the
-                    // adapters' B rows of each chain
-                    tma2_3d(xdst(), &a.zxmap, bar, 0, rows0, l0);
-                    if (GATE_UP) {
-                        tma2_5d(cdst(0), &a.bmap, bar, 0, c0row, 0, e, l0);
-                        tma2_5d(cdst(1), &a.bmap, bar, 0, c0row, 1, e, l0);
-                    } else {
-                        tma2_4d(cdst(0), &a.bmap, bar, 0, c0row, e, l0);
-                        tma2_4d(cdst(1), &a.bmap, bar, 0, c1row, e, l0);
+                    if (!expand) return;
+                    const unsigned long long mask = tt.cmask[tw.chunk];
+                    if (mask == 0ull) return;
+                    if (!z_seen) {
+                        // the expand reads zexp: every shrink item, in both CTAs of its pair, is done
+                        if (!wait_count(a.zdone, 2 * n_sh_tasks)) { ok = false; return; }
+                        // the shrink items' generic stores before the TMA (async proxy) reads
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        z_seen = true;
                     }
-                    advance();
-                }
+                    // expand blocks with an adapter present, dealt over the K splits
+                    for (int g = 0, j = 0; g < n_groups; g++) {
+                        if (!group_present(mask, g)) continue;
+                        if (j++ % ksplit != tw.split) continue;
+                        if (!acquire(bytes_pair, true)) { ok = false; return; }
+                        const uint32_t bar = full0 + (uint32_t)stage * 8u;
+                        const int l0 = g * apb;
+                        // zexp rows of this CTA's pairs (apb adapter sub-tiles; the
+                        // tail's after the main rows), then the adapters' B rows of
+                        // each chain
+                        tma2_3d(xdst(), &a.zxmap, bar, 0, rows0, l0);
+                        if constexpr (tl) tma2_3d(xdst() + kXTail, &a.zxmap_t, bar, 0, rows_t, l0);
+                        if constexpr (GATE_UP) {
+                            tma2_5d(cdst(0, m1, nu), bmap, bar, 0, c0row, 0, e, l0);
+                            tma2_5d(cdst(1, m1, nu), bmap, bar, 0, c0row, 1, e, l0);
+                        } else {
+                            tma2_4d(cdst(0, m1, nu), bmap, bar, 0, c0row, e, l0);
+                            tma2_4d(cdst(1, m1, nu), bmap, bar, 0, c1row, e, l0);
+                        }
+                        advance();
+                    }
+                };
+                if (tw.mode == 0) produce(BoolC<false>{}, BoolC<false>{});
+                else if (tw.n_tail > 0) produce(BoolC<true>{}, BoolC<true>{});
+                else produce(BoolC<true>{}, BoolC<false>{});
             }
             // every issued copy of both CTAs lands before either CTA may exit (the
             // leader's full barriers count both; the peer waits at the final
@@ -638,15 +805,19 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             // descriptor bases of the pair rows and of the chain rows (FP8
             // weights: two rings); a stage adds its offset in 16-byte units
             const uint64_t dxr = umma_desc_sw128(smem_u32(m.ring));
-            const uint64_t dcr = umma_desc_sw128(smem_u32(W8 ? m.wring : m.ring + kSlot));
+            const uint64_t dcr = umma_desc_sw128(smem_u32(W8 ? m.wring : m.ring));
             const uint64_t exr = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
-            const uint64_t ecr = umma_desc_kmajor(smem_u32(W8 ? m.wring : m.ring + kSlot), expand_layout(rp), 8u * rp * 2u);
+            const uint64_t ecr = umma_desc_kmajor(smem_u32(W8 ? m.wring : m.ring), expand_layout(rp), 8u * rp * 2u);
             constexpr uint64_t kSlot16 = kSlot / 16;
-            constexpr uint64_t kX16 = (W8 ? kSlot : kStage2) / 16;      // pair-row stage stride
-            constexpr uint64_t kC16 = (W8 ? 2 * kSlot : kStage2) / 16;  // chain-row stage stride
-            const uint64_t zsub16 = 128u * rp * 2u / 16u, bsub16 = (uint64_t)nu2 * rp * 2u / 16u;
+            constexpr uint64_t kXT16 = kXTail / 16;                       // tail rows in a pair-row stage
+            constexpr uint64_t kX16 = (W8 ? kXSlot8 : kStage2) / 16;      // pair-row stage stride
+            constexpr uint64_t kC16 = (W8 ? kWSlot8 : kStage2) / 16;    // chain-row stage stride
+            const uint64_t zsub16 = 128u * rp * 2u / 16u, ztsub16 = 64u * rp * 2u / 16u;
             auto xoff = [&]() { return (uint64_t)stage * kX16; };
             auto coff = [&]() { return (uint64_t)(W8 ? wst : stage) * kC16; };
+            // chain-0 rows within a chain-row stage, and chain 1 from chain 0
+            auto c0o = [&](int md) { return W8 ? (uint64_t)0 : (uint64_t)c0_off(md) / 16u; };
+            auto c1o = [&](int md, int nu) { return W8 ? (uint64_t)kWSlot8 / 32u : (uint64_t)c1_rel(md, nu) / 16u; };
             auto take = [&]() {
                 if (!mbar_wait_cluster(&m.full[stage], phase)) return false;
                 if (W8 && !mbar_wait_cluster(&m.wready[wst], wph)) return false;
@@ -658,10 +829,10 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 if (++stage == NS) { stage = 0; phase ^= 1; }
                 if (W8) {
                     umma2_commit_both(&m.wempty[wst]);
-                    if (++wst == kNW) { wst = 0; wph ^= 1; }
+                    if (++wst == NW) { wst = 0; wph ^= 1; }
                 }
             };
-            const uint32_t d_c0 = tmem_base, d_c1 = tmem_base + kChain1Col;
+            const uint32_t d_c0 = tmem_base;
             for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
                 // the accumulator is free once both CTAs' epilogues drained the previous task
                 if (!mbar_wait_cluster(m.tempty, ((uint32_t)it & 1u) ^ 1u)) { ok = false; break; }
@@ -673,7 +844,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
                         if (!take()) { ok = false; break; }
-                        const uint64_t da = dxr + xoff(), db = dcr + coff();
+                        const uint64_t da = dxr + xoff(), db = dcr + coff() + c0o(0);
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; kk++)
                             umma2_bf16(d_c0, da + 2 * kk, db + 2 * kk, idesc, (kb != kb0) || (kk != 0));
@@ -683,37 +854,63 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     umma2_commit_both(m.tfull);
                     continue;
                 }
-                Task<kPairRows> tw;
-                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
+                PairTask tw;
+                tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
+                const int nu = tw.nu, nu2 = nu / 2;
                 const uint32_t idesc = umma_idesc_bf16_f32(256, nu);
+                const uint32_t idesc_t = umma_idesc_bf16_f32(128, nu);
+                const uint64_t bsub16 = (uint64_t)nu2 * rp * 2u / 16u;
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                for (int kb = kb0; kb < kb1; kb++) {
-                    if (!take()) { ok = false; break; }
-                    const uint64_t da = dxr + xoff(), db = dcr + coff();
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; kk++) {
-                        const uint32_t acc = (kb != kb0) || (kk != 0);
-                        umma2_bf16(d_c0, da + 2 * kk, db + 2 * kk, idesc, acc);
-                        umma2_bf16(d_c1, da + 2 * kk, db + kSlot16 + 2 * kk, idesc, acc);
-                    }
-                    release();
-                }
                 const unsigned long long mask = expand ? tt.cmask[tw.chunk] : 0ull;
-                for (int g = 0, j = 0; ok && mask != 0ull && g < n_groups; g++) {
-                    if (!group_present(mask, g)) continue;
-                    if (j++ % ksplit != tw.split) continue;
-                    if (!take()) { ok = false; break; }
-                    const uint64_t ex = exr + xoff(), ec = ecr + coff();
-                    for (int q = 0; q < apb; q++) {
-                        const uint64_t za = ex + q * zsub16;
-                        const uint64_t b0 = ec + q * bsub16, b1 = ec + kSlot16 + q * bsub16;
-                        for (int kk = 0; kk < rp / 16; kk++) {
-                            umma2_bf16(d_c0, za + 2 * kk, b0 + 2 * kk, idesc, 1u);
-                            umma2_bf16(d_c1, za + 2 * kk, b1 + 2 * kk, idesc, 1u);
+                // The task's MMAs, with the chunk mode and the tail fixed at
+                // compile time: this one thread issues every MMA of the pair,
+                // and a test per MMA measurably slows the stages.
+                // Accumulators: chain 0 from column 0, chain 1 from column 256
+                // (mode 0) or nu (mode 1); mode-1 tails (64 lanes x nu / 2
+                // columns per chain in each CTA) after both.
+                auto run = [&](auto M1, auto TL) {
+                    constexpr bool m1 = decltype(M1)::value, tl = decltype(TL)::value;
+                    const uint32_t d_c1 = tmem_base + (m1 ? (uint32_t)nu : (uint32_t)kChain1Col);
+                    const uint32_t d_t0 = tmem_base + 2u * (uint32_t)nu, d_t1 = d_t0 + (uint32_t)nu2;
+                    const uint64_t c0 = c0o(m1 ? 1 : 0), c1 = m1 ? c1o(1, nu) : c1o(0, nu);
+                    for (int kb = kb0; kb < kb1; kb++) {
+                        if (!take()) { ok = false; return; }
+                        const uint64_t da = dxr + xoff(), db = dcr + coff() + c0;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; kk++) {
+                            const uint32_t acc = (kb != kb0) || (kk != 0);
+                            umma2_bf16(d_c0, da + 2 * kk, db + 2 * kk, idesc, acc);
+                            umma2_bf16(d_c1, da + 2 * kk, db + c1 + 2 * kk, idesc, acc);
+                            if constexpr (tl) {
+                                umma2_bf16(d_t0, da + kXT16 + 2 * kk, db + 2 * kk, idesc_t, acc);
+                                umma2_bf16(d_t1, da + kXT16 + 2 * kk, db + c1 + 2 * kk, idesc_t, acc);
+                            }
                         }
+                        release();
                     }
-                    release();
-                }
+                    for (int g = 0, j = 0; mask != 0ull && g < n_groups; g++) {
+                        if (!group_present(mask, g)) continue;
+                        if (j++ % ksplit != tw.split) continue;
+                        if (!take()) { ok = false; return; }
+                        const uint64_t ex = exr + xoff(), ec = ecr + coff() + c0;
+                        for (int q = 0; q < apb; q++) {
+                            const uint64_t za = ex + q * zsub16, zt = ex + kXT16 + q * ztsub16;
+                            const uint64_t b0 = ec + q * bsub16, b1 = ec + c1 + q * bsub16;
+                            for (int kk = 0; kk < rp / 16; kk++) {
+                                umma2_bf16(d_c0, za + 2 * kk, b0 + 2 * kk, idesc, 1u);
+                                umma2_bf16(d_c1, za + 2 * kk, b1 + 2 * kk, idesc, 1u);
+                                if constexpr (tl) {
+                                    umma2_bf16(d_t0, zt + 2 * kk, b0 + 2 * kk, idesc_t, 1u);
+                                    umma2_bf16(d_t1, zt + 2 * kk, b1 + 2 * kk, idesc_t, 1u);
+                                }
+                            }
+                        }
+                        release();
+                    }
+                };
+                if (tw.mode == 0) run(BoolC<false>{}, BoolC<false>{});
+                else if (tw.n_tail > 0) run(BoolC<true>{}, BoolC<true>{});
+                else run(BoolC<true>{}, BoolC<false>{});
                 if (!ok) break;
                 umma2_commit_both(m.tfull);
             }
@@ -725,13 +922,13 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
         if (lane == 0) {
             int j = 0;
             uint32_t ph = 0, armed = 0, last_par = 0;
-            const uint32_t bytes = 2u * (uint32_t)nu2 * kBK;
             for (int t = t_first; t < total && ok; t += t_step) {
                 if (t < n_sh) continue;
-                Task<kPairRows> tw;
-                tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-                const int e = tw.e;
-                const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
+                PairTask tw;
+                tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
+                const int e = tw.e, nu = tw.nu, nu2 = nu / 2;
+                const uint32_t bytes = 2u * (uint32_t)nu2 * kBK;
+                const int c0row = chain_row(tw.mt, 0, nu), c1row = chain_row(tw.mt, 1, nu);
                 const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
                 for (int kb = kb0; kb < kb1; kb++) {
                     if (!mbar_wait(&m.w8empty[j], ph ^ 1)) { ok = false; break; }
@@ -739,8 +936,16 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     uint8_t* dst = m.f8 + (size_t)j * kF8Slot;
                     const int k0 = kb * kBK;
                     if (GATE_UP) {
-                        tma_load_4d(dst, &a.w8map, &m.w8full[j], k0, c0row, 0, e);
-                        tma_load_4d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c0row, 1, e);
+                        if (tw.mode) {
+                            tma_load_4d(dst, &a.w8map_t, &m.w8full[j], k0, c0row, 0, e);
+                            tma_load_4d(dst + nu2 * kBK, &a.w8map_t, &m.w8full[j], k0, c0row, 1, e);
+                        } else {
+                            tma_load_4d(dst, &a.w8map, &m.w8full[j], k0, c0row, 0, e);
+                            tma_load_4d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c0row, 1, e);
+                        }
+                    } else if (tw.mode) {
+                        tma_load_3d(dst, &a.w8map_t, &m.w8full[j], k0, c0row, e);
+                        tma_load_3d(dst + nu2 * kBK, &a.w8map_t, &m.w8full[j], k0, c1row, e);
                     } else {
                         tma_load_3d(dst, &a.w8map, &m.w8full[j], k0, c0row, e);
                         tma_load_3d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c1row, e);
@@ -764,7 +969,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
         // only get the arrival.  Each warp then arrives on the leader's
         // wready barrier.
         const int ct = (warp - kConvWarp0) * 32 + lane;
-        const int n_chunks = 8 * nu2;
+        const uint32_t k2p56 = pack_bf16x2(0x1p56f, 0x1p56f);
         int wst = 0, cj = 0;
         uint32_t wph = 0, cjph = 0;
         const uint32_t lead_wready = cluster_addr(m.wready, 0);
@@ -775,7 +980,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 if (leader) mbar_arrive(&m.wready[wst]);
                 else mbar_arrive_cluster(lead_wready + (uint32_t)wst * 8u);
             }
-            if (++wst == kNW) { wst = 0; wph ^= 1; }
+            if (++wst == NW) { wst = 0; wph ^= 1; }
         };
         for (int t = t_first; t < total && ok; t += t_step) {
             if (t < n_sh) {
@@ -788,12 +993,14 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 }
                 continue;
             }
-            Task<kPairRows> tw;
-            tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-            const int c0row = chain_row(tw.mt, 0), c1row = chain_row(tw.mt, 1);
-            // the scale of each of this thread's rows, as s_hi * s_lo with
-            // s_hi * s_lo = scale * 2^120 (one multiply while that is finite)
-            float sh_[4], sl_[4];
+            PairTask tw;
+            tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
+            const int nu2 = tw.nu / 2, n_chunks = 8 * nu2;
+            const int c0row = chain_row(tw.mt, 0, tw.nu), c1row = chain_row(tw.mt, 1, tw.nu);
+            // the factor of each of this thread's rows: bf16x2 of scale * 2^120
+            // (or scale * 2^64, then 2^56, when that is beyond bf16's range)
+            uint32_t fh_[4];
+            bool two_[4];
 #pragma unroll
             for (int n = 0; n < 4; n++) {
                 const int i = ct + 256 * n;
@@ -809,24 +1016,24 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     }
                 }
                 const float s120 = sc * 0x1p120f;
-                const bool fits = fabsf(s120) <= 3.0e38f;
-                sh_[n] = fits ? s120 : sc * 0x1p64f;
-                sl_[n] = fits ? 1.0f : 0x1p56f;
+                two_[n] = !(fabsf(s120) <= 3.0e38f);
+                const float f = two_[n] ? sc * 0x1p64f : s120;
+                fh_[n] = pack_bf16x2(f, f);
             }
             const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
             for (int kb = kb0; kb < kb1 && ok; kb++) {
                 if (!slot_free()) { ok = false; break; }
                 if (!__all_sync(kFull, mbar_wait(&m.w8full[cj], cjph))) { ok = false; break; }
                 const uint8_t* src = m.f8 + (size_t)cj * kF8Slot;
-                uint8_t* dst = m.wring + (size_t)wst * 2 * kSlot;
+                uint8_t* dst = m.wring + (size_t)wst * kWSlot8;
 #pragma unroll
                 for (int n = 0; n < 4; n++) {
                     const int i = ct + 256 * n;
                     if (i < n_chunks) {
                         const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
                         const uint4 code = *reinterpret_cast<const uint4*>(src + (size_t)c * nu2 * kBK + r * kBK + kc * 16);
-                        uint8_t* row = dst + (size_t)c * kSlot + r * 128;
-                        e4m3x16_to_bf16(code, sh_[n], sl_[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
+                        uint8_t* row = dst + (size_t)c * (kWSlot8 / 2) + r * 128;
+                        e4m3x16_to_bf16(code, fh_[n], k2p56, two_[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
                                         reinterpret_cast<uint4*>(row + (((2 * kc + 1) ^ (r & 7)) << 4)));
                     }
                 }
@@ -866,7 +1073,134 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             else mbar_arrive_cluster(lead_tempty);
         };
         const uint32_t t_lane = tmem_base + ((uint32_t)(qd * 32) << 16);
-        const int ngroups = nu / 16;
+        // Column groups of 16 are drained two at a time: the TMEM loads of
+        // the next group are issued before the current one is processed, so
+        // their latency overlaps the arithmetic and the stores.
+        //
+        // gate_up: SiLU(gate) * up of 16 units into act row `arow` from unit u
+        auto act_emit = [&](const uint32_t (&gr)[16], const uint32_t (&ur)[16], int u, bool row_ok, uint16_t* arow) {
+            if (!row_ok) return;
+            float gv[16], uv[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                gv[i] = __uint_as_float(gr[i]);
+                uv[i] = __uint_as_float(ur[i]);
+            }
+            uint4 lo, hi;
+            lo.x = pack_bf16x2(silu_fast(gv[0]) * uv[0], silu_fast(gv[1]) * uv[1]);
+            lo.y = pack_bf16x2(silu_fast(gv[2]) * uv[2], silu_fast(gv[3]) * uv[3]);
+            lo.z = pack_bf16x2(silu_fast(gv[4]) * uv[4], silu_fast(gv[5]) * uv[5]);
+            lo.w = pack_bf16x2(silu_fast(gv[6]) * uv[6], silu_fast(gv[7]) * uv[7]);
+            hi.x = pack_bf16x2(silu_fast(gv[8]) * uv[8], silu_fast(gv[9]) * uv[9]);
+            hi.y = pack_bf16x2(silu_fast(gv[10]) * uv[10], silu_fast(gv[11]) * uv[11]);
+            hi.z = pack_bf16x2(silu_fast(gv[12]) * uv[12], silu_fast(gv[13]) * uv[13]);
+            hi.w = pack_bf16x2(silu_fast(gv[14]) * uv[14], silu_fast(gv[15]) * uv[15]);
+            if (u + 8 <= a.I) *reinterpret_cast<uint4*>(arow + u) = lo;
+            if (u + 16 <= a.I) *reinterpret_cast<uint4*>(arow + u + 8) = hi;
+        };
+        // gate_up: this warp's groups g = half, half + 2, .. < ng, gate at TMEM
+        // address tg + 16 g and up at tu + 16 g, units from u0 + 16 g
+        auto act_pass = [&](uint32_t tg, uint32_t tu, int u0, int ng, bool row_ok, uint16_t* arow) {
+            uint32_t ga[16], ua[16], gb[16], ub[16];
+            int g = half;
+            if (g >= ng) return;
+            if constexpr (W8) {
+                // (the FP8 kernels' extra warps leave no registers for a second group)
+                for (; g < ng; g += 2) {
+                    tmem_ld16_issue(tg + g * 16, ga);
+                    tmem_ld16_issue(tu + g * 16, ua);
+                    tmem_wait_ld(ga, ua);
+                    act_emit(ga, ua, u0 + g * 16, row_ok, arow);
+                }
+                return;
+            }
+            tmem_ld16_issue(tg + g * 16, ga);
+            tmem_ld16_issue(tu + g * 16, ua);
+            tmem_wait_ld(ga, ua);
+            for (;;) {
+                const int g1 = g + 2;
+                if (g1 < ng) {
+                    tmem_ld16_issue(tg + g1 * 16, gb);
+                    tmem_ld16_issue(tu + g1 * 16, ub);
+                }
+                act_emit(ga, ua, u0 + g * 16, row_ok, arow);
+                if (g1 >= ng) break;
+                tmem_wait_ld(gb, ub);
+                const int g2 = g1 + 2;
+                if (g2 < ng) {
+                    tmem_ld16_issue(tg + g2 * 16, ga);
+                    tmem_ld16_issue(tu + g2 * 16, ua);
+                }
+                act_emit(gb, ub, u0 + g1 * 16, row_ok, arow);
+                if (g2 >= ng) break;
+                tmem_wait_ld(ga, ua);
+                g = g2;
+            }
+        };
+        // down: the pair ids and validity of the 4 rows this lane stores
+        // (lane / 4 + 8 i), from the lanes that hold them
+        auto store_rows = [&](int p, bool row_ok, int (&rp_row)[4], bool (&rv)[4]) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int src = (lane >> 2) + 8 * i;
+                rp_row[i] = __shfl_sync(kFull, p, src);
+                rv[i] = __shfl_sync(kFull, row_ok ? 1 : 0, src) != 0;
+            }
+        };
+        // down: w * d of 16 W2 rows from h into the slab.  The warp's 32 rows x
+        // 16 columns go through its tile: each store then writes 64 contiguous
+        // bytes of 8 rows (lane / 4 + 8 i, quarter lane % 4) instead of 16
+        // bytes of 32 rows.
+        float* const trw = m.tr + ew * kTrFloats;
+        auto down_emit = [&](const uint32_t (&vr)[16], float* slab, int h, float w, const int (&rp_row)[4],
+                             const bool (&rv)[4]) {
+            float4* mine = reinterpret_cast<float4*>(trw + lane * kTrStride);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+                mine[j] = make_float4(w * __uint_as_float(vr[4 * j]), w * __uint_as_float(vr[4 * j + 1]),
+                                      w * __uint_as_float(vr[4 * j + 2]), w * __uint_as_float(vr[4 * j + 3]));
+            __syncwarp();
+            const int c4 = lane & 3;
+            const int hh = h + 4 * c4;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int row = (lane >> 2) + 8 * i;
+                const float4 val = *reinterpret_cast<const float4*>(trw + row * kTrStride + 4 * c4);
+                if (rv[i] && hh + 4 <= a.H) *reinterpret_cast<float4*>(slab + (size_t)rp_row[i] * a.H + hh) = val;
+            }
+            __syncwarp();
+        };
+        // down: this warp's groups g = half, half + 2, .. < ng at TMEM address
+        // t0 + 16 g, W2 rows from h0 + 16 g
+        auto down_pass = [&](float* slab, uint32_t t0, int h0, int ng, float w, const int (&rp_row)[4],
+                             const bool (&rv)[4]) {
+            uint32_t va[16], vb[16];
+            int g = half;
+            if (g >= ng) return;
+            if constexpr (W8) {
+                for (; g < ng; g += 2) {
+                    tmem_ld16_issue(t0 + g * 16, va);
+                    tmem_wait_ld(va);
+                    down_emit(va, slab, h0 + g * 16, w, rp_row, rv);
+                }
+                return;
+            }
+            tmem_ld16_issue(t0 + g * 16, va);
+            tmem_wait_ld(va);
+            for (;;) {
+                const int g1 = g + 2;
+                if (g1 < ng) tmem_ld16_issue(t0 + g1 * 16, vb);
+                down_emit(va, slab, h0 + g * 16, w, rp_row, rv);
+                if (g1 >= ng) break;
+                tmem_wait_ld(vb);
+                const int g2 = g1 + 2;
+                if (g2 < ng) tmem_ld16_issue(t0 + g2 * 16, va);
+                down_emit(vb, slab, h0 + g1 * 16, w, rp_row, rv);
+                if (g2 >= ng) break;
+                tmem_wait_ld(va);
+                g = g2;
+            }
+        };
         for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
             if (t < n_sh) {
                 if (!shrink_epilogue_m(a, t, n_lora, it, tmem_base, qd, half, lane, etid, m, rendezvous, release,
@@ -876,80 +1210,59 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 }
                 continue;
             }
-            Task<kPairRows> tw;
-            tw.lookup(tt, n_active, ksplit, ntiles, t - n_sh);
-            // this lane's pair row of the chunk
+            PairTask tw;
+            tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
+            const int nu = tw.nu, nu2 = nu / 2;
+            // accumulator columns: chain 1 from c1col; mode-1 tails from tcol
+            // (chain c at tcol + c * nu / 2)
+            const uint32_t c1col = tw.mode ? (uint32_t)nu : (uint32_t)kChain1Col;
+            const uint32_t tcol = 2u * (uint32_t)nu;
+            // this lane's main pair row of the chunk
             const int row = (int)rank * 128 + qd * 32 + lane;
-            const bool valid = row < tw.n_real;
+            const bool valid = row < tw.n_main;
             const size_t q = (size_t)tw.q0c + row;
-            int p = 0;
-            float w = 0.f;
-            if (!GATE_UP && valid) {
-                p = a.compact_ids[q];
-                w = a.topk_weights[p];
+            // mode-1 tail: TMEM lane qd * 32 + lane holds tail row (qd % 2) * 32
+            // + lane of this CTA's 64 and the half qd / 2 of each chain's columns
+            const bool tail = tw.n_tail > 0;
+            const int rt = (int)rank * (kTailRows / 2) + (qd & 1) * 32 + lane;
+            const bool valid_t = tail && rt < tw.n_tail;
+            const size_t qt = (size_t)tw.q0c + kPairRows + rt;
+            const int hc = qd >> 1;
+            int p = 0, pt = 0;
+            float w = 0.f, wt = 0.f;
+            if (!GATE_UP) {
+                if (valid) {
+                    p = a.compact_ids[q];
+                    w = a.topk_weights[p];
+                }
+                if (valid_t) {
+                    pt = a.compact_ids[qt];
+                    wt = a.topk_weights[pt];
+                }
             }
             // warp-uniform: the TMEM loads below are warp-collective
             if (!__all_sync(kFull, mbar_wait(m.tfull, (uint32_t)it & 1u))) { ok = false; break; }
             tc_fence_after();
             if (GATE_UP) {
-                // units u0 + 16 g .. u0 + 16 g + 15: gate in columns 16 g.., up 256 further
+                // units u0 + 16 g ..: gate in columns 16 g.., up c1col further
                 const int u0 = tw.mt * nu;
-                uint16_t* arow = a.act_out + q * a.I;
-                for (int g = half; g < ngroups; g += 2) {
-                    float gv[16], uv[16];
-                    tmem_ld16x2(t_lane + g * 16, t_lane + kChain1Col + g * 16, gv, uv);
-                    const int u = u0 + g * 16;
-                    if (valid) {
-                        uint4 lo, hi;
-                        lo.x = pack_bf16x2(silu_fast(gv[0]) * uv[0], silu_fast(gv[1]) * uv[1]);
-                        lo.y = pack_bf16x2(silu_fast(gv[2]) * uv[2], silu_fast(gv[3]) * uv[3]);
-                        lo.z = pack_bf16x2(silu_fast(gv[4]) * uv[4], silu_fast(gv[5]) * uv[5]);
-                        lo.w = pack_bf16x2(silu_fast(gv[6]) * uv[6], silu_fast(gv[7]) * uv[7]);
-                        hi.x = pack_bf16x2(silu_fast(gv[8]) * uv[8], silu_fast(gv[9]) * uv[9]);
-                        hi.y = pack_bf16x2(silu_fast(gv[10]) * uv[10], silu_fast(gv[11]) * uv[11]);
-                        hi.z = pack_bf16x2(silu_fast(gv[12]) * uv[12], silu_fast(gv[13]) * uv[13]);
-                        hi.w = pack_bf16x2(silu_fast(gv[14]) * uv[14], silu_fast(gv[15]) * uv[15]);
-                        if (u + 8 <= a.I) *reinterpret_cast<uint4*>(arow + u) = lo;
-                        if (u + 16 <= a.I) *reinterpret_cast<uint4*>(arow + u + 8) = hi;
-                    }
-                }
+                act_pass(t_lane, t_lane + c1col, u0, nu / 16, valid, a.act_out + q * a.I);
+                // tail lanes: units u0 + hc * nu / 2 + 16 g .. of their row
+                if (tail)
+                    act_pass(t_lane + tcol, t_lane + tcol + nu2, u0 + hc * nu2, nu2 / 16, valid_t, a.act_out + qt * a.I);
             } else {
-                // W2 rows h0 + c * nu + 16 g ..: w * d into this split's slab of
-                // pair_out.  A group's 32 rows x 16 columns go through the
-                // warp's tile: each store then writes 64 contiguous bytes of 8
-                // rows (lane / 4 + 8 i, quarter lane % 4) instead of 16 bytes of
-                // 32 rows.
+                // W2 rows h0 + c * nu + 16 g ..: w * d into this split's slab of pair_out
                 float* const slab = a.pair_out + (ksplit > 1 ? (size_t)tw.split * a.pair_split : 0);
-                float* const tr = m.tr + ew * kTrFloats;
-                const int c4 = lane & 3;
                 int rp_row[4];
                 bool rv[4];
-#pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    const int src = (lane >> 2) + 8 * i;
-                    rp_row[i] = __shfl_sync(kFull, p, src);
-                    rv[i] = __shfl_sync(kFull, valid ? 1 : 0, src) != 0;
-                }
-                for (int c = 0; c < 2; c++) {
-                    const int h0 = tw.mt * 2 * nu + c * nu;
-                    for (int g = half; g < ngroups; g += 2) {
-                        float v[16];
-                        tmem_ld16(t_lane + c * kChain1Col + g * 16, v);
-                        float4* mine = reinterpret_cast<float4*>(tr + lane * kTrStride);
-#pragma unroll
-                        for (int j = 0; j < 4; j++)
-                            mine[j] = make_float4(w * v[4 * j], w * v[4 * j + 1], w * v[4 * j + 2], w * v[4 * j + 3]);
-                        __syncwarp();
-                        const int h = h0 + g * 16 + 4 * c4;
-#pragma unroll
-                        for (int i = 0; i < 4; i++) {
-                            const int row = (lane >> 2) + 8 * i;
-                            const float4 val = *reinterpret_cast<const float4*>(tr + row * kTrStride + 4 * c4);
-                            if (rv[i] && h + 4 <= a.H)
-                                *reinterpret_cast<float4*>(slab + (size_t)rp_row[i] * a.H + h) = val;
-                        }
-                        __syncwarp();
-                    }
+                store_rows(p, valid, rp_row, rv);
+                for (int c = 0; c < 2; c++)
+                    down_pass(slab, t_lane + c * c1col, tw.mt * 2 * nu + c * nu, nu / 16, w, rp_row, rv);
+                if (tail) {
+                    store_rows(pt, valid_t, rp_row, rv);
+                    for (int c = 0; c < 2; c++)
+                        down_pass(slab, t_lane + tcol + c * nu2, tw.mt * 2 * nu + c * nu + hc * nu2, nu2 / 16, wt,
+                                  rp_row, rv);
                 }
             }
             tc_fence_before();
@@ -997,14 +1310,14 @@ int max_pairs_of() {
 
 // at least half an SM's shared memory: one CTA per SM, so the whole TMEM
 // allocation never waits for another CTA
-// n8 > 0 (FP8 weights): nstages pair-row stages, kNW chain-row stages and
+// n8 > 0 (FP8 weights): nstages pair-row stages, nw chain-row stages and
 // n8 code staging slots; else nstages full stages
-int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8) {
-    const int nw = n8 > 0 ? kNW : 0;
-    const int rings = n8 > 0 ? nstages * kSlot + nw * 2 * kSlot + n8 * kF8Slot : nstages * kStage2;
+int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8, int nw) {
+    if (n8 <= 0) nw = 0;
+    const int rings = n8 > 0 ? nstages * kXSlot8 + nw * kWSlot8 + n8 * kF8Slot : nstages * kStage2;
     const int bars = (2 * nstages + 2 * nw + 3 + 2 * n8) * 8 + 16;
     const int slots = (3 * kMaxShrinkSlots + 4) * 4;
-    const int table = 8 * max_chunks + (4 * E + 1) * 4;
+    const int table = 8 * max_chunks + (6 * E + 2) * 4;
     const int tr = 16 + kEpiWarps * kTrFloats * 4;
     return std::max(1024 + rings + bars + slots + table + tr, kTcSmemLimit / 2 + 1024);
 }
@@ -1015,19 +1328,21 @@ int tc2_plan_stages(int E, int max_chunks) {
     return 0;
 }
 
-// FP8 weights: the deepest code staging ring that fits (the codes are what
-// streams from HBM), then as many pair-row stages as fit (at least two; they
-// come from L2)
-int tc2_plan_stages_w8(int E, int max_chunks, int* n8) {
-    for (int k = 8; k >= 4; k--) {
-        for (int nx = 4; nx >= 2; nx--) {
-            if (tc2_smem_bytes(E, nx, max_chunks, k) <= kTcSmemLimit) {
+// FP8 weights: rings that fit, preferring (in this order) the deepest code
+// staging ring (the codes are what streams from HBM), two or three pair-row
+// stages (they come from L2), then as many converted chain-row stages as fit
+// beyond two
+int tc2_plan_stages_w8(int E, int max_chunks, int* n8, int* nw) {
+    for (int k = 8; k >= 3; k--)
+        for (int x = 3; x >= 2; x--)
+            if (tc2_smem_bytes(E, x, max_chunks, k, 2) <= kTcSmemLimit) {
+                int w = 2;
+                while (w < kMaxNW8 && tc2_smem_bytes(E, x, max_chunks, k, w + 1) <= kTcSmemLimit) w++;
                 *n8 = k;
-                return nx;
+                *nw = w;
+                return x;
             }
-        }
-    }
-    *n8 = 0;
+    *n8 = *nw = 0;
     return 0;
 }
 
@@ -1053,9 +1368,12 @@ int tc2_max_pairs(bool gate_up) {
 // programmatic-dependent-launch attribute when asked
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl) {
     if (args.nu < 16 || args.nu > 256 || args.nu % 16 != 0) return cudaErrorInvalidValue;
+    if (args.nu_t != 0 && (args.nu_t < 32 || args.nu_t > 160 || args.nu_t % 32 != 0)) return cudaErrorInvalidValue;
     if (args.r > 0 && (128 / args.r) * 2 > kMaxShrinkSlots) return cudaErrorInvalidValue;
-    if (args.w8 && (args.n8 < 1 || args.nstages < 2 || args.wscale == nullptr)) return cudaErrorInvalidValue;
-    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks, args.w8 ? args.n8 : 0);
+    if (args.w8 && (args.n8 < 1 || args.nw < 2 || args.nw > kMaxNW8 || args.nstages < 2 || args.wscale == nullptr ||
+                    args.nu_t > 160))
+        return cudaErrorInvalidValue;
+    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks, args.w8 ? args.n8 : 0, args.nw);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(args.w8 ? kThreadsW8 : kTcThreads);

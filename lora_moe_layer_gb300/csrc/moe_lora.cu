@@ -63,6 +63,7 @@ struct Layout {
     bool pair_cta;   // the GEMMs run as CTA pairs (moe_gemm_2sm.cu)
     int ranks;       // CTAs per GEMM task: 2 with pair_cta, else 1
     int nu_gu, nu_dn;  // CTA pairs: weight rows per MMA chain of the two GEMMs
+    int nt_gu, nt_dn;  // CTA pairs: the same for experts in chunks of 256 + 128 pairs
     bool w8;           // FP8 (E4M3) base weights: always the CTA-pair kernels
     long tiles_gu, tiles_dn;
     long nbl;  // upper bound of (expert, adapter >= 0) buckets with pairs
@@ -185,18 +186,29 @@ double expected_adapters_per_chunk(const moe_lora_dims* d, long P) {
     return d->L * (1.0 - std::pow(1.0 - 1.0 / d->L, pairs));
 }
 
-// Weight rows per MMA chain of the CTA-pair kernel: `rows` split into the
-// fewest chains of at most 256, each a multiple of 16 (2880 -> 12 x 240).
-int chain_rows(long rows) {
-    const long n = (rows + 255) / 256;
-    return (int)(((rows + n - 1) / n + 15) / 16 * 16);
+// `rows` split into the fewest chains of at most `cap` rows, each a multiple of `mult`
+int chain_rows_cap(long rows, long cap, long mult) {
+    const long n = (rows + cap - 1) / cap;
+    return (int)(((rows + n - 1) / n + mult - 1) / mult * mult);
 }
+
+// Weight rows per MMA chain of the CTA-pair kernel: the fewest chains of at
+// most 256, each a multiple of 16 (2880 -> 12 x 240).
+int chain_rows(long rows) { return chain_rows_cap(rows, 256, 16); }
+
+// Weight rows per MMA chain for experts in chunks of 256 + 128 pairs, whose
+// last 128 pairs have accumulators of 64 lanes x rows/2 columns per chain
+// beside the main ones: the fewest chains of at most 160 rows (3 x 160 <= 512
+// TMEM columns), each a multiple of 32 (2880 -> 18 x 160).
+int chain_rows_tail(long rows) { return chain_rows_cap(rows, 160, 32); }
 
 // Wide chunks (more than 48 pairs per expert on average) run on CTA pairs:
 // chunks of 256 pairs, gate_up tasks of nu units (chains: their gate and
-// their up rows), down tasks of 2 nu W2 rows, as long as the pair kernel
-// covers the layer (at most 64 adapters with the tensor-core expand, its
-// chunk masks and zexp buffers within bounds, a ring that fits).
+// their up rows), down tasks of 2 nu W2 rows, or, for experts the kernel
+// finds cheaper that way, chunks of 256 + 128 pairs with chains of nu_t rows;
+// as long as the pair kernel covers the layer (at most 64 adapters with the
+// tensor-core expand, its chunk masks and zexp buffers within bounds, a ring
+// that fits).
 bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long avg_pairs) {
     if (d->L > 0 && (d->L > 64 || L->P * zexp_cols(d->L, d->r) > kMaxZexpElems)) return false;
     const long chunks = experts_max + (L->P + 255) / 256;
@@ -208,9 +220,15 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     L->bn_gu = L->bn_dn = 256;
     L->nu_gu = chain_rows(d->I);
     L->nu_dn = chain_rows((d->H + 1) / 2);
+    L->nt_gu = chain_rows_tail(d->I);
+    L->nt_dn = chain_rows_tail((d->H + 1) / 2);
+    // weight tiles per chunk in the two modes: the larger count bounds the
+    // tasks; the split choice expects mode 0 (chunks of up to 256 pairs)
     const long nt_gu = (d->I + L->nu_gu - 1) / L->nu_gu, nt_dn = (d->H + 2 * L->nu_dn - 1) / (2 * L->nu_dn);
-    L->tiles_gu = nt_gu * chunks;
-    L->tiles_dn = nt_dn * chunks;
+    const long ntt_gu = L->nt_gu ? (d->I + L->nt_gu - 1) / L->nt_gu : 0;
+    const long ntt_dn = L->nt_dn ? (d->H + 2 * L->nt_dn - 1) / (2 * L->nt_dn) : 0;
+    L->tiles_gu = std::max(nt_gu, ntt_gu) * chunks;
+    L->tiles_dn = std::max(nt_dn, ntt_dn) * chunks;
     L->ks_gu = 1;
     L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, std::max(1, L->sms / 2));
     return true;
@@ -224,6 +242,7 @@ bool plan_gemms(const moe_lora_dims* d, Layout* L) {
     L->pair_cta = false;
     L->ranks = 1;
     L->nu_gu = L->nu_dn = 0;
+    L->nt_gu = L->nt_dn = 0;
     // FP8 weights are dequantised in the CTA-pair kernels only, whatever the batch
     if (L->w8) return plan_pair_gemms(d, L, experts_max, std::max<long>(avg_pairs, 1));
     if (!narrow && !(d->options & MOELORA_OPT_SINGLE_CTA) && plan_pair_gemms(d, L, experts_max, avg_pairs)) return true;
@@ -720,22 +739,29 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             // CTA pairs: 128 pair rows per CTA, chains of nu units (each CTA half of them)
             if (!tc.chunk_masks) tc.max_chunks = 0;
             tc.nu = L.nu_gu;
-            const int half = L.nu_gu / 2;
+            tc.nu_t = L.nt_gu;
+            const int half = L.nu_gu / 2, half_t = L.nt_gu / 2;
             if (w8) {
                 tc.w8 = 1;
                 tc.wscale = w8->W1s;
-                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8);
-                if (tc.nstages < 2 || !encode_w1q_map(&tc.w8map, w8->W1q, d->E, d->I, d->H, half))
-                    return tc.nstages < 2 ? MOELORA_EUNSUPPORTED : MOELORA_ECUDA;
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8, &tc.nw);
+                if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+                if (!encode_w1q_map(&tc.w8map, w8->W1q, d->E, d->I, d->H, half) ||
+                    (half_t && !encode_w1q_map(&tc.w8map_t, w8->W1q, d->E, d->I, d->H, half_t)))
+                    return MOELORA_ECUDA;
             } else {
                 tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
                 if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
             }
-            if ((!w8 && !encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H, half)) ||
+            if ((!w8 && (!encode_w1_map(&tc.wmap, W1, d->E, d->I, d->H, half) ||
+                         (half_t && !encode_w1_map(&tc.wmap_t, W1, d->E, d->I, d->H, half_t)))) ||
                 !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.xc), L.P, d->H, 128) ||
+                (half_t && !encode_rows_map(&tc.xmap_t, at<uint16_t>(ws, L.xc), L.P, d->H, 64)) ||
                 (has_lora && !encode_adapter_map(&tc.amap, A1, d->L, d->E, d->r, d->H)) ||
                 (L.tc_expand && (!encode_b1_map(&tc.bmap, B1, d->L, d->E, d->I, d->r, false, half) ||
-                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128))))
+                                 (half_t && !encode_b1_map(&tc.bmap_t, B1, d->L, d->E, d->I, d->r, false, half_t)) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128) ||
+                                 (half_t && !encode_zexp_map(&tc.zxmap_t, tc.zexp, L.P, d->L, d->r, 64)))))
                 return MOELORA_ECUDA;
         } else {
             tc.nstages = tc_plan_stages(true, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
@@ -782,22 +808,29 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             // CTA pairs: 128 act rows per CTA, two chains of nu W2 rows (each CTA half of each)
             if (!tc.chunk_masks) tc.max_chunks = 0;
             tc.nu = L.nu_dn;
-            const int half = L.nu_dn / 2;
+            tc.nu_t = L.nt_dn;
+            const int half = L.nu_dn / 2, half_t = L.nt_dn / 2;
             if (w8) {
                 tc.w8 = 1;
                 tc.wscale = w8->W2s;
-                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8);
-                if (tc.nstages < 2 || !encode_w2q_map(&tc.w8map, w8->W2q, d->E, d->I, d->H, half))
-                    return tc.nstages < 2 ? MOELORA_EUNSUPPORTED : MOELORA_ECUDA;
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8, &tc.nw);
+                if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
+                if (!encode_w2q_map(&tc.w8map, w8->W2q, d->E, d->I, d->H, half) ||
+                    (half_t && !encode_w2q_map(&tc.w8map_t, w8->W2q, d->E, d->I, d->H, half_t)))
+                    return MOELORA_ECUDA;
             } else {
                 tc.nstages = tc2_plan_stages(d->E, tc.max_chunks);
                 if (tc.nstages < 3) return MOELORA_EUNSUPPORTED;
             }
-            if ((!w8 && !encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H, half)) ||
+            if ((!w8 && (!encode_w2_map(&tc.wmap, W2, d->E, d->I, d->H, half) ||
+                         (half_t && !encode_w2_map(&tc.wmap_t, W2, d->E, d->I, d->H, half_t)))) ||
                 !encode_rows_map(&tc.xmap, at<uint16_t>(ws, L.act), L.P, d->I, 128) ||
+                (half_t && !encode_rows_map(&tc.xmap_t, at<uint16_t>(ws, L.act), L.P, d->I, 64)) ||
                 (has_lora && !encode_adapter_map(&tc.amap, A2, d->L, d->E, d->r, d->I)) ||
                 (L.tc_expand && (!encode_b2_map(&tc.bmap, B2, d->L, d->E, d->H, d->r, false, half) ||
-                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128))))
+                                 (half_t && !encode_b2_map(&tc.bmap_t, B2, d->L, d->E, d->H, d->r, false, half_t)) ||
+                                 !encode_zexp_map(&tc.zxmap, tc.zexp, L.P, d->L, d->r, 128) ||
+                                 (half_t && !encode_zexp_map(&tc.zxmap_t, tc.zexp, L.P, d->L, d->r, 64)))))
                 return MOELORA_ECUDA;
         } else {
             tc.nstages = tc_plan_stages(false, bn, tc.r, d->E, L.tc_expand, tc.chunk_masks ? tc.max_chunks : 0);
@@ -875,6 +908,18 @@ MOELORA_API int moe_lora_forward_traced(const moe_lora_dims* d, const void* x,
     if (!kernel_events || n_events < MOELORA_TRACE_EVENTS) return MOELORA_EINVAL;
     return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, W1, W2, A1, B1, A2, B2, out,
                         workspace, workspace_bytes, stream, kernel_events, n_events);
+}
+
+MOELORA_API int moe_lora_forward_w8_traced(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
+                                           const float* topk_weights, const int32_t* token_lora_ids,
+                                           const void* W1q, const float* W1s, const void* W2q, const float* W2s,
+                                           const void* A1, const void* B1, const void* A2, const void* B2,
+                                           void* out, void* workspace, size_t workspace_bytes, void* stream,
+                                           void* const* kernel_events, int32_t n_events) {
+    if (!kernel_events || n_events < MOELORA_TRACE_EVENTS) return MOELORA_EINVAL;
+    const W8Ptrs w8 = {W1q, W1s, W2q, W2s};
+    return forward_impl(d, x, topk_ids, topk_weights, token_lora_ids, nullptr, nullptr, A1, B1, A2, B2, out,
+                        workspace, workspace_bytes, stream, kernel_events, n_events, &w8);
 }
 
 }  // extern "C"

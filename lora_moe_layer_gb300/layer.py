@@ -66,6 +66,17 @@ class DeviceLayer:
                                      self.W1q, self.W1s, self.W2q, self.W2s, self.A1, self.B1, self.A2, self.B2,
                                      o, self.workspace, stream)
 
+    def forward_traced(self, events, stream=None, w8: bool = False) -> int:
+        """The forward (FP8 weights when w8) with an event recorded before each
+        kernel slot and after the last (MOELORA_TRACE_EVENTS events)."""
+        if w8:
+            return B.moe_lora_forward_w8_traced(self.d, self.x, self.topk_ids, self.topk_weights, self.lora_ids,
+                                                self.W1q, self.W1s, self.W2q, self.W2s, self.A1, self.B1, self.A2,
+                                                self.B2, self.out, self.workspace, events, stream)
+        return B.moe_lora_forward_traced(self.d, self.x, self.topk_ids, self.topk_weights, self.lora_ids, self.W1,
+                                         self.W2, self.A1, self.B1, self.A2, self.B2, self.out, self.workspace, events,
+                                         stream)
+
     def status(self, stream=None) -> int:
         return B.moe_lora_get_status(self.workspace, stream)
 

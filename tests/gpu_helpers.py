@@ -42,3 +42,33 @@ def gpu_align(topk_ids: np.ndarray, lora_ids: np.ndarray, E: int, L: int, bm: in
                bucket_count=cnt.cpu().numpy(), bucket_offset=off.cpu().numpy(),
                tail=sorted_ids[n:].cpu().numpy())
     return res, status
+
+
+def _chain_rows(rows, cap, mult):
+    n = (rows + cap - 1) // cap
+    return ((rows + n - 1) // n + mult - 1) // mult * mult
+
+
+def pair_chunk_modes(layer, gate_up=True):
+    """The chunk mode the CTA-pair kernel picks for each active expert of a
+    layer, from the rule it states: chunks of 256 pairs with chains of nu rows
+    (mode 0), or of 256 + 128 pairs with chains of nu_t rows (mode 1),
+    whichever copies fewer rows per K step over the expert's tasks.  Returns
+    [(pairs, mode)] per expert with pairs; used by tests to show that their
+    shapes reach both modes and tails of every size."""
+    ids = layer.topk_ids.ravel()
+    ids = ids[(ids >= 0) & (ids < layer.E)]
+    counts = np.bincount(ids, minlength=layer.E)
+    out_rows = layer.I if gate_up else layer.H
+    chain = layer.I if gate_up else (layer.H + 1) // 2
+    nu0, nu1 = _chain_rows(chain, 256, 16), _chain_rows(chain, 160, 32)
+    tr0, tr1 = (nu0, nu1) if gate_up else (2 * nu0, 2 * nu1)
+    nt0, nt1 = -(-out_rows // tr0), -(-out_rows // tr1)
+    res = []
+    for m in counts[counts > 0]:
+        m = int(m)
+        rows0 = -(-m // 256) * nt0 * (128 + nu0)
+        tails = m // 384 + (1 if m % 384 > 256 else 0)
+        rows1 = nt1 * (-(-m // 384) * (128 + nu1) + tails * 64)
+        res.append((m, 1 if rows1 < rows0 else 0))
+    return res

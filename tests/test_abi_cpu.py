@@ -195,3 +195,26 @@ def test_noalloc_refuses_oversized_problems_on_the_host(lib):
     f = 1 << 20  # never dereferenced; stream 0 (no torch stream on a host without a device)
     st = B.moe_lora_forward_noalloc(B.dims(T + 1, *shape), f, f, f, f, f, f, f, f, f, f, f, stream=0)
     assert st == B.MOELORA_ENOSPC
+
+
+def test_pair_shapes_reach_both_chunk_modes():
+    """The CTA-pair parity shapes put experts in both chunk modes, with tails
+    of every kind: a single pair, only the first CTA's tail rows, both CTAs'
+    partly and fully, and a tail-less chunk after a full one."""
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    from gpu_helpers import pair_chunk_modes
+    from lora_moe_layer_gb300 import workloads as wl
+    from test_forward_gpu import PAIR_SHAPES
+    modes = {0: set(), 1: set()}
+    for gate_up in (True, False):
+        for shape in PAIR_SHAPES:
+            for m, md in pair_chunk_modes(wl.make_random(*shape, seed=7), gate_up):
+                modes[md].add(m)
+    tails = {m % 384 - 256 for m in modes[1] if m % 384 > 256} | {128 for m in modes[1] if m >= 384}
+    assert modes[0] and modes[1]
+    assert 1 in tails and any(t <= 64 for t in tails) and any(64 < t < 128 for t in tails) and 128 in tails
+    assert any(m > 384 and m % 384 <= 256 for m in modes[1])   # a chunk without a tail after a full one
+    # the prefill layer's experts with 257 - 285 pairs take mode 1, the others mode 0
+    for m, md in pair_chunk_modes(wl.make_config(2)):
+        assert md == (1 if m > 256 else 0)

@@ -97,7 +97,10 @@ def test_ragged_shapes(shape):
 # items in one or both CTAs of a pair and split over K, the down GEMM split
 # over K into slabs, chunks with a tail of a few pairs, a layer without
 # adapters, and one with a single adapter (the tensor-core expand on a
-# one-adapter mix)
+# one-adapter mix); experts in chunks of 256 + 128 pairs (mode 1) with tails
+# of 1, 19, 44, 94 and 128 pairs (only the first CTA's tail rows valid, both
+# partly, both full), a mode-1 chunk without a tail after a full one, both
+# modes in one layer and one GEMM in each mode
 PAIR_SHAPES = [
     (300, 256, 520, 2, 2, 0, 0),
     (256, 512, 1024, 1, 1, 4, 16),
@@ -109,6 +112,11 @@ PAIR_SHAPES = [
     (600, 128, 136, 2, 2, 1, 8),
     (520, 264, 200, 2, 1, 9, 16),
     (100, 2048, 512, 1, 1, 7, 24),
+    (257, 128, 96, 1, 1, 3, 16),
+    (384, 256, 160, 1, 1, 2, 32),
+    (350, 192, 272, 1, 1, 4, 8),
+    (385, 128, 128, 1, 1, 0, 0),
+    (700, 136, 200, 1, 1, 5, 64),
 ]
 
 

@@ -3,8 +3,9 @@ bf16 LoRA) on the GPU against the oracle's FP8 forward.
 
 Bar: max|gpu - ref| / max|ref| <= 1e-2 over every output, where ref is the
 fp64 layer on the exact weights scale * value(code).  The kernel rounds each
-scaled weight to bf16 once before its bf16 MMA: a relative error of at most
-2^-9 per weight, well inside the bar.  With power-of-two scales every scaled
+row's scale to bf16 precision (a per-row factor within 2^-9 of 1) and each
+scaled weight to bf16 before its bf16 MMA: a relative error of at most about
+2^-8 per weight, well inside the bar.  With power-of-two scales every scaled
 weight is a bf16 value, so the FP8 forward must equal the bf16 forward on those
 weights bit for bit (same kernel, same MMAs, same bf16 operands).
 """
