@@ -196,6 +196,28 @@ int chain_rows_cap(long rows, long cap, long mult) {
 // most 256, each a multiple of 16 (2880 -> 12 x 240).
 int chain_rows(long rows) { return chain_rows_cap(rows, 256, 16); }
 
+// The same when the tasks are few (at most three rounds over the CTA pairs,
+// e.g. one dense expert): the chain count whose rounds x rows copied per
+// stage (128 pair rows + the chain rows) is smallest, since a last round
+// that only some pairs run costs as much as a full one.  28672 rows on 76
+// pairs: 150 chains of 192 (2 rounds) instead of 112 of 256 (2 rounds of
+// larger stages).
+int chain_rows_balanced(long rows, long chunks, long pairs) {
+    const long n0 = (rows + 255) / 256;
+    int best = chain_rows(rows);
+    if (n0 * chunks > 3 * pairs) return best;
+    long best_cost = (n0 * chunks + pairs - 1) / pairs * (128 + best);
+    for (long n = n0 + 1; n <= (rows + 127) / 128; n++) {
+        const int nu = (int)(((rows + n - 1) / n + 15) / 16 * 16);
+        const long cost = (n * chunks + pairs - 1) / pairs * (128 + nu);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = nu;
+        }
+    }
+    return best;
+}
+
 // Weight rows per MMA chain for experts in chunks of 256 + 128 pairs, whose
 // last 128 pairs have accumulators of 64 lanes x rows/2 columns per chain
 // beside the main ones: the fewest chains of at most 160 rows (3 x 160 <= 512
@@ -218,7 +240,9 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     L->ranks = 2;
     L->tc_expand = d->L > 0;
     L->bn_gu = L->bn_dn = 256;
-    L->nu_gu = chain_rows(d->I);
+    // gate_up takes no K split on CTA pairs, so its chain width balances the
+    // rounds when the tasks are few; down balances them by its K split
+    L->nu_gu = chain_rows_balanced(d->I, experts_max * ((avg_pairs + 255) / 256), std::max(1, L->sms / 2));
     L->nu_dn = chain_rows((d->H + 1) / 2);
     L->nt_gu = chain_rows_tail(d->I);
     L->nt_dn = chain_rows_tail((d->H + 1) / 2);
