@@ -22,8 +22,11 @@
 // The padded outputs (sentinels, per-tile expert and adapter) are written only
 // for the standalone entry point; the forward works on the compact order and
 // places pairs inside a bucket in any order (shared-memory atomics).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
+#include "tma.cuh"
 
 namespace moelora {
 
@@ -361,7 +364,173 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     pdl_trigger();
 }
 
+// The forward's align on several CTAs.  Each CTA takes a contiguous slice of
+// the pairs: it computes their keys, counts them per bucket in shared memory
+// and adds its counts to the global per-bucket counts, whose old values give
+// its base inside each bucket.  The CTA that arrives last then sees every
+// count: it scans them into the bucket offsets, writes the expert and
+// adapter-bucket lists and the shrink task list (as the single-CTA kernel),
+// and raises a flag; every CTA waits for the flag (bounded; all CTAs of the
+// launch are resident, one per SM) and places its pairs at
+//     compact offset of b + its base in b + its own running count of b.
+// The counts and sync words start from zero: the forward clears them with a
+// memset right before the launch.
+__global__ void __launch_bounds__(kAlignThreads, 1) k_align_multi(AlignArgs a) {
+    extern __shared__ __align__(16) int sm_multi[];
+    __shared__ int2 sw[kAlignWarps + 1];
+    __shared__ int4 sw4[kAlignWarps + 1];
+    __shared__ int s_last, s_ok;
+    pdl_wait();
+    const int tid = threadIdx.x;
+    const int P = a.T * a.k, L1 = a.L + 1, NB = a.E * L1;
+    const int G = gridDim.x, cta = blockIdx.x;
+    const int per = (P + G - 1) / G;
+    const int p0 = min(P, cta * per), p1 = min(P, p0 + per);
+    // shared memory: [NB] counts, [NB] bases, [NB] cursors, [NB + 1] offsets,
+    // [NB] adapter-bucket list, [NB] task scan, [per] keys
+    int* cnt = sm_multi;
+    int* cbase = cnt + NB;
+    int* cur = cbase + NB;
+    int* coff = cur + NB;
+    int* lbs = coff + NB + 1;
+    int* tmp = lbs + NB;
+    int* keys = tmp + NB;
+    WsHeader* hdr = a.hdr;
+
+    for (int i = tid; i < NB; i += kAlignThreads) {
+        cnt[i] = 0;
+        cur[i] = 0;
+    }
+    // the counters of the kernels that follow (grid-stride over all CTAs)
+    for (int i = cta * kAlignThreads + tid; i < a.n_zero; i += G * kAlignThreads) a.zero_ints[i] = 0;
+    for (int i = cta * kAlignThreads + tid; i < a.n_zero2; i += G * kAlignThreads) a.zero_ints2[i] = 0;
+    __syncthreads();
+    {
+        int bad = 0;
+#pragma unroll 4
+        for (int p = p0 + tid; p < p1; p += kAlignThreads) {
+            const int e = a.topk_ids[p];
+            const int l = a.lora_ids[p / a.k];
+            const bool e_ok = e >= 0 && e < a.E;
+            const bool l_ok = l >= -1 && l < a.L;
+            const int b = e_ok && l_ok ? e * L1 + (l + 1) : -1;
+            keys[p - p0] = b;
+            if (b >= 0) atomicAdd(&cnt[b], 1);
+            bad |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
+        }
+        if (bad) atomicOr(&a.sync[2], bad);
+    }
+    __syncthreads();
+    // this CTA's share of each bucket, and where it starts inside the bucket
+    for (int b = tid; b < NB; b += kAlignThreads) {
+        const int c = cnt[b];
+        cbase[b] = c ? atomicAdd(&a.gcount[b], c) : 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(&a.sync[0], 1) == G - 1;
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int b = tid; b < NB; b += kAlignThreads) cnt[b] = __ldcg(a.gcount + b);
+        __syncthreads();
+        const int bm = a.bm;
+        const int4 tot = block_scan4(
+            NB,
+            [&](int b) {
+                const int c = cnt[b];
+                const int sub = b % L1;
+                int any = 0;
+                if (sub == 0)
+                    for (int j = 0; j < L1; j++) any |= cnt[b + j];
+                return make_int4((c + bm - 1) / bm * bm, c, sub != 0 && c > 0 ? 1 : 0, any != 0 ? 1 : 0);
+            },
+            [&](int b, int4 pre, int4 v) {
+                a.bucket_count[b] = cnt[b];
+                a.bucket_offset[b] = pre.x;
+                a.compact_offset[b] = pre.y;
+                coff[b] = pre.y;
+                if (v.z) {
+                    a.lora_buckets[pre.z] = b;
+                    lbs[pre.z] = b;
+                }
+                if (v.w) a.active_experts[pre.w] = b / L1;
+            },
+            sw4);
+        if (tid == 0) {
+            coff[NB] = tot.y;
+            a.bucket_offset[NB] = tot.x;
+            a.compact_offset[NB] = tot.y;
+            hdr->num_post_padded = tot.x;
+            hdr->n_valid = tot.y;
+            hdr->n_lora_buckets = tot.z;
+            hdr->n_active = tot.w;
+            hdr->status = __ldcg(a.sync + 2);
+        }
+        __syncthreads();
+        if (a.st_tasks) {
+            // shrink tasks: st_G consecutive adapter buckets per group, each
+            // group's rows (contiguous in bucket order) in chunks of st_BN
+            const int n = tot.z;
+            const int Gs = a.st_G, BN = a.st_BN;
+            const int ng = (n + Gs - 1) / Gs;
+            auto rows = [&](int g) {
+                const int j1 = min(n, g * Gs + Gs) - 1;
+                return make_int2(coff[lbs[g * Gs]], coff[lbs[j1] + 1]);
+            };
+            block_scan_items(
+                ng, [&](int g) { const int2 q = rows(g); return make_int2((q.y - q.x + BN - 1) / BN, 0); }, tmp,
+                nullptr, sw);
+            __syncthreads();
+            for (int g = tid; g < ng; g += kAlignThreads) {
+                const int2 q = rows(g);
+                int at = tmp[g];
+                for (int q0 = q.x; q0 < q.y; q0 += BN) a.st_tasks[at++] = make_int4(g, q0, min(BN, q.y - q0), 0);
+            }
+            if (tid == 0) hdr->n_shrink_tasks = tmp[ng];
+        }
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.sync + 1), "r"(1) : "memory");
+        }
+    }
+    // placement, once the offsets are out
+    if (tid == 0) s_ok = wait_count(a.sync + 1, 1);
+    __syncthreads();
+    if (!s_ok) {
+        if (tid == 0) atomicOr(&hdr->status, kStatusTimeout);
+        return;
+    }
+    if (!s_last)
+        for (int b = tid; b <= NB; b += kAlignThreads) coff[b] = __ldcg(a.compact_offset + b);
+    __syncthreads();
+#pragma unroll 4
+    for (int p = p0 + tid; p < p1; p += kAlignThreads) {
+        const int b = keys[p - p0];
+        if (b >= 0) a.compact_ids[coff[b] + cbase[b] + atomicAdd(&cur[b], 1)] = p;
+    }
+    pdl_trigger();
+}
+
 }  // namespace
+
+int align_multi_ctas(long P, int sms) {
+    return (int)std::max<long>(1, std::min<long>((P + kAlignThreads - 1) / kAlignThreads, sms));
+}
+
+int align_multi_smem_bytes(int E, int L, long P, int ctas) {
+    const long nb = (long)E * (L + 1);
+    const long per = (P + ctas - 1) / std::max(ctas, 1);
+    const long bytes = (6 * nb + 1 + per) * (long)sizeof(int);
+    return bytes <= kAlignMaxSmem ? (int)bytes : 0;
+}
+
+cudaError_t launch_align_multi(const AlignArgs& args, int ctas, int smem_bytes, cudaStream_t stream) {
+    return launch_k(k_align_multi, dim3(ctas), dim3(kAlignThreads), smem_bytes, stream, false, args);
+}
 
 // Optional shared-memory parts after the histogram (which must be there too):
 // the bucket tables first, then the pair keys, as long as the total fits.
@@ -391,7 +560,9 @@ long align_hist_global_ints(int E, int L) {
 }
 
 cudaError_t init_align_attributes() {
-    return cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmem);
+    const cudaError_t e = cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_align_multi, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlignMaxSmem);
 }
 
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream) {

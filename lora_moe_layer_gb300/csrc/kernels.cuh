@@ -42,6 +42,10 @@ struct AlignArgs {
     int tabs_in_smem;          // 1: bucket sizes and offsets also in shared memory
     int full_outputs;          // 1: also sentinels and per-tile expert/adapter (standalone align)
     WsHeader* hdr;
+    // multi-CTA forward align: per-bucket counts and three sync words
+    // (arrivals, offsets ready, OR of the bad-id bits), zeroed before the launch
+    int* gcount;               // [NB]
+    int* sync;                 // [4]
 };
 
 int align_hist_smem_bytes(int E, int L);   // 0 if the histogram must live in global memory
@@ -50,6 +54,12 @@ int align_tabs_smem_bytes(int E, int L);           // 0 if the bucket tables sta
 int align_smem_bytes(int E, int L, long P);        // dynamic shared memory of the align launch
 long align_hist_global_ints(int E, int L);
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream);
+// The forward's align on several CTAs (pairs in any order inside a bucket):
+// 0 bytes if the bucket tables do not fit its shared memory (then the
+// single-CTA kernel runs), and the CTA count for P pairs on `sms` SMs.
+int align_multi_smem_bytes(int E, int L, long P, int ctas);
+int align_multi_ctas(long P, int sms);
+cudaError_t launch_align_multi(const AlignArgs& args, int ctas, int smem_bytes, cudaStream_t stream);
 cudaError_t init_align_attributes();
 
 // ------------------------------------------------------------ tcgen05 GEMM ----

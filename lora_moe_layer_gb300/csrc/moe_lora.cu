@@ -53,8 +53,8 @@ struct Layout {
     int s1, s2, st_G, st_bn;
     long st_tasks_max;
     size_t hdr, sorted_ids, tile_expert, tile_lora, bucket_count, bucket_offset, compact_offset,
-        compact_ids, active_experts, lora_buckets, hist, keys, st_tasks, counters, z1, z1f, xc, act, z2,
-        z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
+        compact_ids, active_experts, lora_buckets, hist, keys, align_sync, st_tasks, counters, z1, z1f, xc, act,
+        z2, z2f, zexp1, zexp2, pair_out, tc_part, tc_counters, total;
     // LoRA expand on the tensor cores (zexp buffers bounded), else on CUDA cores
     bool tc_expand;
     // tensor-core GEMM plan (shared by the launch code and the workspace size):
@@ -242,7 +242,8 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     L->bn_gu = L->bn_dn = 256;
     // gate_up takes no K split on CTA pairs, so its chain width balances the
     // rounds when the tasks are few; down balances them by its K split
-    L->nu_gu = chain_rows_balanced(d->I, experts_max * ((avg_pairs + 255) / 256), std::max(1, L->sms / 2));
+    const long pairs = std::max(1, L->sms / 2), est_chunks = experts_max * ((avg_pairs + 255) / 256);
+    L->nu_gu = chain_rows_balanced(d->I, est_chunks, pairs);
     L->nu_dn = chain_rows((d->H + 1) / 2);
     L->nt_gu = chain_rows_tail(d->I);
     L->nt_dn = chain_rows_tail((d->H + 1) / 2);
@@ -254,7 +255,7 @@ bool plan_pair_gemms(const moe_lora_dims* d, Layout* L, long experts_max, long a
     L->tiles_gu = std::max(nt_gu, ntt_gu) * chunks;
     L->tiles_dn = std::max(nt_dn, ntt_dn) * chunks;
     L->ks_gu = 1;
-    L->ks_dn = pick_ksplit(nt_dn * experts_max * ((avg_pairs + 255) / 256), d->I, std::max(1, L->sms / 2));
+    L->ks_dn = pick_ksplit(nt_dn * est_chunks, d->I, pairs);
     return true;
 }
 
@@ -322,6 +323,8 @@ int make_layout(const moe_lora_dims* d, Layout* L, bool w8 = false) {
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
     L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
+    // the multi-CTA align's sync words and per-bucket counts
+    L->align_sync = take(sizeof(int32_t) * (4 + L->NB));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
     // the two GEMMs' task counters, the split arrivals of the two shrinks'
     // tasks (per CTA of a task), then the two finished-task counts
@@ -689,7 +692,24 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     Tracer tr{events, n_events, s};
     AlignArgs aa = make_align_args(d, L, topk_ids, token_lora_ids, ws);
     tr.mark(0);
-    if (launch_align(aa, align_smem_bytes(d->E, d->L, L.P), s) != cudaSuccess) return MOELORA_ECUDA;
+    {
+        // batches of more than one CTA's pairs, at least 8 per bucket: the
+        // multi-CTA align, its counts and sync words cleared first (its last
+        // CTA scans all buckets alone, so many buckets favour the single-CTA
+        // kernel); else the single-CTA kernel
+        const int actas = align_multi_ctas(L.P, dev->sms);
+        const int msmem =
+            actas > 1 && L.P >= 8 * L.NB ? align_multi_smem_bytes(d->E, d->L, L.P, actas) : 0;
+        if (msmem > 0) {
+            aa.sync = at<int>(ws, L.align_sync);
+            aa.gcount = aa.sync + 4;
+            if (cudaMemsetAsync(aa.sync, 0, sizeof(int) * (4 + L.NB), s) != cudaSuccess ||
+                launch_align_multi(aa, actas, msmem, s) != cudaSuccess)
+                return MOELORA_ECUDA;
+        } else if (launch_align(aa, align_smem_bytes(d->E, d->L, L.P), s) != cudaSuccess) {
+            return MOELORA_ECUDA;
+        }
+    }
     if (d->T == 0) {
         for (int i = 1; i < MOELORA_TRACE_EVENTS; i++) tr.mark(i);
         return tr.ok ? MOELORA_OK : MOELORA_ECUDA;
