@@ -42,8 +42,10 @@
 //     the task's weight tile; a block holds 64 / r_pad consecutive adapters,
 //     and only blocks with an adapter present in the chunk are issued.
 //
-// Roles in each CTA of the pair (one pair per two SMs, persistent, tasks
-// dealt round-robin over the pairs, shrink items first):
+// Roles in each CTA of the pair (one pair per two SMs, persistent; the
+// leader's producer takes the next item from a device counter when it is
+// ready for it, shrink items first, and hands its index to every role of
+// both CTAs through a queue in each CTA's shared memory):
 //   warp 0   TMA producer of this CTA's halves of every stage; the copies of
 //            both CTAs count on the leader's (rank 0) full barrier, which the
 //            leader arms with both byte counts;
@@ -88,6 +90,7 @@ constexpr int kConvWarps = 8;
 constexpr int kConvWarp0 = 2 + kEpiWarps + 1;   // first converter warp
 constexpr int kThreadsW8 = (kConvWarp0 + kConvWarps) * 32;
 constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
+constexpr int kTaskQ2 = 8;                      // task queue slots (in each CTA of the pair)
 // down epilogue: each warp turns its 32 pairs x 16 columns into whole
 // 64-byte runs of 8 rows per store through a padded tile (row stride of 20
 // floats: the 8 rows of a quarter-warp hit distinct banks)
@@ -356,6 +359,9 @@ struct Smem2 {
     uint32_t* tmem_slot;
     uint64_t* w8full;   // [n8] FP8 weights: this CTA's codes of a staging slot landed
     uint64_t* w8empty;  // [n8] FP8 weights: this CTA's converters are done with a staging slot
+    uint64_t* tq_full;  // [kTaskQ2] task index of a queue slot written (in this CTA)
+    uint64_t* tq_empty; // [kTaskQ2] leader: every consumer of both CTAs has read a slot
+    int* tq;            // [kTaskQ2] task indices
     int* s_cb;        // [kMaxShrinkSlots] first row (relative to the item) of each slot's bucket
     int* s_ce;        // [kMaxShrinkSlots] one past its last row
     int* s_sl;        // [kMaxShrinkSlots] adapter of each slot
@@ -382,7 +388,10 @@ __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     m.tmem_slot = reinterpret_cast<uint32_t*>(m.ebar + 1);
     m.w8full = reinterpret_cast<uint64_t*>(m.tmem_slot + 4);
     m.w8empty = m.w8full + n8;
-    m.s_cb = reinterpret_cast<int*>(m.w8empty + n8);
+    m.tq_full = m.w8empty + n8;
+    m.tq_empty = m.tq_full + kTaskQ2;
+    m.tq = reinterpret_cast<int*>(m.tq_empty + kTaskQ2);
+    m.s_cb = m.tq + kTaskQ2;
     m.s_ce = m.s_cb + kMaxShrinkSlots;
     m.s_sl = m.s_ce + kMaxShrinkSlots;
     m.s_misc = m.s_sl + kMaxShrinkSlots;
@@ -588,6 +597,14 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
         mbar_init(m.tfull, 1);
         mbar_init(m.tempty, 2 * kEpiWarps);
         mbar_init(m.ebar, kEpiWarps * 32);
+        // the task queue: one write per slot (the leader's producer, in both
+        // CTAs); reads in each CTA by the MMA thread (leader) or the producer
+        // (peer), every epilogue warp and, with FP8 weights, the code producer
+        // and every converter warp
+        for (int q = 0; q < kTaskQ2; q++) {
+            mbar_init(&m.tq_full[q], 1);
+            mbar_init(&m.tq_empty[q], 2 * (1 + kEpiWarps + (W8 ? 1 + kConvWarps : 0)));
+        }
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc2(m.tmem_slot, kTmem2);
@@ -643,6 +660,28 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     const int g2 = a.r > 0 ? 128 / a.r : 0;  // shrink slots per CTA
     const int total = n_sh + tt.cum[n_active] * ksplit;
     const int t_first = (int)cluster_index(), t_step = (int)cluster_count();
+    // Items are taken in order from a device counter by the leader's producer
+    // when it is ready for the next one (so pairs that drew cheap items take
+    // more), and handed to every role of both CTAs through the task queue;
+    // without a counter they are dealt round-robin over the pairs.
+    const bool dyn = a.task_counter != nullptr;
+    const uint32_t lead_tq_empty = cluster_addr(m.tq_empty, 0);
+    // the consumers' view of item `it`: one thread, or a whole warp (warp_call)
+    auto take_task = [&](int it, bool& good, bool warp_call) -> int {
+        good = true;
+        if (!dyn) return t_first + it * t_step;
+        const int q = it % kTaskQ2;
+        bool got = mbar_wait_cluster(&m.tq_full[q], (uint32_t)(it / kTaskQ2) & 1u);
+        if (warp_call) got = __all_sync(kFull, got);
+        good = got;
+        const int t = got ? m.tq[q] : total;
+        if (warp_call) __syncwarp();
+        if (got && (!warp_call || (threadIdx.x & 31) == 0)) {
+            if (leader) mbar_arrive(&m.tq_empty[q]);
+            else mbar_arrive_cluster(lead_tq_empty + (uint32_t)q * 8u);
+        }
+        return t;
+    };
     const int rp = expand_rpad(a.r);
     const int apb = 64 / rp;  // adapters per expand block
     const int n_groups = a.L > 0 ? (a.L + apb - 1) / apb : 0;
@@ -689,7 +728,25 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 return W8 ? m.wring + (size_t)wst * kWSlot8 + c * (kWSlot8 / 2)
                           : m.ring + (size_t)stage * kStage2 + c0_off(mode) + c * c1_rel(mode, nu);
             };
-            for (int t = t_first; t < total && ok; t += t_step) {
+            const uint32_t peer_tq = cluster_addr(m.tq, 1), peer_tq_full = cluster_addr(m.tq_full, 1);
+            for (int it = 0; ok; it++) {
+                int t;
+                if (dyn && leader) {
+                    // the next item for both CTAs: into each CTA's queue slot,
+                    // once every consumer of both has read the slot's last item
+                    const int q = it % kTaskQ2;
+                    if (!mbar_wait(&m.tq_empty[q], (((uint32_t)(it / kTaskQ2)) & 1u) ^ 1u)) { ok = false; break; }
+                    t = atomicAdd(a.task_counter, 1);
+                    m.tq[q] = t;
+                    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer_tq + (uint32_t)q * 4u), "r"(t) : "memory");
+                    mbar_arrive(&m.tq_full[q]);
+                    mbar_arrive_cluster(peer_tq_full + (uint32_t)q * 8u);  // release: the store above first
+                } else {
+                    bool good;
+                    t = take_task(it, good, false);
+                    if (!good) { ok = false; break; }
+                }
+                if (t >= total) break;
                 if (t < n_sh) {
                     // shrink item: this CTA's 128 pair rows, then the A boxes of its slots
                     ShItem sh;
@@ -833,7 +890,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 }
             };
             const uint32_t d_c0 = tmem_base;
-            for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+            for (int it = 0; ok; it++) {
+                bool good;
+                const int t = take_task(it, good, false);
+                if (!good) { ok = false; break; }
+                if (t >= total) break;
                 // the accumulator is free once both CTAs' epilogues drained the previous task
                 if (!mbar_wait_cluster(m.tempty, ((uint32_t)it & 1u) ^ 1u)) { ok = false; break; }
                 tc_fence_after();
@@ -922,7 +983,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
         if (lane == 0) {
             int j = 0;
             uint32_t ph = 0, armed = 0, last_par = 0;
-            for (int t = t_first; t < total && ok; t += t_step) {
+            for (int it = 0; ok; it++) {
+                bool good;
+                const int t = take_task(it, good, false);
+                if (!good) { ok = false; break; }
+                if (t >= total) break;
                 if (t < n_sh) continue;
                 PairTask tw;
                 tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
@@ -982,7 +1047,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             }
             if (++wst == NW) { wst = 0; wph ^= 1; }
         };
-        for (int t = t_first; t < total && ok; t += t_step) {
+        for (int it = 0; ok; it++) {
+            bool good;
+            const int t = take_task(it, good, true);
+            if (!good) { ok = false; break; }
+            if (t >= total) break;
             if (t < n_sh) {
                 ShItem sh;
                 sh.load(a, t, n_lora);
@@ -1201,7 +1270,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 g = g2;
             }
         };
-        for (int t = t_first, it = 0; t < total && ok; t += t_step, it++) {
+        for (int it = 0; ok; it++) {
+            bool good;
+            const int t = take_task(it, good, true);
+            if (!good) { ok = false; break; }
+            if (t >= total) break;
             if (t < n_sh) {
                 if (!shrink_epilogue_m(a, t, n_lora, it, tmem_base, qd, half, lane, etid, m, rendezvous, release,
                                        (int)rank)) {
@@ -1315,7 +1388,7 @@ int max_pairs_of() {
 int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8, int nw) {
     if (n8 <= 0) nw = 0;
     const int rings = n8 > 0 ? nstages * kXSlot8 + nw * kWSlot8 + n8 * kF8Slot : nstages * kStage2;
-    const int bars = (2 * nstages + 2 * nw + 3 + 2 * n8) * 8 + 16;
+    const int bars = (2 * nstages + 2 * nw + 3 + 2 * n8 + 2 * kTaskQ2) * 8 + 16 + kTaskQ2 * 4;
     const int slots = (3 * kMaxShrinkSlots + 4) * 4;
     const int table = 8 * max_chunks + (6 * E + 2) * 4;
     const int tr = 16 + kEpiWarps * kTrFloats * 4;

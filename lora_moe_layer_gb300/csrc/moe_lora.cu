@@ -767,7 +767,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     {
         const int bn = L.bn_gu;
         tc.ksplit = L.ks_gu;
-        tc.task_counter = pc ? nullptr : task_counters;
+        tc.task_counter = task_counters;
         tc.part = at<float>(ws, L.tc_part);
         tc.tile_counters = at<int>(ws, L.tc_counters);
         tc.B = has_lora ? static_cast<const uint16_t*>(B1) : nullptr;
@@ -836,7 +836,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     {
         const int bn = L.bn_dn;
         tc.ksplit = L.ks_dn;
-        tc.task_counter = pc ? nullptr : task_counters + 1;
+        tc.task_counter = task_counters + 1;
         tc.tile_counters = at<int>(ws, L.tc_counters) + L.tiles_gu;
         tc.B = has_lora ? static_cast<const uint16_t*>(B2) : nullptr;
         tc.z = has_lora ? at<float>(ws, L.z2f) : nullptr;
