@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kAlignThreads = 512;
 constexpr int kAlignWarps = kAlignThreads / 32;
+static_assert(kAlignWarps == kAlignRowsStable, "one histogram row per warp on the stable path");
 
 __device__ __forceinline__ int2 warp_incl_scan2(int2 v, int lane) {
 #pragma unroll
@@ -161,8 +162,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     const int NB = a.E * L1;
     // shared memory: [histogram][bucket tables][pair keys], each part optional
     int* sm = smem_hist;
-    int* hist = a.hist_global ? a.hist_global : sm;  // [kAlignWarps][NB]
-    if (!a.hist_global) sm += kAlignWarps * NB;
+    int* hist = a.hist_global ? a.hist_global : sm;  // [hist_rows][NB] (+1)
+    if (!a.hist_global) sm += a.hist_rows * NB + 1;
     // bucket sizes and padded / compact offsets; later steps read them from here
     int* cnt_t = a.tabs_in_smem ? sm : a.bucket_count;
     int* boff_t = a.tabs_in_smem ? sm + NB : a.bucket_offset;
@@ -181,8 +182,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     // in pass 1 (all rows), ranks in pass 2.
     const bool stable = a.full_outputs != 0;
     const bool lists = a.active_experts != nullptr && !stable;
-    int* e_act = hist + (kAlignWarps - 1) * NB;   // [E] experts with pairs (lists only)
     int* lbs = hist + NB + 1;                      // copy of the adapter-bucket list (lists only)
+    int* e_act = hist + 2 * NB + 1;               // [E] experts with pairs (lists only)
 
     if (threadIdx.x == 0) hdr->status = 0;
     const int n_hist = stable ? kAlignWarps * NB : NB;
@@ -534,29 +535,32 @@ cudaError_t launch_align_multi(const AlignArgs& args, int ctas, int smem_bytes, 
 
 // Optional shared-memory parts after the histogram (which must be there too):
 // the bucket tables first, then the pair keys, as long as the total fits.
-int align_tabs_smem_bytes(int E, int L) {
-    const int hist = align_hist_smem_bytes(E, L);
+// `rows`: histogram rows of NB ints (kAlignWarps for the standalone entry
+// point's per-warp counts, kAlignRowsForward for the forward).
+int align_tabs_smem_bytes(int E, int L, int rows) {
+    const int hist = align_hist_smem_bytes(E, L, rows);
     const long bytes = (3L * E * (L + 1) + 2) * (long)sizeof(int);
     return hist && hist + bytes <= kAlignMaxSmem ? (int)bytes : 0;
 }
 
-int align_keys_smem_bytes(int E, int L, long P) {
+int align_keys_smem_bytes(int E, int L, long P, int rows) {
     const long bytes = P * (long)sizeof(int);
-    return align_hist_smem_bytes(E, L) + align_tabs_smem_bytes(E, L) + bytes <= kAlignMaxSmem ? (int)bytes : 0;
+    return align_hist_smem_bytes(E, L, rows) + align_tabs_smem_bytes(E, L, rows) + bytes <= kAlignMaxSmem ? (int)bytes
+                                                                                                          : 0;
 }
 
-int align_smem_bytes(int E, int L, long P) {
-    return align_hist_smem_bytes(E, L) + align_tabs_smem_bytes(E, L) + align_keys_smem_bytes(E, L, P);
+int align_smem_bytes(int E, int L, long P, int rows) {
+    return align_hist_smem_bytes(E, L, rows) + align_tabs_smem_bytes(E, L, rows) + align_keys_smem_bytes(E, L, P, rows);
 }
 
-int align_hist_smem_bytes(int E, int L) {
+int align_hist_smem_bytes(int E, int L, int rows) {
     const long nb = (long)E * (L + 1);
-    const long bytes = nb * kAlignWarps * (long)sizeof(int);
+    const long bytes = (nb * rows + 1) * (long)sizeof(int);
     return bytes <= kAlignMaxSmemHist ? (int)bytes : 0;
 }
 
 long align_hist_global_ints(int E, int L) {
-    return align_hist_smem_bytes(E, L) ? 0 : (long)E * (L + 1) * kAlignWarps;
+    return align_hist_smem_bytes(E, L, kAlignWarps) ? 0 : (long)E * (L + 1) * kAlignWarps + 1;
 }
 
 cudaError_t init_align_attributes() {

@@ -41,6 +41,7 @@ struct AlignArgs {
     int keys_in_smem;          // 1: keys in shared memory
     int tabs_in_smem;          // 1: bucket sizes and offsets also in shared memory
     int full_outputs;          // 1: also sentinels and per-tile expert/adapter (standalone align)
+    int hist_rows;             // rows of NB ints in the histogram (kAlignRowsStable / kAlignRowsForward)
     WsHeader* hdr;
     // multi-CTA forward align: per-bucket counts and three sync words
     // (arrivals, offsets ready, OR of the bad-id bits), zeroed before the launch
@@ -48,11 +49,15 @@ struct AlignArgs {
     int* sync;                 // [4]
 };
 
-int align_hist_smem_bytes(int E, int L);   // 0 if the histogram must live in global memory
-int align_keys_smem_bytes(int E, int L, long P);  // 0 if the pair keys must live in global memory
-int align_tabs_smem_bytes(int E, int L);           // 0 if the bucket tables stay in global memory only
-int align_smem_bytes(int E, int L, long P);        // dynamic shared memory of the align launch
-long align_hist_global_ints(int E, int L);
+// histogram rows of the single-CTA align: per-warp counts for the standalone
+// entry point (kAlignWarps rows), counts + lists for the forward
+constexpr int kAlignRowsStable = 16;
+constexpr int kAlignRowsForward = 3;
+int align_hist_smem_bytes(int E, int L, int rows);  // 0 if the histogram must live in global memory
+int align_keys_smem_bytes(int E, int L, long P, int rows);  // 0 if the pair keys must live in global memory
+int align_tabs_smem_bytes(int E, int L, int rows);  // 0 if the bucket tables stay in global memory only
+int align_smem_bytes(int E, int L, long P, int rows);  // dynamic shared memory of the align launch
+long align_hist_global_ints(int E, int L);          // global histogram ints (stable rows) when it does not fit
 cudaError_t launch_align(const AlignArgs& args, int smem_bytes, cudaStream_t stream);
 // The forward's align on several CTAs (pairs in any order inside a bucket):
 // 0 bytes if the bucket tables do not fit its shared memory (then the

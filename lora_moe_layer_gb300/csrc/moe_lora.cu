@@ -322,7 +322,8 @@ int make_layout(const moe_lora_dims* d, Layout* L, bool w8 = false) {
     L->active_experts = take(sizeof(int32_t) * d->E);
     L->lora_buckets = take(sizeof(int32_t) * std::max<long>(std::min(L->NB, L->P), 1));
     L->hist = take(sizeof(int32_t) * align_hist_global_ints(d->E, d->L));
-    L->keys = take(sizeof(int32_t) * (align_keys_smem_bytes(d->E, d->L, L->P) ? 0 : std::max<long>(L->P, 1)));
+    L->keys = take(sizeof(int32_t) *
+                   (align_keys_smem_bytes(d->E, d->L, L->P, kAlignRowsStable) ? 0 : std::max<long>(L->P, 1)));
     // the multi-CTA align's sync words and per-bucket counts
     L->align_sync = take(sizeof(int32_t) * (4 + L->NB));
     L->st_tasks = take(sizeof(int4) * std::max<long>(L->st_tasks_max, 1));
@@ -523,8 +524,9 @@ size_t workspace_need(const moe_lora_dims* d) {
 }
 
 AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t* topk_ids,
-                          const int32_t* lora_ids, void* ws) {
+                          const int32_t* lora_ids, void* ws, int rows = kAlignRowsForward) {
     AlignArgs a = {};
+    a.hist_rows = rows;
     a.T = d->T; a.k = d->k; a.E = d->E; a.L = d->L; a.bm = L.bm;
     a.topk_ids = topk_ids;
     a.lora_ids = lora_ids;
@@ -538,9 +540,9 @@ AlignArgs make_align_args(const moe_lora_dims* d, const Layout& L, const int32_t
     a.compact_ids = at<int32_t>(ws, L.compact_ids);
     a.active_experts = at<int32_t>(ws, L.active_experts);
     a.lora_buckets = at<int32_t>(ws, L.lora_buckets);
-    a.hist_global = align_hist_smem_bytes(d->E, d->L) ? nullptr : at<int>(ws, L.hist);
-    a.keys_in_smem = align_keys_smem_bytes(d->E, d->L, L.P) ? 1 : 0;
-    a.tabs_in_smem = align_tabs_smem_bytes(d->E, d->L) ? 1 : 0;
+    a.hist_global = align_hist_smem_bytes(d->E, d->L, rows) ? nullptr : at<int>(ws, L.hist);
+    a.keys_in_smem = align_keys_smem_bytes(d->E, d->L, L.P, rows) ? 1 : 0;
+    a.tabs_in_smem = align_tabs_smem_bytes(d->E, d->L, rows) ? 1 : 0;
     a.keys_global = a.keys_in_smem ? nullptr : at<int>(ws, L.keys);
     a.full_outputs = 0;
     a.zero_ints = at<int>(ws, L.counters);
@@ -622,7 +624,7 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
     if (!aligned16(workspace)) return MOELORA_EUNSUPPORTED;
     DeviceInfo* dev = nullptr;
     if ((st = device_setup(&dev)) != MOELORA_OK) return st;
-    AlignArgs a = make_align_args(d, L, topk_ids, token_lora_ids, workspace);
+    AlignArgs a = make_align_args(d, L, topk_ids, token_lora_ids, workspace, kAlignRowsStable);
     a.sorted_ids = sorted_ids;
     a.tile_expert = tile_expert;
     a.tile_lora = tile_lora;
@@ -631,7 +633,7 @@ MOELORA_API int moe_lora_align(const moe_lora_dims* d, const int32_t* topk_ids,
     a.bucket_offset = bucket_offset;
     a.active_experts = nullptr;  // the standalone entry point skips the forward's work lists
     a.full_outputs = 1;
-    const cudaError_t e = launch_align(a, align_smem_bytes(d->E, d->L, L.P), (cudaStream_t)stream);
+    const cudaError_t e = launch_align(a, align_smem_bytes(d->E, d->L, L.P, kAlignRowsStable), (cudaStream_t)stream);
     return e == cudaSuccess ? MOELORA_OK : MOELORA_ECUDA;
 }
 
@@ -706,7 +708,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             if (cudaMemsetAsync(aa.sync, 0, sizeof(int) * (4 + L.NB), s) != cudaSuccess ||
                 launch_align_multi(aa, actas, msmem, s) != cudaSuccess)
                 return MOELORA_ECUDA;
-        } else if (launch_align(aa, align_smem_bytes(d->E, d->L, L.P), s) != cudaSuccess) {
+        } else if (launch_align(aa, align_smem_bytes(d->E, d->L, L.P, kAlignRowsForward), s) != cudaSuccess) {
             return MOELORA_ECUDA;
         }
     }
