@@ -115,13 +115,12 @@ struct TcArgs {
     // boxes of those tasks (pair rows and zexp 64 rows, weight and B rows nu_t / 2)
     int nu_t;
     CUtensorMap xmap_t, wmap_t, bmap_t, zxmap_t, w8map_t;
-    // CTA-pair kernel with FP8 base weights: E4M3
-    // codes of W1 as {H, I, 2, E} / W2 as {I, H, E}, box 64 codes x nu/2 rows;
-    // one fp32 scale per output row (W1s [E][2I] / W2s [E][H]); n8 slots of the
-    // code staging ring, nw stages of the converted chain-row ring
+    // CTA-pair kernel with FP8 base weights: E4M3 codes of W1 as {H, I, 2, E}
+    // / W2 as {I, H, E}, box 64 codes x nu/2 rows; one fp32 scale per output
+    // row (W1s [E][2I] / W2s [E][H])
     CUtensorMap w8map;
     const float* wscale;
-    int w8, n8, nw;
+    int w8;
 };
 int tc_smem_bytes(bool gate_up, int bn, int r, int E, int nstages, bool tc_expand, int mask_chunks);
 int tc_plan_stages(bool gate_up, int bn, int r, int E, bool tc_expand, int mask_chunks);
@@ -131,11 +130,11 @@ cudaError_t launch_moe_gemm_tc(const TcArgs& args, bool gate_up, int bn, int gri
 // pair rows over the pair (chunks of up to 256 pairs, or 256 + 128 with chains
 // of nu_t rows), two chains of nu weight rows, tensor-core expand only, chunk
 // masks required, gate_up without K split.
-int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8 = 0, int nw = 0);
+int tc2_smem_bytes(int E, int nstages, int max_chunks, bool w8 = false);
 int tc2_plan_stages(int E, int max_chunks);
-// FP8 base weights: pair-row stages (returned; 0 if none fit), code staging
-// slots (n8) and converted chain-row stages (nw)
-int tc2_plan_stages_w8(int E, int max_chunks, int* n8, int* nw);
+// FP8 base weights: ring stages (pair rows, and the chain rows the codes are
+// expanded into), 0 if fewer than two fit
+int tc2_plan_stages_w8(int E, int max_chunks);
 cudaError_t init_tc2_attributes();
 int tc2_max_pairs(bool gate_up);  // co-resident pairs (0: none or query failed)
 cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cudaStream_t stream, bool pdl);

@@ -67,12 +67,6 @@ constexpr int kTmem2 = 512;                     // the whole TMEM of the SM: one
 constexpr int kChain1Col = 256;                 // first TMEM column of chain 1
 constexpr int kSlot = 128 * kBK * 2;            // 16 KiB: 128 rows of one 64-wide K step
 constexpr int kStage2 = 3 * kSlot;              // pair rows, chain-0 rows, chain-1 rows
-// FP8 weights: a converted chain-row stage holds the bf16 rows of both chains
-// (at most 128 rows each per CTA; chain c from byte c * kWSlot8 / 2), a
-// staging slot their codes
-constexpr int kWSlot8 = 2 * kSlot;
-constexpr int kF8Slot = 2 * 128 * kBK;
-constexpr int kMaxNW8 = 8;                      // converted chain-row stages at most
 // Chunks of an expert in mode 1 hold up to 256 + 128 pairs: the last 128 (64
 // per CTA) on an M = 128 MMA that reads the same weight stage.  Its tensor
 // memory is 64 lanes x nu/2 columns per chain, so chains of nu_t <= 160 rows
@@ -83,11 +77,14 @@ constexpr int kTailRows = 128;
 constexpr int kChunkT = kPairRows + kTailRows;
 constexpr int kXTail = kSlot;                   // tail pair rows in a stage (8 KiB)
 constexpr int kC0T = kSlot + kSlot / 2;         // mode 1: chain-0 rows in a bf16 stage
-constexpr int kXSlot8 = kSlot + kSlot / 2;      // FP8 weights: pair-row stage (main + tail rows)
-// FP8 weights: one more warp streams the codes and kConvWarps warps convert
-// them; the pair rows and the converted chain rows get rings of their own
+// FP8 weights: a stage holds the pair rows (main and tail, 24 KiB) and the
+// two chains' rows (16 KiB each, from kC0T); a base K step's codes are
+// copied into the upper half of each chain's slot and expanded in place to
+// bf16 by kConvWarps converter warps.
+constexpr int kStageW8 = kC0T + 2 * kSlot;
+constexpr int kCodeOff = kSlot / 2;            // a chain's codes inside its slot
 constexpr int kConvWarps = 8;
-constexpr int kConvWarp0 = 2 + kEpiWarps + 1;   // first converter warp
+constexpr int kConvWarp0 = 2 + kEpiWarps;      // first converter warp
 constexpr int kThreadsW8 = (kConvWarp0 + kConvWarps) * 32;
 constexpr int kMaxShrinkSlots = 32;             // buckets per shrink item: 256 / r with r >= 8
 constexpr int kTaskQ2 = 8;                      // task queue slots (in each CTA of the pair)
@@ -346,19 +343,16 @@ __device__ void build_pair_table(const TcArgs& a, const PairTable& tt, int n_act
 // Shared memory after the stage ring: barriers, the TMEM base, shrink-slot
 // tables and the task table.
 struct Smem2 {
-    uint8_t* ring;    // [NS][kStage2]; FP8 weights: [NS][kXSlot8] pair rows only
-    uint8_t* wring;   // FP8 weights: [nw][kWSlot8] chain rows (converted, or TMA-copied LoRA rows)
-    uint8_t* f8;      // [n8][kF8Slot] FP8 weights: staged codes
+    uint8_t* ring;    // [NS][kStage2]; FP8 weights: [NS][kStageW8]
     uint64_t* full;   // [NS] leader: both CTAs' copies of stage s landed
-    uint64_t* wready; // FP8 weights: [nw] leader: both CTAs' converters are done with a chain-row stage
-    uint64_t* wempty; // FP8 weights: [nw] the pair's MMAs are done with a chain-row stage
     uint64_t* empty;  // [NS] the pair's MMAs are done with stage s
+    uint64_t* wready; // FP8 weights: [NS] leader: both CTAs' converters are done with stage s
+    uint64_t* cfull;  // FP8 weights: [NS] this CTA's codes of stage s landed (or the stage has none)
     uint64_t* tfull;  // accumulator ready for the epilogue
     uint64_t* tempty; // leader: accumulator drained by both CTAs' epilogues
     uint64_t* ebar;   // epilogue rendezvous
+    uint64_t* cvbar;  // FP8 weights: converter rendezvous
     uint32_t* tmem_slot;
-    uint64_t* w8full;   // [n8] FP8 weights: this CTA's codes of a staging slot landed
-    uint64_t* w8empty;  // [n8] FP8 weights: this CTA's converters are done with a staging slot
     uint64_t* tq_full;  // [kTaskQ2] task index of a queue slot written (in this CTA)
     uint64_t* tq_empty; // [kTaskQ2] leader: every consumer of both CTAs has read a slot
     int* tq;            // [kTaskQ2] task indices
@@ -373,22 +367,18 @@ struct Smem2 {
 __device__ inline Smem2 carve2(uint8_t* base, const TcArgs& a, int NS) {
     Smem2 m;
     m.ring = base;
-    const int n8 = a.w8 ? a.n8 : 0;
-    const int nw = a.w8 ? a.nw : 0;
-    m.wring = base + (size_t)NS * (a.w8 ? kXSlot8 : kStage2);
-    m.f8 = m.wring + (size_t)nw * kWSlot8;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(m.f8 + (size_t)n8 * kF8Slot);
+    const int nw = a.w8 ? NS : 0;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NS * (a.w8 ? kStageW8 : kStage2));
     m.full = bars;
     m.empty = m.full + NS;
     m.wready = m.empty + NS;
-    m.wempty = m.wready + nw;
-    m.tfull = m.wempty + nw;
+    m.cfull = m.wready + nw;
+    m.tfull = m.cfull + nw;
     m.tempty = m.tfull + 1;
     m.ebar = m.tempty + 1;
-    m.tmem_slot = reinterpret_cast<uint32_t*>(m.ebar + 1);
-    m.w8full = reinterpret_cast<uint64_t*>(m.tmem_slot + 4);
-    m.w8empty = m.w8full + n8;
-    m.tq_full = m.w8empty + n8;
+    m.cvbar = m.ebar + 1;
+    m.tmem_slot = reinterpret_cast<uint32_t*>(m.cvbar + 1);
+    m.tq_full = reinterpret_cast<uint64_t*>(m.tmem_slot + 4);
     m.tq_empty = m.tq_full + kTaskQ2;
     m.tq = reinterpret_cast<int*>(m.tq_empty + kTaskQ2);
     m.s_cb = m.tq + kTaskQ2;
@@ -577,33 +567,25 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
     const bool leader = rank == 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int N8 = W8 ? a.n8 : 0;
-    const int NW = W8 ? a.nw : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; s++) {
             mbar_init(&m.full[s], 1);
             mbar_init(&m.empty[s], 1);
-        }
-        if (W8) {
-            for (int s = 0; s < a.nw; s++) {
+            if (W8) {
                 mbar_init(&m.wready[s], 2 * kConvWarps);  // the converter warps of both CTAs
-                mbar_init(&m.wempty[s], 1);
+                mbar_init(&m.cfull[s], 1);                 // this CTA's producer
             }
-        }
-        for (int j = 0; j < N8; j++) {
-            mbar_init(&m.w8full[j], 1);
-            mbar_init(&m.w8empty[j], kConvWarps);
         }
         mbar_init(m.tfull, 1);
         mbar_init(m.tempty, 2 * kEpiWarps);
         mbar_init(m.ebar, kEpiWarps * 32);
+        mbar_init(m.cvbar, kConvWarps * 32);
         // the task queue: one write per slot (the leader's producer, in both
         // CTAs); reads in each CTA by the MMA thread (leader) or the producer
-        // (peer), every epilogue warp and, with FP8 weights, the code producer
-        // and every converter warp
+        // (peer), every epilogue warp and, with FP8 weights, every converter warp
         for (int q = 0; q < kTaskQ2; q++) {
             mbar_init(&m.tq_full[q], 1);
-            mbar_init(&m.tq_empty[q], 2 * (1 + kEpiWarps + (W8 ? 1 + kConvWarps : 0)));
+            mbar_init(&m.tq_empty[q], 2 * (1 + kEpiWarps + (W8 ? kConvWarps : 0)));
         }
         fence_barrier_init();
     }
@@ -706,26 +688,29 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             uint32_t phase = 0, armed = 0, last_par = 0;
             bool z_seen = false;
             const uint32_t full0 = cluster_addr(m.full, 0);  // the leader's full[0]
-            // FP8 weights: the chain rows of a stage live in their own ring (wst);
-            // this thread writes them only for shrink items and expand blocks
-            int wst = 0;
-            uint32_t wph = 0;
-            auto acquire = [&](uint32_t bytes_pair, bool chains) {
+            // Take stage `stage` for copies of `bytes_pair` bytes over both CTAs
+            // (counted on the leader's full barrier).  FP8 weights: this CTA's
+            // `code_bytes` of codes count on its own cfull barrier; a stage
+            // without codes completes its cfull phase at once, so the
+            // converters walk every stage in step.
+            auto acquire = [&](uint32_t bytes_pair, uint32_t code_bytes) {
                 if (!mbar_wait_cluster(&m.empty[stage], phase ^ 1)) return false;
-                if (W8 && chains && !mbar_wait_cluster(&m.wempty[wst], wph ^ 1)) return false;
                 if (leader) mbar_arrive_expect_tx(&m.full[stage], bytes_pair);
+                if (W8) {
+                    if (code_bytes) mbar_arrive_expect_tx(&m.cfull[stage], code_bytes);
+                    else mbar_arrive(&m.cfull[stage]);
+                }
                 return true;
             };
             auto advance = [&]() {
                 armed |= 1u << stage;
                 last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
-                if (W8 && ++wst == NW) { wst = 0; wph ^= 1; }
             };
             // this stage's pair rows and its chain-c rows (shrink items: mode 0)
-            auto xdst = [&]() { return m.ring + (size_t)stage * (W8 ? kXSlot8 : kStage2); };
+            auto xdst = [&]() { return m.ring + (size_t)stage * (W8 ? kStageW8 : kStage2); };
             auto cdst = [&](int c, int mode = 0, int nu = 0) {
-                return W8 ? m.wring + (size_t)wst * kWSlot8 + c * (kWSlot8 / 2)
+                return W8 ? m.ring + (size_t)stage * kStageW8 + kC0T + c * kSlot
                           : m.ring + (size_t)stage * kStage2 + c0_off(mode) + c * c1_rel(mode, nu);
             };
             const uint32_t peer_tq = cluster_addr(m.tq, 1), peer_tq_full = cluster_addr(m.tq_full, 1);
@@ -762,7 +747,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     const int rows0 = sh.q0c + (int)rank * 128;
                     const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                     for (int kb = kb0; kb < kb1; kb++) {
-                        if (!acquire(bytes_pair, true)) { ok = false; break; }
+                        if (!acquire(bytes_pair, 0u)) { ok = false; break; }
                         const uint32_t bar = full0 + (uint32_t)stage * 8u;
                         const int k0 = kb * kBK;
                         tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
@@ -793,14 +778,26 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     constexpr uint32_t xbytes = (uint32_t)kSlot + (tl ? (uint32_t)kSlot / 2u : 0u);
                     const uint32_t bytes_pair = 2u * (xbytes + 2u * (uint32_t)nu2 * kBK * 2u);
                     const uint32_t bytes_base = W8 ? 2u * xbytes : bytes_pair;
+                    const uint32_t code_bytes = W8 ? 2u * (uint32_t)nu2 * kBK : 0u;
+                    const CUtensorMap* qmap = m1 ? &a.w8map_t : &a.w8map;
                     for (int kb = kb0; kb < kb1; kb++) {
-                        if (!acquire(bytes_base, false)) { ok = false; return; }
+                        if (!acquire(bytes_base, code_bytes)) { ok = false; return; }
                         const uint32_t bar = full0 + (uint32_t)stage * 8u;
                         const int k0 = kb * kBK;
                         tma2_2d(xdst(), &a.xmap, bar, k0, rows0);
                         if constexpr (tl) tma2_2d(xdst() + kXTail, &a.xmap_t, bar, k0, rows_t);
                         if constexpr (W8) {
-                            // chain rows come from the converters
+                            // this CTA's codes into the upper half of each chain's
+                            // slot (the converters expand them in place)
+                            uint8_t* d0 = cdst(0) + kCodeOff;
+                            uint8_t* d1 = cdst(1) + kCodeOff;
+                            if constexpr (GATE_UP) {
+                                tma_load_4d(d0, qmap, &m.cfull[stage], k0, c0row, 0, e);
+                                tma_load_4d(d1, qmap, &m.cfull[stage], k0, c0row, 1, e);
+                            } else {
+                                tma_load_3d(d0, qmap, &m.cfull[stage], k0, c0row, e);
+                                tma_load_3d(d1, qmap, &m.cfull[stage], k0, c1row, e);
+                            }
                         } else if constexpr (GATE_UP) {
                             // the gate rows, then the up rows, of this CTA's nu / 2 units
                             tma2_4d(cdst(0, m1, nu), wmap, bar, k0, c0row, 0, e);
@@ -825,7 +822,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                     for (int g = 0, j = 0; g < n_groups; g++) {
                         if (!group_present(mask, g)) continue;
                         if (j++ % ksplit != tw.split) continue;
-                        if (!acquire(bytes_pair, true)) { ok = false; return; }
+                        if (!acquire(bytes_pair, 0u)) { ok = false; return; }
                         const uint32_t bar = full0 + (uint32_t)stage * 8u;
                         const int l0 = g * apb;
                         // zexp rows of this CTA's pairs (apb adapter sub-tiles; the
@@ -853,41 +850,43 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             if (leader)
                 for (int s = 0; s < NS; s++)
                     if ((armed >> s) & 1u) mbar_wait(&m.full[s], (last_par >> s) & 1u);
+            // FP8 weights: and this CTA's code copies
+            if (W8)
+                for (int s = 0; s < NS; s++)
+                    if ((armed >> s) & 1u) mbar_wait(&m.cfull[s], (last_par >> s) & 1u);
         }
     } else if (warp == 1) {
         if (leader && lane == 0) {
             // ------------------------------------------------- MMA issuer (leader)
-            int stage = 0, wst = 0;
-            uint32_t phase = 0, wph = 0;
-            // descriptor bases of the pair rows and of the chain rows (FP8
-            // weights: two rings); a stage adds its offset in 16-byte units
+            int stage = 0;
+            uint32_t phase = 0;
+            // descriptor bases of the stage ring; a stage adds its offset in
+            // 16-byte units
             const uint64_t dxr = umma_desc_sw128(smem_u32(m.ring));
-            const uint64_t dcr = umma_desc_sw128(smem_u32(W8 ? m.wring : m.ring));
+            const uint64_t dcr = dxr;
             const uint64_t exr = umma_desc_kmajor(smem_u32(m.ring), expand_layout(rp), 8u * rp * 2u);
-            const uint64_t ecr = umma_desc_kmajor(smem_u32(W8 ? m.wring : m.ring), expand_layout(rp), 8u * rp * 2u);
+            const uint64_t ecr = exr;
             constexpr uint64_t kSlot16 = kSlot / 16;
-            constexpr uint64_t kXT16 = kXTail / 16;                       // tail rows in a pair-row stage
-            constexpr uint64_t kX16 = (W8 ? kXSlot8 : kStage2) / 16;      // pair-row stage stride
-            constexpr uint64_t kC16 = (W8 ? kWSlot8 : kStage2) / 16;    // chain-row stage stride
+            constexpr uint64_t kXT16 = kXTail / 16;                       // tail rows in a stage
+            constexpr uint64_t kX16 = (W8 ? kStageW8 : kStage2) / 16;    // stage stride
+            constexpr uint64_t kC16 = kX16;
             const uint64_t zsub16 = 128u * rp * 2u / 16u, ztsub16 = 64u * rp * 2u / 16u;
             auto xoff = [&]() { return (uint64_t)stage * kX16; };
-            auto coff = [&]() { return (uint64_t)(W8 ? wst : stage) * kC16; };
-            // chain-0 rows within a chain-row stage, and chain 1 from chain 0
-            auto c0o = [&](int md) { return W8 ? (uint64_t)0 : (uint64_t)c0_off(md) / 16u; };
-            auto c1o = [&](int md, int nu) { return W8 ? (uint64_t)kWSlot8 / 32u : (uint64_t)c1_rel(md, nu) / 16u; };
+            auto coff = [&]() { return (uint64_t)stage * kC16; };
+            // chain-0 rows within a stage, and chain 1 from chain 0
+            auto c0o = [&](int md) { return W8 ? (uint64_t)kC0T / 16u : (uint64_t)c0_off(md) / 16u; };
+            auto c1o = [&](int md, int nu) { return W8 ? kSlot16 : (uint64_t)c1_rel(md, nu) / 16u; };
+            // a stage is ready when both CTAs' copies landed and, with FP8
+            // weights, both CTAs' converters are done with it
             auto take = [&]() {
                 if (!mbar_wait_cluster(&m.full[stage], phase)) return false;
-                if (W8 && !mbar_wait_cluster(&m.wready[wst], wph)) return false;
+                if (W8 && !mbar_wait_cluster(&m.wready[stage], phase)) return false;
                 tc_fence_after();
                 return true;
             };
             auto release = [&]() {
                 umma2_commit_both(&m.empty[stage]);
                 if (++stage == NS) { stage = 0; phase ^= 1; }
-                if (W8) {
-                    umma2_commit_both(&m.wempty[wst]);
-                    if (++wst == NW) { wst = 0; wph ^= 1; }
-                }
             };
             const uint32_t d_c0 = tmem_base;
             for (int it = 0; ok; it++) {
@@ -976,76 +975,39 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 umma2_commit_both(m.tfull);
             }
         }
-    } else if (W8 && warp == kEpiWarps + 2) {
-        // --------------------------------------------- FP8 code producer (TMA)
-        // This CTA's codes of both chains for every base K step, into the
-        // staging ring, ahead of the converters by up to n8 steps.
-        if (lane == 0) {
-            int j = 0;
-            uint32_t ph = 0, armed = 0, last_par = 0;
-            for (int it = 0; ok; it++) {
-                bool good;
-                const int t = take_task(it, good, false);
-                if (!good) { ok = false; break; }
-                if (t >= total) break;
-                if (t < n_sh) continue;
-                PairTask tw;
-                tw.lookup(tt, n_active, ksplit, nu0, nu1, t - n_sh);
-                const int e = tw.e, nu = tw.nu, nu2 = nu / 2;
-                const uint32_t bytes = 2u * (uint32_t)nu2 * kBK;
-                const int c0row = chain_row(tw.mt, 0, nu), c1row = chain_row(tw.mt, 1, nu);
-                const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
-                for (int kb = kb0; kb < kb1; kb++) {
-                    if (!mbar_wait(&m.w8empty[j], ph ^ 1)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&m.w8full[j], bytes);
-                    uint8_t* dst = m.f8 + (size_t)j * kF8Slot;
-                    const int k0 = kb * kBK;
-                    if (GATE_UP) {
-                        if (tw.mode) {
-                            tma_load_4d(dst, &a.w8map_t, &m.w8full[j], k0, c0row, 0, e);
-                            tma_load_4d(dst + nu2 * kBK, &a.w8map_t, &m.w8full[j], k0, c0row, 1, e);
-                        } else {
-                            tma_load_4d(dst, &a.w8map, &m.w8full[j], k0, c0row, 0, e);
-                            tma_load_4d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c0row, 1, e);
-                        }
-                    } else if (tw.mode) {
-                        tma_load_3d(dst, &a.w8map_t, &m.w8full[j], k0, c0row, e);
-                        tma_load_3d(dst + nu2 * kBK, &a.w8map_t, &m.w8full[j], k0, c1row, e);
-                    } else {
-                        tma_load_3d(dst, &a.w8map, &m.w8full[j], k0, c0row, e);
-                        tma_load_3d(dst + nu2 * kBK, &a.w8map, &m.w8full[j], k0, c1row, e);
-                    }
-                    armed |= 1u << j;
-                    last_par = (last_par & ~(1u << j)) | (ph << j);
-                    if (++j == N8) { j = 0; ph ^= 1; }
-                }
-            }
-            // every issued copy lands before the CTA may exit
-            for (int q = 0; q < N8; q++)
-                if ((armed >> q) & 1u) mbar_wait(&m.w8full[q], (last_par >> q) & 1u);
-        }
     } else if (W8 && warp >= kConvWarp0) {
         // ------------------------------------------------ FP8 code converters
-        // For every stage of the chain-row ring, in the order the MMAs use
-        // them: once the pair's MMAs are done with the slot, the base K steps
-        // get bf16(scale * value) of this CTA's staged codes (thread ct
-        // converts 16-code chunks i = ct + 256 n: chain c, row r, chunk kc);
-        // stages whose chain rows TMA brings (shrink items, expand blocks)
-        // only get the arrival.  Each warp then arrives on the leader's
-        // wready barrier.
+        // Every stage of the ring, in the order the producer fills it: once
+        // this CTA's codes of a base K step landed (cfull), each thread reads
+        // its 16-code chunks (i = ct + 256 n: chain c, row r, chunk kc) from
+        // the upper half of the chain slots, the converter warps meet at a
+        // named barrier, and each writes bf16(scale x value) of its chunks in
+        // the 128-byte-swizzled rows the MMA reads, over the codes' slots.
+        // Stages of shrink items and expand blocks (rows by TMA) pass.  Each
+        // warp then arrives on the leader's wready barrier of the stage.
         const int ct = (warp - kConvWarp0) * 32 + lane;
         const uint32_t k2p56 = pack_bf16x2(0x1p56f, 0x1p56f);
-        int wst = 0, cj = 0;
-        uint32_t wph = 0, cjph = 0;
+        int stage = 0;
+        uint32_t phase = 0, cpar = 0;
         const uint32_t lead_wready = cluster_addr(m.wready, 0);
-        auto slot_free = [&]() { return __all_sync(kFull, mbar_wait_cluster(&m.wempty[wst], wph ^ 1)); };
+        // all converter threads meet (bounded); false on timeout, warp-uniform
+        auto rendezvous = [&]() {
+            mbar_arrive(m.cvbar);
+            const bool r_ok = __all_sync(kFull, mbar_wait(m.cvbar, cpar));
+            cpar ^= 1;
+            return r_ok;
+        };
+        // waits for this stage's codes (or the producer's mark of a stage
+        // without codes): the producer takes a stage only after the pair's
+        // MMAs are done with its last use
+        auto stage_in = [&]() { return __all_sync(kFull, mbar_wait(&m.cfull[stage], phase)); };
         auto stage_done = [&]() {
             __syncwarp();
             if (lane == 0) {
-                if (leader) mbar_arrive(&m.wready[wst]);
-                else mbar_arrive_cluster(lead_wready + (uint32_t)wst * 8u);
+                if (leader) mbar_arrive(&m.wready[stage]);
+                else mbar_arrive_cluster(lead_wready + (uint32_t)stage * 8u);
             }
-            if (++wst == NW) { wst = 0; wph ^= 1; }
+            if (++stage == NS) { stage = 0; phase ^= 1; }
         };
         for (int it = 0; ok; it++) {
             bool good;
@@ -1057,7 +1019,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 sh.load(a, t, n_lora);
                 const int kb0 = sh.sp * nkb / sh_ks, kb1 = (sh.sp + 1) * nkb / sh_ks;
                 for (int kb = kb0; kb < kb1 && ok; kb++) {
-                    if (!slot_free()) { ok = false; break; }
+                    if (!stage_in()) { ok = false; break; }
                     stage_done();
                 }
                 continue;
@@ -1091,26 +1053,32 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             }
             const int kb0 = tw.split * nkb / ksplit, kb1 = (tw.split + 1) * nkb / ksplit;
             for (int kb = kb0; kb < kb1 && ok; kb++) {
-                if (!slot_free()) { ok = false; break; }
-                if (!__all_sync(kFull, mbar_wait(&m.w8full[cj], cjph))) { ok = false; break; }
-                const uint8_t* src = m.f8 + (size_t)cj * kF8Slot;
-                uint8_t* dst = m.wring + (size_t)wst * kWSlot8;
+                if (!stage_in()) { ok = false; break; }
+                uint8_t* slot = m.ring + (size_t)stage * kStageW8 + kC0T;
+                uint4 code[4];
 #pragma unroll
                 for (int n = 0; n < 4; n++) {
                     const int i = ct + 256 * n;
                     if (i < n_chunks) {
                         const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
-                        const uint4 code = *reinterpret_cast<const uint4*>(src + (size_t)c * nu2 * kBK + r * kBK + kc * 16);
-                        uint8_t* row = dst + (size_t)c * (kWSlot8 / 2) + r * 128;
-                        e4m3x16_to_bf16(code, fh_[n], k2p56, two_[n], reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
+                        code[n] = *reinterpret_cast<const uint4*>(slot + (size_t)c * kSlot + kCodeOff + r * kBK + kc * 16);
+                    }
+                }
+                // every converter has its codes before any bf16 row overwrites them
+                if (!rendezvous()) { ok = false; break; }
+#pragma unroll
+                for (int n = 0; n < 4; n++) {
+                    const int i = ct + 256 * n;
+                    if (i < n_chunks) {
+                        const int c = i / (4 * nu2), rem = i % (4 * nu2), r = rem >> 2, kc = rem & 3;
+                        uint8_t* row = slot + (size_t)c * kSlot + r * 128;
+                        e4m3x16_to_bf16(code[n], fh_[n], k2p56, two_[n],
+                                        reinterpret_cast<uint4*>(row + (((2 * kc) ^ (r & 7)) << 4)),
                                         reinterpret_cast<uint4*>(row + (((2 * kc + 1) ^ (r & 7)) << 4)));
                     }
                 }
                 // the generic stores before the tensor cores (async proxy) read them
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&m.w8empty[cj]);
-                if (++cj == N8) { cj = 0; cjph ^= 1; }
                 stage_done();
             }
             // the expand blocks of the task (bf16 rows by TMA): only the arrival
@@ -1118,7 +1086,7 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             for (int g = 0, jj = 0; ok && mask != 0ull && g < n_groups; g++) {
                 if (!group_present(mask, g)) continue;
                 if (jj++ % ksplit != tw.split) continue;
-                if (!slot_free()) { ok = false; break; }
+                if (!stage_in()) { ok = false; break; }
                 stage_done();
             }
         }
@@ -1383,12 +1351,10 @@ int max_pairs_of() {
 
 // at least half an SM's shared memory: one CTA per SM, so the whole TMEM
 // allocation never waits for another CTA
-// n8 > 0 (FP8 weights): nstages pair-row stages, nw chain-row stages and
-// n8 code staging slots; else nstages full stages
-int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8, int nw) {
-    if (n8 <= 0) nw = 0;
-    const int rings = n8 > 0 ? nstages * kXSlot8 + nw * kWSlot8 + n8 * kF8Slot : nstages * kStage2;
-    const int bars = (2 * nstages + 2 * nw + 3 + 2 * n8 + 2 * kTaskQ2) * 8 + 16 + kTaskQ2 * 4;
+// (nstages stages of kStageW8 with FP8 weights, else of kStage2)
+int tc2_smem_bytes(int E, int nstages, int max_chunks, bool w8) {
+    const int rings = nstages * (w8 ? kStageW8 : kStage2);
+    const int bars = (2 * nstages + (w8 ? 2 * nstages : 0) + 4 + 2 * kTaskQ2) * 8 + 16 + kTaskQ2 * 4;
     const int slots = (3 * kMaxShrinkSlots + 4) * 4;
     const int table = 8 * max_chunks + (6 * E + 2) * 4;
     const int tr = 16 + kEpiWarps * kTrFloats * 4;
@@ -1397,25 +1363,14 @@ int tc2_smem_bytes(int E, int nstages, int max_chunks, int n8, int nw) {
 
 int tc2_plan_stages(int E, int max_chunks) {
     for (int ns = 8; ns >= 3; ns--)
-        if (tc2_smem_bytes(E, ns, max_chunks) <= kTcSmemLimit) return ns;
+        if (tc2_smem_bytes(E, ns, max_chunks, false) <= kTcSmemLimit) return ns;
     return 0;
 }
 
-// FP8 weights: rings that fit, preferring (in this order) the deepest code
-// staging ring (the codes are what streams from HBM), two or three pair-row
-// stages (they come from L2), then as many converted chain-row stages as fit
-// beyond two
-int tc2_plan_stages_w8(int E, int max_chunks, int* n8, int* nw) {
-    for (int k = 8; k >= 3; k--)
-        for (int x = 3; x >= 2; x--)
-            if (tc2_smem_bytes(E, x, max_chunks, k, 2) <= kTcSmemLimit) {
-                int w = 2;
-                while (w < kMaxNW8 && tc2_smem_bytes(E, x, max_chunks, k, w + 1) <= kTcSmemLimit) w++;
-                *n8 = k;
-                *nw = w;
-                return x;
-            }
-    *n8 = *nw = 0;
+// FP8 weights: the deepest ring of 56 KiB stages that fits (at least two)
+int tc2_plan_stages_w8(int E, int max_chunks) {
+    for (int ns = 8; ns >= 2; ns--)
+        if (tc2_smem_bytes(E, ns, max_chunks, true) <= kTcSmemLimit) return ns;
     return 0;
 }
 
@@ -1443,10 +1398,8 @@ cudaError_t launch_moe_gemm_2sm(const TcArgs& args, bool gate_up, int grid, cuda
     if (args.nu < 16 || args.nu > 256 || args.nu % 16 != 0) return cudaErrorInvalidValue;
     if (args.nu_t != 0 && (args.nu_t < 32 || args.nu_t > 160 || args.nu_t % 32 != 0)) return cudaErrorInvalidValue;
     if (args.r > 0 && (128 / args.r) * 2 > kMaxShrinkSlots) return cudaErrorInvalidValue;
-    if (args.w8 && (args.n8 < 1 || args.nw < 2 || args.nw > kMaxNW8 || args.nstages < 2 || args.wscale == nullptr ||
-                    args.nu_t > 160))
-        return cudaErrorInvalidValue;
-    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks, args.w8 ? args.n8 : 0, args.nw);
+    if (args.w8 && (args.nstages < 2 || args.wscale == nullptr)) return cudaErrorInvalidValue;
+    const int smem = tc2_smem_bytes(args.E, args.nstages, args.max_chunks, args.w8 != 0);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(args.w8 ? kThreadsW8 : kTcThreads);

@@ -790,7 +790,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             if (w8) {
                 tc.w8 = 1;
                 tc.wscale = w8->W1s;
-                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8, &tc.nw);
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks);
                 if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
                 if (!encode_w1q_map(&tc.w8map, w8->W1q, d->E, d->I, d->H, half) ||
                     (half_t && !encode_w1q_map(&tc.w8map_t, w8->W1q, d->E, d->I, d->H, half_t)))
@@ -859,7 +859,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
             if (w8) {
                 tc.w8 = 1;
                 tc.wscale = w8->W2s;
-                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks, &tc.n8, &tc.nw);
+                tc.nstages = tc2_plan_stages_w8(d->E, tc.max_chunks);
                 if (tc.nstages < 2) return MOELORA_EUNSUPPORTED;
                 if (!encode_w2q_map(&tc.w8map, w8->W2q, d->E, d->I, d->H, half) ||
                     (half_t && !encode_w2q_map(&tc.w8map_t, w8->W2q, d->E, d->I, d->H, half_t)))
