@@ -29,6 +29,11 @@
 // gate_up puts a unit's gate value and its up value in the same thread (the
 // same pair's TMEM lane, 256 columns apart), so SiLU(gate) * up is local.
 //
+// Experts whose pairs fill one 256-row chunk and part of a second (257 - 384
+// pairs) may instead run in chunks of 256 + 128 pairs with chains of
+// nu_t <= 160 rows: the last 128 pairs (64 per CTA) go through an M = 128
+// MMA that reads the same weight stage, so the expert's weights stream once.
+//
 // LoRA, in the same orientation:
 //   shrink items (the blog's shrink, section "Kernel optimizations"): the A
 //     matrices of 256 / r consecutive (expert, adapter) buckets stacked on N
@@ -53,7 +58,10 @@
 //            the leader one thread issues every MMA of the pair and commits
 //            stage releases and accumulator completion to both CTAs;
 //   warps 2-9 epilogue of this CTA's 128 TMEM lanes (= pairs); the peer's
-//            warps free the accumulator on the leader's barrier.
+//            warps free the accumulator on the leader's barrier;
+//   warps 10-17 (FP8 weights only) expand the E4M3 codes the producer copies
+//            into a stage's chain-row slots into bf16 weights, in place, and
+//            tell the leader's MMA thread (wready).
 // Every wait is bounded; on a timeout the CTA records kStatusTimeout, stops
 // waiting, drains its copies, frees TMEM and exits at the final pair barrier.
 #include "gemm_tasks.cuh"

@@ -171,12 +171,14 @@ def test_intermediates_config0():
         assert norm_err(pair_out[p], w * ref["d"]) < 1e-2
 
 
-@pytest.mark.parametrize("which", ["config0", "config3"])
+@pytest.mark.parametrize("which", ["config0", "config3", "config2"])
 def test_forward_groups_pairs_by_bucket(which):
     """The forward's own bucketing (compact order in the workspace): bucket b's
     rows hold exactly the pairs with key e*(L+1)+(l+1), in any order (the
-    standalone align's ascending order is checked bit-exact elsewhere)."""
-    layer = wl.make_config(0) if which == "config0" else wl.make_config(3)
+    standalone align's ascending order is checked bit-exact elsewhere).  The
+    prefill layer (8192 pairs, 288 buckets) takes the multi-CTA align, the
+    others the single-CTA one."""
+    layer = wl.make_config({"config0": 0, "config3": 3, "config2": 2}[which])
     dl, st = run(layer)
     assert st == 0
     P, L1 = layer.P, layer.L + 1
@@ -286,6 +288,31 @@ def test_out_of_range_ids_are_flagged_and_left_out():
     dl.set_batch(layer.x, layer.topk_ids, layer.topk_weights, layer.lora_ids)
     B.check(dl.forward())
     assert dl.status() == 0
+
+
+def test_out_of_range_ids_flagged_by_the_multi_cta_align():
+    """A batch of 1200 pairs in 12 buckets takes the multi-CTA align: bad
+    ids seen by any of its CTAs reach the status word, their pairs are left
+    out, and a clean batch afterwards reports OK."""
+    layer = wl.make_random(600, 128, 136, 2, 2, 5, 32, seed=7)
+    tk = layer.topk_ids.copy()
+    tk[3, 1] = layer.E          # first CTA's pairs
+    tk[590, 0] = -1             # last CTA's pairs
+    lo = layer.lora_ids.copy()
+    lo[300] = layer.L           # a middle CTA's token
+    bad = dataclasses.replace(layer, topk_ids=tk, lora_ids=lo)
+    dl, st = run(bad)
+    assert st == B.MOELORA_EDEVICE_ID
+    ref, inv = oracle.forward(bad)
+    assert inv == 2 + layer.k
+    got = dl.out_f64()
+    assert norm_err(got, ref) <= TOL
+    assert np.all(got[300] == 0)
+    dl.set_batch(layer.x, layer.topk_ids, layer.topk_weights, layer.lora_ids)
+    B.check(dl.forward())
+    assert dl.status() == 0
+    ref, _ = oracle.forward(layer)
+    assert norm_err(dl.out_f64(), ref) <= TOL
 
 
 def test_all_pairs_on_one_expert_and_all_base_only():
