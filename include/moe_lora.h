@@ -299,7 +299,9 @@ typedef struct moe_lora_ws_layout {
                                 adapter pairs only; other rows are left undefined) */
     size_t act;              /* bf16 [P][I]: SiLU(gate)*up per row */
     size_t z2;               /* float [P][r]: down LoRA shrink A2 act per row (same rows) */
-    size_t pair_out;         /* float [down_splits][P][H]: w * d per pair id p, one slab per
+    size_t pair_out;         /* w * d per pair id p: bf16 [P][H] when pair_out_bf16 (the down
+                                GEMM does not split K: the activation type, rounded to nearest
+                                even once), else float [down_splits][P][H], one slab per
                                 K-split of the down GEMM (their sum is the pair's output) */
     int32_t s1, s2;          /* K-split counts the two shrinks used */
     int32_t down_splits;     /* K-splits of the down GEMM (>= 1) */
@@ -307,6 +309,7 @@ typedef struct moe_lora_ws_layout {
     int32_t gemm_ctas;       /* CTAs per GEMM task: 2 on the CTA-pair kernel (wide chunks), else 1 */
     int32_t tc_expand;       /* 1: the LoRA expand runs as tensor-core K blocks of the base GEMMs;
                                 0: on CUDA cores in the epilogue (or no adapters) */
+    int32_t pair_out_bf16;   /* 1: pair_out holds bf16 (down_splits == 1); 0: fp32 slabs */
     size_t total;            /* == moe_lora_workspace_bytes */
 } moe_lora_ws_layout;
 

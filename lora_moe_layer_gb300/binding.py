@@ -51,7 +51,7 @@ class moe_lora_ws_layout(ctypes.Structure):
                 ("z1", ctypes.c_size_t), ("act", ctypes.c_size_t), ("z2", ctypes.c_size_t),
                 ("pair_out", ctypes.c_size_t), ("s1", ctypes.c_int32), ("s2", ctypes.c_int32),
                 ("down_splits", ctypes.c_int32), ("launches", ctypes.c_int32), ("gemm_ctas", ctypes.c_int32),
-                ("tc_expand", ctypes.c_int32), ("total", ctypes.c_size_t)]
+                ("tc_expand", ctypes.c_int32), ("pair_out_bf16", ctypes.c_int32), ("total", ctypes.c_size_t)]
 
 
 _lib = None

@@ -37,6 +37,14 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
+// fp32 -> bf16 bits by the hardware conversion (round to nearest even; the
+// same bits as f32_to_bf16_rne for finite inputs, one instruction)
+__device__ __forceinline__ uint16_t f32_to_bf16_cvt(float f) {
+    uint16_t h;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(h) : "f"(f));
+    return h;
+}
+
 // 8 bf16 (one 16-byte chunk) dotted with 8 fp32, accumulated into acc
 __device__ __forceinline__ float dot8(const uint4 w, const float* v, float acc) {
     acc = fmaf(bf_lo(w.x), v[0], acc);

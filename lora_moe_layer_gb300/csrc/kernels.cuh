@@ -100,7 +100,8 @@ struct TcArgs {
     const int32_t* compact_ids;
     WsHeader* hdr;
     uint16_t* act_out;           // gate_up: [P][I] bf16
-    float* pair_out;             // down: [ksplit][P][H] fp32 by pair id, one slab per K-split
+    float* pair_out;             // down, split K: [ksplit][P][H] fp32 by pair id, one slab per K-split
+    uint16_t* pair_out16;        // down, one split: [P][H] bf16 by pair id (then pair_out is unused)
     size_t pair_split;           // down: elements between two K-splits' slabs (P * H)
     int nstages;
     int ksplit;                  // K-splits per weight tile (1: none)
@@ -156,7 +157,8 @@ cudaError_t launch_gather_rows(const GatherArgs& args, int grid, cudaStream_t st
 constexpr int kMaxSplitSlabs = 8;  // the host plans at most 8 K-splits per GEMM
 struct ReduceArgs {
     int T, k, H, E, L;
-    const float* pair_out;       // [nsplit][P][H]: the down GEMM's K-split slabs
+    const float* pair_out;       // [nsplit][P][H]: the down GEMM's K-split slabs (fp32)
+    const uint16_t* pair_out16;  // or, when the down GEMM does not split K, its [P][H] bf16 output
     int nsplit;                  // 1 .. kMaxSplitSlabs
     size_t split_stride;         // elements between slabs
     const int32_t* topk_ids;

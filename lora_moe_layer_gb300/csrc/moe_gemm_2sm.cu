@@ -1192,10 +1192,11 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 rv[i] = __shfl_sync(kFull, row_ok ? 1 : 0, src) != 0;
             }
         };
-        // down: w * d of 16 W2 rows from h into the slab.  The warp's 32 rows x
-        // 16 columns go through its tile: each store then writes 64 contiguous
-        // bytes of 8 rows (lane / 4 + 8 i, quarter lane % 4) instead of 16
-        // bytes of 32 rows.
+        // down: w * d of 16 W2 rows from h into the fp32 slab, or into the bf16
+        // output when K is not split (slab null).  The warp's 32 rows x 16
+        // columns go through its tile: each store then writes 64 (bf16: 32)
+        // contiguous bytes of 8 rows (lane / 4 + 8 i, quarter lane % 4) instead
+        // of 16 (8) bytes of 32 rows.
         float* const trw = m.tr + ew * kTrFloats;
         auto down_emit = [&](const uint32_t (&vr)[16], float* slab, int h, float w, const int (&rp_row)[4],
                              const bool (&rv)[4]) {
@@ -1211,7 +1212,14 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
             for (int i = 0; i < 4; i++) {
                 const int row = (lane >> 2) + 8 * i;
                 const float4 val = *reinterpret_cast<const float4*>(trw + row * kTrStride + 4 * c4);
-                if (rv[i] && hh + 4 <= a.H) *reinterpret_cast<float4*>(slab + (size_t)rp_row[i] * a.H + hh) = val;
+                if (rv[i] && hh + 4 <= a.H) {
+                    if (slab) {
+                        *reinterpret_cast<float4*>(slab + (size_t)rp_row[i] * a.H + hh) = val;
+                    } else {
+                        const uint2 o = make_uint2(pack_bf16x2(val.x, val.y), pack_bf16x2(val.z, val.w));
+                        *reinterpret_cast<uint2*>(a.pair_out16 + (size_t)rp_row[i] * a.H + hh) = o;
+                    }
+                }
             }
             __syncwarp();
         };
@@ -1300,8 +1308,9 @@ __global__ void __launch_bounds__(W8 ? kThreadsW8 : kTcThreads, 1) k_moe_gemm_2s
                 if (tail)
                     act_pass(t_lane + tcol, t_lane + tcol + nu2, u0 + hc * nu2, nu2 / 16, valid_t, a.act_out + qt * a.I);
             } else {
-                // W2 rows h0 + c * nu + 16 g ..: w * d into this split's slab of pair_out
-                float* const slab = a.pair_out + (ksplit > 1 ? (size_t)tw.split * a.pair_split : 0);
+                // W2 rows h0 + c * nu + 16 g ..: w * d into this split's fp32 slab
+                // of pair_out, or (no K split) into the bf16 pair_out16
+                float* const slab = ksplit > 1 ? a.pair_out + (size_t)tw.split * a.pair_split : nullptr;
                 int rp_row[4];
                 bool rv[4];
                 store_rows(p, valid, rp_row, rv);

@@ -79,15 +79,18 @@ struct EpiRow {
     int e, w_row, cur_l;
     bool row_ok;
     size_t rows_per_expert;
-    float* pout;         // down: this K-split's [P][H] slab
+    float* pout;         // down: this K-split's [P][H] fp32 slab, or
+    uint16_t* pout16;    // the [P][H] bf16 output when K is not split
     uint4 bg[8], bu[8];  // r <= 64 bf16 each
 
-    __device__ void init(const TcArgs& a, int e_, int w_row_, bool row_ok_, size_t rpe, float* pout_) {
+    __device__ void init(const TcArgs& a, int e_, int w_row_, bool row_ok_, size_t rpe, float* pout_,
+                         uint16_t* pout16_) {
         e = e_;
         w_row = w_row_;
         row_ok = row_ok_;
         rows_per_expert = rpe;
         pout = pout_;
+        pout16 = pout16_;
         cur_l = -2;
     }
 
@@ -136,6 +139,8 @@ struct EpiRow {
         if (row_ok) {
             if (GATE_UP)
                 a.act_out[(size_t)q * a.I + w_row] = f32_to_bf16_rne(silu_f(vg) * vu);
+            else if (pout16)
+                pout16[(size_t)p * a.H + w_row] = f32_to_bf16_cvt(w * vg);
             else
                 pout[(size_t)p * a.H + w_row] = w * vg;
         }
@@ -600,10 +605,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
             // split-K of gate_up: partial tiles go to global memory; the split
             // that arrives last adds the others' partials (in split order) to
             // its own.  Split-K of down: every split writes w * its partial to
-            // its own slab of pair_out (the reduce kernel adds the slabs in
-            // split order), so no split waits for another.
+            // its own fp32 slab of pair_out (the reduce kernel adds the slabs in
+            // split order), so no split waits for another; without a split,
+            // w * d goes out in bf16.
             const bool slab = !GATE_UP && ksplit > 1;
-            float* const pout = GATE_UP ? nullptr : a.pair_out + (slab ? (size_t)tw.split * a.pair_split : 0);
+            float* const pout = GATE_UP || !slab ? nullptr : a.pair_out + (size_t)tw.split * a.pair_split;
+            uint16_t* const pout16 = GATE_UP || slab ? nullptr : a.pair_out16;
             bool finish = true;
             float* part_tile = nullptr;
             if (ksplit > 1 && !slab) {
@@ -640,7 +647,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                             const int cc = c0 + c;
                             if (cc < n_real) {
                                 if (GATE_UP)
-                                    a.act_out[(size_t)(q0c + cc) * a.I + w_row] = f32_to_bf16_rne(silu_fast(g[c]) * u[c]);
+                                    a.act_out[(size_t)(q0c + cc) * a.I + w_row] = f32_to_bf16_cvt(silu_fast(g[c]) * u[c]);
+                                else if (!slab)
+                                    pout16[(size_t)s_pair[cc] * a.H + w_row] = f32_to_bf16_cvt(s_w[cc] * g[c]);
                                 else
                                     pout[(size_t)s_pair[cc] * a.H + w_row] = s_w[cc] * g[c];
                             }
@@ -650,7 +659,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_moe_gemm_tc(const __grid_cons
                 finish = false;
             }
             EpiRow<GATE_UP> er;
-            er.init(a, e, w_row, row_ok, rows_per_expert, pout);
+            er.init(a, e, w_row, row_ok, rows_per_expert, pout, pout16);
             // the CUDA-core expand is added once: by split 0 when splits write slabs
             const bool add_lora = has_lora && (!slab || tw.split == 0);
             for (int c0 = half * 16; finish && c0 < n_cols; c0 += 32) {

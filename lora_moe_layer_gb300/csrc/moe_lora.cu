@@ -339,8 +339,11 @@ int make_layout(const moe_lora_dims* d, Layout* L, bool w8 = false) {
     const size_t zx = L->tc_expand ? sizeof(uint16_t) * (size_t)L->P * zexp_cols(d->L, d->r) : 0;
     L->zexp1 = take(zx);
     L->zexp2 = take(zx);
-    // one [P][H] slab per K-split of the down GEMM (summed by the reduce)
-    L->pair_out = take(sizeof(float) * (size_t)std::max(1, L->ks_dn) * L->P * d->H);
+    // w * d per pair: bf16 [P][H] when the down GEMM does not split K (the
+    // activation type, like the per-pair outputs the reduce sums), else one
+    // fp32 [P][H] slab per K-split (partial sums stay exact until the reduce)
+    L->pair_out = take(L->ks_dn > 1 ? sizeof(float) * (size_t)L->ks_dn * L->P * d->H
+                                    : sizeof(uint16_t) * (size_t)L->P * d->H);
     const size_t part_gu = L->ks_gu > 1 ? (size_t)L->tiles_gu * L->ks_gu * 2 * L->bn_gu * 128 : 0;
     L->tc_part = take(sizeof(float) * part_gu);
     L->tc_counters = take(sizeof(int32_t) * (L->tiles_gu + L->tiles_dn));
@@ -604,6 +607,7 @@ MOELORA_API int moe_lora_workspace_layout(const moe_lora_dims* d, moe_lora_ws_la
     out->launches = 5;  // align, gather, gate_up, down, reduce
     out->gemm_ctas = L.ranks;
     out->tc_expand = L.tc_expand ? 1 : 0;
+    out->pair_out_bf16 = L.ks_dn > 1 ? 0 : 1;
     out->total = workspace_need(d);
     return MOELORA_OK;
 }
@@ -751,7 +755,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     tc.compact_ids = at<int32_t>(ws, L.compact_ids);
     tc.hdr = hdr;
     tc.act_out = at<uint16_t>(ws, L.act);
-    tc.pair_out = at<float>(ws, L.pair_out);
+    tc.pair_out = L.ks_dn > 1 ? at<float>(ws, L.pair_out) : nullptr;
+    tc.pair_out16 = L.ks_dn > 1 ? nullptr : at<uint16_t>(ws, L.pair_out);
     int* task_counters = at<int>(ws, L.counters);  // gate_up, down; then the shrink counters
     int* sh_counters = task_counters + 2;
     tc.tc_expand = L.tc_expand ? 1 : 0;
@@ -905,7 +910,8 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
 
     ReduceArgs ra = {};
     ra.T = d->T; ra.k = d->k; ra.H = d->H; ra.E = d->E; ra.L = d->L;
-    ra.pair_out = at<float>(ws, L.pair_out);
+    ra.pair_out = L.ks_dn > 1 ? at<float>(ws, L.pair_out) : nullptr;
+    ra.pair_out16 = L.ks_dn > 1 ? nullptr : at<uint16_t>(ws, L.pair_out);
     ra.nsplit = std::max(1, L.ks_dn);
     ra.split_stride = (size_t)L.P * d->H;
     ra.topk_ids = topk_ids;
@@ -913,7 +919,7 @@ int forward_impl(const moe_lora_dims* d, const void* x, const int32_t* topk_ids,
     ra.out = static_cast<uint16_t*>(out);
     tr.mark(4);
     {
-        const long n = (long)d->T * (d->H / 4);
+        const long n = (long)d->T * (d->H / (ra.pair_out16 ? 8 : 4));  // hidden elements per thread
         const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, (long)sms * 8));
         if (launch_reduce(ra, grid, s, pdl) != cudaSuccess) return MOELORA_ECUDA;
     }

@@ -91,3 +91,14 @@ class DeviceLayer:
         off = lay[name]
         n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
         return self.workspace[off:off + n].view(dtype).view(*shape)
+
+    def pair_outputs(self) -> np.ndarray:
+        """w * d per pair id of the last forward as fp64 [P][H]: the bf16 per-pair
+        outputs, or the sum of the fp32 K-split slabs when the down GEMM split K."""
+        lay = B.moe_lora_workspace_layout(self.d)
+        P, H = self.d.T * self.d.k, self.d.H
+        if lay["pair_out_bf16"]:
+            bits = self.workspace_view("pair_out", torch.int16, (P, H)).cpu().numpy().view(np.uint16)
+            return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        s = lay["down_splits"]
+        return self.workspace_view("pair_out", torch.float32, (s, P, H)).cpu().numpy().astype(np.float64).sum(0)

@@ -57,24 +57,30 @@ def test_workspace_bytes_and_layout(lib):
     for s in (lay["s1"], lay["s2"]):
         assert 1 < s <= min(32, (2880 // 64) // 2)
     # regions are disjoint and inside the workspace
-    assert lay["down_splits"] == 1
+    assert lay["down_splits"] == 1 and lay["pair_out_bf16"] == 1
     assert lay["launches"] == 5  # align, gather, gate_up, down, reduce
     regions = sorted([(lay["compact_ids"], 4 * P), (lay["z1"], 4 * P * 32),
                       (lay["act"], 2 * P * 2880), (lay["z2"], 4 * P * 32),
-                      (lay["pair_out"], 4 * P * 2880 * lay["down_splits"])])
+                      (lay["pair_out"], pair_bytes(lay, P, 2880))])
     for (a, na), (b, _) in zip(regions, regions[1:]):
         assert a + na <= b
     assert regions[-1][0] + regions[-1][1] <= n
     assert all(off % 256 == 0 for off, _ in regions)
 
 
+def pair_bytes(lay, P, H):
+    """pair_out's size: bf16 [P][H] without a down K-split, else fp32 [splits][P][H]."""
+    assert lay["pair_out_bf16"] == (1 if lay["down_splits"] == 1 else 0)
+    return 2 * P * H if lay["pair_out_bf16"] else 4 * P * H * lay["down_splits"]
+
+
 def test_layout_of_split_and_expand_workloads(lib):
-    # one expert with few weight tiles: the down GEMM splits K, one pair_out
-    # slab per split
+    # one expert with few weight tiles: the down GEMM splits K, one fp32
+    # pair_out slab per split
     d = B.dims(256, 8192, 28672, 1, 1, 32, 64)
     lay = B.moe_lora_workspace_layout(d)
-    assert 1 < lay["down_splits"] <= 8
-    assert lay["pair_out"] + 4 * 256 * 8192 * lay["down_splits"] <= lay["total"]
+    assert 1 < lay["down_splits"] <= 8 and lay["pair_out_bf16"] == 0
+    assert lay["pair_out"] + pair_bytes(lay, 256, 8192) <= lay["total"]
 
 
 def test_split_plan_follows_the_sm_count(lib):
@@ -98,9 +104,9 @@ def test_split_plan_follows_the_sm_count(lib):
     assert dn[1] == 1 and 1 < dn[38] < dn[152] <= 8
     for n in (1, 38, 76, 152, 304):
         L = lay(n, *dense)
-        assert L["pair_out"] + 4 * 256 * 8192 * L["down_splits"] <= L["total"]
+        assert L["pair_out"] + pair_bytes(L, 256, 8192) <= L["total"]
         L = lay(n, *decode)
-        assert L["pair_out"] + 4 * 64 * 2880 * L["down_splits"] <= L["total"]
+        assert L["pair_out"] + pair_bytes(L, 64, 2880) <= L["total"]
     assert B.moe_lora_workspace_bytes(B.dims(*decode, sm_count=-1)) == 0
     assert B.moe_lora_workspace_bytes(B.dims(*decode, sm_count=5000)) == 0
 
