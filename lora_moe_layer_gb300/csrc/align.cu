@@ -115,18 +115,36 @@ __device__ __forceinline__ int4 warp_incl_scan4(int4 v, int lane) {
     return v;
 }
 
-// Exclusive scan over n items of four counts each: item(i) gives them, and
-// emit(i, prefix, item) is called once per item in order within each
-// thread's contiguous run.  Every thread gets the totals.  sw needs
-// kAlignWarps + 1 entries.  Contains __syncthreads.
+// Exclusive scan over n bucket items of four counts each: item(b, sub, e)
+// gives them (sub = b % L1 and e = b / L1, kept by increments along each
+// thread's contiguous run), and emit(b, e, prefix, item) is called once per
+// item in order within the run.  The first kScanCache items of a run are
+// evaluated once and kept in registers; longer runs evaluate the rest again
+// in the second pass.  Every thread gets the totals.  sw needs kAlignWarps + 1
+// entries.  Contains __syncthreads.
+constexpr int kScanCache = 8;
 template <typename F, typename G>
-__device__ int4 block_scan4(int n, F item, G emit, int4* sw) {
+__device__ int4 block_scan4(int n, int L1, F item, G emit, int4* sw) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per = (n + kAlignThreads - 1) / kAlignThreads;
     const int beg = min(n, (int)threadIdx.x * per);
     const int end = min(n, beg + per);
+    const int sub0 = beg % L1, e0 = beg / L1;
     int4 local = make_int4(0, 0, 0, 0);
-    for (int i = beg; i < end; i++) local = add4(local, item(i));
+    int4 cache[kScanCache];
+    int sub = sub0, e = e0;
+#pragma unroll
+    for (int k = 0; k < kScanCache; k++) {
+        if (beg + k < end) {
+            cache[k] = item(beg + k, sub, e);
+            local = add4(local, cache[k]);
+            if (++sub == L1) { sub = 0; e++; }
+        }
+    }
+    for (int i = beg + kScanCache; i < end; i++) {
+        local = add4(local, item(i, sub, e));
+        if (++sub == L1) { sub = 0; e++; }
+    }
     const int4 inc = warp_incl_scan4(local, lane);
     if (lane == 31) sw[warp] = inc;
     __syncthreads();
@@ -139,10 +157,21 @@ __device__ int4 block_scan4(int n, F item, G emit, int4* sw) {
     __syncthreads();
     int4 run = add4(sw[warp], sub4(inc, local));
     const int4 total = sw[kAlignWarps];
-    for (int i = beg; i < end; i++) {
-        const int4 v = item(i);
-        emit(i, run, v);
+    sub = sub0;
+    e = e0;
+#pragma unroll
+    for (int k = 0; k < kScanCache; k++) {
+        if (beg + k < end) {
+            emit(beg + k, e, run, cache[k]);
+            run = add4(run, cache[k]);
+            if (++sub == L1) { sub = 0; e++; }
+        }
+    }
+    for (int i = beg + kScanCache; i < end; i++) {
+        const int4 v = item(i, sub, e);
+        emit(i, e, run, v);
         run = add4(run, v);
+        if (++sub == L1) { sub = 0; e++; }
     }
     __syncthreads();
     return total;
@@ -193,16 +222,33 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     for (int i = threadIdx.x; i < a.n_zero; i += kAlignThreads) a.zero_ints[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
     {
+        // keys may live in global memory, where the compiler must assume they
+        // alias the ids: the first kKeyBatch pairs of each thread are loaded
+        // into registers before any key is stored, so their loads overlap
         int bad = 0;
-#pragma unroll 8
-        for (int p = threadIdx.x; p < P; p += kAlignThreads) {
-            const int e = a.topk_ids[p];
-            const int l = a.lora_ids[p / a.k];
+        auto key = [&](int e, int l) {
             const bool e_ok = e >= 0 && e < a.E;
             const bool l_ok = l >= -1 && l < a.L;
-            keys[p] = e_ok && l_ok ? e * L1 + (l + 1) : -1;
             bad |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
+            return e_ok && l_ok ? e * L1 + (l + 1) : -1;
+        };
+        constexpr int kKeyBatch = 8;
+        int ev[kKeyBatch], lv[kKeyBatch];
+#pragma unroll
+        for (int i = 0; i < kKeyBatch; i++) {
+            const int p = threadIdx.x + i * kAlignThreads;
+            if (p < P) {
+                ev[i] = a.topk_ids[p];
+                lv[i] = a.lora_ids[p / a.k];
+            }
         }
+#pragma unroll
+        for (int i = 0; i < kKeyBatch; i++) {
+            const int p = threadIdx.x + i * kAlignThreads;
+            if (p < P) keys[p] = key(ev[i], lv[i]);
+        }
+        for (int p = threadIdx.x + kKeyBatch * kAlignThreads; p < P; p += kAlignThreads)
+            keys[p] = key(a.topk_ids[p], a.lora_ids[p / a.k]);
         if (bad) atomicOr(&hdr->status, bad);
     }
     __syncthreads();
@@ -260,17 +306,16 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     // one scan over the buckets: padded offsets (bucket_offset), compact
     // offsets, and for the forward the list of (e, l >= 0) buckets with pairs
     // and the list of experts with pairs (counted at each expert's first bucket)
-    const int bm = a.bm;
+    const int bm = a.bm;  // a power of two
     const int* cnt = cnt_t;
     const int4 tot = block_scan4(
-        NB,
-        [&](int b) {
+        NB, L1,
+        [&](int b, int sub, int e) {
             const int c = cnt[b];
-            const int sub = b % L1;
-            return make_int4((c + bm - 1) / bm * bm, c, lists && sub != 0 && c > 0 ? 1 : 0,
-                             lists && sub == 0 && e_act[b / L1] ? 1 : 0);
+            return make_int4((c + bm - 1) & -bm, c, lists && sub != 0 && c > 0 ? 1 : 0,
+                             lists && sub == 0 && e_act[e] ? 1 : 0);
         },
-        [&](int b, int4 pre, int4 v) {
+        [&](int b, int e, int4 pre, int4 v) {
             boff_t[b] = pre.x;
             coff_t[b] = pre.y;
             if (a.tabs_in_smem) {
@@ -281,7 +326,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
                 a.lora_buckets[pre.z] = b;
                 lbs[pre.z] = b;
             }
-            if (v.w) a.active_experts[pre.w] = b / L1;
+            if (v.w) a.active_experts[pre.w] = e;
         },
         sw4);
     if (threadIdx.x == 0) {
@@ -437,18 +482,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align_multi(AlignArgs a) {
         __threadfence();
         for (int b = tid; b < NB; b += kAlignThreads) cnt[b] = __ldcg(a.gcount + b);
         __syncthreads();
-        const int bm = a.bm;
+        const int bm = a.bm;  // a power of two
         const int4 tot = block_scan4(
-            NB,
-            [&](int b) {
+            NB, L1,
+            [&](int b, int sub, int) {
                 const int c = cnt[b];
-                const int sub = b % L1;
                 int any = 0;
                 if (sub == 0)
                     for (int j = 0; j < L1; j++) any |= cnt[b + j];
-                return make_int4((c + bm - 1) / bm * bm, c, sub != 0 && c > 0 ? 1 : 0, any != 0 ? 1 : 0);
+                return make_int4((c + bm - 1) & -bm, c, sub != 0 && c > 0 ? 1 : 0, any != 0 ? 1 : 0);
             },
-            [&](int b, int4 pre, int4 v) {
+            [&](int b, int e, int4 pre, int4 v) {
                 a.bucket_count[b] = cnt[b];
                 a.bucket_offset[b] = pre.x;
                 a.compact_offset[b] = pre.y;
@@ -457,7 +501,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align_multi(AlignArgs a) {
                     a.lora_buckets[pre.z] = b;
                     lbs[pre.z] = b;
                 }
-                if (v.w) a.active_experts[pre.w] = b / L1;
+                if (v.w) a.active_experts[pre.w] = e;
             },
             sw4);
         if (tid == 0) {
