@@ -214,6 +214,20 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
     int* lbs = hist + NB + 1;                      // copy of the adapter-bucket list (lists only)
     int* e_act = hist + 2 * NB + 1;               // [E] experts with pairs (lists only)
 
+    // The first kKeyBatch pairs of each thread: their ids are loaded into
+    // registers before the clearing below and before any key is stored (keys
+    // may live in global memory, where the compiler must assume they alias
+    // the ids), so the loads overlap one another and the clearing.
+    constexpr int kKeyBatch = 8;
+    int ev[kKeyBatch], lv[kKeyBatch];
+#pragma unroll
+    for (int i = 0; i < kKeyBatch; i++) {
+        const int p = threadIdx.x + i * kAlignThreads;
+        if (p < P) {
+            ev[i] = a.topk_ids[p];
+            lv[i] = a.lora_ids[p / a.k];
+        }
+    }
     if (threadIdx.x == 0) hdr->status = 0;
     const int n_hist = stable ? kAlignWarps * NB : NB;
     for (int i = threadIdx.x; i < n_hist; i += kAlignThreads) hist[i] = 0;
@@ -221,27 +235,14 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         for (int i = threadIdx.x; i < a.E; i += kAlignThreads) e_act[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero; i += kAlignThreads) a.zero_ints[i] = 0;
     for (int i = threadIdx.x; i < a.n_zero2; i += kAlignThreads) a.zero_ints2[i] = 0;
+    int bad = 0;
     {
-        // keys may live in global memory, where the compiler must assume they
-        // alias the ids: the first kKeyBatch pairs of each thread are loaded
-        // into registers before any key is stored, so their loads overlap
-        int bad = 0;
         auto key = [&](int e, int l) {
             const bool e_ok = e >= 0 && e < a.E;
             const bool l_ok = l >= -1 && l < a.L;
             bad |= (e_ok ? 0 : kStatusBadExpert) | (l_ok ? 0 : kStatusBadLora);
             return e_ok && l_ok ? e * L1 + (l + 1) : -1;
         };
-        constexpr int kKeyBatch = 8;
-        int ev[kKeyBatch], lv[kKeyBatch];
-#pragma unroll
-        for (int i = 0; i < kKeyBatch; i++) {
-            const int p = threadIdx.x + i * kAlignThreads;
-            if (p < P) {
-                ev[i] = a.topk_ids[p];
-                lv[i] = a.lora_ids[p / a.k];
-            }
-        }
 #pragma unroll
         for (int i = 0; i < kKeyBatch; i++) {
             const int p = threadIdx.x + i * kAlignThreads;
@@ -249,9 +250,10 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
         }
         for (int p = threadIdx.x + kKeyBatch * kAlignThreads; p < P; p += kAlignThreads)
             keys[p] = key(a.topk_ids[p], a.lora_ids[p / a.k]);
-        if (bad) atomicOr(&hdr->status, bad);
     }
     __syncthreads();
+    // after the barrier, so thread 0's clearing of the status word comes first
+    if (bad) atomicOr(&hdr->status, bad);
 
     // each warp owns pairs [seg_beg, seg_end), walked 32 at a time
     const int seg = ((P + kAlignWarps - 1) / kAlignWarps + 31) & ~31;
@@ -299,7 +301,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             hist[b] = 0;
         }
         cnt_t[b] = run;
-        if (a.tabs_in_smem) a.bucket_count[b] = run;
+        // (the forward's kernels read only the compact offsets)
+        if (a.tabs_in_smem && !lists) a.bucket_count[b] = run;
     }
     __syncthreads();
 
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignArgs a) {
             boff_t[b] = pre.x;
             coff_t[b] = pre.y;
             if (a.tabs_in_smem) {
-                a.bucket_offset[b] = pre.x;
+                if (!lists) a.bucket_offset[b] = pre.x;
                 a.compact_offset[b] = pre.y;
             }
             if (v.z) {
@@ -493,8 +496,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align_multi(AlignArgs a) {
                 return make_int4((c + bm - 1) & -bm, c, sub != 0 && c > 0 ? 1 : 0, any != 0 ? 1 : 0);
             },
             [&](int b, int e, int4 pre, int4 v) {
-                a.bucket_count[b] = cnt[b];
-                a.bucket_offset[b] = pre.x;
+                // (the forward's kernels read only the compact offsets)
                 a.compact_offset[b] = pre.y;
                 coff[b] = pre.y;
                 if (v.z) {
@@ -506,7 +508,6 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align_multi(AlignArgs a) {
             sw4);
         if (tid == 0) {
             coff[NB] = tot.y;
-            a.bucket_offset[NB] = tot.x;
             a.compact_offset[NB] = tot.y;
             hdr->num_post_padded = tot.x;
             hdr->n_valid = tot.y;
