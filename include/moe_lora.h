@@ -146,9 +146,11 @@ MOELORA_API int moe_lora_align(const moe_lora_dims *d, const int32_t *topk_ids,
 
 /*
  * The layer forward described at the top of this header, computed by the
- * library's kernels in bf16 inputs / fp32 accumulation with one rounding of
- * the result to bf16 (round to nearest even).  Intermediates (the LoRA
- * shrink outputs and the activation) are kept in fp32 and bf16 respectively.
+ * library's kernels in bf16 inputs / fp32 accumulation, the sum over the k
+ * slots in fp32 and rounded once to bf16 (round to nearest even).
+ * Intermediates: the LoRA shrink outputs in fp32, the activation in bf16, and
+ * each pair's weighted down output in bf16 (fp32 partial sums when the down
+ * GEMM splits K; see moe_lora_ws_layout).
  * A1, B1, A2, B2 may be NULL only when L == 0.  `out` [T][H] bf16 is fully
  * overwritten.  The workspace must hold moe_lora_workspace_bytes(d) bytes;
  * its contents on entry do not matter.  Results are deterministic (no

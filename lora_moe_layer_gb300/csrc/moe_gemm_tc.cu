@@ -42,8 +42,9 @@
 //   warps 2-9 epilogue: each thread owns one weight row (its TMEM lane; two
 //            warps per lane quadrant take alternate 16-column chunks), adds the
 //            LoRA expand B[l][e][row] . z[pair] on CUDA cores when the tensor
-//            cores do not take it, and writes bf16 SiLU(gate)*up or fp32 w * d
-//            (down with split K: one slab per split, added by the reduce).  Per task the column metadata (pair,
+//            cores do not take it, and writes bf16 SiLU(gate)*up or bf16 w * d
+//            (down with split K: fp32, one slab per split, added by the
+//            reduce).  Per task the column metadata (pair,
 //            adapter, weight) and the chunk's z rows are first staged in
 //            shared memory, while the task's MMAs are still running.
 // The two accumulators alternate, so one task's epilogue overlaps the next
