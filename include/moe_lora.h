@@ -266,8 +266,7 @@ MOELORA_API int moe_lora_get_status(const void *workspace, void *stream);
  *     MOELORA_ENOSPC before anything is launched (e.g. the decode layer
  *     T=16, H=I=2880, E=32, top-4, r=32 needs about 1.3 MiB).
  *   - The first call on each device looks the buffer's device address up
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *     (cudaGetSymbolAddress, with that device current).
  *   - All calls in the process share the one buffer per device, and each call
  *     leaves its intermediates in it.  Calls whose work overlaps on the GPU
  *     (two streams, or two host threads, of the same device) race on it:
